@@ -1,0 +1,217 @@
+"""CPU oracle of the compressed bf16 stream and the fused compressed reduce.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg (``bench.py``) may import this package.  The GPU
+library never imports, links or calls it, and it shares no code with the GPU
+library.
+
+The arithmetic lives in ``cccl_oracle.c`` (plain single-threaded C, built with
+``-O2 -ffp-contract=off``, no fast-math).  This module only builds it and
+marshals numpy arrays.  Method source: "CCCL: In-GPU Compression-Coupled
+Collective Communication", sections 4.1, 4.3, 4.4 and 5, and Figure 2.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "cccl_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT = 0, 1, 2, 3
+CHUNK_ELEMS = 4096
+
+
+def build(force: bool = False) -> str:
+    """Compile ``cccl_oracle.c`` into ``liboracle.so`` next to it."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp.%d" % os.getpid()
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+             "-Wall", "-Wextra", "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    sz, u8p, u16p = ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p
+    lib.oracle_n_chunks.argtypes = [sz]
+    lib.oracle_n_chunks.restype = sz
+    lib.oracle_data_start.argtypes = [sz]
+    lib.oracle_data_start.restype = sz
+    lib.oracle_compress_bound.argtypes = [sz]
+    lib.oracle_compress_bound.restype = sz
+    lib.oracle_plane_position.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_uint),
+                                          ctypes.POINTER(ctypes.c_uint)]
+    lib.oracle_chunk_choice.argtypes = [u16p, sz] + [ctypes.POINTER(ctypes.c_uint)] * 3 + \
+        [ctypes.POINTER(sz)] * 2
+    lib.oracle_encode_chunk.argtypes = [u16p, sz, u8p, ctypes.POINTER(sz)]
+    lib.oracle_compress.argtypes = [u16p, sz, u8p, sz, ctypes.POINTER(sz)]
+    lib.oracle_decompress.argtypes = [u8p, sz, u16p, sz]
+    lib.oracle_round_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_round_bf16.restype = ctypes.c_uint16
+    lib.oracle_sum_ranks.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, sz, u16p]
+    lib.oracle_reduce.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(sz), ctypes.c_int, sz,
+                                  u8p, sz, ctypes.POINTER(sz)]
+    for f in ("oracle_chunk_choice", "oracle_encode_chunk", "oracle_compress", "oracle_decompress",
+              "oracle_reduce"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.oracle_sum_ranks.restype = None
+    lib.oracle_plane_position.restype = None
+    return lib
+
+
+_lib = None
+_override = None  # a library built from another source (the mutation tests use it)
+
+
+def _load():
+    global _lib
+    if _override is not None:
+        return _override
+    if _lib is None:
+        _lib = _bind(build())
+    return _lib
+
+
+class use_library:
+    """Context manager: route this module's calls to another build of the
+    oracle source (used only to check that the pins catch planted mistakes)."""
+
+    def __init__(self, path: str):
+        self.lib = _bind(path)
+
+    def __enter__(self):
+        global _override
+        _override = self.lib
+        return self
+
+    def __exit__(self, *exc):
+        global _override
+        _override = None
+        return False
+
+
+def build_from(src: str, out: str) -> str:
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+                           "-w", "-o", out, src])
+    return out
+
+
+class OracleError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s failed with status %d" % (what, status))
+        self.status = status
+
+
+def _u16(x) -> np.ndarray:
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.uint16:
+        a = a.view(np.uint16) if a.dtype.itemsize == 2 else a.astype(np.uint16)
+    return a
+
+
+def n_chunks(n: int) -> int:
+    return _load().oracle_n_chunks(n)
+
+
+def data_start(n: int) -> int:
+    return _load().oracle_data_start(n)
+
+
+def compress_bound(n: int) -> int:
+    return _load().oracle_compress_bound(n)
+
+
+def plane_position(i: int) -> tuple[int, int]:
+    w, b = ctypes.c_uint(), ctypes.c_uint()
+    _load().oracle_plane_position(i, ctypes.byref(w), ctypes.byref(b))
+    return w.value, b.value
+
+
+def chunk_choice(x) -> dict:
+    """Encoding decision for one chunk: raw, k, base, n_esc, bytes."""
+    a = _u16(x)
+    raw, k, base = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+    n_esc, nbytes = ctypes.c_size_t(), ctypes.c_size_t()
+    st = _load().oracle_chunk_choice(a.ctypes.data, a.size, ctypes.byref(raw), ctypes.byref(k), ctypes.byref(base),
+                                     ctypes.byref(n_esc), ctypes.byref(nbytes))
+    if st != OK:
+        raise OracleError(st, "oracle_chunk_choice")
+    return dict(raw=raw.value, k=k.value, base=base.value, n_esc=n_esc.value, bytes=nbytes.value)
+
+
+def encode_chunk(x) -> bytes:
+    """One chunk (header included) encoded on its own."""
+    a = _u16(x)
+    out = np.zeros(16 + 2 * CHUNK_ELEMS, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_encode_chunk(a.ctypes.data, a.size, out.ctypes.data, ctypes.byref(nb))
+    if st != OK:
+        raise OracleError(st, "oracle_encode_chunk")
+    return out[:nb.value].tobytes()
+
+
+def compress(x) -> np.ndarray:
+    """bf16 bits (uint16 array) -> compressed stream (uint8 array)."""
+    a = _u16(x).reshape(-1)
+    cap = compress_bound(a.size)
+    out = np.empty(cap, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_compress(a.ctypes.data, a.size, out.ctypes.data, cap, ctypes.byref(nb))
+    if st != OK:
+        raise OracleError(st, "oracle_compress")
+    return out[:nb.value]
+
+
+def decompress(s, n: int) -> np.ndarray:
+    """Compressed stream -> n bf16 bit patterns; raises OracleError on a bad stream."""
+    b = np.ascontiguousarray(np.frombuffer(bytes(s), np.uint8) if isinstance(s, (bytes, bytearray)) else s,
+                             dtype=np.uint8)
+    out = np.empty(n, np.uint16)
+    st = _load().oracle_decompress(b.ctypes.data, b.size, out.ctypes.data, n)
+    if st != OK:
+        raise OracleError(st, "oracle_decompress")
+    return out
+
+
+def decompress_status(s, n: int) -> int:
+    try:
+        decompress(s, n)
+        return OK
+    except OracleError as e:
+        return e.status
+
+
+def round_bf16(f: float) -> int:
+    return int(_load().oracle_round_bf16(ctypes.c_float(f)))
+
+
+def sum_ranks(xs) -> np.ndarray:
+    """Element-wise binary32 sum in rank order, rounded once to bf16."""
+    arrs = [_u16(x).reshape(-1) for x in xs]
+    n = arrs[0].size
+    ptrs = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    out = np.empty(n, np.uint16)
+    _load().oracle_sum_ranks(ptrs, len(arrs), n, out.ctypes.data)
+    return out
+
+
+def reduce(streams, n: int) -> np.ndarray:
+    """R compressed streams -> compressed stream of their rounded binary32 sum."""
+    bs = [np.ascontiguousarray(s, dtype=np.uint8) for s in streams]
+    ptrs = (ctypes.c_void_p * len(bs))(*[b.ctypes.data for b in bs])
+    sizes = (ctypes.c_size_t * len(bs))(*[b.size for b in bs])
+    cap = compress_bound(n)
+    out = np.empty(cap, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_reduce(ptrs, sizes, len(bs), n, out.ctypes.data, cap, ctypes.byref(nb))
+    if st != OK:
+        raise OracleError(st, "oracle_reduce")
+    return out[:nb.value]

@@ -1,0 +1,517 @@
+/*
+ * cccl_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU definition of what the compressed
+ * collective hot path computes.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load it.  The GPU library shares no code,
+ * header, table or helper with this file, and this file includes none of the
+ * GPU library's headers.
+ *
+ * Source of the method: "CCCL: In-GPU Compression-Coupled Collective
+ * Communication" (arXiv 2604.17172):
+ *   - section 4.1 "Compression Principle": a bf16 value splits into sign,
+ *     8-bit exponent and fraction; sign and fraction travel raw, only the
+ *     skewed exponent is re-encoded;
+ *   - section 4.3 "Localized Frequency Tables": every block derives its own
+ *     exponent table from its own data, and every exponent symbol gets a
+ *     fixed-length bit code;
+ *   - section 4.4 "Reducing Global Memory Access": each block writes straight
+ *     into its final place in one preallocated output;
+ *   - section 5 "Handling data alignment": data outside whole chunks travels
+ *     uncompressed;
+ *   - section 5 (CopyReducePacks) and Figure 2: the reduce step of an
+ *     allreduce is receive -> decompress -> reduce -> compress -> send.
+ *
+ * The pages fix no bitstream.  This file DEFINES one (every field, every
+ * choice); the readings taken where the pages are silent are listed in the
+ * design notes of the repository.  In short:
+ *   - chunks of 4096 elements; the exponent table of a chunk is its exact
+ *     minimum exponent `base` plus a code width k (0..7): element i stores
+ *     code = e_i - base when that is below S = 2^k - 1, else the sentinel S
+ *     and its raw exponent goes to an escape list (ascending element order);
+ *   - k minimises 512*k + pad16(#escapes); ties go to the smaller k; the
+ *     chunk is stored raw when no k beats the 4096 bytes of exponents;
+ *   - the last chunk, when shorter than 4096 elements, is stored raw;
+ *   - the reduce adds in binary32, rank 0 first, and rounds once to bf16
+ *     (round to nearest even; every NaN becomes 0x7FC0).
+ *
+ * Little endian throughout.  All stored integers are written byte by byte.
+ */
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* status codes (same numbering as the library's, defined independently) */
+#define ORC_OK 0
+#define ORC_ERR_INVALID_ARG 1
+#define ORC_ERR_CAPACITY 2
+#define ORC_ERR_CORRUPT 3
+
+#define CHUNK_ELEMS 4096u
+#define STREAM_HEADER_BYTES 64u
+#define CHUNK_HEADER_BYTES 16u
+#define STREAM_MAGIC 0x31424343u /* "CCB1" */
+#define STREAM_VERSION 1u
+#define DTYPE_BF16 1u
+#define MODE_PACKED 0u
+#define MODE_RAW 1u
+#define SM_PLANE_BYTES 4096u /* one sign+fraction byte per element */
+#define BIT_PLANE_BYTES 512u /* one bit per element */
+
+/* ------------------------------------------------------------------ */
+/* little-endian byte access                                           */
+/* ------------------------------------------------------------------ */
+static void put_u16(uint8_t *p, uint32_t v)
+{
+    p[0] = (uint8_t)(v & 0xFF);
+    p[1] = (uint8_t)((v >> 8) & 0xFF);
+}
+static void put_u32(uint8_t *p, uint32_t v)
+{
+    for (int b = 0; b < 4; b++)
+        p[b] = (uint8_t)((v >> (8 * b)) & 0xFF);
+}
+static void put_u64(uint8_t *p, uint64_t v)
+{
+    for (int b = 0; b < 8; b++)
+        p[b] = (uint8_t)((v >> (8 * b)) & 0xFF);
+}
+static uint32_t get_u16(const uint8_t *p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8);
+}
+static uint32_t get_u32(const uint8_t *p)
+{
+    uint32_t v = 0;
+    for (int b = 3; b >= 0; b--)
+        v = (v << 8) | p[b];
+    return v;
+}
+static uint64_t get_u64(const uint8_t *p)
+{
+    uint64_t v = 0;
+    for (int b = 7; b >= 0; b--)
+        v = (v << 8) | p[b];
+    return v;
+}
+
+static size_t pad16(size_t x)
+{
+    return (x + 15) / 16 * 16;
+}
+
+/* ------------------------------------------------------------------ */
+/* stream geometry                                                     */
+/* ------------------------------------------------------------------ */
+size_t oracle_n_chunks(size_t n)
+{
+    return (n + CHUNK_ELEMS - 1) / CHUNK_ELEMS;
+}
+
+/* number of elements in chunk c of an n-element buffer */
+static size_t chunk_len(size_t n, size_t c)
+{
+    size_t start = c * CHUNK_ELEMS;
+    size_t left = n - start;
+    return left < CHUNK_ELEMS ? left : CHUNK_ELEMS;
+}
+
+/* byte offset of the first chunk: stream header, then the offset table
+ * (one u64 per chunk) padded to 16 bytes */
+size_t oracle_data_start(size_t n)
+{
+    return STREAM_HEADER_BYTES + pad16(8 * oracle_n_chunks(n));
+}
+
+/* size of a raw chunk of n_c elements, header included */
+static size_t raw_chunk_bytes(size_t n_c)
+{
+    return CHUNK_HEADER_BYTES + pad16(2 * n_c);
+}
+
+/* size of a packed chunk, header included */
+static size_t packed_chunk_bytes(unsigned k, size_t n_esc)
+{
+    return CHUNK_HEADER_BYTES + SM_PLANE_BYTES + (size_t)BIT_PLANE_BYTES * k + pad16(n_esc);
+}
+
+/* Largest stream n elements can produce: every chunk raw.  A packed chunk is
+ * chosen only when it is strictly smaller than the raw one. */
+size_t oracle_compress_bound(size_t n)
+{
+    size_t bytes = oracle_data_start(n);
+    for (size_t c = 0; c < oracle_n_chunks(n); c++)
+        bytes += raw_chunk_bytes(chunk_len(n, c));
+    return bytes;
+}
+
+/* ------------------------------------------------------------------ */
+/* bf16 components (section 4.1)                                       */
+/* ------------------------------------------------------------------ */
+static unsigned exponent_of(uint16_t b)
+{
+    return (b >> 7) & 0xFFu;
+}
+/* sign bit moved to bit 7, the 7 fraction bits kept in bits 0..6 */
+static unsigned sign_fraction_of(uint16_t b)
+{
+    return ((b >> 8) & 0x80u) | (b & 0x7Fu);
+}
+static uint16_t join_bf16(unsigned sign_fraction, unsigned exponent)
+{
+    return (uint16_t)(((sign_fraction & 0x80u) << 8) | ((exponent & 0xFFu) << 7) | (sign_fraction & 0x7Fu));
+}
+
+/* Where bit p of the code of element i sits inside bit-plane p: word index
+ * (0..127, u32 little-endian words) and bit index (0..31).
+ * With j = i / 256, l = (i / 8) % 32, s = i % 8:
+ *   word = (j / 4) * 32 + l
+ *   bit  = 8 * (s % 4) + 2 * (j % 4) + s / 4
+ * This is a fixed permutation of the 4096 elements; it is this format's own
+ * choice (the pages fix no bit order). */
+void oracle_plane_position(unsigned i, unsigned *word, unsigned *bit)
+{
+    unsigned j = i / 256, l = (i / 8) % 32, s = i % 8;
+    *word = (j / 4) * 32 + l;
+    *bit = 8 * (s % 4) + 2 * (j % 4) + s / 4;
+}
+
+/* ------------------------------------------------------------------ */
+/* encoding choice of one full chunk (section 4.3)                     */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    unsigned raw;   /* 1: stored raw */
+    unsigned k;     /* code width, 0..7 */
+    unsigned base;  /* minimum exponent of the chunk */
+    size_t n_esc;   /* escapes at width k */
+    size_t bytes;   /* chunk size, header included */
+} chunk_choice;
+
+/* Count of elements whose exponent offset from base is >= threshold. */
+static size_t count_at_or_above(const uint16_t *x, size_t n_c, unsigned base, unsigned threshold)
+{
+    size_t count = 0;
+    for (size_t i = 0; i < n_c; i++)
+        if (exponent_of(x[i]) - base >= threshold)
+            count++;
+    return count;
+}
+
+static chunk_choice choose_encoding(const uint16_t *x, size_t n_c)
+{
+    chunk_choice best;
+    best.raw = 1;
+    best.k = 0;
+    best.base = 0;
+    best.n_esc = 0;
+    best.bytes = raw_chunk_bytes(n_c);
+    if (n_c != CHUNK_ELEMS) /* a partial chunk travels raw (section 5) */
+        return best;
+
+    unsigned emin = 255, emax = 0;
+    for (size_t i = 0; i < n_c; i++) {
+        unsigned e = exponent_of(x[i]);
+        if (e < emin)
+            emin = e;
+        if (e > emax)
+            emax = e;
+    }
+
+    /* size of the exponent part of a packed chunk: k bit-planes + escapes */
+    int have = 0;
+    unsigned best_k = 0;
+    size_t best_size = 0, best_esc = 0;
+    if (emax == emin) { /* one symbol: width 0, no planes, no escapes */
+        have = 1;
+        best_k = 0;
+        best_size = 0;
+        best_esc = 0;
+    } else {
+        for (unsigned k = 1; k <= 7; k++) {
+            unsigned sentinel = (1u << k) - 1;
+            size_t n_esc = count_at_or_above(x, n_c, emin, sentinel);
+            size_t size = (size_t)BIT_PLANE_BYTES * k + pad16(n_esc);
+            if (!have || size < best_size) { /* strict: ties keep the smaller k */
+                have = 1;
+                best_k = k;
+                best_size = size;
+                best_esc = n_esc;
+            }
+        }
+    }
+    if (best_size >= SM_PLANE_BYTES) /* no gain over 8-bit exponents: raw (ties too) */
+        return best;
+    best.raw = 0;
+    best.k = best_k;
+    best.base = emin;
+    best.n_esc = best_esc;
+    best.bytes = packed_chunk_bytes(best_k, best_esc);
+    return best;
+}
+
+/* Encoding statistics of one chunk without writing it (for tests). */
+int oracle_chunk_choice(const uint16_t *x, size_t n_c, unsigned *raw, unsigned *k, unsigned *base,
+                        size_t *n_esc, size_t *bytes)
+{
+    if (n_c == 0 || n_c > CHUNK_ELEMS)
+        return ORC_ERR_INVALID_ARG;
+    chunk_choice ch = choose_encoding(x, n_c);
+    *raw = ch.raw;
+    *k = ch.k;
+    *base = ch.base;
+    *n_esc = ch.n_esc;
+    *bytes = ch.bytes;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* chunk encoder                                                       */
+/* ------------------------------------------------------------------ */
+/* Writes one chunk (header + body + zero padding) at out; out must hold
+ * ch.bytes bytes.  Returns the number of bytes written. */
+static size_t write_chunk(const uint16_t *x, size_t n_c, chunk_choice ch, uint8_t *out)
+{
+    memset(out, 0, ch.bytes);
+    out[0] = (uint8_t)(ch.raw ? MODE_RAW : MODE_PACKED);
+    out[1] = (uint8_t)ch.k;
+    out[2] = (uint8_t)ch.base;
+    out[3] = 0;
+    put_u16(out + 4, (uint32_t)n_c);
+    put_u16(out + 6, (uint32_t)ch.n_esc);
+    put_u32(out + 8, (uint32_t)ch.bytes);
+    put_u32(out + 12, 0);
+    uint8_t *body = out + CHUNK_HEADER_BYTES;
+
+    if (ch.raw) {
+        for (size_t i = 0; i < n_c; i++)
+            put_u16(body + 2 * i, x[i]);
+        return ch.bytes;
+    }
+
+    /* sign+fraction plane */
+    for (size_t i = 0; i < n_c; i++)
+        body[i] = (uint8_t)sign_fraction_of(x[i]);
+
+    /* bit-planes and escapes */
+    uint8_t *planes = body + SM_PLANE_BYTES;
+    uint8_t *escapes = planes + (size_t)BIT_PLANE_BYTES * ch.k;
+    size_t n_esc = 0;
+    if (ch.k > 0) {
+        unsigned sentinel = (1u << ch.k) - 1;
+        for (unsigned i = 0; i < n_c; i++) {
+            unsigned e = exponent_of(x[i]);
+            unsigned code = e - ch.base;
+            if (code >= sentinel) {
+                code = sentinel;
+                escapes[n_esc++] = (uint8_t)e;
+            }
+            unsigned word, bit;
+            oracle_plane_position(i, &word, &bit);
+            for (unsigned p = 0; p < ch.k; p++) {
+                if ((code >> p) & 1u) {
+                    size_t byte = (size_t)BIT_PLANE_BYTES * p + 4 * (size_t)word + bit / 8;
+                    planes[byte] = (uint8_t)(planes[byte] | (1u << (bit % 8)));
+                }
+            }
+        }
+    }
+    (void)n_esc; /* equals ch.n_esc by construction of the count */
+    return ch.bytes;
+}
+
+/* One chunk on its own, header included (for sampled checks of big streams).
+ * out must hold 16 + 8192 bytes. */
+int oracle_encode_chunk(const uint16_t *x, size_t n_c, uint8_t *out, size_t *bytes)
+{
+    if (n_c == 0 || n_c > CHUNK_ELEMS)
+        return ORC_ERR_INVALID_ARG;
+    chunk_choice ch = choose_encoding(x, n_c);
+    *bytes = write_chunk(x, n_c, ch, out);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* stream encoder                                                      */
+/* ------------------------------------------------------------------ */
+int oracle_compress(const uint16_t *x, size_t n, uint8_t *out, size_t capacity, size_t *out_bytes)
+{
+    if (n == 0 || x == NULL || out == NULL)
+        return ORC_ERR_INVALID_ARG;
+    size_t n_chunks = oracle_n_chunks(n);
+    size_t start = oracle_data_start(n);
+    if (capacity < start)
+        return ORC_ERR_CAPACITY;
+
+    /* placement: each chunk starts where the previous one ended */
+    size_t pos = start;
+    memset(out, 0, start);
+    for (size_t c = 0; c < n_chunks; c++) {
+        size_t n_c = chunk_len(n, c);
+        chunk_choice ch = choose_encoding(x + c * CHUNK_ELEMS, n_c);
+        if (pos + ch.bytes > capacity)
+            return ORC_ERR_CAPACITY;
+        put_u64(out + STREAM_HEADER_BYTES + 8 * c, pos);
+        write_chunk(x + c * CHUNK_ELEMS, n_c, ch, out + pos);
+        pos += ch.bytes;
+    }
+
+    put_u32(out + 0, STREAM_MAGIC);
+    put_u16(out + 4, STREAM_VERSION);
+    put_u16(out + 6, DTYPE_BF16);
+    put_u32(out + 8, CHUNK_ELEMS);
+    put_u32(out + 12, 0);
+    put_u64(out + 16, n);
+    put_u64(out + 24, n_chunks);
+    put_u64(out + 32, pos);
+    /* bytes 40..63 stay zero */
+    *out_bytes = pos;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* stream decoder                                                      */
+/* ------------------------------------------------------------------ */
+/* Decodes one chunk of n_c elements from `chunk` (chunk_size bytes). */
+static int read_chunk(const uint8_t *chunk, size_t chunk_size, size_t n_c, uint16_t *x)
+{
+    if (chunk_size < CHUNK_HEADER_BYTES)
+        return ORC_ERR_CORRUPT;
+    unsigned mode = chunk[0], k = chunk[1], base = chunk[2];
+    size_t stored_n = get_u16(chunk + 4), n_esc = get_u16(chunk + 6);
+    size_t bytes = get_u32(chunk + 8);
+    if (bytes != chunk_size || stored_n != n_c)
+        return ORC_ERR_CORRUPT;
+    const uint8_t *body = chunk + CHUNK_HEADER_BYTES;
+
+    if (mode == MODE_RAW) {
+        if (k != 0 || base != 0 || n_esc != 0 || bytes != raw_chunk_bytes(n_c))
+            return ORC_ERR_CORRUPT;
+        for (size_t i = 0; i < n_c; i++)
+            x[i] = (uint16_t)get_u16(body + 2 * i);
+        return ORC_OK;
+    }
+    if (mode != MODE_PACKED || n_c != CHUNK_ELEMS || k > 7)
+        return ORC_ERR_CORRUPT;
+    if (k == 0 && n_esc != 0)
+        return ORC_ERR_CORRUPT;
+    if (bytes != packed_chunk_bytes(k, n_esc))
+        return ORC_ERR_CORRUPT;
+
+    const uint8_t *planes = body + SM_PLANE_BYTES;
+    const uint8_t *escapes = planes + (size_t)BIT_PLANE_BYTES * k;
+    unsigned sentinel = (1u << k) - 1;
+    size_t used = 0;
+    for (unsigned i = 0; i < n_c; i++) {
+        unsigned word, bit, code = 0;
+        oracle_plane_position(i, &word, &bit);
+        for (unsigned p = 0; p < k; p++) {
+            uint8_t byte = planes[(size_t)BIT_PLANE_BYTES * p + 4 * (size_t)word + bit / 8];
+            code |= ((byte >> (bit % 8)) & 1u) << p;
+        }
+        unsigned e;
+        if (k > 0 && code == sentinel) {
+            if (used >= n_esc)
+                return ORC_ERR_CORRUPT;
+            e = escapes[used++];
+        } else {
+            e = base + code;
+            if (e > 255)
+                return ORC_ERR_CORRUPT;
+        }
+        x[i] = join_bf16(body[i], e);
+    }
+    if (used != n_esc)
+        return ORC_ERR_CORRUPT;
+    return ORC_OK;
+}
+
+int oracle_decompress(const uint8_t *s, size_t s_bytes, uint16_t *x, size_t n)
+{
+    if (s == NULL || x == NULL || n == 0)
+        return ORC_ERR_INVALID_ARG;
+    if (s_bytes < STREAM_HEADER_BYTES)
+        return ORC_ERR_CORRUPT;
+    size_t n_chunks = oracle_n_chunks(n);
+    size_t start = oracle_data_start(n);
+    if (get_u32(s + 0) != STREAM_MAGIC || get_u16(s + 4) != STREAM_VERSION || get_u16(s + 6) != DTYPE_BF16 ||
+        get_u32(s + 8) != CHUNK_ELEMS || get_u64(s + 16) != n || get_u64(s + 24) != n_chunks)
+        return ORC_ERR_CORRUPT;
+    size_t total = get_u64(s + 32);
+    if (total > s_bytes || total < start)
+        return ORC_ERR_CORRUPT;
+    for (size_t c = 0; c < n_chunks; c++) {
+        size_t off = get_u64(s + STREAM_HEADER_BYTES + 8 * c);
+        size_t end = (c + 1 < n_chunks) ? get_u64(s + STREAM_HEADER_BYTES + 8 * (c + 1)) : total;
+        if (c == 0 && off != start)
+            return ORC_ERR_CORRUPT;
+        if (off % 16 != 0 || end <= off || end > total)
+            return ORC_ERR_CORRUPT;
+        int st = read_chunk(s + off, end - off, chunk_len(n, c), x + c * CHUNK_ELEMS);
+        if (st != ORC_OK)
+            return st;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* reduce (section 5, CopyReducePacks; Figure 2)                       */
+/* ------------------------------------------------------------------ */
+static float bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* binary32 -> bf16, round to nearest, ties to even; every NaN -> 0x7FC0 */
+uint16_t oracle_round_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
+        return 0x7FC0;
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* Element-wise sum of R bf16 vectors: binary32 accumulator starting from
+ * rank 0's value, ranks added in order 1..R-1, one final rounding. */
+void oracle_sum_ranks(const uint16_t *const *xs, int R, size_t n, uint16_t *out)
+{
+    for (size_t i = 0; i < n; i++) {
+        float acc = bf16_to_float(xs[0][i]);
+        for (int r = 1; r < R; r++)
+            acc = acc + bf16_to_float(xs[r][i]);
+        out[i] = oracle_round_bf16(acc);
+    }
+}
+
+/* Decompress R streams, sum them as above, compress the sum. */
+int oracle_reduce(const uint8_t *const *ins, const size_t *in_bytes, int R, size_t n, uint8_t *out, size_t capacity,
+                  size_t *out_bytes)
+{
+    if (R < 1 || R > 64 || n == 0 || ins == NULL || in_bytes == NULL || out == NULL)
+        return ORC_ERR_INVALID_ARG;
+    uint16_t **xs = (uint16_t **)calloc((size_t)R, sizeof(uint16_t *));
+    uint16_t *sum = (uint16_t *)malloc(n * sizeof(uint16_t));
+    int st = (xs && sum) ? ORC_OK : ORC_ERR_INVALID_ARG;
+    for (int r = 0; r < R && st == ORC_OK; r++) {
+        xs[r] = (uint16_t *)malloc(n * sizeof(uint16_t));
+        if (!xs[r])
+            st = ORC_ERR_INVALID_ARG;
+        else
+            st = oracle_decompress(ins[r], in_bytes[r], xs[r], n);
+    }
+    if (st == ORC_OK) {
+        oracle_sum_ranks((const uint16_t *const *)xs, R, n, sum);
+        st = oracle_compress(sum, n, out, capacity, out_bytes);
+    }
+    if (xs)
+        for (int r = 0; r < R; r++)
+            free(xs[r]);
+    free(xs);
+    free(sum);
+    return st;
+}

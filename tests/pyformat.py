@@ -1,0 +1,174 @@
+"""Second, independent reading of the compressed bf16 stream format, in Python.
+
+Used only to pin the C oracle: a decoder, and an encoder that takes the code
+width k as an argument so that the choice of k can be brute-forced (encode at
+every k, keep the shortest).  Written from the format definition, not from
+the oracle's code.
+
+Format (little endian):
+  stream  = 64-byte header | u64 offset per chunk, zero-padded to 16 | chunks
+  header  = magic "CCB1" u32, version u16 = 1, dtype u16 = 1 (bf16),
+            chunk_elems u32 = 4096, u32 0, n_elems u64, n_chunks u64,
+            total_bytes u64, 24 zero bytes
+  chunk   = mode u8 (0 packed, 1 raw), k u8, base u8, u8 0, n_c u16,
+            n_esc u16, chunk_bytes u32, u32 0, then the body, zero-padded
+            to 16 bytes
+  raw     = the n_c bf16 values
+  packed  = 4096 sign+fraction bytes ((b >> 8) & 0x80 | b & 0x7F),
+            k bit-planes of 128 u32 words, escape bytes (raw exponents of
+            the elements whose code is the sentinel 2^k - 1, ascending
+            element order)
+  element i = 256 j + 8 l + s (j < 16, l < 32, s < 8) keeps bit p of its
+  code in plane p, word 32 (j // 4) + l, bit 8 (s % 4) + 2 (j % 4) + s // 4.
+"""
+
+from __future__ import annotations
+
+import struct
+
+import numpy as np
+
+CHUNK = 4096
+MAGIC = 0x31424343
+
+
+def _rup16(v: int) -> int:
+    return -(-v // 16) * 16
+
+
+def _element_slots():
+    i = np.arange(CHUNK)
+    j, l, s = i >> 8, (i >> 3) & 31, i & 7
+    word = (j // 4) * 32 + l
+    bit = 8 * (s % 4) + 2 * (j % 4) + s // 4
+    return word, bit
+
+
+WORD_OF, BIT_OF = _element_slots()
+
+
+def split(x: np.ndarray):
+    x = x.astype(np.uint32)
+    expo = (x >> 7) & 0xFF
+    sm = ((x >> 8) & 0x80) | (x & 0x7F)
+    return expo, sm
+
+
+def encode_chunk_at(x: np.ndarray, k: int | None) -> bytes | None:
+    """Chunk bytes for a given width k (None = raw); None if k cannot
+    represent the chunk (k = 0 needs a single exponent)."""
+    n_c = x.size
+    if k is None:
+        body = x.astype("<u2").tobytes()
+        size = 16 + _rup16(len(body))
+        hdr = struct.pack("<BBBBHHII", 1, 0, 0, 0, n_c, 0, size, 0)
+        return (hdr + body).ljust(size, b"\0")
+    assert n_c == CHUNK
+    expo, sm = split(x)
+    base = int(expo.min())
+    off = expo - base
+    if k == 0:
+        if off.max() != 0:
+            return None
+        esc = b""
+        planes = b""
+    else:
+        sent = (1 << k) - 1
+        code = np.minimum(off, sent)
+        escaped = off >= sent
+        esc = expo[escaped].astype(np.uint8).tobytes()
+        words = np.zeros((k, 128), np.uint64)
+        for p in range(k):
+            bits = ((code >> p) & 1).astype(np.uint64) << BIT_OF.astype(np.uint64)
+            np.add.at(words[p], WORD_OF, bits)
+        planes = words.astype("<u4").tobytes()
+    body = sm.astype(np.uint8).tobytes() + planes + esc
+    size = 16 + _rup16(len(body))
+    hdr = struct.pack("<BBBBHHII", 0, k, base, 0, n_c, len(esc), size, 0)
+    return (hdr + body).ljust(size, b"\0")
+
+
+def brute_force_chunk(x: np.ndarray) -> tuple[str, int | None, bytes]:
+    """Encode at every candidate and keep the shortest; ties keep the smaller
+    k, and raw wins every tie with a packed candidate."""
+    raw = encode_chunk_at(x, None)
+    if x.size != CHUNK:
+        return "raw", None, raw
+    best_k, best = None, None
+    for k in range(8):
+        enc = encode_chunk_at(x, k)
+        if enc is not None and (best is None or len(enc) < len(best)):
+            best_k, best = k, enc
+    if best is None or len(best) >= len(raw):
+        return "raw", None, raw
+    return "packed", best_k, best
+
+
+def encode_stream(x: np.ndarray) -> bytes:
+    """Whole stream built from brute-forced chunks."""
+    n = x.size
+    nch = -(-n // CHUNK)
+    start = 64 + _rup16(8 * nch)
+    chunks = [brute_force_chunk(x[c * CHUNK:(c + 1) * CHUNK])[2] for c in range(nch)]
+    offs, pos = [], start
+    for ch in chunks:
+        offs.append(pos)
+        pos += len(ch)
+    hdr = struct.pack("<IHHIIQQQ", MAGIC, 1, 1, CHUNK, 0, n, nch, pos).ljust(64, b"\0")
+    table = struct.pack("<%dQ" % nch, *offs).ljust(start - 64, b"\0")
+    return hdr + table + b"".join(chunks)
+
+
+class Corrupt(ValueError):
+    pass
+
+
+def decode_chunk(buf: bytes, n_c: int) -> np.ndarray:
+    mode, k, base, zero, nc, n_esc, size, zero2 = struct.unpack_from("<BBBBHHII", buf, 0)
+    if nc != n_c or size != len(buf):
+        raise Corrupt("chunk header")
+    body = buf[16:]
+    if mode == 1:
+        return np.frombuffer(body[:2 * n_c], "<u2").astype(np.uint16)
+    if mode != 0 or n_c != CHUNK or k > 7:
+        raise Corrupt("mode")
+    sm = np.frombuffer(body[:CHUNK], np.uint8).astype(np.uint32)
+    words = np.frombuffer(body[CHUNK:CHUNK + 512 * k], "<u4").reshape(k, 128).astype(np.uint32)
+    esc = np.frombuffer(body[CHUNK + 512 * k:CHUNK + 512 * k + n_esc], np.uint8).astype(np.uint32)
+    code = np.zeros(CHUNK, np.uint32)
+    for p in range(k):
+        code |= ((words[p, WORD_OF] >> BIT_OF.astype(np.uint32)) & 1) << p
+    expo = base + code
+    if k > 0:
+        where = np.nonzero(code == (1 << k) - 1)[0]
+        if where.size != n_esc:
+            raise Corrupt("escape count")
+        expo[where] = esc
+    if expo.max() > 255:
+        raise Corrupt("exponent range")
+    return (((sm & 0x80) << 8) | (expo << 7) | (sm & 0x7F)).astype(np.uint16)
+
+
+def decode_stream(s: bytes, n: int) -> np.ndarray:
+    s = bytes(s)
+    magic, ver, dt, ce, _, n_el, nch, total = struct.unpack_from("<IHHIIQQQ", s, 0)
+    if (magic, ver, dt, ce, n_el, nch) != (MAGIC, 1, 1, CHUNK, n, -(-n // CHUNK)):
+        raise Corrupt("stream header")
+    offs = list(struct.unpack_from("<%dQ" % nch, s, 64)) + [total]
+    out = np.empty(n, np.uint16)
+    for c in range(nch):
+        n_c = min(CHUNK, n - c * CHUNK)
+        out[c * CHUNK:c * CHUNK + n_c] = decode_chunk(s[offs[c]:offs[c + 1]], n_c)
+    return out
+
+
+def chunk_headers(s: bytes):
+    """(offset, mode, k, base, n_c, n_esc, chunk_bytes) for every chunk."""
+    s = bytes(s)
+    nch, total = struct.unpack_from("<QQ", s, 24)
+    offs = struct.unpack_from("<%dQ" % nch, s, 64)
+    out = []
+    for o in offs:
+        mode, k, base, _, n_c, n_esc, size, _ = struct.unpack_from("<BBBBHHII", s, o)
+        out.append((o, mode, k, base, n_c, n_esc, size))
+    return out

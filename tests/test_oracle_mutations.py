@@ -1,0 +1,121 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch each one.  The mistakes are planted in C source copied to a temporary
+directory and built there; the committed oracle is never modified.
+"""
+
+import os
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import pyformat as pf
+
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "cccl_oracle.c")
+CHUNK = 4096
+
+MUTATIONS = [
+    ("tie_keeps_larger_k", "if (!have || size < best_size)", "if (!have || size <= best_size)"),
+    ("raw_tie_goes_packed", "if (best_size >= SM_PLANE_BYTES)", "if (best_size > SM_PLANE_BYTES)"),
+    ("sign_bit_dropped", "return ((b >> 8) & 0x80u) | (b & 0x7Fu);", "return (b & 0x7Fu);"),
+    ("plane_bit_order_swapped", "*bit = 8 * (s % 4) + 2 * (j % 4) + s / 4;", "*bit = 8 * (s % 4) + 2 * (s / 4) + j % 4;"),
+    ("plane_word_order_swapped", "*word = (j / 4) * 32 + l;", "*word = l * 4 + j / 4;"),
+    ("escape_padding_dropped", "SM_PLANE_BYTES + (size_t)BIT_PLANE_BYTES * k + pad16(n_esc);",
+     "SM_PLANE_BYTES + (size_t)BIT_PLANE_BYTES * k + n_esc;"),
+    ("escape_padding_ignored_in_choice", "size_t size = (size_t)BIT_PLANE_BYTES * k + pad16(n_esc);",
+     "size_t size = (size_t)BIT_PLANE_BYTES * k + n_esc;"),
+    ("escape_threshold_off_by_one", "if (code >= sentinel) {", "if (code > sentinel) {"),
+    ("count_threshold_off_by_one", "count_at_or_above(x, n_c, emin, sentinel);",
+     "count_at_or_above(x, n_c, emin, sentinel + 1);"),
+    ("rounding_half_up", "u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0x8000u;"),
+    ("nan_not_canonical", "if ((u & 0x7FFFFFFFu) > 0x7F800000u)\n        return 0x7FC0;", ""),
+    ("accumulate_from_zero", "float acc = bf16_to_float(xs[0][i]);\n        for (int r = 1; r < R; r++)",
+     "float acc = 0.0f;\n        for (int r = 0; r < R; r++)"),
+    ("rank_order_reversed", "acc = acc + bf16_to_float(xs[r][i]);", "acc = acc + bf16_to_float(xs[R - r][i]);"),
+    ("tail_chunk_packed", "if (n_c != CHUNK_ELEMS) /* a partial chunk travels raw (section 5) */",
+     "if (n_c == 0)"),
+    ("base_is_max", "best.base = emin;", "best.base = emax;"),
+    ("offset_table_relative", "put_u64(out + STREAM_HEADER_BYTES + 8 * c, pos);",
+     "put_u64(out + STREAM_HEADER_BYTES + 8 * c, pos - start);"),
+]
+
+
+def _f32(x):
+    return (x.astype(np.uint32) << 16).view(np.float32)
+
+
+def _torch_bf16(f32):
+    t = torch.from_numpy(np.ascontiguousarray(f32, np.float32)).to(torch.bfloat16)
+    out = t.view(torch.int16).numpy().view(np.uint16).copy()
+    out[np.isnan(f32)] = 0x7FC0
+    return out
+
+
+def _golden_like_chunks():
+    rng = np.random.default_rng(99)
+    groups = [
+        [(120, 4000), (121, 96)], [(100, 3599), (101, 497)], [(100, 3583), (101, 513)],
+        [(0, 512), (1, 512), (3, 512), (7, 512), (15, 512), (31, 512), (63, 512), (200, 512)],
+        [(0, 528), (1, 512), (3, 512), (7, 512), (15, 512), (31, 512), (63, 512), (200, 496)],
+        [(e, 292) for e in range(50, 64)] + [(64, 7), (65, 1)],
+        [(0, 513), (1, 512), (3, 512), (7, 512), (15, 512), (31, 512), (63, 512), (200, 511)],
+    ]
+    for g in groups:
+        e = np.concatenate([np.full(c, v, np.uint16) for v, c in g])
+        e = e[rng.permutation(e.size)]
+        sm = rng.integers(0, 256, e.size).astype(np.uint16)
+        yield ((sm & 0x80) << 8) | (e << 7) | (sm & 0x7F)
+
+
+def _battery(orc, wl):
+    """Run the pins; return the names of the ones that fail."""
+    failed = []
+
+    def check(name, fn):
+        try:
+            if not fn():
+                failed.append(name)
+        except Exception:  # a crash in the mutant counts as caught
+            failed.append(name)
+
+    allp = np.random.default_rng(1).permutation(65536).astype(np.uint16)
+    check("lossless_all_patterns", lambda: np.array_equal(orc.decompress(orc.compress(allp), allp.size), allp))
+    check("python_decoder", lambda: np.array_equal(pf.decode_stream(orc.compress(allp).tobytes(), allp.size), allp))
+    samples = [wl.generate(1, 0, count=8 * CHUNK), wl.generate(2, 0, count=8 * CHUNK + 99)]
+    samples += list(_golden_like_chunks())
+    check("brute_force_streams", lambda: all(orc.compress(x).tobytes() == pf.encode_stream(x) for x in samples))
+    rng = np.random.default_rng(4)
+    a = rng.integers(0, 65536, 1 << 16).astype(np.uint16)
+    b = rng.integers(0, 65536, 1 << 16).astype(np.uint16)
+    with np.errstate(over="ignore", invalid="ignore"):
+        exact = (_f32(a).astype(np.float64) + _f32(b).astype(np.float64)).astype(np.float32)
+    check("sum_two_vs_binary64", lambda: np.array_equal(orc.sum_ranks([a, b]), _torch_bf16(exact)))
+    sp_a = np.array([0x7F80, 0x8000, 0x7FC1, 0x4E80], np.uint16)
+    sp_b = np.array([0xFF80, 0x8000, 0x3F80, 0xCE80], np.uint16)
+    sp_c = np.array([0x0000, 0x8000, 0x0000, 0x3F80], np.uint16)
+    check("special_values", lambda: np.array_equal(orc.sum_ranks([sp_a, sp_b, sp_c]),
+                                                   np.array([0x7FC0, 0x8000, 0x7FC0, 0x3F80], np.uint16)))
+    check("rank_order", lambda: orc.sum_ranks([sp_b[3:], sp_c[3:], sp_a[3:]])[0] == 0)
+    return failed
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(ORACLE_SRC) as f:
+        return f.read()
+
+
+def test_unmutated_oracle_passes_battery(orc, wl):
+    assert _battery(orc, wl) == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(orc, wl, source, tmp_path, name, old, new):
+    assert source.count(old) == 1, "mutation anchor not found: " + name
+    src = tmp_path / ("oracle_%08x.c" % zlib.crc32(name.encode()))
+    src.write_text(source.replace(old, new))
+    lib = orc.build_from(str(src), str(tmp_path / "mutant.so"))
+    with orc.use_library(lib):
+        failed = _battery(orc, wl)
+    assert failed, "planted mistake %r was not caught by any pin" % name

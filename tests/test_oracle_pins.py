@@ -1,0 +1,362 @@
+"""Pins of the CPU oracle against things other than itself.
+
+- losslessness over every one of the 65,536 bf16 bit patterns;
+- a second, independent Python reading of the format (decoder, and a
+  brute-force encoder that tries every code width k);
+- hand-derived chunk decisions (tests/golden/chunk_choices.txt);
+- closed-form sizes and offsets of every chunk;
+- the binary32 sum and the bf16 rounding against numpy and torch;
+- the special cases of the reduce.
+"""
+
+import os
+import struct
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import pyformat as pf
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "chunk_choices.txt")
+CHUNK = 4096
+
+
+def _rup16(v):
+    return -(-v // 16) * 16
+
+
+# ---------------------------------------------------------------- lossless
+def test_all_bf16_patterns_round_trip_in_order(orc):
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    s = orc.compress(x)
+    assert np.array_equal(orc.decompress(s, x.size), x)
+    assert np.array_equal(pf.decode_stream(s.tobytes(), x.size), x)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_all_bf16_patterns_round_trip_shuffled(orc, seed):
+    x = np.random.default_rng(seed).permutation(65536).astype(np.uint16)
+    s = orc.compress(x)
+    assert np.array_equal(orc.decompress(s, x.size), x)
+    assert np.array_equal(pf.decode_stream(s.tobytes(), x.size), x)
+
+
+def test_sorted_patterns_use_every_mode(orc):
+    """Chunks of consecutive bit patterns (one exponent pair per chunk) give
+    packed chunks; their round trip pins sign and fraction bits."""
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    hdrs = pf.chunk_headers(orc.compress(x).tobytes())
+    # 4096 consecutive patterns = 32 exponents x 128: width 5 with escapes
+    assert {h[1] for h in hdrs} == {0} and {h[2] for h in hdrs} == {5}
+
+
+# ---------------------------------------------------------------- independent reading
+def _samples(wl):
+    rng = np.random.default_rng(7)
+    yield "n01", wl.generate(1, 0, count=16 * CHUNK)
+    yield "n2", wl.generate(2, 0, count=16 * CHUNK)
+    yield "kv", wl.generate(4, 0, count=16 * CHUNK, n=1 << 22)
+    yield "worst_lo", wl.generate(5, 0, count=8 * CHUNK, n=1 << 20)
+    yield "worst_hi", wl.generate(5, 0, start=1 << 19, count=8 * CHUNK, n=1 << 20)
+    yield "uniform_bits", rng.integers(0, 65536, 4 * CHUNK).astype(np.uint16)
+    yield "const", np.full(3 * CHUNK, 0x3F80, np.uint16)
+    yield "zeros", np.zeros(2 * CHUNK + 5, np.uint16)
+    few = rng.choice(np.array([0x3C00, 0x3C80, 0x3D00, 0xBC00, 0x4000], np.uint16), 5 * CHUNK + 77)
+    yield "few_symbols", few
+
+
+def test_oracle_matches_brute_force_stream(orc, wl):
+    for name, x in _samples(wl):
+        s = orc.compress(x).tobytes()
+        assert s == pf.encode_stream(x), name
+        assert np.array_equal(pf.decode_stream(s, x.size), x), name
+        assert np.array_equal(orc.decompress(np.frombuffer(s, np.uint8), x.size), x), name
+
+
+def test_brute_force_choice_on_random_exponent_mixes(orc):
+    """Random chunks built from 1 to 4 exponent clusters with random counts:
+    the oracle's choice equals encoding at every k and keeping the shortest."""
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        n_sym = rng.integers(1, 5)
+        exps = rng.choice(256, n_sym, replace=False)
+        weights = rng.dirichlet(np.ones(n_sym) * rng.choice([0.05, 0.5, 5.0]))
+        e = rng.choice(exps, CHUNK, p=weights).astype(np.uint16)
+        sm = rng.integers(0, 256, CHUNK).astype(np.uint16)
+        x = ((sm & 0x80) << 8) | (e << 7) | (sm & 0x7F)
+        mode, k, enc = pf.brute_force_chunk(x)
+        got = orc.encode_chunk(x)
+        assert got == enc, (trial, mode, k)
+        ch = orc.chunk_choice(x)
+        assert ch["bytes"] == len(enc)
+        assert ch["raw"] == (mode == "raw")
+        if mode == "packed":
+            assert ch["k"] == k
+
+
+# ---------------------------------------------------------------- golden, hand derived
+def _golden_cases():
+    cases, cur = [], None
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            if key == "case":
+                cur = {"name": rest, "n": CHUNK}
+                cases.append(cur)
+            elif key == "n":
+                cur["n"] = int(rest)
+            elif key == "groups":
+                cur["groups"] = [tuple(int(v) for v in g.split(":")) for g in rest.split()]
+            elif key == "expect":
+                parts = rest.split()
+                cur["mode"] = parts[0]
+                cur.update({kv.split("=")[0]: int(kv.split("=")[1]) for kv in parts[1:]})
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_golden_chunk_choice(orc, case):
+    rng = np.random.default_rng(zlib.crc32(case["name"].encode()))
+    e = np.concatenate([np.full(c, ex, np.uint16) for ex, c in case["groups"]])
+    assert e.size == case["n"]
+    e = e[rng.permutation(e.size)]
+    sm = rng.integers(0, 256, e.size).astype(np.uint16)
+    x = ((sm & 0x80) << 8) | (e << 7) | (sm & 0x7F)
+    ch = orc.chunk_choice(x)
+    assert ch["raw"] == (case["mode"] == "raw")
+    assert ch["bytes"] == case["bytes"]
+    if case["mode"] == "packed":
+        assert (ch["k"], ch["base"], ch["n_esc"]) == (case["k"], case["base"], case["n_esc"])
+    enc = orc.encode_chunk(x)
+    mode, k, base, _, n_c, n_esc, nbytes, _ = struct.unpack_from("<BBBBHHII", enc, 0)
+    assert (mode, n_c, nbytes, len(enc)) == (1 if case["mode"] == "raw" else 0, case["n"], case["bytes"],
+                                             case["bytes"])
+    assert np.array_equal(pf.decode_chunk(enc, case["n"]), x)
+
+
+# ---------------------------------------------------------------- closed-form sizes
+@pytest.mark.parametrize("n", [1, 2, 7, 4095, 4096, 4097, 8191, 8192, 12289, 65536 + 3])
+def test_closed_form_sizes_and_offsets(orc, wl, n):
+    x = wl.generate(2, 0, count=n, n=max(n, 1))
+    s = orc.compress(x).tobytes()
+    magic, ver, dt, ce, res, n_el, nch, total = struct.unpack_from("<IHHIIQQQ", s, 0)
+    assert (magic, ver, dt, ce, res, n_el) == (0x31424343, 1, 1, CHUNK, 0, n)
+    assert nch == -(-n // CHUNK) and total == len(s)
+    assert s[40:64] == bytes(24)
+    start = 64 + _rup16(8 * nch)
+    assert orc.data_start(n) == start
+    assert s[64 + 8 * nch:start] == bytes(start - 64 - 8 * nch)
+    pos = start
+    for c, (off, mode, k, base, n_c, n_esc, nbytes) in enumerate(pf.chunk_headers(s)):
+        assert off == pos and off % 16 == 0
+        assert n_c == min(CHUNK, n - c * CHUNK)
+        if mode == 1:
+            assert (k, base, n_esc) == (0, 0, 0)
+            assert nbytes == 16 + _rup16(2 * n_c)
+        else:
+            assert n_c == CHUNK and k <= 7
+            assert nbytes == 16 + 4096 + 512 * k + _rup16(n_esc)
+        pos += nbytes
+    assert pos == total
+    assert total <= orc.compress_bound(n)
+
+
+def test_bound_is_reached_by_incompressible_input(orc):
+    rng = np.random.default_rng(5)
+    for n in (4096, 3 * 4096 + 11):
+        x = rng.integers(0, 65536, n).astype(np.uint16)
+        x[::64] = 0  # exponent 0 next to exponent 255 in every chunk
+        x[1::64] = 0x7F80
+        assert orc.compress(x).size == orc.compress_bound(n)
+
+
+def test_padding_and_reserved_bytes_are_zero(orc, wl):
+    x = wl.generate(2, 0, count=40 * CHUNK + 123, n=1 << 20)
+    s = orc.compress(x).tobytes()
+    for off, mode, k, base, n_c, n_esc, nbytes in pf.chunk_headers(s):
+        assert s[off + 3] == 0 and s[off + 12:off + 16] == bytes(4)
+        used = 2 * n_c if mode == 1 else 4096 + 512 * k + n_esc
+        assert s[off + 16 + used:off + nbytes] == bytes(nbytes - 16 - used)
+
+
+def test_plane_position_is_a_permutation(orc):
+    seen = set()
+    for i in range(CHUNK):
+        w, b = orc.plane_position(i)
+        assert 0 <= w < 128 and 0 <= b < 32
+        seen.add(32 * w + b)
+        assert (w, b) == (pf.WORD_OF[i], pf.BIT_OF[i])
+    assert len(seen) == CHUNK
+
+
+def test_single_escape_lands_where_defined(orc):
+    """One element one exponent above the rest: k=1, its plane-0 bit and its
+    escape byte are the only non-zero bytes after the sign+fraction plane."""
+    for i in (0, 1, 4, 7, 8, 255, 256, 1023, 1024, 4095):
+        x = np.full(CHUNK, 0x3F00, np.uint16)  # exponent 126, fraction 0
+        x[i] = 0x3F80  # exponent 127
+        enc = orc.encode_chunk(x)
+        mode, k, base, _, n_c, n_esc, nbytes, _ = struct.unpack_from("<BBBBHHII", enc, 0)
+        assert (mode, k, base, n_esc, nbytes) == (0, 1, 126, 1, 16 + 4096 + 512 + 16)
+        plane = np.frombuffer(enc[16 + 4096:16 + 4096 + 512], "<u4")
+        w, b = orc.plane_position(i)
+        want = np.zeros(128, np.uint32)
+        want[w] = 1 << b
+        assert np.array_equal(plane, want)
+        assert enc[16 + 4096 + 512] == 127 and enc[16 + 4096 + 513:] == bytes(15)
+
+
+def test_escapes_in_ascending_element_order(orc):
+    x = np.full(CHUNK, 0x3F00, np.uint16)
+    pos = [4000, 3, 700, 2048, 9]
+    vals = [130, 140, 150, 160, 170]
+    for p, e in zip(pos, vals):
+        x[p] = e << 7
+    enc = orc.encode_chunk(x)
+    _, k, base, _, _, n_esc, _, _ = struct.unpack_from("<BBBBHHII", enc, 0)
+    assert (k, base, n_esc) == (1, 126, 5)
+    order = [e for _, e in sorted(zip(pos, vals))]
+    assert list(enc[16 + 4096 + 512:16 + 4096 + 512 + 5]) == order
+
+
+# ---------------------------------------------------------------- reduce arithmetic
+def _f32(x):
+    return (x.astype(np.uint32) << 16).view(np.float32)
+
+
+def _torch_bf16(f32):
+    return torch.from_numpy(np.ascontiguousarray(f32, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def test_round_bf16_matches_torch_on_every_upper_half(orc):
+    """Every binary32 whose low 16 bits sit at the rounding boundaries (and
+    random ones), for all 65,536 upper halves: equal to torch's RNE
+    conversion; NaNs become 0x7FC0."""
+    hi = np.arange(65536, dtype=np.uint32) << 16
+    lows = np.array([0, 1, 0x7FFF, 0x8000, 0x8001, 0xFFFF, 0x4000, 0xC000], np.uint32)
+    u = (hi[:, None] | lows[None, :]).reshape(-1)
+    f = u.view(np.float32)
+    ref = _torch_bf16(f)
+    nan = np.isnan(f)
+    ref[nan] = 0x7FC0
+    got = np.array([orc.round_bf16(v) for v in f[::7]], np.uint16)  # C call per value: sample
+    assert np.array_equal(got, ref[::7])
+    # the vectorised path of the oracle: R=1 sum of bf16 values is the identity
+    xs = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    out = orc.sum_ranks([xs])
+    want = xs.copy()
+    want[np.isnan(_f32(xs))] = 0x7FC0
+    assert np.array_equal(out, want)
+
+
+def test_sum_of_two_matches_binary64_then_round(orc):
+    """R=2: binary32 a+b equals (float)((double)a + (double)b), because
+    binary64 carries more than 2*24+2 bits (double rounding is innocuous for
+    a single addition); then torch rounds it to bf16."""
+    rng = np.random.default_rng(3)
+    a = rng.integers(0, 65536, 1 << 20).astype(np.uint16)
+    b = rng.integers(0, 65536, 1 << 20).astype(np.uint16)
+    with np.errstate(over="ignore", invalid="ignore"):
+        exact = (_f32(a).astype(np.float64) + _f32(b).astype(np.float64)).astype(np.float32)
+    want = _torch_bf16(exact)
+    want[np.isnan(exact)] = 0x7FC0
+    assert np.array_equal(orc.sum_ranks([a, b]), want)
+
+
+def test_sum_of_many_is_sequential_binary32(orc, wl):
+    R = 8
+    xs = [wl.generate(3, r, count=1 << 16) for r in range(R)]
+    acc = _f32(xs[0]).copy()
+    for r in range(1, R):
+        acc = (acc + _f32(xs[r])).astype(np.float32)  # numpy binary32 add, RNE
+    assert np.array_equal(orc.sum_ranks(xs), _torch_bf16(acc))
+
+
+def test_sum_rank_order_matters_and_is_kept(orc):
+    """(big + -big) + small != big + (-big + small) in binary32: the result
+    must be the rank-0-first order."""
+    big, small = np.float32(2.0 ** 30), np.float32(1.0)
+    bits = lambda f: np.array([np.float32(f)]).view(np.uint32)[0] >> 16
+    a = np.array([bits(big)], np.uint16)
+    b = np.array([bits(-big)], np.uint16)
+    c = np.array([bits(small)], np.uint16)
+    assert orc.sum_ranks([a, b, c])[0] == 0x3F80  # (2^30 - 2^30) + 1 = 1
+    assert orc.sum_ranks([b, c, a])[0] == 0x0000  # (-2^30 + 1) + 2^30 = 0 in binary32
+
+
+def test_reduce_special_values(orc):
+    pinf, ninf, pz, nz, one = 0x7F80, 0xFF80, 0x0000, 0x8000, 0x3F80
+    a = np.array([pinf, pz, nz, nz, 0x7F7F, 0x7FC1, 0x0001, one], np.uint16)
+    b = np.array([ninf, nz, nz, pz, 0x7F7F, one, 0x0001, 0xFFC0], np.uint16)
+    want = np.array([0x7FC0, 0x0000, 0x8000, 0x0000, 0x7F80, 0x7FC0, 0x0002, 0x7FC0], np.uint16)
+    assert np.array_equal(orc.sum_ranks([a, b]), want)
+
+
+def test_reduce_single_rank_is_identity_without_nan(orc, wl):
+    x = wl.generate(1, 0, count=8 * CHUNK + 100)
+    s = orc.compress(x)
+    assert np.array_equal(orc.reduce([s], x.size), s)
+
+
+def test_reduce_equals_compress_of_rounded_sum(orc, wl):
+    n = 10 * CHUNK + 17
+    xs = [wl.generate(5, r, count=n, start=(1 << 19) - 5 * CHUNK, n=1 << 20) for r in range(4)]
+    streams = [orc.compress(x) for x in xs]
+    out = orc.reduce(streams, n)
+    assert np.array_equal(out, orc.compress(orc.sum_ranks(xs)))
+    dec = pf.decode_stream(out.tobytes(), n)
+    acc = _f32(xs[0]).copy()
+    with np.errstate(over="ignore", invalid="ignore"):
+        for x in xs[1:]:
+            acc = (acc + _f32(x)).astype(np.float32)
+    want = _torch_bf16(acc)
+    want[np.isnan(acc)] = 0x7FC0
+    assert np.array_equal(dec, want)
+
+
+# ---------------------------------------------------------------- corrupt streams
+def _corrupt_cases(orc, wl):
+    x = wl.generate(2, 0, count=3 * CHUNK + 10, n=1 << 20)
+    s = bytearray(orc.compress(x).tobytes())
+    hdrs = pf.chunk_headers(bytes(s))
+    packed = next(h for h in hdrs if h[1] == 0)
+    o = packed[0]
+
+    def mut(fn):
+        t = bytearray(s)
+        fn(t)
+        return bytes(t)
+
+    yield "magic", mut(lambda t: t.__setitem__(0, 0))
+    yield "version", mut(lambda t: t.__setitem__(4, 2))
+    yield "n_elems", mut(lambda t: struct.pack_into("<Q", t, 16, x.size + 1))
+    yield "total_bytes", mut(lambda t: struct.pack_into("<Q", t, 32, len(s) + 16))
+    yield "offset_misaligned", mut(lambda t: struct.pack_into("<Q", t, 64 + 8, hdrs[1][0] + 8))
+    yield "k_too_big", mut(lambda t: t.__setitem__(o + 1, 8))
+    yield "mode_bad", mut(lambda t: t.__setitem__(o, 2))
+    yield "n_esc_wrong", mut(lambda t: struct.pack_into("<H", t, o + 6, packed[5] + 16))
+    yield "chunk_bytes_wrong", mut(lambda t: struct.pack_into("<I", t, o + 8, packed[6] + 16))
+    yield "tail_n_c", mut(lambda t: struct.pack_into("<H", t, hdrs[-1][0] + 4, 11))
+    yield "truncated", bytes(s[:-16])
+
+
+def test_oracle_rejects_corrupt_streams(orc, wl):
+    for name, bad in _corrupt_cases(orc, wl):
+        assert orc.decompress_status(np.frombuffer(bad, np.uint8), 3 * CHUNK + 10) == orc.ERR_CORRUPT, name
+
+
+def test_oracle_rejects_exponent_overflow(orc):
+    """base + code above 255 cannot come from an encoder: reported corrupt."""
+    x = np.full(CHUNK, 250 << 7, np.uint16)
+    x[:2096] = 251 << 7  # k=2 (1024) beats k=1 (512 + 2096): offsets 0 and 1 are plain codes
+    s = bytearray(orc.compress(x).tobytes())
+    o = pf.chunk_headers(bytes(s))[0][0]
+    assert s[o + 1] == 2
+    s[o + 2] = 255  # base 255: code 1 -> exponent 256
+    assert orc.decompress_status(np.frombuffer(bytes(s), np.uint8), CHUNK) == orc.ERR_CORRUPT
