@@ -1,0 +1,148 @@
+/*
+ * cccl.h -- C ABI of libcccl: lossless compression of bf16 communication
+ * buffers and the compressed reduce step of an allreduce, on one GPU.
+ *
+ * Method: "CCCL: In-GPU Compression-Coupled Collective Communication"
+ * (arXiv 2604.17172).
+ *   - section 4.1, "Compression Principle": a bf16 value splits into sign,
+ *     exponent and fraction; sign and fraction travel raw and only the
+ *     skewed 8-bit exponent is re-encoded;
+ *   - section 4.3, "Localized Frequency Tables": each block builds its own
+ *     exponent table from its own data and gives every exponent symbol a
+ *     fixed-length bit code;
+ *   - section 4.4, "Reducing Global Memory Access": each block writes its
+ *     compressed output straight into its final place in one preallocated
+ *     buffer (one global-memory round, no coalescing pass);
+ *   - section 5, "Handling data alignment": data that does not fill a
+ *     whole chunk travels uncompressed;
+ *   - section 5 (CopyReducePacks) and Figure 2: the reduce step of an
+ *     allreduce is receive -> decompress -> reduce -> compress -> send.
+ *
+ * The pages fix no bitstream; this library's stream (little endian):
+ *   64-byte header  magic "CCB1" (u32 0x31424343), version u16 = 1,
+ *                   dtype u16 = 1 (bf16), chunk_elems u32 = 4096, u32 0,
+ *                   n_elems u64, n_chunks u64, total_bytes u64, 24 zero bytes
+ *   offset table    n_chunks x u64 absolute byte offsets, zero-padded to 16
+ *   chunks          contiguous in chunk order, each a multiple of 16 bytes:
+ *     16-byte header  mode u8 (0 packed, 1 raw), k u8, base u8, u8 0,
+ *                     n_c u16, n_esc u16, chunk_bytes u32, u32 0
+ *     packed body     4096 sign+fraction bytes, k bit-planes of 512 bytes,
+ *                     n_esc escape bytes, zero padding to 16
+ *     raw body        n_c bf16 values, zero padding to 16
+ *   A full chunk is packed with width k (offsets e - base below 2^k - 1 are
+ *   codes, the rest escape with their raw exponent) when that is smaller
+ *   than its raw form; the last chunk, when shorter than 4096 elements, is
+ *   raw.  Exactly one stream is valid for each input.
+ *
+ * Conventions for every entry point:
+ *   - The caller owns every buffer.  The library allocates nothing and keeps
+ *     no state between calls; calls with distinct workspaces may run
+ *     concurrently.
+ *   - d_* pointers are device pointers (cudaMalloc'd or managed), 16-byte
+ *     aligned.  h_* pointers are host pointers.
+ *   - Work is enqueued on `stream` (NULL: the legacy default stream) and
+ *     runs asynchronously.  Argument errors are detected on the host before
+ *     anything is enqueued and return immediately.  Errors found on the
+ *     device (corrupt input, a wait that ran out) and the compressed size
+ *     land in the workspace; read them with cccl_get_result.
+ *   - n_elems counts bf16 values (passed as their uint16 bit patterns).
+ */
+#ifndef CCCL_H
+#define CCCL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream).  NULL: the legacy default stream. */
+typedef struct CUstream_st *cccl_stream_t;
+
+typedef enum {
+    CCCL_OK = 0,
+    CCCL_ERR_INVALID_ARG = 1,   /* bad pointer, alignment, size or count */
+    CCCL_ERR_CAPACITY = 2,      /* output capacity below cccl_compress_bound */
+    CCCL_ERR_CORRUPT = 3,       /* input stream malformed or not for n_elems */
+    CCCL_ERR_TIMEOUT = 4,       /* a bounded device wait ran out */
+    CCCL_ERR_CUDA = 5,          /* a CUDA call failed (launch, memset, copy) */
+    CCCL_ERR_UNIMPLEMENTED = 6
+} cccl_status;
+
+/* Largest number of elements one call accepts (2^40). */
+#define CCCL_MAX_ELEMS ((size_t)1 << 40)
+
+/* Worst-case stream size for n_elems values (every chunk raw):
+ * 64 + pad16(8 * n_chunks) + sum over chunks of 16 + pad16(2 * n_c).
+ * Returns 0 when n_elems is 0 or above CCCL_MAX_ELEMS. */
+size_t cccl_compress_bound(size_t n_elems);
+
+/* Workspace bytes for a call on n_elems values: a 16-byte status header
+ * (chunk ticket u32, device error u32, stream size u64) plus one u64
+ * placement word per chunk.  Returns 0 when n_elems is 0 or too large. */
+size_t cccl_workspace_bytes(size_t n_elems);
+
+/* Compress n_elems bf16 values (sections 4.1, 4.3, 4.4; section 5 for the
+ * partial last chunk).
+ *   d_in          n_elems uint16 bf16 bit patterns, read only.
+ *   d_out         receives the stream; out_capacity must be at least
+ *                 cccl_compress_bound(n_elems).  Bytes past the stream's
+ *                 total size are left untouched.
+ *   d_ws          ws_bytes >= cccl_workspace_bytes(n_elems); overwritten.
+ * The stream size (the header's total_bytes) is readable with
+ * cccl_get_result once the work is done.
+ * Returns INVALID_ARG (null or misaligned pointer, n_elems 0 or above the
+ * limit, small workspace), CAPACITY, CUDA, or OK. */
+cccl_status cccl_compress(const uint16_t *d_in, size_t n_elems, void *d_out, size_t out_capacity, void *d_ws,
+                          size_t ws_bytes, cccl_stream_t stream);
+
+/* Decompress a stream made for n_elems values (the inverse of section 4.1's
+ * split; the "Decomp." stage of Figure 2).
+ *   d_in          the stream; in_bytes is the size of the readable buffer
+ *                 (at least the stream's total_bytes).  Nothing past
+ *                 in_bytes is read.
+ *   d_out         receives n_elems uint16 bf16 bit patterns.
+ *   d_ws          ws_bytes >= 16 (cccl_workspace_bytes(n_elems) is enough).
+ * A stream that is malformed or was made for another n_elems is reported
+ * as CORRUPT by cccl_get_result; the contents of d_out are then undefined.
+ * Returns INVALID_ARG, CUDA or OK synchronously. */
+cccl_status cccl_decompress(const void *d_in, size_t in_bytes, uint16_t *d_out, size_t n_elems, void *d_ws,
+                            size_t ws_bytes, cccl_stream_t stream);
+
+/* The reduce step of a compressed allreduce over R ranks whose buffers are
+ * resident in this GPU's memory (section 5, CopyReducePacks; Figure 2:
+ * decompress -> reduce -> compress, fused in one kernel).
+ *   h_ins         host array of R device pointers to compressed streams,
+ *                 each made for n_elems values; h_in_bytes their readable
+ *                 sizes.  1 <= R <= 64.
+ *   d_out         receives the compressed element-wise sum; out_capacity
+ *                 must be at least cccl_compress_bound(n_elems).
+ *   d_ws          ws_bytes >= cccl_workspace_bytes(n_elems).
+ * The sum of element i is acc = x_0[i] in binary32, then acc = acc + x_r[i]
+ * for r = 1..R-1 in that order (round to nearest even, subnormals kept),
+ * rounded once to bf16 (nearest even; every NaN becomes 0x7FC0), and the
+ * result is compressed exactly as cccl_compress would.
+ * Input errors are reported as CORRUPT by cccl_get_result.
+ * Returns INVALID_ARG, CAPACITY, CUDA or OK synchronously. */
+cccl_status cccl_reduce_compressed(const void *const *h_ins, const size_t *h_in_bytes, int R, size_t n_elems,
+                                   void *d_out, size_t out_capacity, void *d_ws, size_t ws_bytes,
+                                   cccl_stream_t stream);
+
+/* Wait for the work enqueued on `stream` and read the outcome stored in the
+ * workspace of the last call that used it.
+ *   out_bytes     (may be NULL) the compressed stream size of a compress or
+ *                 reduce call; 0 after a decompress.
+ *   dev_status    (may be NULL) OK, CORRUPT or TIMEOUT.
+ * Synchronises `stream`.  Returns INVALID_ARG for a null or misaligned
+ * workspace, CUDA if the copy or the synchronisation failed, else OK. */
+cccl_status cccl_get_result(const void *d_ws, cccl_stream_t stream, uint64_t *out_bytes, cccl_status *dev_status);
+
+/* Static, human-readable name of a status code. */
+const char *cccl_status_string(cccl_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCCL_H */

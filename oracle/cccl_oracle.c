@@ -397,6 +397,10 @@ static int read_chunk(const uint8_t *chunk, size_t chunk_size, size_t n_c, uint1
         return ORC_ERR_CORRUPT;
     if (bytes != packed_chunk_bytes(k, n_esc))
         return ORC_ERR_CORRUPT;
+    /* a chunk is packed only when that beats its raw form, so a packed
+     * chunk is never as large as a raw one */
+    if ((size_t)BIT_PLANE_BYTES * k + pad16(n_esc) >= SM_PLANE_BYTES)
+        return ORC_ERR_CORRUPT;
 
     const uint8_t *planes = body + SM_PLANE_BYTES;
     const uint8_t *escapes = planes + (size_t)BIT_PLANE_BYTES * k;

@@ -351,6 +351,25 @@ def test_oracle_rejects_corrupt_streams(orc, wl):
         assert orc.decompress_status(np.frombuffer(bad, np.uint8), 3 * CHUNK + 10) == orc.ERR_CORRUPT, name
 
 
+def test_oracle_rejects_packed_chunk_not_smaller_than_raw(orc):
+    """k=7 with 512 escapes is 4096 bytes of exponents: an encoder stores that
+    chunk raw, so a packed one is malformed even though it could be decoded."""
+    rng = np.random.default_rng(8)
+    e = np.full(CHUNK, 10, np.uint16)
+    e[rng.choice(CHUNK, 600, replace=False)] = 200
+    x = (e << 7).astype(np.uint16)
+    enc = pf.encode_chunk_at(x, 7)
+    assert len(enc) == 16 + 4096 + 3584 + 608
+    body = enc.ljust(len(enc), b"\0")
+    start = 64 + 16
+    total = start + len(body)
+    hdr = struct.pack("<IHHIIQQQ", 0x31424343, 1, 1, CHUNK, 0, CHUNK, 1, total).ljust(64, b"\0")
+    table = struct.pack("<Q", start).ljust(16, b"\0")
+    s = hdr + table + body
+    assert np.array_equal(pf.decode_stream(s, CHUNK), x)  # decodable in principle
+    assert orc.decompress_status(np.frombuffer(s, np.uint8), CHUNK) == orc.ERR_CORRUPT
+
+
 def test_oracle_rejects_exponent_overflow(orc):
     """base + code above 255 cannot come from an encoder: reported corrupt."""
     x = np.full(CHUNK, 250 << 7, np.uint16)
