@@ -1,0 +1,452 @@
+"""Benchmark of the compressed data-parallel reduce step on GB300.
+
+One step = the whole hot path over one batch of synthetic input: the 64 MiB
+gradient-like bf16 buffer (33,554,432 values ~ N(0, 1e-3), 1% of positions
+x100) of R = 2 simulated data-parallel ranks held in this GPU's memory:
+    compress(rank 0), compress(rank 1)            split, exponent table, look-back placement
+    fused reduce(stream 0, stream 1)              decompress -> binary32 sum -> bf16 -> compress
+    decompress(reduced stream)                    the receiver's decode
+`value` = uncompressed gradient bytes entering the step (R * 2n) / step time,
+timed on the device with CUDA events, L2 flushed (256 MiB write) before every
+step, max over ranks.  N GPUs under torchrun run N independent replicas
+(weak scaling); nothing crosses GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "compress / decompress / fused-reduce uncompressed GB/s and % of HBM roofline; ratio"
+WORKLOAD = 2          # the 64 MiB gradient-like buffer
+RANKS_PER_GPU = 2     # simulated data-parallel ranks reduced on each GPU
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["cccl_device.cuh", "cccl_encode.cuh", "cccl_decode.cuh", "cccl_compress.cu",
+                  "cccl_decompress.cu", "cccl_reduce.cu"]
+
+
+# ---------------------------------------------------------------- host logic (also tested on CPU with gloo)
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def simulated_ranks(gpu_rank: int) -> list[int]:
+    """Seeds (rank ids of the workload) reduced by one GPU: disjoint across GPUs."""
+    return [RANKS_PER_GPU * gpu_rank + j for j in range(RANKS_PER_GPU)]
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "compression_coupled_collectives_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[tuple[float, str]] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        sm, smax, reasons = [], [], set()
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the oracle as a CPU baseline
+def oracle_step_seconds(xs, chunks: int) -> tuple[float, int]:
+    """Time the oracle doing the step on the first `chunks` chunks of each rank."""
+    import oracle
+
+    n = min(xs[0].size, chunks * 4096)
+    part = [x[:n] for x in xs]
+    t = time.perf_counter()
+    streams = [oracle.compress(p) for p in part]
+    red = oracle.reduce(streams, n)
+    oracle.decompress(red, n)
+    return time.perf_counter() - t, n
+
+
+def cpu_baseline(xs, budget_s: float = 12.0) -> dict:
+    import oracle
+
+    oracle.build()
+    n_full = xs[0].size
+    total_t, total_n, reps = 0.0, 0, 0
+    chunks = n_full // 4096
+    while total_t < budget_s and reps < 8:
+        dt, n = oracle_step_seconds(xs, chunks)
+        total_t += dt
+        total_n += n
+        reps += 1
+    gbs = len(xs) * 2 * total_n / total_t / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "the full step on the whole workload (%d ranks x %d values), %d repetition(s), "
+                      "%.1f s, single-threaded C oracle" % (len(xs), n_full, reps, total_t)}
+
+
+def run_reference(args, rank: int, world: int) -> None:
+    """The reference arm: the CPU oracle, as it stands, on this host's cores."""
+    import numpy as np  # noqa: F401
+
+    import oracle
+    import workloads
+
+    oracle.build()
+    workloads.build()
+    if rank != 0:
+        return
+    n = workloads.SIZES[WORKLOAD]
+    xs = [workloads.generate(WORKLOAD, r) for r in simulated_ranks(0)]
+    steps, warmup = args.steps, max(args.warmup, 3)
+    # each step: a bounded sample of chunks, rotating through the workload, so
+    # that the whole run stays within about two minutes
+    per_step_s = 100.0 / (steps + warmup)
+    probe_t, probe_n = oracle_step_seconds(xs, 64)
+    chunks = max(1, min(n // 4096, int(per_step_s / (probe_t / 64))))
+    offs = 0
+    total_t, total_n = 0.0, 0
+    for i in range(warmup + steps):
+        a = (offs % (n // 4096)) * 4096
+        b = min(n, a + chunks * 4096)
+        part = [x[a:b] for x in xs]
+        t = time.perf_counter()
+        streams = [oracle.compress(p) for p in part]
+        red = oracle.reduce(streams, b - a)
+        oracle.decompress(red, b - a)
+        dt = time.perf_counter() - t
+        offs += chunks
+        if i >= warmup:
+            total_t += dt
+            total_n += b - a
+    value = RANKS_PER_GPU * 2 * total_n / total_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(1e3 * total_t / steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8+f32",
+        "data": "synthetic", "config": workload_config(),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d chunks of each rank per step, rotating through the workload" % chunks},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config() -> dict:
+    return {"workload": "gradient-like bf16 buffer, 33,554,432 values (64 MiB) ~ N(0, 1e-3) with 1% of "
+                        "positions x100, on %d simulated data-parallel ranks per GPU: compress each, fused "
+                        "reduce (R=%d), decompress the result" % (RANKS_PER_GPU, RANKS_PER_GPU),
+            "n_elems": 33554432, "ranks_per_gpu": RANKS_PER_GPU, "chunk_elems": 4096,
+            "l2": "flushed before every timed step (256 MiB write, untimed)",
+            "parallelism": "replicas (weak scaling, no cross-GPU traffic)"}
+
+
+# ---------------------------------------------------------------- the GPU arm
+def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
+    import numpy as np
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import compression_coupled_collectives_gb300 as cc
+    import workloads
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+
+    seeds = simulated_ranks(rank)
+    xs_host = [workloads.generate(WORKLOAD, r) for r in seeds]
+    n = xs_host[0].size
+    R = len(xs_host)
+    pinned = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
+    xs = [p.to(device) for p in pinned]
+    cap = cc.cccl_compress_bound(n)
+    streams = [torch.empty(cap, dtype=torch.uint8, device=device) for _ in range(R)]
+    red = torch.empty(cap, dtype=torch.uint8, device=device)
+    y = torch.empty(n, dtype=torch.int16, device=device)
+    y_host = torch.empty(n, dtype=torch.int16).pin_memory()
+    wsb = cc.cccl_workspace_bytes(n)
+    ws = [torch.empty(wsb, dtype=torch.uint8, device=device) for _ in range(R + 2)]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        # ev: list of (start, end) event pairs, one per op
+        for r in range(R):
+            if ev is not None:
+                ev[r][0].record(stream)
+            cc.cccl_compress(xs[r], streams[r], ws[r], stream)
+            if ev is not None:
+                ev[r][1].record(stream)
+        if ev is not None:
+            ev[R][0].record(stream)
+        cc.cccl_reduce_compressed(streams, n, red, ws[R], stream=stream)
+        if ev is not None:
+            ev[R][1].record(stream)
+            ev[R + 1][0].record(stream)
+        cc.cccl_decompress(red, y, ws[R + 1], stream=stream)
+        if ev is not None:
+            ev[R + 1][1].record(stream)
+
+    # one untimed pass: sizes, ratios and a sampled check against the oracle
+    step()
+    sizes = [cc.cccl_get_result(w, stream)[0] for w in ws[:R]]
+    red_bytes, red_status = cc.cccl_get_result(ws[R], stream)
+    _, dec_status = cc.cccl_get_result(ws[R + 1], stream)
+    if red_status or dec_status or 0 in sizes:
+        raise RuntimeError("device status %d/%d during the first step" % (red_status, dec_status))
+    check = check_against_oracle(xs_host, streams, sizes, y, n)
+
+    warmup = max(args.warmup, 3)
+    for _ in range(warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    op_ms = [[] for _ in range(R + 2)]
+    step_ms = []
+    t_wall0 = time.time()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R + 2)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        step(evs[k])
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    for k in range(args.steps):
+        e = evs[k]
+        for i in range(R + 2):
+            op_ms[i].append(e[i][0].elapsed_time(e[i][1]))
+        step_ms.append(e[0][0].elapsed_time(e[R + 1][1]))
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+
+    # end to end through the same calls: pinned host inputs in, decoded result out
+    e2e_steps = max(1, min(args.steps, 400))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_total = 0.0
+    for k in range(e2e_steps):
+        flush.fill_(k & 0xFF)
+        e0.record(stream)
+        for r in range(R):
+            xs[r].copy_(pinned[r], non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_total += e0.elapsed_time(e1)
+    e2e_total = max_over_ranks(e2e_total, world, device)
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    bytes_step = R * 2 * n
+    value = world * bytes_step * args.steps / (total_ms * 1e-3) / 1e9
+    e2e_value = world * bytes_step * e2e_steps / (e2e_total * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peaks()
+    mean = lambda v: sum(v) / len(v)
+    ops = {}
+    total_in = sum(sizes)
+    algo = {"compress": 2 * n + mean(sizes), "reduce": total_in + red_bytes, "decompress": red_bytes + 2 * n}
+    comp_ms = mean([mean(op_ms[r]) for r in range(R)])
+    ops["compress"] = {"ms": comp_ms, "launches_per_step": R}
+    ops["reduce"] = {"ms": mean(op_ms[R]), "launches_per_step": 1}
+    ops["decompress"] = {"ms": mean(op_ms[R + 1]), "launches_per_step": 1}
+    for name, o in ops.items():
+        o["ms"] = round(o["ms"], 5)
+        o["uncompressed_gbs"] = round((R if name == "reduce" else 1) * 2 * n / (o["ms"] * 1e-3) / 1e9, 1)
+        o["algorithmic_bytes"] = int(algo[name])
+        o["hbm_gbs"] = round(algo[name] / (o["ms"] * 1e-3) / 1e9, 1)
+        o["frac_of_measured_copy"] = round(o["hbm_gbs"] / peak, 4)
+        o["frac_of_8tbs_nominal"] = round(o["hbm_gbs"] / 8000.0, 4)
+    dominant = max(ops, key=lambda k: ops[k]["ms"] * ops[k]["launches_per_step"])
+    kname = {"compress": "compress_kernel", "reduce": "reduce_kernel", "decompress": "decompress_kernel"}[dominant]
+    traffic = recorded_traffic(kname)
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": ops[dominant]["hbm_gbs"], "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": ops[dominant]["frac_of_measured_copy"],
+                "traffic": None if traffic is None else traffic["bytes_per_launch_scaled"],
+                "algorithmic_bytes_per_launch": ops[dominant]["algorithmic_bytes"]}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8+f32", "data": "synthetic",
+        "config": workload_config(),
+        "ratio": {"compress": round(mean(sizes) / (2 * n), 5), "reduce_out": round(red_bytes / (2 * n), 5)},
+        "ops": ops, "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": R * 2 * n,
+                "d2h_bytes_per_step": 2 * n, "steps": e2e_steps},
+        "gpu_launches": (R + 2) * args.steps,
+        "clocks": clocks, "check": check,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(xs_host)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def check_against_oracle(xs_host, streams, sizes, y, n, chunks: int = 64) -> dict:
+    """Byte-exact check of sampled chunks against the oracle (not timed)."""
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    import struct
+
+    ok = True
+    for x, s, nb in zip(xs_host, streams, sizes):
+        head = s[:min(nb, 64 + 8 * (chunks + 1))].cpu().numpy().tobytes()
+        offs = struct.unpack_from("<%dQ" % (chunks + 1), head, 64)
+        body = s[offs[0]:offs[chunks]].cpu().numpy().tobytes()
+        ref = b"".join(oracle.encode_chunk(x[c * 4096:(c + 1) * 4096]) for c in range(chunks))
+        ok = ok and body == ref
+    want = oracle.sum_ranks([x[:chunks * 4096] for x in xs_host])
+    got = y[:chunks * 4096].cpu().numpy().view(np.uint16)
+    ok = ok and bool(np.array_equal(want, got))
+    return {"bit_exact_sample": ok, "sample": "first %d chunks of every stream and of the decoded sum" % chunks}
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local_rank)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

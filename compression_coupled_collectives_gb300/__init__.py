@@ -1,0 +1,167 @@
+"""Python binding of libcccl: compressed bf16 communication buffers and the
+fused compressed reduce, on one GB300 GPU.
+
+Every function here marshals arguments for the C ABI of ``include/cccl.h``
+(same names) and calls it; all compute runs in the library's sm_103a kernels.
+torch supplies device memory and streams only.  There is no fallback: importing
+this package raises ImportError when ``libcccl.so`` has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcccl.so")
+
+CCCL_OK = 0
+CCCL_ERR_INVALID_ARG = 1
+CCCL_ERR_CAPACITY = 2
+CCCL_ERR_CORRUPT = 3
+CCCL_ERR_TIMEOUT = 4
+CCCL_ERR_CUDA = 5
+CCCL_ERR_UNIMPLEMENTED = 6
+CHUNK_ELEMS = 4096
+MAX_RANKS = 64
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libcccl.so is not built (run __graft_entry__.build() or "
+                      "python compression_coupled_collectives_gb300/build.py)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_sz, _vp, _i = ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
+_lib.cccl_compress_bound.argtypes = [_sz]
+_lib.cccl_compress_bound.restype = _sz
+_lib.cccl_workspace_bytes.argtypes = [_sz]
+_lib.cccl_workspace_bytes.restype = _sz
+_lib.cccl_compress.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp]
+_lib.cccl_compress.restype = _i
+_lib.cccl_decompress.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp]
+_lib.cccl_decompress.restype = _i
+_lib.cccl_reduce_compressed.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _vp, _sz, _vp, _sz, _vp]
+_lib.cccl_reduce_compressed.restype = _i
+_lib.cccl_get_result.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_i)]
+_lib.cccl_get_result.restype = _i
+_lib.cccl_status_string.argtypes = [_i]
+_lib.cccl_status_string.restype = ctypes.c_char_p
+
+
+class CcclError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s: %s" % (what, cccl_status_string(status)))
+        self.status = status
+
+
+def cccl_status_string(status: int) -> str:
+    return _lib.cccl_status_string(int(status)).decode()
+
+
+def cccl_compress_bound(n_elems: int) -> int:
+    return int(_lib.cccl_compress_bound(n_elems))
+
+
+def cccl_workspace_bytes(n_elems: int) -> int:
+    return int(_lib.cccl_workspace_bytes(n_elems))
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, what: str) -> None:
+    if status != CCCL_OK:
+        raise CcclError(status, what)
+
+
+def _bf16_bits(x: torch.Tensor) -> torch.Tensor:
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError("expected bf16 values (bfloat16, or their int16/uint16 bit patterns)")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x
+
+
+def cccl_compress(x: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    """Enqueue compression of ``x`` (n bf16 values) into ``out`` (uint8, at least
+    cccl_compress_bound(n) bytes) using workspace ``ws``."""
+    x = _bf16_bits(x)
+    _check(_lib.cccl_compress(x.data_ptr(), x.numel(), out.data_ptr(), out.numel() * out.element_size(),
+                              ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)), "cccl_compress")
+
+
+def cccl_decompress(s: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, in_bytes: int | None = None,
+                    stream=None) -> None:
+    """Enqueue decompression of stream ``s`` into ``out`` (out.numel() bf16 values)."""
+    out = _bf16_bits(out)
+    nbytes = s.numel() * s.element_size() if in_bytes is None else int(in_bytes)
+    _check(_lib.cccl_decompress(s.data_ptr(), nbytes, out.data_ptr(), out.numel(), ws.data_ptr(),
+                                ws.numel() * ws.element_size(), _stream(stream)), "cccl_decompress")
+
+
+def cccl_reduce_compressed(ins: Sequence[torch.Tensor], n_elems: int, out: torch.Tensor, ws: torch.Tensor,
+                           in_bytes: Sequence[int] | None = None, stream=None) -> None:
+    """Enqueue the fused decompress -> binary32 sum in rank order -> bf16 ->
+    compress of the R streams ``ins`` into ``out``."""
+    R = len(ins)
+    ptrs = (_vp * max(R, 1))(*[t.data_ptr() for t in ins])
+    sizes = [t.numel() * t.element_size() for t in ins] if in_bytes is None else list(in_bytes)
+    szs = (_sz * max(R, 1))(*sizes)
+    _check(_lib.cccl_reduce_compressed(ptrs, szs, R, n_elems, out.data_ptr(), out.numel() * out.element_size(),
+                                       ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "cccl_reduce_compressed")
+
+
+def cccl_get_result(ws: torch.Tensor, stream=None) -> tuple[int, int]:
+    """Synchronise ``stream``; return (stream bytes of the last compress/reduce, device status)."""
+    nbytes = ctypes.c_uint64(0)
+    dev = ctypes.c_int(0)
+    _check(_lib.cccl_get_result(ws.data_ptr(), _stream(stream), ctypes.byref(nbytes), ctypes.byref(dev)),
+           "cccl_get_result")
+    return int(nbytes.value), int(dev.value)
+
+
+# ---------------------------------------------------------------- conveniences
+def empty_stream(n_elems: int, device=None) -> torch.Tensor:
+    """A uint8 buffer large enough for any stream of n_elems values."""
+    return torch.empty(cccl_compress_bound(n_elems), dtype=torch.uint8, device=device or "cuda")
+
+
+def empty_workspace(n_elems: int, device=None) -> torch.Tensor:
+    return torch.empty(cccl_workspace_bytes(n_elems), dtype=torch.uint8, device=device or "cuda")
+
+
+def compress(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """Compress and wait; returns the stream trimmed to its size."""
+    out = empty_stream(x.numel(), x.device)
+    ws = empty_workspace(x.numel(), x.device)
+    cccl_compress(x, out, ws, stream)
+    nbytes, dev = cccl_get_result(ws, stream)
+    _check(dev, "cccl_compress (device)")
+    return out[:nbytes]
+
+
+def decompress(s: torch.Tensor, n_elems: int, stream=None) -> torch.Tensor:
+    """Decompress and wait; returns n_elems bf16 bit patterns (int16)."""
+    out = torch.empty(n_elems, dtype=torch.int16, device=s.device)
+    ws = empty_workspace(n_elems, s.device)
+    cccl_decompress(s, out, ws, stream=stream)
+    _, dev = cccl_get_result(ws, stream)
+    _check(dev, "cccl_decompress (device)")
+    return out
+
+
+def reduce_compressed(streams: Sequence[torch.Tensor], n_elems: int, stream=None) -> torch.Tensor:
+    """Fused compressed reduce and wait; returns the output stream trimmed."""
+    dev0 = streams[0].device
+    out = empty_stream(n_elems, dev0)
+    ws = empty_workspace(n_elems, dev0)
+    cccl_reduce_compressed(streams, n_elems, out, ws, stream=stream)
+    nbytes, dev = cccl_get_result(ws, stream)
+    _check(dev, "cccl_reduce_compressed (device)")
+    return out[:nbytes]

@@ -1,0 +1,147 @@
+// cccl_api.cu -- the C ABI (include/cccl.h): argument checks, workspace reset
+// and kernel launches.  Nothing here allocates memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/cccl.h"
+#include "cccl_device.cuh"
+#include "cccl_launch.h"
+
+namespace {
+
+using cccl::kChunkElems;
+
+uint64_t n_chunks_of(size_t n) { return (n + kChunkElems - 1) / kChunkElems; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuMemGetAddressRange, resolved once through the runtime so that the library
+// loads (and its pure host functions work) on machines without a driver.
+using AddrRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+AddrRangeFn addr_range_fn() {
+    static const AddrRangeFn fn = []() -> AddrRangeFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        return reinterpret_cast<AddrRangeFn>(p);
+    }();
+    return fn;
+}
+
+// True if [p, p + bytes) lies inside one device (or managed) allocation.
+bool device_range(const void* p, size_t bytes) {
+    const AddrRangeFn range = addr_range_fn();
+    if (p == nullptr || range == nullptr) return false;
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return a >= base && bytes <= size && a - base <= size - bytes;
+}
+
+cccl_status clear_ws(void* ws, size_t bytes, cudaStream_t s) {
+    return cudaMemsetAsync(ws, 0, bytes, s) == cudaSuccess ? CCCL_OK : CCCL_ERR_CUDA;
+}
+
+size_t ws_used(size_t n) { return sizeof(cccl::WsHeader) + 8 * n_chunks_of(n); }
+
+}  // namespace
+
+extern "C" {
+
+size_t cccl_compress_bound(size_t n_elems) {
+    if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return 0;
+    const uint64_t full = n_elems / kChunkElems, tail = n_elems % kChunkElems;
+    uint64_t bytes = cccl::data_start(n_chunks_of(n_elems)) + full * cccl::kMaxChunkBytes;
+    if (tail) bytes += 16 + cccl::pad16(2 * tail);
+    return (size_t)bytes;
+}
+
+size_t cccl_workspace_bytes(size_t n_elems) {
+    if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return 0;
+    return (size_t)cccl::pad16(ws_used(n_elems));
+}
+
+cccl_status cccl_compress(const uint16_t* d_in, size_t n_elems, void* d_out, size_t out_capacity, void* d_ws,
+                          size_t ws_bytes, cccl_stream_t stream) {
+    if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_in) || !aligned16(d_out) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < cccl_workspace_bytes(n_elems)) return CCCL_ERR_INVALID_ARG;
+    if (out_capacity < cccl_compress_bound(n_elems)) return CCCL_ERR_CAPACITY;
+    if (!device_range(d_in, 2 * n_elems) || !device_range(d_out, out_capacity) || !device_range(d_ws, ws_bytes))
+        return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    if (cccl::launch_compress(d_in, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
+cccl_status cccl_decompress(const void* d_in, size_t in_bytes, uint16_t* d_out, size_t n_elems, void* d_ws,
+                            size_t ws_bytes, cccl_stream_t stream) {
+    if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS || in_bytes == 0) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_in) || !aligned16(d_out) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < sizeof(cccl::WsHeader)) return CCCL_ERR_INVALID_ARG;
+    if (!device_range(d_in, in_bytes) || !device_range(d_out, 2 * n_elems) || !device_range(d_ws, ws_bytes))
+        return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, sizeof(cccl::WsHeader), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    if (cccl::launch_decompress(static_cast<const uint8_t*>(d_in), in_bytes, d_out, n_elems, d_ws, s) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
+cccl_status cccl_reduce_compressed(const void* const* h_ins, const size_t* h_in_bytes, int R, size_t n_elems,
+                                   void* d_out, size_t out_capacity, void* d_ws, size_t ws_bytes,
+                                   cccl_stream_t stream) {
+    if (h_ins == nullptr || h_in_bytes == nullptr || R < 1 || R > cccl::kMaxRanks) return CCCL_ERR_INVALID_ARG;
+    if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_out) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < cccl_workspace_bytes(n_elems)) return CCCL_ERR_INVALID_ARG;
+    if (out_capacity < cccl_compress_bound(n_elems)) return CCCL_ERR_CAPACITY;
+    if (!device_range(d_out, out_capacity) || !device_range(d_ws, ws_bytes)) return CCCL_ERR_INVALID_ARG;
+    cccl::ReduceInputs inputs{};
+    for (int r = 0; r < R; ++r) {
+        if (!aligned16(h_ins[r]) || h_in_bytes[r] == 0 || !device_range(h_ins[r], h_in_bytes[r]))
+            return CCCL_ERR_INVALID_ARG;
+        inputs.in[r] = static_cast<const uint8_t*>(h_ins[r]);
+        inputs.in_bytes[r] = h_in_bytes[r];
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    if (cccl::launch_reduce(inputs, R, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
+cccl_status cccl_get_result(const void* d_ws, cccl_stream_t stream, uint64_t* out_bytes, cccl_status* dev_status) {
+    if (d_ws == nullptr || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    cccl::WsHeader h{};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&h, d_ws, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CCCL_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CCCL_ERR_CUDA;
+    if (out_bytes) *out_bytes = h.error ? 0 : h.total_bytes;
+    if (dev_status) *dev_status = static_cast<cccl_status>(h.error);
+    return CCCL_OK;
+}
+
+const char* cccl_status_string(cccl_status status) {
+    switch (status) {
+        case CCCL_OK: return "CCCL_OK";
+        case CCCL_ERR_INVALID_ARG: return "CCCL_ERR_INVALID_ARG";
+        case CCCL_ERR_CAPACITY: return "CCCL_ERR_CAPACITY";
+        case CCCL_ERR_CORRUPT: return "CCCL_ERR_CORRUPT";
+        case CCCL_ERR_TIMEOUT: return "CCCL_ERR_TIMEOUT";
+        case CCCL_ERR_CUDA: return "CCCL_ERR_CUDA";
+        case CCCL_ERR_UNIMPLEMENTED: return "CCCL_ERR_UNIMPLEMENTED";
+    }
+    return "CCCL_ERR_UNKNOWN";
+}
+
+}  // extern "C"

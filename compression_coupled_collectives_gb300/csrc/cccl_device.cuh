@@ -1,0 +1,398 @@
+// cccl_device.cuh -- device building blocks shared by the compress, decompress
+// and fused-reduce kernels (sm_103a).
+//
+// Thread layout of every kernel: one CTA of 128 threads per 4096-element
+// chunk.  Thread t = 32 q + l (warp q, lane l) owns the 32 elements
+//   i = 256 j + 8 l + s,   j = 4 q + jj (jj < 4),  s < 8,
+// i.e. four 16-byte rows of the chunk; a warp's 32 lanes cover 512
+// contiguous bytes per row, so every global load and store is a fully
+// coalesced 16-byte access.  The stream's bit-plane word 32 q + l holds
+// exactly these 32 elements (bit 8 (s % 4) + 2 jj + s / 4), so packing and
+// unpacking the exponent codes never leaves the thread.
+//
+// Inside a thread, 4 elements travel in one 32-bit word, one byte each
+// ("quads", element s = 4 h + b in byte b): m = 2 jj + h indexes the 8
+// quads.  All exponent work is byte-SIMD on these words.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace cccl {
+
+constexpr uint32_t kChunkElems = 4096;
+constexpr uint32_t kThreads = 128;
+constexpr uint32_t kStreamHeaderBytes = 64;
+constexpr uint32_t kChunkHeaderBytes = 16;
+constexpr uint32_t kSmPlaneBytes = 4096;
+constexpr uint32_t kPlaneBytes = 512;
+constexpr uint32_t kMaxChunkBytes = kChunkHeaderBytes + 2 * kChunkElems;  // 8208: a raw full chunk
+constexpr uint32_t kMagic = 0x31424343u;                                  // "CCB1"
+constexpr uint32_t kVersion = 1;
+constexpr uint32_t kDtypeBf16 = 1;
+constexpr uint32_t kModePacked = 0;
+constexpr uint32_t kModeRaw = 1;
+
+// device status codes (same values as cccl_status)
+constexpr uint32_t kStatusCorrupt = 3;
+constexpr uint32_t kStatusTimeout = 4;
+
+// Workspace: 16-byte header, then one placement word per chunk.
+struct WsHeader {
+    uint32_t ticket;       // next chunk index to hand out (compress, reduce)
+    uint32_t error;        // 0 or the largest device status seen
+    uint64_t total_bytes;  // stream size, written by the last chunk
+};
+
+// Placement word of the decoupled look-back: flag in bits 62..63.
+constexpr uint64_t kFlagAggregate = 1ull << 62;  // value = this chunk's bytes
+constexpr uint64_t kFlagPrefix = 2ull << 62;     // value = end offset of this chunk
+constexpr uint64_t kFlagPoison = 3ull << 62;     // a predecessor failed; give up
+constexpr uint64_t kValueMask = (1ull << 62) - 1;
+
+// Bounded waits: every spin gives up after kWaitLimitNs of GPU time (read
+// from %globaltimer), records kStatusTimeout and returns; nothing waits
+// forever.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__host__ __device__ constexpr uint64_t pad16(uint64_t x) { return (x + 15) & ~uint64_t(15); }
+__host__ __device__ constexpr uint64_t data_start(uint64_t n_chunks) { return kStreamHeaderBytes + pad16(8 * n_chunks); }
+
+// ---------------------------------------------------------------------------
+// small PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t vmin_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void record_error(WsHeader* ws, uint32_t status) { atomicMax(&ws->error, status); }
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------------------
+// bulk (TMA) copy global -> shared, completion on an mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// One thread: expect `bytes` on `bar` and start the copy (bytes % 16 == 0,
+// both addresses 16-byte aligned, checked by the caller).
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+// Bounded wait for phase `parity` of `bar`; false if kWaitLimitNs ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_addr(bar);
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((it & 63) == 0) {
+            const uint64_t now = globaltimer_ns();
+            if (it == 0)
+                t0 = now;
+            else if (now - t0 > kWaitLimitNs)
+                return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 split / join on quads (section 4.1: sign and fraction travel raw,
+// only the 8-bit exponent is re-encoded)
+// ---------------------------------------------------------------------------
+// A, B: two words of two bf16 each (elements 4h+0, 4h+1 in A; 4h+2, 4h+3 in B).
+// e:  the four exponents, one per byte.
+// sm: the four sign+fraction bytes ((b >> 8) & 0x80 | b & 0x7F).
+__device__ __forceinline__ void split_quad(uint32_t A, uint32_t B, uint32_t& e, uint32_t& sm) {
+    const uint32_t lo = __byte_perm(A, B, 0x6420);  // low bytes of the 4 values
+    const uint32_t hi = __byte_perm(A, B, 0x7531);  // high bytes
+    sm = (lo & 0x7F7F7F7Fu) | (hi & 0x80808080u);
+    e = ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
+}
+__device__ __forceinline__ void join_quad(uint32_t e, uint32_t sm, uint32_t& A, uint32_t& B) {
+    const uint32_t lo = (sm & 0x7F7F7F7Fu) | ((e << 7) & 0x80808080u);
+    const uint32_t hi = (sm & 0x80808080u) | ((e >> 1) & 0x7F7F7F7Fu);
+    A = __byte_perm(lo, hi, 0x5140);
+    B = __byte_perm(lo, hi, 0x7362);
+}
+
+// Byte flags (0x80 per byte) of the bytes of `off` that are >= S, 1 <= S <= 127;
+// kb = (128 - S) * 0x01010101.  No carry crosses a byte.
+__device__ __forceinline__ uint32_t ge_flags(uint32_t off, uint32_t kb) {
+    return (off | ((off & 0x7F7F7F7Fu) + kb)) & 0x80808080u;
+}
+// 0x80 flags -> 0xFF byte masks
+__device__ __forceinline__ uint32_t flags_to_mask(uint32_t f) { return f | (f - (f >> 7)); }
+// Count of 0x80 flags over 8 quads (one popc).
+__device__ __forceinline__ uint32_t count_flags8(const uint32_t f[8]) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc |= f[m] >> (7 - m);
+    return __popc(acc & 0xFFFFFFFFu);
+}
+
+// ---------------------------------------------------------------------------
+// bit-planes: plane p word = sum over quads m, bytes b of bit p of code(m, b)
+// at bit 8 b + m
+// ---------------------------------------------------------------------------
+template <int K>
+__device__ __forceinline__ void pack_planes(const uint32_t code[8], uint32_t w[7]) {
+#pragma unroll
+    for (int p = 0; p < K; ++p) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const uint32_t t = (m >= p) ? (code[m] << (m - p)) : (code[m] >> (p - m));
+            acc |= t & (0x01010101u << m);
+        }
+        w[p] = acc;
+    }
+}
+template <int K>
+__device__ __forceinline__ void unpack_planes(const uint32_t w[7], uint32_t code[8]) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int p = 0; p < K; ++p) {
+            const uint32_t t = (p >= m) ? (w[p] << (p - m)) : (w[p] >> (m - p));
+            acc |= t & (0x01010101u << p);
+        }
+        code[m] = acc;
+    }
+}
+__device__ __forceinline__ void pack_planes_k(int k, const uint32_t code[8], uint32_t w[7]) {
+    switch (k) {
+        case 1: pack_planes<1>(code, w); break;
+        case 2: pack_planes<2>(code, w); break;
+        case 3: pack_planes<3>(code, w); break;
+        case 4: pack_planes<4>(code, w); break;
+        case 5: pack_planes<5>(code, w); break;
+        case 6: pack_planes<6>(code, w); break;
+        case 7: pack_planes<7>(code, w); break;
+        default: break;
+    }
+}
+__device__ __forceinline__ void unpack_planes_k(int k, const uint32_t w[7], uint32_t code[8]) {
+    switch (k) {
+        case 1: unpack_planes<1>(w, code); break;
+        case 2: unpack_planes<2>(w, code); break;
+        case 3: unpack_planes<3>(w, code); break;
+        case 4: unpack_planes<4>(w, code); break;
+        case 5: unpack_planes<5>(w, code); break;
+        case 6: unpack_planes<6>(w, code); break;
+        case 7: unpack_planes<7>(w, code); break;
+        default:
+#pragma unroll
+            for (int m = 0; m < 8; ++m) code[m] = 0;
+            break;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// escape list order: ascending element index.  Each thread knows how many
+// escapes each of its four rows (j = 4 q + jj) holds; this turns those
+// counts into the index of the row's first escape.  Block-wide: every
+// thread of the CTA must call it.  Returns the chunk's escape total.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t escape_row_bases(const uint32_t cnt[4], uint32_t base[4], uint32_t* s_row_tot) {
+    const uint32_t lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+    const uint32_t own_a = cnt[0] | (cnt[1] << 16), own_b = cnt[2] | (cnt[3] << 16);
+    uint32_t a = own_a, b = own_b;  // 16-bit fields: at most 256 per row
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t ta = __shfl_up_sync(0xFFFFFFFFu, a, d), tb = __shfl_up_sync(0xFFFFFFFFu, b, d);
+        if (lane >= (uint32_t)d) {
+            a += ta;
+            b += tb;
+        }
+    }
+    if (lane == 31) {
+        s_row_tot[4 * q + 0] = a & 0xFFFFu;
+        s_row_tot[4 * q + 1] = a >> 16;
+        s_row_tot[4 * q + 2] = b & 0xFFFFu;
+        s_row_tot[4 * q + 3] = b >> 16;
+    }
+    const uint32_t ea = a - own_a, eb = b - own_b;  // exclusive over lanes
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const uint32_t v = s_row_tot[r];
+        if ((uint32_t)r < 4 * q) before += v;
+        total += v;
+    }
+    const uint32_t r0 = s_row_tot[4 * q], r1 = s_row_tot[4 * q + 1], r2 = s_row_tot[4 * q + 2];
+    base[0] = before + (ea & 0xFFFFu);
+    base[1] = before + r0 + (ea >> 16);
+    base[2] = before + r0 + r1 + (eb & 0xFFFFu);
+    base[3] = before + r0 + r1 + r2 + (eb >> 16);
+    return total;
+}
+
+// ---------------------------------------------------------------------------
+// decoupled look-back (one warp).  Chunks are numbered in the order their
+// CTAs took a ticket, so every predecessor is already running and publishes
+// its size without waiting on anything later: the wait always ends.
+// Returns the byte offset of chunk c, or kFlagPoison if a predecessor failed
+// or the bounded wait ran out (then kStatusTimeout is recorded).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t lookback_offset(uint64_t* status, uint32_t c, uint32_t bytes, uint64_t start,
+                                                    WsHeader* ws) {
+    const uint32_t lane = threadIdx.x & 31;
+    if (c == 0) {
+        if (lane == 0) st_relaxed_u64(&status[0], kFlagPrefix | (start + bytes));
+        return start;
+    }
+    if (lane == 0) st_relaxed_u64(&status[c], kFlagAggregate | bytes);
+    uint64_t excl = 0;
+    int64_t end = c;  // predecessors still to account for: [0, end)
+    uint32_t ns = 32;
+    uint64_t t0 = 0;
+    while (true) {
+        const int64_t idx = end - 1 - (int64_t)lane;
+        const uint64_t v = idx >= 0 ? ld_relaxed_u64(&status[idx]) : kFlagPrefix;
+        const uint32_t flag = (uint32_t)(v >> 62);
+        const uint32_t terminal = __ballot_sync(0xFFFFFFFFu, flag >= 2);
+        const uint32_t pending = __ballot_sync(0xFFFFFFFFu, flag == 0);
+        const uint32_t first = terminal ? (uint32_t)(__ffs(terminal) - 1) : 32u;
+        const uint32_t before = first == 32 ? 0xFFFFFFFFu : ((1u << first) - 1u);
+        if (pending & before) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            if (now - t0 > kWaitLimitNs) {
+                if (lane == 0) {
+                    record_error(ws, kStatusTimeout);
+                    st_relaxed_u64(&status[c], kFlagPoison);
+                }
+                return kFlagPoison;
+            }
+            __nanosleep(ns);
+            if (ns < 1024) ns <<= 1;
+            continue;
+        }
+        const uint32_t part = (lane < first) ? (uint32_t)(v & kValueMask) : 0u;  // aggregates, < 2^14 each
+        excl += __reduce_add_sync(0xFFFFFFFFu, part);
+        if (first < 32) {
+            const uint64_t tv = __shfl_sync(0xFFFFFFFFu, v, first);
+            if ((tv >> 62) == 3) {
+                if (lane == 0) st_relaxed_u64(&status[c], kFlagPoison);
+                return kFlagPoison;
+            }
+            excl += tv & kValueMask;
+            break;
+        }
+        end -= 32;
+    }
+    if (lane == 0) st_relaxed_u64(&status[c], kFlagPrefix | (excl + bytes));
+    return excl;
+}
+
+// ---------------------------------------------------------------------------
+// stream header / chunk header validation (shared by decompress and reduce)
+// ---------------------------------------------------------------------------
+struct ChunkView {
+    uint64_t offset;  // byte offset of the chunk in its stream
+    uint32_t bytes;   // chunk size (<= kMaxChunkBytes once validated)
+    uint32_t ok;      // 1 if the stream header and this chunk's table entries are valid
+};
+
+__device__ __forceinline__ uint64_t ld_u64_aligned(const uint8_t* p) { return *reinterpret_cast<const uint64_t*>(p); }
+__device__ __forceinline__ uint32_t ld_u32_aligned(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// One thread: check the stream header against (n_elems, in_bytes) and locate
+// chunk c through the offset table.  Every read stays inside in_bytes.
+__device__ __forceinline__ ChunkView locate_chunk(const uint8_t* s, uint64_t in_bytes, uint64_t n_elems,
+                                                  uint64_t n_chunks, uint64_t c) {
+    ChunkView v{0, 0, 0};
+    const uint64_t start = data_start(n_chunks);
+    if (in_bytes < start) return v;
+    const uint32_t w0 = ld_u32_aligned(s + 0), w1 = ld_u32_aligned(s + 4), w2 = ld_u32_aligned(s + 8);
+    if (w0 != kMagic || w1 != (kVersion | (kDtypeBf16 << 16)) || w2 != kChunkElems) return v;
+    if (ld_u64_aligned(s + 16) != n_elems || ld_u64_aligned(s + 24) != n_chunks) return v;
+    const uint64_t total = ld_u64_aligned(s + 32);
+    if (total > in_bytes || total < start) return v;
+    const uint64_t off = ld_u64_aligned(s + kStreamHeaderBytes + 8 * c);
+    const uint64_t end = (c + 1 < n_chunks) ? ld_u64_aligned(s + kStreamHeaderBytes + 8 * (c + 1)) : total;
+    if (c == 0 && off != start) return v;
+    if ((off & 15) != 0 || end <= off || end > total || off < start) return v;
+    // the bulk copy needs a size that is a multiple of 16; every valid chunk is
+    if (end - off > kMaxChunkBytes || ((end - off) & 15) != 0) return v;
+    v.offset = off;
+    v.bytes = (uint32_t)(end - off);
+    v.ok = 1;
+    return v;
+}
+
+// Decoded chunk header (16 bytes at the start of a staged chunk).
+struct ChunkHeader {
+    uint32_t mode, k, base, n_c, n_esc, bytes;
+};
+__device__ __forceinline__ ChunkHeader read_chunk_header(const uint8_t* h) {
+    const uint32_t w0 = ld_u32_aligned(h), w1 = ld_u32_aligned(h + 4), w2 = ld_u32_aligned(h + 8);
+    ChunkHeader ch;
+    ch.mode = w0 & 0xFF;
+    ch.k = (w0 >> 8) & 0xFF;
+    ch.base = (w0 >> 16) & 0xFF;
+    ch.n_c = w1 & 0xFFFF;
+    ch.n_esc = w1 >> 16;
+    ch.bytes = w2;
+    return ch;
+}
+// Same rules as the format: raw chunks carry no table; a packed chunk is a
+// full chunk whose exponent part is smaller than 4096 bytes.
+__device__ __forceinline__ bool chunk_header_valid(const ChunkHeader& h, uint32_t staged_bytes, uint32_t n_c) {
+    if (h.bytes != staged_bytes || h.n_c != n_c) return false;
+    if (h.mode == kModeRaw) return h.k == 0 && h.base == 0 && h.n_esc == 0 && h.bytes == 16 + pad16(2 * n_c);
+    if (h.mode != kModePacked || n_c != kChunkElems || h.k > 7) return false;
+    if (h.k == 0 && h.n_esc != 0) return false;
+    if (h.bytes != 16 + kSmPlaneBytes + kPlaneBytes * h.k + pad16(h.n_esc)) return false;
+    return kPlaneBytes * h.k + pad16(h.n_esc) < kSmPlaneBytes;
+}
+
+}  // namespace cccl

@@ -1,0 +1,26 @@
+// cccl_launch.h -- launchers of the three kernels (host side, internal).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace cccl {
+
+constexpr int kMaxRanks = 64;
+
+struct ReduceInputs {
+    const uint8_t* in[kMaxRanks];
+    uint64_t in_bytes[kMaxRanks];
+};
+
+// All pointers are device pointers already validated by the C ABI layer; the
+// workspace header and placement words have been cleared on `stream`.
+cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
+                            cudaStream_t stream);
+cudaError_t launch_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t n_elems, void* ws,
+                              cudaStream_t stream);
+cudaError_t launch_reduce(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
+                          cudaStream_t stream);
+
+}  // namespace cccl

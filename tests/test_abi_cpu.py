@@ -1,0 +1,102 @@
+"""The C ABI library on a machine without a GPU: it loads, exports every entry
+point that include/cccl.h declares, and its pure host functions and host-side
+argument checks behave as documented (no compute is launched)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cccl.h")
+
+
+@pytest.fixture(scope="module")
+def cc():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import compression_coupled_collectives_gb300 as m
+
+    return m
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cccl_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert names == sorted(["cccl_compress_bound", "cccl_workspace_bytes", "cccl_compress", "cccl_decompress",
+                            "cccl_reduce_compressed", "cccl_get_result", "cccl_status_string"]), names
+
+
+def test_library_exports_every_declared_symbol(cc):
+    lib = ctypes.CDLL(cc.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+@pytest.mark.parametrize("n", [1, 2, 4095, 4096, 4097, 1 << 20, (1 << 28) + 3])
+def test_bound_matches_oracle(cc, orc, n):
+    assert cc.cccl_compress_bound(n) == orc.compress_bound(n)
+    nch = -(-n // 4096)
+    assert cc.cccl_workspace_bytes(n) == -(-(16 + 8 * nch) // 16) * 16
+
+
+def test_bound_and_workspace_limits(cc):
+    assert cc.cccl_compress_bound(0) == 0
+    assert cc.cccl_workspace_bytes(0) == 0
+    assert cc.cccl_compress_bound((1 << 40) + 1) == 0
+    assert cc.cccl_compress_bound(1 << 40) > 0
+
+
+def test_status_strings(cc):
+    for code, name in [(0, "CCCL_OK"), (1, "CCCL_ERR_INVALID_ARG"), (2, "CCCL_ERR_CAPACITY"),
+                       (3, "CCCL_ERR_CORRUPT"), (4, "CCCL_ERR_TIMEOUT"), (5, "CCCL_ERR_CUDA"),
+                       (6, "CCCL_ERR_UNIMPLEMENTED"), (99, "CCCL_ERR_UNKNOWN")]:
+        assert cc.cccl_status_string(code) == name
+
+
+def test_host_side_argument_checks(cc):
+    """Errors found before anything is enqueued; none of these touch a GPU."""
+    lib = cc._lib
+    n = 10 * 4096
+    bound, wsb = cc.cccl_compress_bound(n), cc.cccl_workspace_bytes(n)
+    A, B, W = 0x10000, 0x20000, 0x30000  # aligned addresses that are never dereferenced
+    assert lib.cccl_compress(A, 0, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress(A + 2, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress(A, n, B + 8, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress(A, n, B, bound, W, wsb - 16, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress(A, n, B, bound - 1, W, wsb, None) == cc.CCCL_ERR_CAPACITY
+    assert lib.cccl_compress(None, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress(A, (1 << 40) + 1, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_decompress(A, 0, B, n, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_decompress(A, 4096, B, n, W, 8, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_decompress(A, 4096, B + 2, n, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    ptrs = (ctypes.c_void_p * 2)(A, A + 0x1000)
+    sizes = (ctypes.c_size_t * 2)(100, 100)
+    assert lib.cccl_reduce_compressed(ptrs, sizes, 0, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_compressed(ptrs, sizes, 65, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_compressed(None, sizes, 2, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_compressed(ptrs, sizes, 2, n, B, bound - 1, W, wsb, None) == cc.CCCL_ERR_CAPACITY
+    bad = (ctypes.c_void_p * 2)(A, A + 8)
+    assert lib.cccl_reduce_compressed(bad, sizes, 2, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_get_result(None, None, None, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_get_result(W + 4, None, None, None) == cc.CCCL_ERR_INVALID_ARG
+
+
+def test_host_pointers_are_refused(cc):
+    """Without a device allocation behind them, buffers are refused on the host
+    (a kernel is never handed a host address)."""
+    n = 4096
+    x = np.zeros(n + 16, np.uint16)
+    out = np.zeros(cc.cccl_compress_bound(n) + 16, np.uint8)
+    ws = np.zeros(cc.cccl_workspace_bytes(n) + 16, np.uint8)
+    al = lambda a: (a.ctypes.data + 15) // 16 * 16
+    r = cc._lib.cccl_compress(al(x), n, al(out), cc.cccl_compress_bound(n), al(ws), cc.cccl_workspace_bytes(n), None)
+    assert r == cc.CCCL_ERR_INVALID_ARG

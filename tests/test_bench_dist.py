@@ -1,0 +1,65 @@
+"""The benchmark's multi-process host logic on CPU: two gloo ranks agree on
+the slowest rank's time and on the total, and reduce disjoint simulated ranks
+(weak scaling: every GPU gets its own seeds)."""
+
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import bench
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        r, w, lr = bench.dist_env()
+        mx = bench.max_over_ranks(10.0 + 5.0 * r, w)
+        sm = bench.sum_over_ranks(1.0 + r, w)
+        seeds = bench.simulated_ranks(r)
+        gathered = [None] * w
+        dist.all_gather_object(gathered, seeds)
+        q.put((r, w, lr, mx, sm, gathered))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r, w, lr, mx, sm, gathered in out:
+        assert w == world and lr == r
+        assert mx == 15.0  # the slowest rank's time
+        assert sm == 3.0
+        flat = [s for g in gathered for s in g]
+        assert len(flat) == len(set(flat)) == world * 2  # disjoint seeds per GPU
+
+
+def test_single_process_defaults(monkeypatch):
+    import bench
+
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_env() == (0, 1, 0)
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.simulated_ranks(0) == [0, 1]
+    assert bench.simulated_ranks(3) == [6, 7]
