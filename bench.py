@@ -242,7 +242,7 @@ def run_reference(args, rank: int, world: int) -> None:
 
 
 def workload_config() -> dict:
-    return {"workload": "gradient-like bf16 buffer, 33,554,432 values (64 MiB) ~ N(0, 1e-3) with 1% of "
+    return {"workload": "gradient-like bf16 buffer, 33,554,432 values (64 MiB) ~ N(0, 1e-3) with 1%% of "
                         "positions x100, on %d simulated data-parallel ranks per GPU: compress each, fused "
                         "reduce (R=%d), decompress the result" % (RANKS_PER_GPU, RANKS_PER_GPU),
             "n_elems": 33554432, "ranks_per_gpu": RANKS_PER_GPU, "chunk_elems": 4096,

@@ -5,7 +5,7 @@
 
 #include <cstdint>
 
-#include "../../include/cccl.h"
+#include "cccl.h"
 #include "cccl_device.cuh"
 #include "cccl_launch.h"
 

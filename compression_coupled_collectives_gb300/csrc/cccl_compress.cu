@@ -1,62 +1,110 @@
-// cccl_compress.cu -- the compress kernel: one CTA per 4096-element chunk,
-// load -> split -> exponent table -> place by decoupled look-back -> write
-// ("CCCL: In-GPU Compression-Coupled Collective Communication", sections
-// 4.1, 4.3, 4.4; section 5 for the raw partial chunk).
+// cccl_compress.cu -- the compress kernel ("CCCL: In-GPU Compression-Coupled
+// Collective Communication", sections 4.1, 4.3, 4.4; section 5 for the raw
+// partial chunk).
+//
+// One CTA of kGroup warps per group of kGroup consecutive chunks: one bulk
+// (TMA) copy per chunk stages the input in shared memory, each warp sizes its
+// chunk (exponent table, width, escapes), one decoupled look-back places the
+// whole group, and each warp writes its chunk straight to its final offset.
+#include <mutex>
+
 #include "cccl_encode.cuh"
 #include "cccl_launch.h"
 
 namespace cccl {
 
-__device__ __forceinline__ void load_full_chunk(const uint16_t* in, uint64_t c, uint32_t P[16]) {
-    const uint32_t lane = threadIdx.x & 31, q = threadIdx.x >> 5;
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(in + c * kChunkElems);
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-        const uint4 v = ld_stream_v4(src + 512 * (4 * q + jj) + 16 * lane);
-        P[4 * jj] = v.x;
-        P[4 * jj + 1] = v.y;
-        P[4 * jj + 2] = v.z;
-        P[4 * jj + 3] = v.w;
+constexpr int kGroup = 8;
+constexpr size_t kCompressSmemBytes = (size_t)kGroup * 2 * kChunkElems;
+
+// Thread 0: bulk-copy the full chunks of group g into the stage buffers.
+__device__ __forceinline__ void load_group(const uint16_t* in, uint64_t g, uint64_t n_full, uint8_t* stage,
+                                           uint64_t* bars) {
+    for (int i = 0; i < kGroup; ++i) {
+        const uint64_t c = g * kGroup + i;
+        if (c < n_full) bulk_load(stage + (size_t)i * 2 * kChunkElems, in + c * kChunkElems, 2 * kChunkElems, &bars[i]);
     }
 }
 
-__global__ void __launch_bounds__(kThreads) compress_kernel(const uint16_t* __restrict__ in, StreamOut so) {
-    __shared__ EncodeSmem sm;
-    __shared__ uint32_t s_ticket;
+__global__ void __launch_bounds__(32 * kGroup, 3) compress_kernel(const uint16_t* __restrict__ in, StreamOut so) {
+    extern __shared__ __align__(128) uint8_t stage[];
+    __shared__ __align__(8) uint64_t bars[kGroup];
+    __shared__ uint32_t s_bytes[kGroup], s_parity[kGroup];
+    __shared__ uint64_t s_offset[kGroup];
+    __shared__ uint64_t s_group;
+    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint64_t n_full = so.n_elems / kChunkElems;
 
-    // Chunks are processed in ticket order (the look-back's forward-progress
-    // guarantee).  Tickets normally follow blockIdx, so the load of chunk
-    // blockIdx.x starts before the ticket arrives and is redone otherwise.
-    uint32_t P[16];
-    const uint64_t guess = blockIdx.x;
-    if (guess < n_full) load_full_chunk(in, guess, P);
-    if (threadIdx.x == 0) s_ticket = atomicAdd(&so.ws->ticket, 1u);
+    // Groups are placed in ticket order (the look-back's forward-progress
+    // guarantee).  Tickets normally follow blockIdx, so the copies of group
+    // blockIdx.x start before the ticket arrives and are redone otherwise.
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kGroup; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        const uint64_t guess = blockIdx.x;
+        load_group(in, guess, n_full, stage, bars);
+        const uint64_t g = atomicAdd(&so.ws->ticket, 1u);
+        for (int i = 0; i < kGroup; ++i) s_parity[i] = 0;
+        if (g != guess) {
+            for (int i = 0; i < kGroup; ++i) {
+                if (guess * kGroup + i < n_full) {
+                    mbar_wait(&bars[i], 0);  // the stage must be idle before it is refilled
+                    s_parity[i] = 1;
+                }
+            }
+            load_group(in, g, n_full, stage, bars);
+        }
+        s_group = g;
+    }
     __syncthreads();
-    const uint64_t c = s_ticket;
+    const uint64_t g = s_group;
+    const uint64_t c = g * kGroup + w;
+    const uint8_t* chunk = stage + (size_t)w * 2 * kChunkElems;
+
+    // phase A: size of this warp's chunk
+    ChunkPlan pl{};
+    uint32_t bytes = 0;
+    bool failed = false;
     if (c < n_full) {
-        if (c != guess) load_full_chunk(in, c, P);
-        encode_full_chunk(P, c, so, sm);
+        if (mbar_wait(&bars[w], s_parity[w])) {
+            pl = plan_chunk_warp(chunk);
+            bytes = pl.bytes;
+        } else {
+            failed = true;
+            if (lane == 0) record_error(so.ws, kStatusTimeout);
+        }
+    } else if (c < so.n_chunks) {
+        bytes = tail_chunk_bytes((uint32_t)(so.n_elems - c * kChunkElems));
+    }
+    if (lane == 0) s_bytes[w] = bytes;
+
+    // placement of the whole group
+    const uint64_t off = place_group<kGroup>(so, g, s_bytes, s_offset, failed);
+    if (off == kFlagPoison || bytes == 0) return;
+    if (off + bytes > so.capacity) {  // cannot happen for a correct placement; never write past the buffer
+        if (lane == 0) record_error(so.ws, kStatusCorrupt);
         return;
     }
-    // partial last chunk
-    const uint32_t n_c = (uint32_t)(so.n_elems - c * kChunkElems);
-    const uint16_t* src = in + c * kChunkElems;
-    const uint32_t lane = threadIdx.x & 31, q = threadIdx.x >> 5;
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const uint32_t i = 256 * (4 * q + jj) + 8 * lane + 2 * w;
-            const uint32_t lo = i < n_c ? src[i] : 0u, hi = i + 1 < n_c ? src[i + 1] : 0u;
-            P[4 * jj + w] = lo | (hi << 16);
-        }
+
+    // phase B: write the chunk at its offset
+    uint8_t* dst = so.out + off;
+    if (c < n_full) {
+        write_chunk_warp(chunk, pl, dst);
+    } else {
+        const uint16_t* src = in + c * kChunkElems;
+        write_tail_chunk_warp([src](uint32_t i) { return src[i]; }, (uint32_t)(so.n_elems - c * kChunkElems), dst);
     }
-    encode_tail_chunk(P, c, n_c, so, sm);
+    if (lane == 0) finish_chunk(so, c, off, bytes);
 }
 
 cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
                             cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kCompressSmemBytes);
+    });
+    if (attr != cudaSuccess) return attr;
     StreamOut so;
     so.out = out;
     so.capacity = capacity;
@@ -64,7 +112,8 @@ cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, 
     so.status = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + sizeof(WsHeader));
     so.n_elems = n_elems;
     so.n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
-    compress_kernel<<<(unsigned)so.n_chunks, kThreads, 0, stream>>>(in, so);
+    const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
+    compress_kernel<<<(unsigned)n_groups, 32 * kGroup, kCompressSmemBytes, stream>>>(in, so);
     return cudaGetLastError();
 }
 

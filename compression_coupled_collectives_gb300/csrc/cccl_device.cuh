@@ -276,60 +276,84 @@ __device__ __forceinline__ uint32_t escape_row_bases(const uint32_t cnt[4], uint
 }
 
 // ---------------------------------------------------------------------------
-// decoupled look-back (one warp).  Chunks are numbered in the order their
-// CTAs took a ticket, so every predecessor is already running and publishes
-// its size without waiting on anything later: the wait always ends.
-// Returns the byte offset of chunk c, or kFlagPoison if a predecessor failed
+// decoupled look-back (one warp) over placement units (groups of chunks).
+// Units are numbered in the order their CTAs took a ticket, so every
+// predecessor is already running and publishes its size without waiting on
+// anything later: the wait always ends.  Each round trip reads 256
+// predecessors (8 independent loads per lane), so a look-back that must walk
+// past the units still in flight needs few round trips.
+// Returns the byte offset of unit g, or kFlagPoison if a predecessor failed
 // or the bounded wait ran out (then kStatusTimeout is recorded).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t lookback_offset(uint64_t* status, uint32_t c, uint32_t bytes, uint64_t start,
-                                                    WsHeader* ws) {
+constexpr int kLookbackPerLane = 8;
+constexpr uint32_t kLookbackWindow = 32 * kLookbackPerLane;
+
+__device__ __forceinline__ uint64_t lookback_offset_wide(uint64_t* status, uint64_t g, uint32_t bytes, uint64_t start,
+                                                         WsHeader* ws) {
     const uint32_t lane = threadIdx.x & 31;
-    if (c == 0) {
+    if (g == 0) {
         if (lane == 0) st_relaxed_u64(&status[0], kFlagPrefix | (start + bytes));
         return start;
     }
-    if (lane == 0) st_relaxed_u64(&status[c], kFlagAggregate | bytes);
+    if (lane == 0) st_relaxed_u64(&status[g], kFlagAggregate | bytes);
     uint64_t excl = 0;
-    int64_t end = c;  // predecessors still to account for: [0, end)
+    int64_t end = (int64_t)g;  // predecessors still to account for: [0, end)
     uint32_t ns = 32;
     uint64_t t0 = 0;
     while (true) {
-        const int64_t idx = end - 1 - (int64_t)lane;
-        const uint64_t v = idx >= 0 ? ld_relaxed_u64(&status[idx]) : kFlagPrefix;
-        const uint32_t flag = (uint32_t)(v >> 62);
-        const uint32_t terminal = __ballot_sync(0xFFFFFFFFu, flag >= 2);
-        const uint32_t pending = __ballot_sync(0xFFFFFFFFu, flag == 0);
-        const uint32_t first = terminal ? (uint32_t)(__ffs(terminal) - 1) : 32u;
-        const uint32_t before = first == 32 ? 0xFFFFFFFFu : ((1u << first) - 1u);
-        if (pending & before) {
+        uint64_t v[kLookbackPerLane];
+#pragma unroll
+        for (int i = 0; i < kLookbackPerLane; ++i) {
+            const int64_t idx = end - 1 - (int64_t)(lane + 32 * i);
+            v[i] = idx >= 0 ? ld_relaxed_u64(&status[idx]) : kFlagPrefix;  // before unit 0: prefix 0
+        }
+        // nearest terminal (prefix or poison) entry, counted from unit end - 1
+        uint32_t first = kLookbackWindow;
+#pragma unroll
+        for (int i = 0; i < kLookbackPerLane; ++i) {
+            const uint32_t t = __ballot_sync(0xFFFFFFFFu, (v[i] >> 62) >= 2);
+            if (first == kLookbackWindow && t) first = 32 * i + __ffs(t) - 1;
+        }
+        bool pending = false;
+#pragma unroll
+        for (int i = 0; i < kLookbackPerLane; ++i)
+            pending |= (lane + 32 * i < first) && (v[i] >> 62) == 0;
+        if (__any_sync(0xFFFFFFFFu, pending)) {
             const uint64_t now = globaltimer_ns();
             if (t0 == 0) t0 = now;
             if (now - t0 > kWaitLimitNs) {
                 if (lane == 0) {
                     record_error(ws, kStatusTimeout);
-                    st_relaxed_u64(&status[c], kFlagPoison);
+                    st_relaxed_u64(&status[g], kFlagPoison);
                 }
                 return kFlagPoison;
             }
             __nanosleep(ns);
-            if (ns < 1024) ns <<= 1;
+            if (ns < 512) ns <<= 1;
             continue;
         }
-        const uint32_t part = (lane < first) ? (uint32_t)(v & kValueMask) : 0u;  // aggregates, < 2^14 each
+        uint32_t part = 0;  // aggregates are unit sizes (< 2^17 each)
+#pragma unroll
+        for (int i = 0; i < kLookbackPerLane; ++i)
+            if (lane + 32 * i < first) part += (uint32_t)(v[i] & kValueMask);
         excl += __reduce_add_sync(0xFFFFFFFFu, part);
-        if (first < 32) {
-            const uint64_t tv = __shfl_sync(0xFFFFFFFFu, v, first);
+        if (first < kLookbackWindow) {
+            uint64_t tv = 0;
+#pragma unroll
+            for (int i = 0; i < kLookbackPerLane; ++i) {
+                const uint64_t cand = __shfl_sync(0xFFFFFFFFu, v[i], first & 31);
+                if ((uint32_t)i == (first >> 5)) tv = cand;
+            }
             if ((tv >> 62) == 3) {
-                if (lane == 0) st_relaxed_u64(&status[c], kFlagPoison);
+                if (lane == 0) st_relaxed_u64(&status[g], kFlagPoison);
                 return kFlagPoison;
             }
             excl += tv & kValueMask;
             break;
         }
-        end -= 32;
+        end -= kLookbackWindow;
     }
-    if (lane == 0) st_relaxed_u64(&status[c], kFlagPrefix | (excl + bytes));
+    if (lane == 0) st_relaxed_u64(&status[g], kFlagPrefix | (excl + bytes));
     return excl;
 }
 

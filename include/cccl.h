@@ -39,7 +39,12 @@
  *     no state between calls; calls with distinct workspaces may run
  *     concurrently.
  *   - d_* pointers are device pointers (cudaMalloc'd or managed), 16-byte
- *     aligned.  h_* pointers are host pointers.
+ *     aligned.  h_* pointers are host pointers.  Each device buffer, with the
+ *     size passed for it, must lie inside one device allocation; a range that
+ *     does not is refused with CCCL_ERR_INVALID_ARG before anything is
+ *     enqueued.  (The check sees allocations, not sub-allocations: a size
+ *     that overruns a tensor but stays inside its allocator's segment is the
+ *     caller's error and is not detected.)
  *   - Work is enqueued on `stream` (NULL: the legacy default stream) and
  *     runs asynchronously.  Argument errors are detected on the host before
  *     anything is enqueued and return immediately.  Errors found on the

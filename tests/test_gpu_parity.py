@@ -142,7 +142,7 @@ def test_repeated_calls_reuse_workspace_and_buffers(cc, orc, wl):
 
 def test_two_streams_two_workspaces(cc, orc, wl):
     n = 300 * CHUNK
-    xs = [wl.generate(1, r, count=n) for r in range(2)]
+    xs = [wl.generate(3, r, count=n) for r in range(2)]
     outs = [cc.empty_stream(n) for _ in xs]
     wss = [cc.empty_workspace(n) for _ in xs]
     streams = [torch.cuda.Stream() for _ in xs]
@@ -326,10 +326,13 @@ def test_argument_errors(cc):
     with pytest.raises(cc.CcclError) as e:
         cc.cccl_compress(big[1:n + 1], out, ws)  # 2-byte misaligned input
     assert e.value.status == cc.CCCL_ERR_INVALID_ARG
-    # a size larger than the allocation is refused before any launch
+    # a size larger than the device allocation is refused before any launch
+    # (the check works at allocation granularity: torch sub-allocates tensors
+    # from larger segments, so claim more than any segment holds)
     small_out = torch.empty(1024, dtype=torch.uint8, device="cuda")
-    r = cc._lib.cccl_compress(x.data_ptr(), n, small_out.data_ptr(), cc.cccl_compress_bound(n), ws.data_ptr(),
-                              ws.numel(), None)
+    r = cc._lib.cccl_compress(x.data_ptr(), n, small_out.data_ptr(), 1 << 40, ws.data_ptr(), ws.numel(), None)
+    assert r == cc.CCCL_ERR_INVALID_ARG
+    r = cc._lib.cccl_decompress(out.data_ptr(), 1 << 40, x.data_ptr(), n, ws.data_ptr(), ws.numel(), None)
     assert r == cc.CCCL_ERR_INVALID_ARG
     host = np.zeros(n + 8, np.uint16)
     hp = (host.ctypes.data + 15) // 16 * 16  # aligned, but pageable host memory
