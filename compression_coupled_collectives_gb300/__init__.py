@@ -40,6 +40,8 @@ _lib.cccl_workspace_bytes.argtypes = [_sz]
 _lib.cccl_workspace_bytes.restype = _sz
 _lib.cccl_compress.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_compress.restype = _i
+_lib.cccl_compress_noalloc.argtypes = [_vp, _sz, _vp, _sz, _vp]
+_lib.cccl_compress_noalloc.restype = _i
 _lib.cccl_decompress.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_decompress.restype = _i
 _lib.cccl_reduce_compressed.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _vp, _sz, _vp, _sz, _vp]
@@ -93,6 +95,15 @@ def cccl_compress(x: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, stream=N
     x = _bf16_bits(x)
     _check(_lib.cccl_compress(x.data_ptr(), x.numel(), out.data_ptr(), out.numel() * out.element_size(),
                               ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)), "cccl_compress")
+
+
+def cccl_compress_noalloc(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """Enqueue the same compression as cccl_compress using the library's static
+    device scratch instead of a caller workspace (nothing is allocated).  The
+    stream size is then bytes 32..39 of ``out`` (0 if a device wait ran out)."""
+    x = _bf16_bits(x)
+    _check(_lib.cccl_compress_noalloc(x.data_ptr(), x.numel(), out.data_ptr(), out.numel() * out.element_size(),
+                                      _stream(stream)), "cccl_compress_noalloc")
 
 
 def cccl_decompress(s: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, in_bytes: int | None = None,

@@ -83,6 +83,18 @@ cccl_status cccl_compress(const uint16_t* d_in, size_t n_elems, void* d_out, siz
     return CCCL_OK;
 }
 
+cccl_status cccl_compress_noalloc(const uint16_t* d_in, size_t n_elems, void* d_out, size_t out_capacity,
+                                  cccl_stream_t stream) {
+    if (n_elems == 0 || n_elems > CCCL_NOALLOC_MAX_ELEMS) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_in) || !aligned16(d_out)) return CCCL_ERR_INVALID_ARG;
+    if (out_capacity < cccl_compress_bound(n_elems)) return CCCL_ERR_CAPACITY;
+    if (!device_range(d_in, 2 * n_elems) || !device_range(d_out, out_capacity)) return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cccl::launch_compress_noalloc(d_in, n_elems, static_cast<uint8_t*>(d_out), out_capacity, s) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
 cccl_status cccl_decompress(const void* d_in, size_t in_bytes, uint16_t* d_out, size_t n_elems, void* d_ws,
                             size_t ws_bytes, cccl_stream_t stream) {
     if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS || in_bytes == 0) return CCCL_ERR_INVALID_ARG;

@@ -8,6 +8,8 @@
 // whole group, and each warp writes its chunk straight to its final offset.
 #include <mutex>
 
+#include "cccl.h"
+
 #include "cccl_encode.cuh"
 #include "cccl_launch.h"
 
@@ -115,6 +117,61 @@ cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, 
     const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
     compress_kernel<<<(unsigned)n_groups, 32 * kGroup, kCompressSmemBytes, stream>>>(in, so);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Compress without any allocation by the caller: the scratch that
+// cccl_compress takes as a workspace (status header + one placement word per
+// group) lives in this file-scope device array instead.  Every GPU that loads
+// the library holds it until the process exits.
+// ---------------------------------------------------------------------------
+constexpr uint64_t kNoAllocMaxGroups = CCCL_NOALLOC_MAX_ELEMS / kChunkElems / kGroup;
+constexpr size_t kNoAllocScratchBytes = sizeof(WsHeader) + 8 * kNoAllocMaxGroups;
+static_assert(CCCL_NOALLOC_MAX_ELEMS % ((uint64_t)kChunkElems * kGroup) == 0, "whole groups");
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so its address is looked up once
+// per device (with that device current) and cached.
+cudaError_t noalloc_scratch(void** ptr) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_compress_noalloc(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity,
+                                    cudaStream_t stream) {
+    if (n_elems == 0 || n_elems > CCCL_NOALLOC_MAX_ELEMS) return cudaErrorInvalidValue;
+    void* scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return e;
+    const uint64_t n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
+    const uint64_t n_groups = (n_chunks + kGroup - 1) / kGroup;
+    // the scratch keeps the previous call's contents: clear what must start at
+    // zero, and the stream header, whose size field then stays 0 unless the
+    // whole stream was placed
+    e = cudaMemsetAsync(scratch, 0, sizeof(WsHeader) + 8 * n_groups, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(out, 0, kStreamHeaderBytes, stream);
+    if (e != cudaSuccess) return e;
+    return launch_compress(in, n_elems, out, capacity, scratch, stream);
 }
 
 }  // namespace cccl

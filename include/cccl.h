@@ -102,6 +102,34 @@ size_t cccl_workspace_bytes(size_t n_elems);
 cccl_status cccl_compress(const uint16_t *d_in, size_t n_elems, void *d_out, size_t out_capacity, void *d_ws,
                           size_t ws_bytes, cccl_stream_t stream);
 
+/* Largest n_elems cccl_compress_noalloc accepts (2^30 values, 2 GiB). */
+#define CCCL_NOALLOC_MAX_ELEMS ((size_t)1 << 30)
+
+/* cccl_compress for callers that cannot allocate device memory: code that
+ * runs while another component owns the memory pool and forbids side
+ * allocations, paths that must not call cudaMalloc because it can
+ * synchronise the device or is not allowed at that point, and embeddings
+ * without an allocator at all.  It has no counterpart in the paper.
+ * It produces exactly the stream cccl_compress produces, without a workspace
+ * argument: its scratch (about 256 KiB: the status header and one placement
+ * word per group of 8 chunks for CCCL_NOALLOC_MAX_ELEMS values) is a static
+ * device array that every GPU which loads this library keeps until the
+ * process exits.  Nothing is allocated per call.
+ *   d_in, n_elems, d_out, out_capacity, stream: as for cccl_compress.
+ *   n_elems must be 1..CCCL_NOALLOC_MAX_ELEMS, else CCCL_ERR_INVALID_ARG.
+ * The first call on a device looks up the scratch's device address (with
+ * that device current) and caches it; make that first call before capturing
+ * the stream into a CUDA graph.  Each call clears the scratch it uses and the
+ * 64-byte stream header on `stream` before compressing.
+ * The compressed size is the stream header's total_bytes (bytes 32..39 of
+ * d_out) once the work is done; it stays 0 if a device-side wait ran out.
+ * All calls on a device share the one scratch array: calls that may overlap
+ * on the GPU (different streams without ordering between them) race and must
+ * not be issued; calls on one stream are ordered and safe.
+ * Returns INVALID_ARG, CAPACITY, CUDA or OK synchronously. */
+cccl_status cccl_compress_noalloc(const uint16_t *d_in, size_t n_elems, void *d_out, size_t out_capacity,
+                                  cccl_stream_t stream);
+
 /* Decompress a stream made for n_elems values (the inverse of section 4.1's
  * split; the "Decomp." stage of Figure 2).
  *   d_in          the stream; in_bytes is the size of the readable buffer

@@ -31,8 +31,9 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    assert names == sorted(["cccl_compress_bound", "cccl_workspace_bytes", "cccl_compress", "cccl_decompress",
-                            "cccl_reduce_compressed", "cccl_get_result", "cccl_status_string"]), names
+    assert names == sorted(["cccl_compress_bound", "cccl_workspace_bytes", "cccl_compress", "cccl_compress_noalloc",
+                            "cccl_decompress", "cccl_reduce_compressed", "cccl_get_result",
+                            "cccl_status_string"]), names
 
 
 def test_library_exports_every_declared_symbol(cc):
