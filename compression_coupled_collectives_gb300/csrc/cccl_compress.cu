@@ -2,100 +2,207 @@
 // Collective Communication", sections 4.1, 4.3, 4.4; section 5 for the raw
 // partial chunk).
 //
-// One CTA of kGroup warps per group of kGroup consecutive chunks: one bulk
-// (TMA) copy per chunk stages the input in shared memory, each warp sizes its
-// chunk (exponent table, width, escapes), one decoupled look-back places the
-// whole group, and each warp writes its chunk straight to its final offset.
+// Persistent and pipelined: one CTA per SM, kGroup compute warps plus one
+// control warp, and a ring of kRing stages, each holding one group of kGroup
+// consecutive chunks staged by bulk (TMA) copies.  Per group:
+//   control warp  takes a ticket (the group index), issues the copies two
+//                 groups ahead, and once the compute warps have sized the
+//                 group, places it with one decoupled look-back;
+//   compute warp  sizes its chunk of group i+1 (exponent table, width,
+//                 escapes; the sign+fraction plane replaces the consumed
+//                 input in shared memory) while the control warp places
+//                 group i, then writes its chunk of group i at the final
+//                 offset: byte planes by bulk (TMA) stores, bit-planes and
+//                 escapes from registers.
+// So the look-back's wait for earlier groups overlaps with the sizing of the
+// next group, and the next copies are in flight during both.
+// Tickets hand out groups in order to CTAs that are already running, so every
+// group a look-back waits on belongs to a running CTA: the waits always end.
 #include <mutex>
 
 #include "cccl.h"
-
 #include "cccl_encode.cuh"
 #include "cccl_launch.h"
 
 namespace cccl {
 
-constexpr int kGroup = 8;
-constexpr size_t kCompressSmemBytes = (size_t)kGroup * 2 * kChunkElems;
+constexpr int kGroup = 8;                     // chunks per group = compute warps
+constexpr int kRing = 3;                      // groups staged per CTA
+constexpr int kCtrl = kGroup;                 // warp index of the control warp
+constexpr int kCompressThreads = 32 * (kGroup + 1);
+constexpr size_t kChunkBytesRaw = 2 * kChunkElems;
+constexpr size_t kCompressSmemBytes = (size_t)kRing * kGroup * kChunkBytesRaw;
 
-// Thread 0: bulk-copy the full chunks of group g into the stage buffers.
-__device__ __forceinline__ void load_group(const uint16_t* in, uint64_t g, uint64_t n_full, uint8_t* stage,
-                                           uint64_t* bars) {
-    for (int i = 0; i < kGroup; ++i) {
-        const uint64_t c = g * kGroup + i;
-        if (c < n_full) bulk_load(stage + (size_t)i * 2 * kChunkElems, in + c * kChunkElems, 2 * kChunkElems, &bars[i]);
+struct CompressSmem {
+    uint64_t load[kRing][kGroup];  // stage filled (one per compute warp)
+    uint64_t sized[kRing];         // all compute warps sized the stage's group
+    uint64_t free_[kRing];         // all compute warps wrote the stage's group out
+    uint64_t placed[2];            // control warp published the offsets
+    uint64_t group[kRing];         // group index held by each stage (>= n_groups: none)
+    unsigned long long tally[kRing];  // sized warps (high word) and their bytes (low word)
+    uint32_t size[kRing][kGroup];
+    uint64_t off[2][kGroup];       // chunk offsets, or kFlagPoison
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Control lane: fill stage s with group g (or mark it empty).
+__device__ __forceinline__ void issue_group(const uint16_t* in, uint64_t g, uint64_t n_groups, uint64_t n_full,
+                                            uint8_t* stage, CompressSmem& sm, int s) {
+    sm.group[s] = g;
+    sm.tally[s] = 0;
+    for (int w = 0; w < kGroup; ++w) {
+        const uint64_t c = g * kGroup + w;
+        if (g < n_groups && c < n_full)
+            bulk_load(stage + ((size_t)s * kGroup + w) * kChunkBytesRaw, in + c * kChunkElems, kChunkBytesRaw,
+                      &sm.load[s][w]);
+        else
+            mbar_arrive(&sm.load[s][w]);  // nothing to copy: complete the phase at once
     }
 }
 
-__global__ void __launch_bounds__(32 * kGroup, 3) compress_kernel(const uint16_t* __restrict__ in, StreamOut so) {
-    extern __shared__ __align__(128) uint8_t stage[];
-    __shared__ __align__(8) uint64_t bars[kGroup];
-    __shared__ uint32_t s_bytes[kGroup], s_parity[kGroup];
-    __shared__ uint64_t s_offset[kGroup];
-    __shared__ uint64_t s_group;
+// Compute warp, one group: size this warp's chunk of group i (into cur) and
+// then write its chunk of group i - 1 (from prev).  Returns false once the
+// groups are exhausted (after writing group i - 1).  The loop keeps one copy
+// of it: instruction-cache space, not register moves, is the scarce resource.
+struct WarpChunk {
+    ChunkRegs regs;
+    ChunkPlan plan;
+    uint32_t bytes;
+    uint64_t c;
+};
+
+__device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__ in, const StreamOut& so,
+                                             uint8_t* stage, CompressSmem& sm, WarpChunk& cur, WarpChunk& prev) {
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint64_t n_full = so.n_elems / kChunkElems;
-
-    // Groups are placed in ticket order (the look-back's forward-progress
-    // guarantee).  Tickets normally follow blockIdx, so the copies of group
-    // blockIdx.x start before the ticket arrives and are redone otherwise.
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kGroup; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
-        const uint64_t guess = blockIdx.x;
-        load_group(in, guess, n_full, stage, bars);
-        const uint64_t g = atomicAdd(&so.ws->ticket, 1u);
-        for (int i = 0; i < kGroup; ++i) s_parity[i] = 0;
-        if (g != guess) {
-            for (int i = 0; i < kGroup; ++i) {
-                if (guess * kGroup + i < n_full) {
-                    mbar_wait(&bars[i], 0);  // the stage must be idle before it is refilled
-                    s_parity[i] = 1;
+    const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
+    const int s = i % kRing;
+    const bool filled = mbar_wait(&sm.load[s][w], (uint32_t)(i / kRing) & 1u);
+    const uint64_t g = sm.group[s];
+    const bool live = filled && g < n_groups;
+    if (live) {
+        cur.c = g * kGroup + w;
+        cur.bytes = 0;
+        if (cur.c < n_full) {
+            cur.plan = plan_chunk_warp(stage + ((size_t)s * kGroup + w) * kChunkBytesRaw, cur.regs);
+            cur.bytes = cur.plan.bytes;
+        } else if (cur.c < so.n_chunks) {
+            cur.bytes = tail_chunk_bytes((uint32_t)(so.n_elems - cur.c * kChunkElems));
+        }
+        __syncwarp();
+        if (lane == 0) {
+            sm.size[s][w] = cur.bytes;
+            // the last warp to size the group publishes its size at once, so
+            // the look-backs of later groups need not wait for this CTA's
+            // control warp
+            const unsigned long long old = atomicAdd(&sm.tally[s], (1ull << 32) | cur.bytes);
+            if ((old >> 32) == kGroup - 1)
+                publish_unit_size(so.status, g, (uint32_t)old + cur.bytes, data_start(so.n_chunks));
+            mbar_arrive(&sm.sized[s]);
+        }
+    } else if (!filled && lane == 0) {
+        record_error(so.ws, kStatusTimeout);
+    }
+    if (i > 0) {  // write group i - 1
+        const int ip = i - 1, sp = ip % kRing;
+        if (mbar_wait(&sm.placed[ip & 1], (uint32_t)(ip >> 1) & 1u)) {
+            const uint64_t off = sm.off[ip & 1][w];
+            if (off != kFlagPoison && prev.bytes > 0) {
+                if (off + prev.bytes > so.capacity) {  // cannot happen for a correct placement
+                    if (lane == 0) record_error(so.ws, kStatusCorrupt);
+                } else {
+                    uint8_t* dst = so.out + off;
+                    if (prev.c < n_full) {
+                        write_chunk_warp(prev.regs, prev.plan, stage + ((size_t)sp * kGroup + w) * kChunkBytesRaw,
+                                         dst);
+                    } else {
+                        const uint16_t* src = in + prev.c * kChunkElems;
+                        write_tail_chunk_warp([src](uint32_t e) { return src[e]; },
+                                              (uint32_t)(so.n_elems - prev.c * kChunkElems), dst);
+                    }
+                    if (lane == 0) finish_chunk(so, prev.c, off, prev.bytes);
                 }
             }
-            load_group(in, g, n_full, stage, bars);
+        } else if (lane == 0) {
+            record_error(so.ws, kStatusTimeout);
         }
-        s_group = g;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.free_[sp]);  // this warp is done with stage sp
+    }
+    return live;
+}
+
+__global__ void __launch_bounds__(kCompressThreads, 1) compress_kernel(const uint16_t* __restrict__ in, StreamOut so) {
+    extern __shared__ __align__(128) uint8_t stage[];
+    __shared__ CompressSmem sm;
+    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint64_t n_full = so.n_elems / kChunkElems;
+    const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRing; ++s) {
+            for (int i = 0; i < kGroup; ++i) mbar_init(&sm.load[s][i], 1);
+            mbar_init(&sm.sized[s], kGroup);
+            mbar_init(&sm.free_[s], kGroup);
+        }
+        for (int x = 0; x < 2; ++x) mbar_init(&sm.placed[x], 1);
+        fence_mbar_init();
     }
     __syncthreads();
-    const uint64_t g = s_group;
-    const uint64_t c = g * kGroup + w;
-    const uint8_t* chunk = stage + (size_t)w * 2 * kChunkElems;
 
-    // phase A: size of this warp's chunk
-    ChunkPlan pl{};
-    uint32_t bytes = 0;
-    bool failed = false;
-    if (c < n_full) {
-        if (mbar_wait(&bars[w], s_parity[w])) {
-            pl = plan_chunk_warp(chunk);
-            bytes = pl.bytes;
-        } else {
-            failed = true;
-            if (lane == 0) record_error(so.ws, kStatusTimeout);
+    if (w == kCtrl) {
+        // ---------------------------------------------------------------- control warp
+        if (lane == 0)
+            for (int s = 0; s < kRing; ++s) issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, s);
+        __syncwarp();
+        for (int i = 0;; ++i) {
+            const int s = i % kRing;
+            const uint64_t g = sm.group[s];
+            if (g >= n_groups) break;
+            if (!mbar_wait(&sm.sized[s], (uint32_t)(i / kRing) & 1u)) {
+                if (lane == 0) record_error(so.ws, kStatusTimeout);
+                break;
+            }
+            const uint32_t mine = lane < (uint32_t)kGroup ? sm.size[s][lane] : 0u;
+            uint32_t incl = mine;
+#pragma unroll
+            for (int d = 1; d < kGroup; d <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= (uint32_t)d) incl += t;
+            }
+            const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, kGroup - 1);
+            const uint64_t go = lookback_offset_wide(so.status, g, total, data_start(so.n_chunks), so.ws, true);
+            if (lane < (uint32_t)kGroup) sm.off[i & 1][lane] = go == kFlagPoison ? kFlagPoison : go + (incl - mine);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.placed[i & 1]);
+            // group i-1 is written out: refill its stage, for group i+2
+            if (i >= 1) {
+                const int sp = (i - 1) % kRing;
+                if (!mbar_wait(&sm.free_[sp], (uint32_t)((i - 1) / kRing) & 1u)) {
+                    if (lane == 0) record_error(so.ws, kStatusTimeout);
+                    break;
+                }
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, sp);
+                }
+                __syncwarp();
+            }
         }
-    } else if (c < so.n_chunks) {
-        bytes = tail_chunk_bytes((uint32_t)(so.n_elems - c * kChunkElems));
-    }
-    if (lane == 0) s_bytes[w] = bytes;
-
-    // placement of the whole group
-    const uint64_t off = place_group<kGroup>(so, g, s_bytes, s_offset, failed);
-    if (off == kFlagPoison || bytes == 0) return;
-    if (off + bytes > so.capacity) {  // cannot happen for a correct placement; never write past the buffer
-        if (lane == 0) record_error(so.ws, kStatusCorrupt);
         return;
     }
 
-    // phase B: write the chunk at its offset
-    uint8_t* dst = so.out + off;
-    if (c < n_full) {
-        write_chunk_warp(chunk, pl, dst);
-    } else {
-        const uint16_t* src = in + c * kChunkElems;
-        write_tail_chunk_warp([src](uint32_t i) { return src[i]; }, (uint32_t)(so.n_elems - c * kChunkElems), dst);
+    // -------------------------------------------------------------------- compute warps
+    WarpChunk cur, prev;  // the chunk being sized and the one being written
+    cur.bytes = prev.bytes = 0;
+    cur.c = prev.c = 0;
+    for (int i = 0;; ++i) {
+        if (!compute_step(i, in, so, stage, sm, cur, prev)) break;
+        prev = cur;
     }
-    if (lane == 0) finish_chunk(so, c, off, bytes);
 }
 
 cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
@@ -107,6 +214,10 @@ cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, 
                                     (int)kCompressSmemBytes);
     });
     if (attr != cudaSuccess) return attr;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     StreamOut so;
     so.out = out;
     so.capacity = capacity;
@@ -115,7 +226,8 @@ cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, 
     so.n_elems = n_elems;
     so.n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
     const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
-    compress_kernel<<<(unsigned)n_groups, 32 * kGroup, kCompressSmemBytes, stream>>>(in, so);
+    const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
+    compress_kernel<<<grid, kCompressThreads, kCompressSmemBytes, stream>>>(in, so);
     return cudaGetLastError();
 }
 

@@ -4,7 +4,7 @@
 // Inverse of the split of "CCCL: In-GPU Compression-Coupled Collective
 // Communication", section 4.1: each exponent is base + code, or, where the
 // code is the sentinel 2^k - 1, the next byte of the chunk's escape list
-// (ascending element order); sign and fraction come back from their byte.
+// (bit-plane order); sign and fraction come back from their byte.
 #pragma once
 
 #include "cccl_device.cuh"
@@ -34,18 +34,21 @@ __device__ __forceinline__ bool decode_full_chunk(const uint8_t* buf, const Chun
         return true;
     }
     const int k = (int)h.k;
-    uint32_t S[8], code[8], W[7];
+    uint32_t S[8], code[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
         const uint2 v = *reinterpret_cast<const uint2*>(body + 256 * (4 * q + jj) + 8 * lane);
         S[2 * jj] = v.x;
         S[2 * jj + 1] = v.y;
     }
-#pragma unroll
-    for (int p = 0; p < 7; ++p)
-        W[p] = (p < k) ? *reinterpret_cast<const uint32_t*>(body + kSmPlaneBytes + kPlaneBytes * p + 4 * (32 * q + lane))
-                       : 0u;
-    unpack_planes_k(k, W, code);
+    uint32_t sent = 0xFFFFFFFFu;  // bit set where the code is the sentinel (all k bits set)
+    const uint8_t* col = body + kSmPlaneBytes + 4 * (32 * q + lane);
+#pragma unroll 1
+    for (uint32_t p = 0; p < (uint32_t)k; ++p) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(col + kPlaneBytes * p);
+        unpack_plane(w, p, code);
+        sent &= w;
+    }
     const uint32_t base4 = h.base * 0x01010101u;
     uint32_t E[8];
     if (k == 0) {
@@ -53,10 +56,6 @@ __device__ __forceinline__ bool decode_full_chunk(const uint8_t* buf, const Chun
         for (int m = 0; m < 8; ++m) E[m] = base4;
         special = (h.base == 255);
     } else {
-        uint32_t sent = 0xFFFFFFFFu;  // bit set where the code is the sentinel (all k bits set)
-#pragma unroll
-        for (int p = 0; p < 7; ++p)
-            if (p < k) sent &= W[p];
         uint32_t FF[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
@@ -77,29 +76,41 @@ __device__ __forceinline__ bool decode_full_chunk(const uint8_t* buf, const Chun
         if (h.n_esc == 0) {
             if (__syncthreads_or(sent != 0u)) return false;
         } else {
-            uint32_t cnt[4], rb[4];
+            // escapes are listed in bit-plane order: plane word 32 q + l, then
+            // bit; this thread's sentinel bits are exactly its word's escapes
+            const uint32_t mine = __popc(sent);
+            uint32_t incl = mine;
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) cnt[jj] = (uint32_t)__popc(sent & (0x03030303u << (2 * jj)));
-            const uint32_t total = escape_row_bases(cnt, rb, s_row_tot);
-            if (total != h.n_esc) return false;
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t t2 = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= (uint32_t)d) incl += t2;
+            }
+            if (lane == 31) s_row_tot[q] = incl;
+            __syncthreads();
+            uint32_t before = 0, total = 0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t v = s_row_tot[r];
+                if ((uint32_t)r < q) before += v;
+                total += v;
+            }
+            if (total != h.n_esc) return false;  // CTA-uniform
+            const uint32_t first = before + incl - mine;
             const uint8_t* esc = body + kSmPlaneBytes + kPlaneBytes * k;
             bool inf_nan = false;
+            if (sent) {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                uint32_t idx = rb[jj];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int m = 2 * jj + hh;
+                for (int m = 0; m < 8; ++m)
 #pragma unroll
                     for (int b = 0; b < 4; ++b) {
-                        if ((FF[m] >> (8 * b)) & 1u) {
+                        const uint32_t bit = 8 * b + m;
+                        if ((sent >> bit) & 1u) {
+                            const uint32_t idx = first + __popc(sent & ((1u << bit) - 1u));
                             const uint32_t e = idx < h.n_esc ? esc[idx] : 0u;
-                            ++idx;
                             E[m] |= e << (8 * b);
                             inf_nan |= (e == 255u);
                         }
                     }
-                }
             }
             special = special || inf_nan;
         }

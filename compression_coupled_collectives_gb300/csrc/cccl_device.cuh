@@ -119,25 +119,37 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, 
         "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
 }
+// One thread: bulk (TMA) copy shared -> global (bytes % 16 == 0, both
+// addresses 16-byte aligned); completion tracked by bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst_gmem, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
+                 "r"(smem_addr(src_smem)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the committed bulk stores of this thread have read their source.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Bounded wait for phase `parity` of `bar`; false if kWaitLimitNs ran out.
+// Each try suspends the warp in hardware (up to kSuspendHintNs) until the
+// phase completes, so a waiting warp costs no issue slots.
+constexpr uint32_t kSuspendHintNs = 100000;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     const uint32_t a = smem_addr(bar);
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         uint32_t ok;
         asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
             : "=r"(ok)
-            : "r"(a), "r"(parity)
+            : "r"(a), "r"(parity), "r"(kSuspendHintNs)
             : "memory");
         if (ok) return true;
-        if ((it & 63) == 0) {
-            const uint64_t now = globaltimer_ns();
-            if (it == 0)
-                t0 = now;
-            else if (now - t0 > kWaitLimitNs)
-                return false;
-        }
+        const uint64_t now = globaltimer_ns();
+        if (it == 0)
+            t0 = now;
+        else if (now - t0 > kWaitLimitNs)
+            return false;
     }
 }
 
@@ -177,102 +189,25 @@ __device__ __forceinline__ uint32_t count_flags8(const uint32_t f[8]) {
 }
 
 // ---------------------------------------------------------------------------
-// bit-planes: plane p word = sum over quads m, bytes b of bit p of code(m, b)
-// at bit 8 b + m
+// bit-planes: plane p word = over quads m and bytes b, bit p of code(m, b) at
+// bit 8 b + m.  Moving bit 8 b + p to 8 b + m is a rotation by (p - m) mod 32
+// that never wraps (8 b + m and 8 b + p both lie in 0..31), so one funnel
+// rotate and one masked OR per (quad, plane) serve every width at run time.
 // ---------------------------------------------------------------------------
-template <int K>
-__device__ __forceinline__ void pack_planes(const uint32_t code[8], uint32_t w[7]) {
-#pragma unroll
-    for (int p = 0; p < K; ++p) {
-        uint32_t acc = 0;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const uint32_t t = (m >= p) ? (code[m] << (m - p)) : (code[m] >> (p - m));
-            acc |= t & (0x01010101u << m);
-        }
-        w[p] = acc;
-    }
-}
-template <int K>
-__device__ __forceinline__ void unpack_planes(const uint32_t w[7], uint32_t code[8]) {
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        uint32_t acc = 0;
-#pragma unroll
-        for (int p = 0; p < K; ++p) {
-            const uint32_t t = (p >= m) ? (w[p] << (p - m)) : (w[p] >> (m - p));
-            acc |= t & (0x01010101u << p);
-        }
-        code[m] = acc;
-    }
-}
-__device__ __forceinline__ void pack_planes_k(int k, const uint32_t code[8], uint32_t w[7]) {
-    switch (k) {
-        case 1: pack_planes<1>(code, w); break;
-        case 2: pack_planes<2>(code, w); break;
-        case 3: pack_planes<3>(code, w); break;
-        case 4: pack_planes<4>(code, w); break;
-        case 5: pack_planes<5>(code, w); break;
-        case 6: pack_planes<6>(code, w); break;
-        case 7: pack_planes<7>(code, w); break;
-        default: break;
-    }
-}
-__device__ __forceinline__ void unpack_planes_k(int k, const uint32_t w[7], uint32_t code[8]) {
-    switch (k) {
-        case 1: unpack_planes<1>(w, code); break;
-        case 2: unpack_planes<2>(w, code); break;
-        case 3: unpack_planes<3>(w, code); break;
-        case 4: unpack_planes<4>(w, code); break;
-        case 5: unpack_planes<5>(w, code); break;
-        case 6: unpack_planes<6>(w, code); break;
-        case 7: unpack_planes<7>(w, code); break;
-        default:
-#pragma unroll
-            for (int m = 0; m < 8; ++m) code[m] = 0;
-            break;
-    }
-}
+__device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funnelshift_r(x, x, n); }
 
-// ---------------------------------------------------------------------------
-// escape list order: ascending element index.  Each thread knows how many
-// escapes each of its four rows (j = 4 q + jj) holds; this turns those
-// counts into the index of the row's first escape.  Block-wide: every
-// thread of the CTA must call it.  Returns the chunk's escape total.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t escape_row_bases(const uint32_t cnt[4], uint32_t base[4], uint32_t* s_row_tot) {
-    const uint32_t lane = threadIdx.x & 31, q = threadIdx.x >> 5;
-    const uint32_t own_a = cnt[0] | (cnt[1] << 16), own_b = cnt[2] | (cnt[3] << 16);
-    uint32_t a = own_a, b = own_b;  // 16-bit fields: at most 256 per row
+// Plane p of 8 quads of codes (bits of codes above p are ignored).
+__device__ __forceinline__ uint32_t pack_plane(const uint32_t* code, uint32_t p) {
+    uint32_t acc = 0;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t ta = __shfl_up_sync(0xFFFFFFFFu, a, d), tb = __shfl_up_sync(0xFFFFFFFFu, b, d);
-        if (lane >= (uint32_t)d) {
-            a += ta;
-            b += tb;
-        }
-    }
-    if (lane == 31) {
-        s_row_tot[4 * q + 0] = a & 0xFFFFu;
-        s_row_tot[4 * q + 1] = a >> 16;
-        s_row_tot[4 * q + 2] = b & 0xFFFFu;
-        s_row_tot[4 * q + 3] = b >> 16;
-    }
-    const uint32_t ea = a - own_a, eb = b - own_b;  // exclusive over lanes
-    __syncthreads();
-    uint32_t before = 0, total = 0;
+    for (int m = 0; m < 8; ++m) acc |= rotr(code[m], (p - (uint32_t)m) & 31u) & (0x01010101u << m);
+    return acc;
+}
+// OR plane word w (plane p) into 8 quads of codes.
+__device__ __forceinline__ void unpack_plane(uint32_t w, uint32_t p, uint32_t* code) {
+    const uint32_t mask = 0x01010101u << p;
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        const uint32_t v = s_row_tot[r];
-        if ((uint32_t)r < 4 * q) before += v;
-        total += v;
-    }
-    const uint32_t r0 = s_row_tot[4 * q], r1 = s_row_tot[4 * q + 1], r2 = s_row_tot[4 * q + 2];
-    base[0] = before + (ea & 0xFFFFu);
-    base[1] = before + r0 + (ea >> 16);
-    base[2] = before + r0 + r1 + (eb & 0xFFFFu);
-    base[3] = before + r0 + r1 + r2 + (eb >> 16);
-    return total;
+    for (int m = 0; m < 8; ++m) code[m] |= rotr(w, ((uint32_t)m - p) & 31u) & mask;
 }
 
 // ---------------------------------------------------------------------------
@@ -288,14 +223,17 @@ __device__ __forceinline__ uint32_t escape_row_bases(const uint32_t cnt[4], uint
 constexpr int kLookbackPerLane = 8;
 constexpr uint32_t kLookbackWindow = 32 * kLookbackPerLane;
 
+// Publish unit g's size: its end offset when g == 0, else its aggregate.
+__device__ __forceinline__ void publish_unit_size(uint64_t* status, uint64_t g, uint32_t bytes, uint64_t start) {
+    st_relaxed_u64(&status[g], g == 0 ? (kFlagPrefix | (start + bytes)) : (kFlagAggregate | bytes));
+}
+
+// `published`: the unit's size was already published with publish_unit_size.
 __device__ __forceinline__ uint64_t lookback_offset_wide(uint64_t* status, uint64_t g, uint32_t bytes, uint64_t start,
-                                                         WsHeader* ws) {
+                                                         WsHeader* ws, bool published = false) {
     const uint32_t lane = threadIdx.x & 31;
-    if (g == 0) {
-        if (lane == 0) st_relaxed_u64(&status[0], kFlagPrefix | (start + bytes));
-        return start;
-    }
-    if (lane == 0) st_relaxed_u64(&status[g], kFlagAggregate | bytes);
+    if (!published && lane == 0) publish_unit_size(status, g, bytes, start);
+    if (g == 0) return start;
     uint64_t excl = 0;
     int64_t end = (int64_t)g;  // predecessors still to account for: [0, end)
     uint32_t ns = 32;

@@ -33,10 +33,23 @@ struct StreamOut {
 struct ChunkPlan {
     uint32_t raw;    // 1: stored raw
     uint32_t k;      // code width
-    uint32_t base;   // minimum exponent
+    uint32_t base;   // header base: minimum exponent (0 when raw)
     uint32_t n_esc;  // escapes at width k
-    uint32_t kfull;  // narrowest width without escapes (0 when one symbol; 8, 9: none)
+    uint32_t emin;   // minimum exponent (kept for raw chunks too)
+    uint32_t k1;     // width whose escape bits are kept in ChunkRegs::esc
     uint32_t bytes;  // chunk size, header included
+};
+
+// One lane's share of a full chunk, kept in registers between sizing and
+// writing: its 128 elements as 32 quads of exponent offsets from the chunk
+// minimum, quad 8 q + m holding row 4 q + m / 2, elements 4 (m % 2) .. +3 of
+// the lane's 8.  esc[q] holds the escape bits at width k1 in bit-plane layout
+// (bit 8 b + m: byte b of quad 8 q + m).  The sign+fraction bytes wait in
+// shared memory instead: sizing writes them over the first half of the
+// chunk's own (consumed) input slot, in stream order.
+struct ChunkRegs {
+    uint32_t off[32];
+    uint32_t esc[4];
 };
 
 // This lane's 4 pair-words of row j (elements 256 j + 8 l .. + 7).
@@ -44,50 +57,61 @@ __device__ __forceinline__ uint4 lds_row(const uint8_t* chunk, uint32_t j, uint3
     return *reinterpret_cast<const uint4*>(chunk + 512 * j + 16 * lane);
 }
 
-// Number of this lane's elements among 8 quads whose offset is >= 2^k - 1.
-__device__ __forceinline__ uint32_t count_escapes8(const uint32_t* off, uint32_t k) {
+// Escape bits (bit-plane layout) of 8 quads of offsets at width k, and their
+// number: the bits of element (m, b) sit at 8 b + m.
+__device__ __forceinline__ uint32_t escape_bits8(const uint32_t* off, uint32_t k) {
     const uint32_t kb = (128u - ((1u << k) - 1u)) * 0x01010101u;
-    uint32_t f[8];
+    uint32_t acc = 0;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) f[m] = ge_flags(off[m], kb);
-    return count_flags8(f);
+    for (int m = 0; m < 8; ++m) acc |= ge_flags(off[m], kb) >> (7 - m);
+    return acc;
 }
 
 // Phase A: exponent table and size of the full chunk at `chunk` (8192 bytes
-// of bf16 in shared memory).  One warp; every lane returns the same plan.
-__device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk) {
+// of bf16 in shared memory), leaving the offsets in `r` and the chunk's
+// sign+fraction plane over the first 4096 bytes of `chunk`.  One warp; every
+// lane returns the same plan.
+__device__ __forceinline__ ChunkPlan plan_chunk_warp(uint8_t* chunk, ChunkRegs& r) {
     const uint32_t lane = threadIdx.x & 31;
-    uint32_t off[32];  // exponents of this lane's 128 elements (quads), later offsets
+    // pass 1: exponent extremes
     uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int j = 0; j < 16; ++j) {
+        const uint4 v = lds_row(chunk, j, lane);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const uint4 v = lds_row(chunk, 4 * q + jj, lane);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t mag = w[i] & 0x7FFF7FFFu;  // |x| orders like the exponent
-                mn = vmin_u16x2(mn, mag);
-                mx = vmax_u16x2(mx, mag);
-            }
-            uint32_t sm_unused;
-            split_quad(w[0], w[1], off[8 * q + 2 * jj], sm_unused);
-            split_quad(w[2], w[3], off[8 * q + 2 * jj + 1], sm_unused);
+        for (int i = 0; i < 4; ++i) {
+            // doubling drops each value's sign; a low lane's sign lands in the
+            // high lane's last fraction bit, which cannot move its exponent
+            const uint32_t mag2 = w[i] << 1;
+            mn = vmin_u16x2(mn, mag2);
+            mx = vmax_u16x2(mx, mag2);
         }
     }
-    const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, min(mn & 0xFFFFu, mn >> 16) >> 7);
-    const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, max(mx & 0xFFFFu, mx >> 16) >> 7);
+    const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, min(mn & 0xFFFFu, mn >> 16) >> 8);
+    const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, max(mx & 0xFFFFu, mx >> 16) >> 8);
     const uint32_t base4 = emin * 0x01010101u;
+    // pass 2: split every row; its sign+fraction bytes go to their place in
+    // the stream's byte plane (row j -> bytes 256 j ..), over input already read
 #pragma unroll
-    for (int m = 0; m < 32; ++m) off[m] -= base4;  // no borrow: every exponent >= emin
+    for (int j = 0; j < 16; ++j) {
+        const uint4 v = lds_row(chunk, j, lane);
+        uint32_t s0, s1;
+        split_quad(v.x, v.y, r.off[2 * j], s0);
+        split_quad(v.z, v.w, r.off[2 * j + 1], s1);
+        r.off[2 * j] -= base4;  // no borrow: every exponent >= emin
+        r.off[2 * j + 1] -= base4;
+        __syncwarp();  // all lanes have read row j (and row j / 2 before it)
+        *reinterpret_cast<uint2*>(chunk + 256 * j + 8 * lane) = make_uint2(s0, s1);
+    }
 
-    ChunkPlan pl{0u, 0u, emin, 0u, 0u, 0u};
+    ChunkPlan pl{0u, 0u, emin, 0u, emin, 0u, 0u};
     const uint32_t range = emax - emin;
     uint32_t best = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) r.esc[q] = 0;
     if (range > 0) {
         const uint32_t kfull = 32 - __clz(range + 1);  // 2..9
-        pl.kfull = kfull;
         int bk = -1;
         uint32_t bsize = 0xFFFFFFFFu, besc = 0;
         if (kfull <= 7) {
@@ -97,9 +121,13 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk) {
         // widths below k1 can only win when 512 k + pad16(n_esc(k1)) does not
         // exceed the best size (n_esc never shrinks as k shrinks)
         const uint32_t k1 = min(kfull - 1, 7u);
+        pl.k1 = k1;
         uint32_t c1 = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) c1 += count_escapes8(off + 8 * q, k1);
+        for (int q = 0; q < 4; ++q) {
+            r.esc[q] = escape_bits8(r.off + 8 * q, k1);
+            c1 += __popc(r.esc[q]);
+        }
         const uint32_t n1 = __reduce_add_sync(0xFFFFFFFFu, c1);
         const uint32_t s1 = kPlaneBytes * k1 + (uint32_t)pad16(n1);
         if (s1 <= bsize) {  // k1 < kfull: a tie keeps the smaller width
@@ -113,7 +141,7 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk) {
             for (int k2 = kk; k2 >= 1; --k2) {
                 uint32_t ck = 0;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) ck += count_escapes8(off + 8 * q, (uint32_t)k2);
+                for (int q = 0; q < 4; ++q) ck += __popc(escape_bits8(r.off + 8 * q, (uint32_t)k2));
                 const uint32_t nk = __reduce_add_sync(0xFFFFFFFFu, ck);
                 const uint32_t sk = kPlaneBytes * k2 + (uint32_t)pad16(nk);
                 if (sk <= bsize) {
@@ -140,101 +168,102 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk) {
     return pl;
 }
 
-// 4 flag bytes (0x80 each) -> 4 bits in element order
-__device__ __forceinline__ uint32_t gather_msb4(uint32_t f) { return ((f & 0x80808080u) * 0x00204081u) >> 28; }
-
-// Phase B: write the full chunk at `chunk` (shared memory) to `dst` (global,
-// 16-byte aligned) following `pl`.  One warp.
-__device__ __forceinline__ void write_chunk_warp(const uint8_t* chunk, const ChunkPlan& pl, uint8_t* dst) {
+// Escape bytes of a packed chunk, in bit-plane order: plane word 32 q + l,
+// then bit.  e0..e3: this lane's escape bits of quarters 0..3, i.e. exactly
+// the sentinel bits of its plane words; offw: this lane's 32 offset words,
+// word m at offw[32 m] (shared memory, one column per lane).
+__device__ __forceinline__ void write_escapes(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3, const uint32_t* offw,
+                                              uint32_t base, uint32_t n_esc, uint8_t* esc_out) {
     const uint32_t lane = threadIdx.x & 31;
+    // escapes before word (q, lane): all of quarters < q, then lanes < lane of quarter q
+    const uint32_t c01 = __popc(e0) | (__popc(e1) << 16), c23 = __popc(e2) | (__popc(e3) << 16);
+    uint32_t a = c01, b = c23;  // 16-bit fields: at most 1024 per quarter
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t ta = __shfl_up_sync(0xFFFFFFFFu, a, d), tb = __shfl_up_sync(0xFFFFFFFFu, b, d);
+        if (lane >= (uint32_t)d) {
+            a += ta;
+            b += tb;
+        }
+    }
+    const uint32_t ta = __shfl_sync(0xFFFFFFFFu, a, 31), tb = __shfl_sync(0xFFFFFFFFu, b, 31);
+    const uint32_t t0 = ta & 0xFFFFu, t1 = ta >> 16, t2 = tb & 0xFFFFu;
+    const uint32_t ea = a - c01, eb = b - c23;  // exclusive over lanes
+    const uint32_t qb[4] = {ea & 0xFFFFu, t0 + (ea >> 16), t0 + t1 + (eb & 0xFFFFu), t0 + t1 + t2 + (eb >> 16)};
+    const uint32_t em[4] = {e0, e1, e2, e3};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t rest = em[q];
+        while (rest) {
+            const uint32_t bit = __ffs(rest) - 1;
+            rest &= rest - 1;
+            const uint32_t idx = qb[q] + __popc(em[q] & ((1u << bit) - 1u));
+            const uint32_t ow = offw[32 * (8 * q + (bit & 7))];
+            if (idx < n_esc) esc_out[idx] = (uint8_t)(((ow >> (8 * (bit >> 3))) & 0xFFu) + base);
+        }
+    }
+}
+
+// Phase B: write the full chunk held in `r` (offsets) and `chunk` (its
+// sign+fraction plane, in shared memory) to `dst` (global, 16-byte aligned)
+// following `pl`.  One warp.  A packed chunk's byte plane leaves by one bulk
+// (TMA) store issued by lane 0, which waits until it has read `chunk` before
+// returning; a raw chunk's values are rebuilt in registers.  Uses the second
+// half of `chunk` (consumed input) as scratch.
+__device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const ChunkPlan& pl, uint8_t* chunk,
+                                                 uint8_t* dst) {
+    const uint32_t lane = threadIdx.x & 31;
+    uint8_t* body = dst + kChunkHeaderBytes;
     if (lane == 0)
         *reinterpret_cast<uint4*>(dst) =
             make_uint4((pl.raw ? kModeRaw : kModePacked) | (pl.k << 8) | (pl.base << 16), kChunkElems | (pl.n_esc << 16),
                        pl.bytes, 0u);
-    uint8_t* body = dst + kChunkHeaderBytes;
-    if (pl.raw) {
+    if (pl.raw) {  // rebuild the values from the offsets and the sign+fraction plane
+        const uint32_t base4 = pl.emin * 0x01010101u;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<uint4*>(body + 512 * j + 16 * lane) = lds_row(chunk, j, lane);
+        for (int j = 0; j < 16; ++j) {
+            const uint2 sv = *reinterpret_cast<const uint2*>(chunk + 256 * j + 8 * lane);
+            uint4 v;
+            join_quad(r.off[2 * j] + base4, sv.x, v.x, v.y);
+            join_quad(r.off[2 * j + 1] + base4, sv.y, v.z, v.w);
+            *reinterpret_cast<uint4*>(body + 512 * j + 16 * lane) = v;
+        }
         return;
     }
+    // the sign+fraction plane was written by generic stores: order them before
+    // the bulk copy's reads
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        bulk_store(body, chunk, kSmPlaneBytes);
+        bulk_commit();
+    }
     const uint32_t k = pl.k;
-    const uint32_t base4 = pl.base * 0x01010101u;
-    const bool escapes = pl.n_esc > 0;
-    const uint32_t sent = (1u << k) - 1u;
-    const uint32_t kb = (128u - sent) * 0x01010101u;
-    uint8_t* esc_out = body + kSmPlaneBytes + kPlaneBytes * k;
-    uint32_t esc_done = 0;  // escapes written for the rows before (warp-uniform)
+    if (k > 0) {
+        const bool escapes = pl.n_esc > 0;
+        uint32_t em[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // escaped elements carry the sentinel (all k bits set): OR their
+            // bits into every plane; the offset bits of the others are their codes
+            if (escapes) em[q] = (k == pl.k1) ? r.esc[q] : escape_bits8(r.off + 8 * q, k);
+            uint8_t* col = body + kSmPlaneBytes + 4 * (32 * q + lane);
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-        uint32_t E[8], S[8];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const uint4 v = lds_row(chunk, 4 * q + jj, lane);
-            split_quad(v.x, v.y, E[2 * jj], S[2 * jj]);
-            split_quad(v.z, v.w, E[2 * jj + 1], S[2 * jj + 1]);
-            *reinterpret_cast<uint2*>(body + 256 * (4 * q + jj) + 8 * lane) = make_uint2(S[2 * jj], S[2 * jj + 1]);
+            for (uint32_t p = 0; p < k; ++p)
+                *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = pack_plane(r.off + 8 * q, p) | em[q];
         }
-        if (k == 0) continue;
-        uint32_t code[8], emask = 0;  // emask: escaped elements, bit 8 jj + s
+        if (escapes) {
+            uint32_t* offw = reinterpret_cast<uint32_t*>(chunk + kSmPlaneBytes) + lane;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const uint32_t off = E[m] - base4;
-            if (escapes) {
-                const uint32_t f = ge_flags(off, kb);
-                const uint32_t ff = flags_to_mask(f);
-                code[m] = (off & ~ff) | ((sent * 0x01010101u) & ff);
-                emask |= gather_msb4(f) << (4 * m);
-            } else {
-                code[m] = off;
-            }
-        }
-        uint32_t W[7];
-        pack_planes_k((int)k, code, W);
-#pragma unroll
-        for (int p = 0; p < 7; ++p)
-            if ((uint32_t)p < k)
-                *reinterpret_cast<uint32_t*>(body + kSmPlaneBytes + kPlaneBytes * p + 4 * (32 * q + lane)) = W[p];
-        if (escapes && __any_sync(0xFFFFFFFFu, emask != 0u)) {
-            // ascending element order: row j = 4q + jj, then lane, then s
-            const uint32_t c01 = __popc(emask & 0xFFu) | (__popc(emask & 0xFF00u) << 16);
-            const uint32_t c23 = __popc(emask & 0xFF0000u) | (__popc(emask >> 24) << 16);
-            uint32_t a = c01, b = c23;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t ta = __shfl_up_sync(0xFFFFFFFFu, a, d), tb = __shfl_up_sync(0xFFFFFFFFu, b, d);
-                if (lane >= (uint32_t)d) {
-                    a += ta;
-                    b += tb;
-                }
-            }
-            const uint32_t ta = __shfl_sync(0xFFFFFFFFu, a, 31), tb = __shfl_sync(0xFFFFFFFFu, b, 31);
-            const uint32_t row_tot[4] = {ta & 0xFFFFu, ta >> 16, tb & 0xFFFFu, tb >> 16};
-            const uint32_t ea = a - c01, eb = b - c23;  // exclusive over lanes
-            uint32_t row_base[4];
-            row_base[0] = esc_done + (ea & 0xFFFFu);
-            row_base[1] = esc_done + row_tot[0] + (ea >> 16);
-            row_base[2] = esc_done + row_tot[0] + row_tot[1] + (eb & 0xFFFFu);
-            row_base[3] = esc_done + row_tot[0] + row_tot[1] + row_tot[2] + (eb >> 16);
-            esc_done += row_tot[0] + row_tot[1] + row_tot[2] + row_tot[3];
-            uint32_t rest = emask;
-            while (rest) {
-                const uint32_t bit = __ffs(rest) - 1;
-                rest &= rest - 1;
-                const uint32_t jj = bit >> 3, m = bit >> 2, b = bit & 3;
-                uint32_t rbase = 0, eword = 0;  // select without run-time register indexing
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    if ((uint32_t)r == jj) rbase = row_base[r];
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    if ((uint32_t)r == m) eword = E[r];
-                const uint32_t idx = rbase + __popc(emask & ((1u << bit) - 1u) & (0xFFu << (8 * jj)));
-                if (idx < pl.n_esc) esc_out[idx] = (uint8_t)(eword >> (8 * b));
-            }
+            for (int m = 0; m < 32; ++m) offw[32 * m] = r.off[m];
+            __syncwarp();
+            uint8_t* esc_out = body + kSmPlaneBytes + kPlaneBytes * k;
+            write_escapes(em[0], em[1], em[2], em[3], offw, pl.emin, pl.n_esc, esc_out);
+            if (lane < 16 && pl.n_esc + lane < pad16(pl.n_esc)) esc_out[pl.n_esc + lane] = 0;
         }
     }
-    if (escapes && lane < 16 && pl.n_esc + lane < pad16(pl.n_esc)) esc_out[pl.n_esc + lane] = 0;
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
 }
 
 // The partial last chunk (n_c < 4096 elements) is stored raw (section 5,

@@ -178,12 +178,13 @@ __global__ void __launch_bounds__(32 * kRGroup, 3) reduce_kernel(ReduceInputs in
 
     // encode: warp w sizes and writes output chunk c0 + w
     const uint64_t c = c0 + q;
-    const uint8_t* chunk = park + (size_t)q * 2 * kChunkElems;
+    uint8_t* chunk = park + (size_t)q * 2 * kChunkElems;
     const uint64_t n_full = so.n_elems / kChunkElems;
     ChunkPlan pl{};
+    ChunkRegs regs;
     uint32_t bytes = 0;
     if (c < n_full) {
-        pl = plan_chunk_warp(chunk);
+        pl = plan_chunk_warp(chunk, regs);
         bytes = pl.bytes;
     } else if (c < so.n_chunks) {
         bytes = tail_chunk_bytes((uint32_t)(so.n_elems - c * kChunkElems));
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(32 * kRGroup, 3) reduce_kernel(ReduceInputs in
     }
     uint8_t* dst = so.out + off;
     if (c < n_full) {
-        write_chunk_warp(chunk, pl, dst);
+        write_chunk_warp(regs, pl, chunk, dst);
     } else {
         const uint16_t* vals = reinterpret_cast<const uint16_t*>(chunk);
         write_tail_chunk_warp([vals](uint32_t e) { return vals[e]; }, (uint32_t)(so.n_elems - c * kChunkElems), dst);

@@ -49,6 +49,8 @@ def _bind(path: str):
     lib.oracle_compress_bound.restype = sz
     lib.oracle_plane_position.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_uint),
                                           ctypes.POINTER(ctypes.c_uint)]
+    lib.oracle_plane_element.argtypes = [ctypes.c_uint, ctypes.c_uint]
+    lib.oracle_plane_element.restype = ctypes.c_uint
     lib.oracle_chunk_choice.argtypes = [u16p, sz] + [ctypes.POINTER(ctypes.c_uint)] * 3 + \
         [ctypes.POINTER(sz)] * 2
     lib.oracle_encode_chunk.argtypes = [u16p, sz, u8p, ctypes.POINTER(sz)]
@@ -133,6 +135,10 @@ def plane_position(i: int) -> tuple[int, int]:
     w, b = ctypes.c_uint(), ctypes.c_uint()
     _load().oracle_plane_position(i, ctypes.byref(w), ctypes.byref(b))
     return w.value, b.value
+
+
+def plane_element(word: int, bit: int) -> int:
+    return int(_load().oracle_plane_element(word, bit))
 
 
 def chunk_choice(x) -> dict:

@@ -28,7 +28,8 @@
  *   - chunks of 4096 elements; the exponent table of a chunk is its exact
  *     minimum exponent `base` plus a code width k (0..7): element i stores
  *     code = e_i - base when that is below S = 2^k - 1, else the sentinel S
- *     and its raw exponent goes to an escape list (ascending element order);
+ *     and its raw exponent goes to an escape list (in bit-plane order: the
+ *     order in which the elements' bits appear in the planes);
  *   - k minimises 512*k + pad16(#escapes); ties go to the smaller k; the
  *     chunk is stored raw when no k beats the 4096 bytes of exponents;
  *   - the last chunk, when shorter than 4096 elements, is stored raw;
@@ -177,6 +178,15 @@ void oracle_plane_position(unsigned i, unsigned *word, unsigned *bit)
     *bit = 8 * (s % 4) + 2 * (j % 4) + s / 4;
 }
 
+/* The element at bit `bit` of plane word `word` (inverse of the above):
+ * with q = word / 32, l = word % 32, b = bit / 8, m = bit % 8:
+ *   i = 256 * (4 q + m / 2) + 8 l + 4 (m % 2) + b */
+unsigned oracle_plane_element(unsigned word, unsigned bit)
+{
+    unsigned q = word / 32, l = word % 32, b = bit / 8, m = bit % 8;
+    return 256 * (4 * q + m / 2) + 8 * l + 4 * (m % 2) + b;
+}
+
 /* ------------------------------------------------------------------ */
 /* encoding choice of one full chunk (section 4.3)                     */
 /* ------------------------------------------------------------------ */
@@ -293,19 +303,15 @@ static size_t write_chunk(const uint16_t *x, size_t n_c, chunk_choice ch, uint8_
     for (size_t i = 0; i < n_c; i++)
         body[i] = (uint8_t)sign_fraction_of(x[i]);
 
-    /* bit-planes and escapes */
+    /* bit-planes */
     uint8_t *planes = body + SM_PLANE_BYTES;
     uint8_t *escapes = planes + (size_t)BIT_PLANE_BYTES * ch.k;
-    size_t n_esc = 0;
     if (ch.k > 0) {
         unsigned sentinel = (1u << ch.k) - 1;
         for (unsigned i = 0; i < n_c; i++) {
-            unsigned e = exponent_of(x[i]);
-            unsigned code = e - ch.base;
-            if (code >= sentinel) {
+            unsigned code = exponent_of(x[i]) - ch.base;
+            if (code >= sentinel)
                 code = sentinel;
-                escapes[n_esc++] = (uint8_t)e;
-            }
             unsigned word, bit;
             oracle_plane_position(i, &word, &bit);
             for (unsigned p = 0; p < ch.k; p++) {
@@ -315,8 +321,27 @@ static size_t write_chunk(const uint16_t *x, size_t n_c, chunk_choice ch, uint8_
                 }
             }
         }
+        /* escapes: raw exponents of the elements whose code is the sentinel,
+         * in bit-plane order (word by word, bit by bit) */
+        unsigned element_at[CHUNK_ELEMS];
+        for (unsigned pos = 0; pos < CHUNK_ELEMS; pos++)
+            element_at[pos] = CHUNK_ELEMS; /* none: only if the layout were not a permutation */
+        for (unsigned i = 0; i < n_c; i++) {
+            unsigned word, bit;
+            oracle_plane_position(i, &word, &bit);
+            if (word < 128 && bit < 32)
+                element_at[32 * word + bit] = i;
+        }
+        size_t n_esc = 0;
+        for (unsigned pos = 0; pos < CHUNK_ELEMS; pos++) {
+            if (element_at[pos] >= n_c)
+                continue;
+            unsigned e = exponent_of(x[element_at[pos]]);
+            if (e - ch.base >= sentinel)
+                escapes[n_esc++] = (uint8_t)e;
+        }
+        (void)n_esc; /* equals ch.n_esc by construction of the count */
     }
-    (void)n_esc; /* equals ch.n_esc by construction of the count */
     return ch.bytes;
 }
 
@@ -406,9 +431,9 @@ static int read_chunk(const uint8_t *chunk, size_t chunk_size, size_t n_c, uint1
     const uint8_t *escapes = planes + (size_t)BIT_PLANE_BYTES * k;
     unsigned sentinel = (1u << k) - 1;
     size_t used = 0;
-    for (unsigned i = 0; i < n_c; i++) {
-        unsigned word, bit, code = 0;
-        oracle_plane_position(i, &word, &bit);
+    /* visit the elements in bit-plane order, the order of the escape list */
+    for (unsigned pos = 0; pos < CHUNK_ELEMS; pos++) {
+        unsigned word = pos / 32, bit = pos % 32, code = 0;
         for (unsigned p = 0; p < k; p++) {
             uint8_t byte = planes[(size_t)BIT_PLANE_BYTES * p + 4 * (size_t)word + bit / 8];
             code |= ((byte >> (bit % 8)) & 1u) << p;
@@ -423,6 +448,9 @@ static int read_chunk(const uint8_t *chunk, size_t chunk_size, size_t n_c, uint1
             if (e > 255)
                 return ORC_ERR_CORRUPT;
         }
+        unsigned i = oracle_plane_element(word, bit);
+        if (i >= n_c)
+            return ORC_ERR_CORRUPT;
         x[i] = join_bf16(body[i], e);
     }
     if (used != n_esc)

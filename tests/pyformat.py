@@ -16,8 +16,8 @@ Format (little endian):
   raw     = the n_c bf16 values
   packed  = 4096 sign+fraction bytes ((b >> 8) & 0x80 | b & 0x7F),
             k bit-planes of 128 u32 words, escape bytes (raw exponents of
-            the elements whose code is the sentinel 2^k - 1, ascending
-            element order)
+            the elements whose code is the sentinel 2^k - 1, in bit-plane
+            order: by word, then by bit)
   element i = 256 j + 8 l + s (j < 16, l < 32, s < 8) keeps bit p of its
   code in plane p, word 32 (j // 4) + l, bit 8 (s % 4) + 2 (j % 4) + s // 4.
 """
@@ -76,7 +76,8 @@ def encode_chunk_at(x: np.ndarray, k: int | None) -> bytes | None:
         sent = (1 << k) - 1
         code = np.minimum(off, sent)
         escaped = off >= sent
-        esc = expo[escaped].astype(np.uint8).tobytes()
+        order = np.argsort(32 * WORD_OF + BIT_OF)  # elements in bit-plane order
+        esc = expo[order][escaped[order]].astype(np.uint8).tobytes()
         words = np.zeros((k, 128), np.uint64)
         for p in range(k):
             bits = ((code >> p) & 1).astype(np.uint64) << BIT_OF.astype(np.uint64)
@@ -140,7 +141,8 @@ def decode_chunk(buf: bytes, n_c: int) -> np.ndarray:
         code |= ((words[p, WORD_OF] >> BIT_OF.astype(np.uint32)) & 1) << p
     expo = base + code
     if k > 0:
-        where = np.nonzero(code == (1 << k) - 1)[0]
+        order = np.argsort(32 * WORD_OF + BIT_OF)  # elements in bit-plane order
+        where = order[code[order] == (1 << k) - 1]
         if where.size != n_esc:
             raise Corrupt("escape count")
         expo[where] = esc

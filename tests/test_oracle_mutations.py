@@ -25,7 +25,8 @@ MUTATIONS = [
      "SM_PLANE_BYTES + (size_t)BIT_PLANE_BYTES * k + n_esc;"),
     ("escape_padding_ignored_in_choice", "size_t size = (size_t)BIT_PLANE_BYTES * k + pad16(n_esc);",
      "size_t size = (size_t)BIT_PLANE_BYTES * k + n_esc;"),
-    ("escape_threshold_off_by_one", "if (code >= sentinel) {", "if (code > sentinel) {"),
+    ("escape_threshold_off_by_one", "if (e - ch.base >= sentinel)", "if (e - ch.base > sentinel)"),
+    ("escapes_in_element_order", "unsigned e = exponent_of(x[element_at[pos]]);", "unsigned e = exponent_of(x[pos]);"),
     ("count_threshold_off_by_one", "count_at_or_above(x, n_c, emin, sentinel);",
      "count_at_or_above(x, n_c, emin, sentinel + 1);"),
     ("rounding_half_up", "u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0x8000u;"),

@@ -211,17 +211,30 @@ def test_single_escape_lands_where_defined(orc):
         assert enc[16 + 4096 + 512] == 127 and enc[16 + 4096 + 513:] == bytes(15)
 
 
-def test_escapes_in_ascending_element_order(orc):
+def test_escapes_in_bit_plane_order(orc):
+    """Escapes follow the order of their elements' bits in the planes: plane
+    word (q, l) = 32 q + l, then bit 8 b + m.  Hand-placed: element 9 (row 0,
+    lane 1, s 1: word 1, bit 8), element 3 (lane 0, s 3: word 0, bit 24),
+    element 700 (row 2, lane 23, s 4: word 23, bit 5), element 2048 (row 8:
+    word 64, bit 0), element 4000 (row 15, lane 20, s 0: word 3*32+20 = 116,
+    bit 2*(15 % 4) = 6)."""
     x = np.full(CHUNK, 0x3F00, np.uint16)
-    pos = [4000, 3, 700, 2048, 9]
-    vals = [130, 140, 150, 160, 170]
-    for p, e in zip(pos, vals):
+    placed = {9: 130, 3: 140, 700: 150, 2048: 160, 4000: 170}
+    for p, e in placed.items():
         x[p] = e << 7
     enc = orc.encode_chunk(x)
     _, k, base, _, _, n_esc, _, _ = struct.unpack_from("<BBBBHHII", enc, 0)
     assert (k, base, n_esc) == (1, 126, 5)
-    order = [e for _, e in sorted(zip(pos, vals))]
-    assert list(enc[16 + 4096 + 512:16 + 4096 + 512 + 5]) == order
+    # by (word, bit): 3 (0, 24), 9 (1, 8), 700 (23, 5), 2048 (64, 0), 4000 (116, 6)
+    assert list(enc[16 + 4096 + 512:16 + 4096 + 512 + 5]) == [140, 130, 150, 160, 170]
+    for i, (w, b) in {3: (0, 24), 9: (1, 8), 700: (23, 5), 2048: (64, 0), 4000: (116, 6)}.items():
+        assert orc.plane_position(i) == (w, b)
+        assert orc.plane_element(w, b) == i
+
+
+def test_plane_element_inverts_plane_position(orc):
+    for i in range(CHUNK):
+        assert orc.plane_element(*orc.plane_position(i)) == i
 
 
 # ---------------------------------------------------------------- reduce arithmetic
