@@ -196,6 +196,28 @@ __device__ __forceinline__ uint32_t count_flags8(const uint32_t f[8]) {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funnelshift_r(x, x, n); }
 
+// All 8 planes at once: 8 quads hold, per byte lane b, an 8x8 bit matrix
+// (row m = quad m, column p = bit p); transposing it turns codes into plane
+// words and back (plane p = row p).  Recursive block transpose by three
+// rounds of masked delta swaps (4x4, 2x2, 1x1 blocks), the same for every
+// byte lane since no swap crosses a byte.
+__device__ __forceinline__ void delta_swap(uint32_t& a, uint32_t& b, uint32_t s, uint32_t mask) {
+    const uint32_t t = ((a >> s) ^ b) & mask;
+    b ^= t;
+    a ^= t << s;
+}
+__device__ __forceinline__ void transpose8x8x4(uint32_t* v) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) delta_swap(v[m], v[m + 4], 4, 0x0F0F0F0Fu);
+#pragma unroll
+    for (int m = 0; m < 8; m += 4) {
+        delta_swap(v[m], v[m + 2], 2, 0x33333333u);
+        delta_swap(v[m + 1], v[m + 3], 2, 0x33333333u);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; m += 2) delta_swap(v[m], v[m + 1], 1, 0x55555555u);
+}
+
 // Plane p of 8 quads of codes (bits of codes above p are ignored).
 __device__ __forceinline__ uint32_t pack_plane(const uint32_t* code, uint32_t p) {
     uint32_t acc = 0;
@@ -324,6 +346,35 @@ __device__ __forceinline__ ChunkView locate_chunk(const uint8_t* s, uint64_t in_
     if (c == 0 && off != start) return v;
     if ((off & 15) != 0 || end <= off || end > total || off < start) return v;
     // the bulk copy needs a size that is a multiple of 16; every valid chunk is
+    if (end - off > kMaxChunkBytes || ((end - off) & 15) != 0) return v;
+    v.offset = off;
+    v.bytes = (uint32_t)(end - off);
+    v.ok = 1;
+    return v;
+}
+
+// One thread: check a stream's header against (n_elems, in_bytes); returns
+// the stream's total_bytes, or 0 if the header is not valid.
+__device__ __forceinline__ uint64_t stream_total(const uint8_t* s, uint64_t in_bytes, uint64_t n_elems,
+                                                 uint64_t n_chunks) {
+    const uint64_t start = data_start(n_chunks);
+    if (in_bytes < start) return 0;
+    const uint32_t w0 = ld_u32_aligned(s + 0), w1 = ld_u32_aligned(s + 4), w2 = ld_u32_aligned(s + 8);
+    if (w0 != kMagic || w1 != (kVersion | (kDtypeBf16 << 16)) || w2 != kChunkElems) return 0;
+    if (ld_u64_aligned(s + 16) != n_elems || ld_u64_aligned(s + 24) != n_chunks) return 0;
+    const uint64_t total = ld_u64_aligned(s + 32);
+    if (total > in_bytes || total < start) return 0;
+    return total;
+}
+// One thread: locate chunk c of a stream whose header passed stream_total.
+__device__ __forceinline__ ChunkView locate_in_stream(const uint8_t* s, uint64_t total, uint64_t n_chunks, uint64_t c) {
+    ChunkView v{0, 0, 0};
+    if (total == 0) return v;
+    const uint64_t start = data_start(n_chunks);
+    const uint64_t off = ld_u64_aligned(s + kStreamHeaderBytes + 8 * c);
+    const uint64_t end = (c + 1 < n_chunks) ? ld_u64_aligned(s + kStreamHeaderBytes + 8 * (c + 1)) : total;
+    if (c == 0 && off != start) return v;
+    if ((off & 15) != 0 || end <= off || end > total || off < start) return v;
     if (end - off > kMaxChunkBytes || ((end - off) & 15) != 0) return v;
     v.offset = off;
     v.bytes = (uint32_t)(end - off);

@@ -248,9 +248,19 @@ __device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const Chunk
             // bits into every plane; the offset bits of the others are their codes
             if (escapes) em[q] = (k == pl.k1) ? r.esc[q] : escape_bits8(r.off + 8 * q, k);
             uint8_t* col = body + kSmPlaneBytes + 4 * (32 * q + lane);
+            if (k >= 4) {  // one 8x8 bit transpose makes every plane
+                uint32_t W[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) W[m] = r.off[8 * q + m];
+                transpose8x8x4(W);
+#pragma unroll
+                for (int p = 0; p < 8; ++p)
+                    if ((uint32_t)p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = W[p] | em[q];
+            } else {
 #pragma unroll 1
-            for (uint32_t p = 0; p < k; ++p)
-                *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = pack_plane(r.off + 8 * q, p) | em[q];
+                for (uint32_t p = 0; p < k; ++p)
+                    *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = pack_plane(r.off + 8 * q, p) | em[q];
+            }
         }
         if (escapes) {
             uint32_t* offw = reinterpret_cast<uint32_t*>(chunk + kSmPlaneBytes) + lane;

@@ -24,11 +24,6 @@ constexpr int kStages = 4;
 constexpr size_t kParkBytes = (size_t)kRGroup * 2 * kChunkElems;
 constexpr size_t kReduceSmemBytes = kParkBytes + (size_t)kStages * kMaxChunkBytes;
 
-__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 // binary32 pair -> bf16 pair, round to nearest even (hi lane from the upper word)
 __device__ __forceinline__ uint32_t round_pair_bf16(uint64_t v) {
     uint32_t d;
@@ -42,11 +37,6 @@ __device__ __forceinline__ uint32_t canonical_nan_pair(uint32_t d) {
     const uint32_t mask = (nan >> 15) * 0xFFFFu;
     return (d & ~mask) | (0x7FC07FC0u & mask);
 }
-// bf16 pair -> binary32 pair (exact)
-__device__ __forceinline__ uint64_t widen_pair(uint32_t p) {
-    return (uint64_t)(p << 16) | ((uint64_t)(p & 0xFFFF0000u) << 32);
-}
-
 __global__ void __launch_bounds__(32 * kRGroup, 3) reduce_kernel(ReduceInputs inputs, int R, StreamOut so) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* park = smem;                // kRGroup rounded bf16 chunks
