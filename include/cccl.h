@@ -29,6 +29,10 @@
  *     packed body     4096 sign+fraction bytes, k bit-planes of 512 bytes,
  *                     n_esc escape bytes, zero padding to 16
  *     raw body        n_c bf16 values, zero padding to 16
+ *   Bit-plane p (p = 0 the code's least significant bit) is 128 u32 words;
+ *   element i = 256 j + 8 l + s (j < 16, l < 32, s < 8) keeps its bit in
+ *   word 32 (j / 4) + l, bit 8 (s % 4) + 2 (j % 4) + s / 4.  The escape bytes
+ *   follow bit-plane order: by word, then by bit.
  *   A full chunk is packed with width k (offsets e - base below 2^k - 1 are
  *   codes, the rest escape with their raw exponent) when that is smaller
  *   than its raw form; the last chunk, when shorter than 4096 elements, is
