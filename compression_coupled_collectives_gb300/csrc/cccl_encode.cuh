@@ -35,21 +35,16 @@ struct ChunkPlan {
     uint32_t k;      // code width
     uint32_t base;   // header base: minimum exponent (0 when raw)
     uint32_t n_esc;  // escapes at width k
-    uint32_t emin;   // minimum exponent (kept for raw chunks too)
-    uint32_t k1;     // width whose escape bits are kept in ChunkRegs::esc
     uint32_t bytes;  // chunk size, header included
 };
 
 // One lane's share of a full chunk, kept in registers between sizing and
-// writing: its 128 elements as 32 quads of exponent offsets from the chunk
-// minimum, quad 8 q + m holding row 4 q + m / 2, elements 4 (m % 2) .. +3 of
-// the lane's 8.  esc[q] holds the escape bits at width k1 in bit-plane layout
-// (bit 8 b + m: byte b of quad 8 q + m).  The sign+fraction bytes wait in
-// shared memory instead: sizing writes them over the first half of the
-// chunk's own (consumed) input slot, in stream order.
+// writing: the bit-planes of its four plane words.  P[8 q + p] is plane p of
+// word 32 q + l (lane l), i.e. bit p of the exponent offsets (e - base) of
+// the 32 elements that word covers: bit 8 b + m holds element 256 (4 q + m / 2)
+// + 8 l + 4 (m % 2) + b.  Sign and fraction stay in the staged chunk.
 struct ChunkRegs {
-    uint32_t off[32];
-    uint32_t esc[4];
+    uint32_t P[32];
 };
 
 // This lane's 4 pair-words of row j (elements 256 j + 8 l .. + 7).
@@ -57,104 +52,86 @@ __device__ __forceinline__ uint4 lds_row(const uint8_t* chunk, uint32_t j, uint3
     return *reinterpret_cast<const uint4*>(chunk + 512 * j + 16 * lane);
 }
 
-// Escape bits (bit-plane layout) of 8 quads of offsets at width k, and their
-// number: the bits of element (m, b) sit at 8 b + m.
-__device__ __forceinline__ uint32_t escape_bits8(const uint32_t* off, uint32_t k) {
-    const uint32_t kb = (128u - ((1u << k) - 1u)) * 0x01010101u;
-    uint32_t acc = 0;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) acc |= ge_flags(off[m], kb) >> (7 - m);
-    return acc;
+// Sign+fraction bytes of 4 values held as two pair-words (section 4.1).
+__device__ __forceinline__ uint32_t sign_fraction_quad(uint32_t A, uint32_t B) {
+    const uint32_t lo = __byte_perm(A, B, 0x6420), hi = __byte_perm(A, B, 0x7531);
+    return (lo & 0x7F7F7F7Fu) | (hi & 0x80808080u);
 }
 
-// Phase A: exponent table and size of the full chunk at `chunk` (8192 bytes
-// of bf16 in shared memory), leaving the offsets in `r` and the chunk's
-// sign+fraction plane over the first 4096 bytes of `chunk`.  One warp; every
-// lane returns the same plan.
-__device__ __forceinline__ ChunkPlan plan_chunk_warp(uint8_t* chunk, ChunkRegs& r) {
+// Escape bits at width k (1..7) of one plane word from its 8 planes: the
+// offset is at least 2^k - 1 when a bit at or above k is set (the offset
+// reaches 2^k) or when bits 0..k-1 are all set.
+__device__ __forceinline__ uint32_t escape_word(const uint32_t* P, uint32_t k) {
+    uint32_t lowAnd = 0xFFFFFFFFu, highOr = 0u;
+#pragma unroll
+    for (uint32_t p = 0; p < 8; ++p) {
+        if (p < k)
+            lowAnd &= P[p];
+        else
+            highOr |= P[p];
+    }
+    return lowAnd | highOr;
+}
+
+// Phase A: exponent table and size of the full chunk staged at `chunk` (8192
+// bytes of bf16 in shared memory, left untouched), leaving the bit-planes of
+// the exponent offsets in `r`.  One warp; every lane returns the same plan.
+//
+// The sizes of every width come from the planes at once: with
+// low_k = AND of planes 0..k-1 and high_k = OR of planes k..7, the escapes at
+// width k are exactly low_k | high_k, so seven popcounts per plane word give
+// the seven escape counts (section 4.3's per-block table, exact).
+__device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk, ChunkRegs& r) {
     const uint32_t lane = threadIdx.x & 31;
-    // pass 1: exponent extremes
+    // exponent quads (r.P[2 j + h]: row j, elements 4 h .. 4 h + 3 of the
+    // lane's 8) and the exponent extremes.  Doubling a pair-word puts each
+    // value's exponent in the high byte of its 16-bit lane (a low value's sign
+    // lands in the high lane's low byte, which cannot change its high byte).
     uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const uint4 v = lds_row(chunk, j, lane);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            // doubling drops each value's sign; a low lane's sign lands in the
-            // high lane's last fraction bit, which cannot move its exponent
-            const uint32_t mag2 = w[i] << 1;
-            mn = vmin_u16x2(mn, mag2);
-            mx = vmax_u16x2(mx, mag2);
-        }
+        const uint32_t t0 = v.x << 1, t1 = v.y << 1, t2 = v.z << 1, t3 = v.w << 1;
+        mn = vmin_u16x2(mn, vmin_u16x2(vmin_u16x2(t0, t1), vmin_u16x2(t2, t3)));
+        mx = vmax_u16x2(mx, vmax_u16x2(vmax_u16x2(t0, t1), vmax_u16x2(t2, t3)));
+        r.P[2 * j] = __byte_perm(t0, t1, 0x7531);
+        r.P[2 * j + 1] = __byte_perm(t2, t3, 0x7531);
     }
-    const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, min(mn & 0xFFFFu, mn >> 16) >> 8);
-    const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, max(mx & 0xFFFFu, mx >> 16) >> 8);
+    const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
+    const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
     const uint32_t base4 = emin * 0x01010101u;
-    // pass 2: split every row; its sign+fraction bytes go to their place in
-    // the stream's byte plane (row j -> bytes 256 j ..), over input already read
+    uint32_t cnt[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // escapes at width k (k = 1..7)
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const uint4 v = lds_row(chunk, j, lane);
-        uint32_t s0, s1;
-        split_quad(v.x, v.y, r.off[2 * j], s0);
-        split_quad(v.z, v.w, r.off[2 * j + 1], s1);
-        r.off[2 * j] -= base4;  // no borrow: every exponent >= emin
-        r.off[2 * j + 1] -= base4;
-        __syncwarp();  // all lanes have read row j (and row j / 2 before it)
-        *reinterpret_cast<uint2*>(chunk + 256 * j + 8 * lane) = make_uint2(s0, s1);
+    for (int q = 0; q < 4; ++q) {
+        uint32_t* P = r.P + 8 * q;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) P[m] -= base4;  // no borrow: every exponent >= emin
+        transpose8x8x4(P);                          // quads of offsets -> planes
+        uint32_t high[8];
+        high[7] = P[7];
+#pragma unroll
+        for (int k = 6; k >= 1; --k) high[k] = high[k + 1] | P[k];
+        uint32_t low = P[0];
+#pragma unroll
+        for (int k = 1; k <= 7; ++k) {
+            cnt[k] += __popc(low | high[k]);
+            if (k < 7) low &= P[k];
+        }
     }
-
-    ChunkPlan pl{0u, 0u, emin, 0u, emin, 0u, 0u};
-    const uint32_t range = emax - emin;
+    ChunkPlan pl{0u, 0u, emin, 0u, 0u};
     uint32_t best = 0;
+    if (emax > emin) {
+        best = 0xFFFFFFFFu;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) r.esc[q] = 0;
-    if (range > 0) {
-        const uint32_t kfull = 32 - __clz(range + 1);  // 2..9
-        int bk = -1;
-        uint32_t bsize = 0xFFFFFFFFu, besc = 0;
-        if (kfull <= 7) {
-            bk = (int)kfull;
-            bsize = kPlaneBytes * kfull;
-        }
-        // widths below k1 can only win when 512 k + pad16(n_esc(k1)) does not
-        // exceed the best size (n_esc never shrinks as k shrinks)
-        const uint32_t k1 = min(kfull - 1, 7u);
-        pl.k1 = k1;
-        uint32_t c1 = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            r.esc[q] = escape_bits8(r.off + 8 * q, k1);
-            c1 += __popc(r.esc[q]);
-        }
-        const uint32_t n1 = __reduce_add_sync(0xFFFFFFFFu, c1);
-        const uint32_t s1 = kPlaneBytes * k1 + (uint32_t)pad16(n1);
-        if (s1 <= bsize) {  // k1 < kfull: a tie keeps the smaller width
-            bk = (int)k1;
-            bsize = s1;
-            besc = n1;
-        }
-        for (int kk = (int)k1 - 1; kk >= 1; --kk) {
-            if (kPlaneBytes * kk + (uint32_t)pad16(n1) > bsize) continue;  // bound grows with kk
-            // kk is the widest remaining candidate: evaluate kk down to 1
-            for (int k2 = kk; k2 >= 1; --k2) {
-                uint32_t ck = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) ck += __popc(escape_bits8(r.off + 8 * q, (uint32_t)k2));
-                const uint32_t nk = __reduce_add_sync(0xFFFFFFFFu, ck);
-                const uint32_t sk = kPlaneBytes * k2 + (uint32_t)pad16(nk);
-                if (sk <= bsize) {
-                    bk = k2;
-                    bsize = sk;
-                    besc = nk;
-                }
+        for (int k = 1; k <= 7; ++k) {
+            const uint32_t n = __reduce_add_sync(0xFFFFFFFFu, cnt[k]);
+            const uint32_t size = kPlaneBytes * k + (uint32_t)pad16(n);
+            if (size < best) {  // ascending k: a tie keeps the smaller width
+                best = size;
+                pl.k = (uint32_t)k;
+                pl.n_esc = n;
             }
-            break;
         }
-        pl.k = (uint32_t)bk;
-        pl.n_esc = besc;
-        best = bsize;
     }
     pl.raw = best >= kSmPlaneBytes ? 1u : 0u;
     if (pl.raw) {
@@ -168,16 +145,56 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp(uint8_t* chunk, ChunkRegs& 
     return pl;
 }
 
-// Escape bytes of a packed chunk, in bit-plane order: plane word 32 q + l,
-// then bit.  e0..e3: this lane's escape bits of quarters 0..3, i.e. exactly
-// the sentinel bits of its plane words; offw: this lane's 32 offset words,
-// word m at offw[32 m] (shared memory, one column per lane).
-__device__ __forceinline__ void write_escapes(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3, const uint32_t* offw,
-                                              uint32_t base, uint32_t n_esc, uint8_t* esc_out) {
+// Phase B: write the full chunk staged at `chunk` (unchanged since phase A)
+// with its planes `r` to `dst` (global, 16-byte aligned) following `pl`.  One
+// warp.  A raw chunk leaves by one bulk (TMA) store issued by lane 0, which
+// waits until the copy has read `chunk` before returning; the caller must
+// have ordered any generic writes of `chunk` before it with
+// fence.proxy.async.  A packed chunk is written by coalesced stores: the
+// sign+fraction plane, the k planes (escaped elements carry the sentinel,
+// all k bits set), then the escape bytes in bit-plane order, read back from
+// the staged values.
+__device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const ChunkPlan& pl, const uint8_t* chunk,
+                                                 uint8_t* dst) {
     const uint32_t lane = threadIdx.x & 31;
-    // escapes before word (q, lane): all of quarters < q, then lanes < lane of quarter q
-    const uint32_t c01 = __popc(e0) | (__popc(e1) << 16), c23 = __popc(e2) | (__popc(e3) << 16);
-    uint32_t a = c01, b = c23;  // 16-bit fields: at most 1024 per quarter
+    uint8_t* body = dst + kChunkHeaderBytes;
+    if (lane == 0)
+        *reinterpret_cast<uint4*>(dst) =
+            make_uint4((pl.raw ? kModeRaw : kModePacked) | (pl.k << 8) | (pl.base << 16), kChunkElems | (pl.n_esc << 16),
+                       pl.bytes, 0u);
+    if (pl.raw) {
+        if (lane == 0) {
+            bulk_store(body, chunk, 2 * kChunkElems);
+            bulk_commit();
+            bulk_wait_read();
+        }
+        __syncwarp();
+        return;
+    }
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+        const uint4 v = lds_row(chunk, j, lane);
+        *reinterpret_cast<uint2*>(body + 256 * j + 8 * lane) =
+            make_uint2(sign_fraction_quad(v.x, v.y), sign_fraction_quad(v.z, v.w));
+    }
+    const uint32_t k = pl.k;
+    if (k == 0) return;
+    uint32_t esc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t* P = r.P + 8 * q;
+        esc[q] = escape_word(P, k);
+        uint8_t* col = body + kSmPlaneBytes + 4 * (32 * q + lane);
+#pragma unroll
+        for (uint32_t p = 0; p < 8; ++p)
+            if (p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = P[p] | esc[q];
+    }
+    const uint32_t n_esc = pl.n_esc;
+    if (n_esc == 0) return;
+    // escapes before word (q, lane): all of quarters < q, then lanes < lane of
+    // quarter q (16-bit fields: at most 1024 per quarter)
+    const uint32_t c01 = __popc(esc[0]) | (__popc(esc[1]) << 16), c23 = __popc(esc[2]) | (__popc(esc[3]) << 16);
+    uint32_t a = c01, b = c23;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const uint32_t ta = __shfl_up_sync(0xFFFFFFFFu, a, d), tb = __shfl_up_sync(0xFFFFFFFFu, b, d);
@@ -189,91 +206,24 @@ __device__ __forceinline__ void write_escapes(uint32_t e0, uint32_t e1, uint32_t
     const uint32_t ta = __shfl_sync(0xFFFFFFFFu, a, 31), tb = __shfl_sync(0xFFFFFFFFu, b, 31);
     const uint32_t t0 = ta & 0xFFFFu, t1 = ta >> 16, t2 = tb & 0xFFFFu;
     const uint32_t ea = a - c01, eb = b - c23;  // exclusive over lanes
-    const uint32_t qb[4] = {ea & 0xFFFFu, t0 + (ea >> 16), t0 + t1 + (eb & 0xFFFFu), t0 + t1 + t2 + (eb >> 16)};
-    const uint32_t em[4] = {e0, e1, e2, e3};
+    const uint32_t first[4] = {ea & 0xFFFFu, t0 + (ea >> 16), t0 + t1 + (eb & 0xFFFFu), t0 + t1 + t2 + (eb >> 16)};
+    const uint16_t* vals = reinterpret_cast<const uint16_t*>(chunk);
+    uint8_t* esc_out = body + kSmPlaneBytes + kPlaneBytes * k;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint32_t rest = em[q];
-        while (rest) {
-            const uint32_t bit = __ffs(rest) - 1;
-            rest &= rest - 1;
-            const uint32_t idx = qb[q] + __popc(em[q] & ((1u << bit) - 1u));
-            const uint32_t ow = offw[32 * (8 * q + (bit & 7))];
-            if (idx < n_esc) esc_out[idx] = (uint8_t)(((ow >> (8 * (bit >> 3))) & 0xFFu) + base);
-        }
-    }
-}
-
-// Phase B: write the full chunk held in `r` (offsets) and `chunk` (its
-// sign+fraction plane, in shared memory) to `dst` (global, 16-byte aligned)
-// following `pl`.  One warp.  A packed chunk's byte plane leaves by one bulk
-// (TMA) store issued by lane 0, which waits until it has read `chunk` before
-// returning; a raw chunk's values are rebuilt in registers.  Uses the second
-// half of `chunk` (consumed input) as scratch.
-__device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const ChunkPlan& pl, uint8_t* chunk,
-                                                 uint8_t* dst) {
-    const uint32_t lane = threadIdx.x & 31;
-    uint8_t* body = dst + kChunkHeaderBytes;
-    if (lane == 0)
-        *reinterpret_cast<uint4*>(dst) =
-            make_uint4((pl.raw ? kModeRaw : kModePacked) | (pl.k << 8) | (pl.base << 16), kChunkElems | (pl.n_esc << 16),
-                       pl.bytes, 0u);
-    if (pl.raw) {  // rebuild the values from the offsets and the sign+fraction plane
-        const uint32_t base4 = pl.emin * 0x01010101u;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const uint2 sv = *reinterpret_cast<const uint2*>(chunk + 256 * j + 8 * lane);
-            uint4 v;
-            join_quad(r.off[2 * j] + base4, sv.x, v.x, v.y);
-            join_quad(r.off[2 * j + 1] + base4, sv.y, v.z, v.w);
-            *reinterpret_cast<uint4*>(body + 512 * j + 16 * lane) = v;
-        }
-        return;
-    }
-    // the sign+fraction plane was written by generic stores: order them before
-    // the bulk copy's reads
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncwarp();
-    if (lane == 0) {
-        bulk_store(body, chunk, kSmPlaneBytes);
-        bulk_commit();
-    }
-    const uint32_t k = pl.k;
-    if (k > 0) {
-        const bool escapes = pl.n_esc > 0;
-        uint32_t em[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            // escaped elements carry the sentinel (all k bits set): OR their
-            // bits into every plane; the offset bits of the others are their codes
-            if (escapes) em[q] = (k == pl.k1) ? r.esc[q] : escape_bits8(r.off + 8 * q, k);
-            uint8_t* col = body + kSmPlaneBytes + 4 * (32 * q + lane);
-            if (k >= 4) {  // one 8x8 bit transpose makes every plane
-                uint32_t W[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) W[m] = r.off[8 * q + m];
-                transpose8x8x4(W);
-#pragma unroll
-                for (int p = 0; p < 8; ++p)
-                    if ((uint32_t)p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = W[p] | em[q];
-            } else {
-#pragma unroll 1
-                for (uint32_t p = 0; p < k; ++p)
-                    *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = pack_plane(r.off + 8 * q, p) | em[q];
+        uint32_t rest = esc[q], idx = first[q];
+        while (__any_sync(0xFFFFFFFFu, rest != 0u)) {
+            if (rest) {
+                const uint32_t bit = __ffs(rest) - 1;
+                rest &= rest - 1;
+                const uint32_t m = bit & 7, bb = bit >> 3;
+                const uint32_t i = 256 * (4 * q + (m >> 1)) + 8 * lane + 4 * (m & 1) + bb;
+                if (idx < n_esc) esc_out[idx] = (uint8_t)(vals[i] >> 7);
+                ++idx;
             }
         }
-        if (escapes) {
-            uint32_t* offw = reinterpret_cast<uint32_t*>(chunk + kSmPlaneBytes) + lane;
-#pragma unroll
-            for (int m = 0; m < 32; ++m) offw[32 * m] = r.off[m];
-            __syncwarp();
-            uint8_t* esc_out = body + kSmPlaneBytes + kPlaneBytes * k;
-            write_escapes(em[0], em[1], em[2], em[3], offw, pl.emin, pl.n_esc, esc_out);
-            if (lane < 16 && pl.n_esc + lane < pad16(pl.n_esc)) esc_out[pl.n_esc + lane] = 0;
-        }
     }
-    if (lane == 0) bulk_wait_read();
-    __syncwarp();
+    if (lane < 16 && n_esc + lane < pad16(n_esc)) esc_out[n_esc + lane] = 0;
 }
 
 // The partial last chunk (n_c < 4096 elements) is stored raw (section 5,

@@ -164,7 +164,10 @@ __global__ void __launch_bounds__(32 * kRGroup, 3) reduce_kernel(ReduceInputs in
         }
         return;
     }
-    __syncthreads();  // the parked chunks are complete
+    // the parked chunks were written by generic stores and a raw chunk leaves
+    // by a bulk copy: order them for the async proxy, then for every warp
+    fence_proxy_async_smem();
+    __syncthreads();
 
     // encode: warp w sizes and writes output chunk c0 + w
     const uint64_t c = c0 + q;
