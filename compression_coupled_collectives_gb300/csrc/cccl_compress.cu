@@ -44,10 +44,6 @@ struct CompressSmem {
     uint64_t off[2][kGroup];       // chunk offsets, or kFlagPoison
 };
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // Control lane: fill stage s with group g (or mark it empty).
 __device__ __forceinline__ void issue_group(const uint16_t* in, uint64_t g, uint64_t n_groups, uint64_t n_full,
                                             uint8_t* stage, CompressSmem& sm, int s) {
@@ -80,7 +76,7 @@ __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__
     const uint64_t n_full = so.n_elems / kChunkElems;
     const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
     const int s = i % kRing;
-    const bool filled = mbar_wait(&sm.load[s][w], (uint32_t)(i / kRing) & 1u);
+    const bool filled = __all_sync(0xFFFFFFFFu, mbar_wait(&sm.load[s][w], (uint32_t)(i / kRing) & 1u));
     const uint64_t g = sm.group[s];
     const bool live = filled && g < n_groups;
     if (live) {
@@ -108,7 +104,7 @@ __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__
     }
     if (i > 0) {  // write group i - 1
         const int ip = i - 1, sp = ip % kRing;
-        if (mbar_wait(&sm.placed[ip & 1], (uint32_t)(ip >> 1) & 1u)) {
+        if (__all_sync(0xFFFFFFFFu, mbar_wait(&sm.placed[ip & 1], (uint32_t)(ip >> 1) & 1u))) {
             const uint64_t off = sm.off[ip & 1][w];
             if (off != kFlagPoison && prev.bytes > 0) {
                 if (off + prev.bytes > so.capacity) {  // cannot happen for a correct placement
@@ -155,16 +151,31 @@ __global__ void __launch_bounds__(kCompressThreads, 1) compress_kernel(const uin
 
     if (w == kCtrl) {
         // ---------------------------------------------------------------- control warp
-        if (lane == 0)
-            for (int s = 0; s < kRing; ++s) issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, s);
+        // Tickets fix the placement order, so they are taken in the order the
+        // groups will be sized: the second when the first group's data has
+        // landed, the third once the first group is sized, later ones as
+        // stages free up.  (Taken all at once, every CTA's third ticket would
+        // be sized two iterations later than its number says, and every
+        // look-back behind it would wait for that.)
+        if (lane == 0) issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 0);
+        __syncwarp();
+        const bool first_landed = __all_sync(0xFFFFFFFFu, mbar_wait(&sm.load[0][0], 0u));
+        if (lane == 0) {
+            if (!first_landed) record_error(so.ws, kStatusTimeout);
+            issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 1);
+        }
         __syncwarp();
         for (int i = 0;; ++i) {
             const int s = i % kRing;
             const uint64_t g = sm.group[s];
             if (g >= n_groups) break;
-            if (!mbar_wait(&sm.sized[s], (uint32_t)(i / kRing) & 1u)) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sm.sized[s], (uint32_t)(i / kRing) & 1u))) {
                 if (lane == 0) record_error(so.ws, kStatusTimeout);
                 break;
+            }
+            if (i == 0) {
+                if (lane == 0) issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 2);
+                __syncwarp();
             }
             const uint32_t mine = lane < (uint32_t)kGroup ? sm.size[s][lane] : 0u;
             uint32_t incl = mine;
@@ -181,7 +192,7 @@ __global__ void __launch_bounds__(kCompressThreads, 1) compress_kernel(const uin
             // group i-1 is written out: refill its stage, for group i+2
             if (i >= 1) {
                 const int sp = (i - 1) % kRing;
-                if (!mbar_wait(&sm.free_[sp], (uint32_t)((i - 1) / kRing) & 1u)) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sm.free_[sp], (uint32_t)((i - 1) / kRing) & 1u))) {
                     if (lane == 0) record_error(so.ws, kStatusTimeout);
                     break;
                 }

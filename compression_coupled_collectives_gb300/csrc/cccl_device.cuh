@@ -102,6 +102,9 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -129,6 +132,27 @@ __device__ __forceinline__ void bulk_store(void* dst_gmem, const void* src_smem,
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the committed bulk stores of this thread have read their source.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Barriers over the threads that decode one chunk together: the whole CTA,
+// or a named barrier over the first N threads (N a multiple of 32; every
+// participating warp executes it as a whole).
+struct CtaBarrier {
+    __device__ static void sync() { __syncthreads(); }
+    __device__ static bool any(bool p) { return __syncthreads_or(p) != 0; }
+};
+template <int Id, int N>
+struct NamedBarrier {
+    __device__ static void sync() { asm volatile("bar.sync %0, %1;" ::"n"(Id), "n"(N) : "memory"); }
+    __device__ static bool any(bool p) {
+        uint32_t r;
+        asm volatile(
+            "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, %2, %3, pi; selp.u32 %0, 1, 0, po; }"
+            : "=r"(r)
+            : "r"((uint32_t)p), "n"(Id), "n"(N)
+            : "memory");
+        return r != 0;
+    }
+};
 
 // Bounded wait for phase `parity` of `bar`; false if kWaitLimitNs ran out.
 // Each try suspends the warp in hardware (up to kSuspendHintNs) until the

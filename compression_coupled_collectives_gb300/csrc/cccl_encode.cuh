@@ -209,17 +209,19 @@ __device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const Chunk
     const uint32_t first[4] = {ea & 0xFFFFu, t0 + (ea >> 16), t0 + t1 + (eb & 0xFFFFu), t0 + t1 + t2 + (eb >> 16)};
     const uint16_t* vals = reinterpret_cast<const uint16_t*>(chunk);
     uint8_t* esc_out = body + kSmPlaneBytes + kPlaneBytes * k;
+    // one escape of every quarter per step: four independent load -> store
+    // chains in flight per lane
+    uint32_t idx[4] = {first[0], first[1], first[2], first[3]};
+    while (__any_sync(0xFFFFFFFFu, (esc[0] | esc[1] | esc[2] | esc[3]) != 0u)) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t rest = esc[q], idx = first[q];
-        while (__any_sync(0xFFFFFFFFu, rest != 0u)) {
-            if (rest) {
-                const uint32_t bit = __ffs(rest) - 1;
-                rest &= rest - 1;
+        for (int q = 0; q < 4; ++q) {
+            if (esc[q]) {
+                const uint32_t bit = __ffs(esc[q]) - 1;
+                esc[q] &= esc[q] - 1;
                 const uint32_t m = bit & 7, bb = bit >> 3;
                 const uint32_t i = 256 * (4 * q + (m >> 1)) + 8 * lane + 4 * (m & 1) + bb;
-                if (idx < n_esc) esc_out[idx] = (uint8_t)(vals[i] >> 7);
-                ++idx;
+                if (idx[q] < n_esc) esc_out[idx[q]] = (uint8_t)(vals[i] >> 7);
+                ++idx[q];
             }
         }
     }
