@@ -14,15 +14,16 @@ namespace cccl {
 // Decode the full chunk staged at `buf` (header already validated against
 // the stream) into this thread's 16 words of bf16 pairs: thread t (warp
 // q = t / 32, lane l) gets rows 4 q .. 4 q + 3, elements 8 l .. 8 l + 7 of
-// each, as P[4 jj + w] = elements 2 w, 2 w + 1 of row 4 q + jj.  The 128
-// threads 0..127 call it together and meet at `Barrier`; every branch on the
-// header is uniform over them.  Returns false if the chunk body is malformed (a sentinel
+// each, as P[4 jj + w] = elements 2 w, 2 w + 1 of row 4 q + jj.  The four
+// warps of a team (four consecutive warps starting at a multiple of four;
+// q = warp index mod 4) call it together and meet at `Barrier`; every branch
+// on the header is uniform over them.  Returns false if the chunk body is malformed (a sentinel
 // count that disagrees with n_esc, or base + code above 255).  `special` is
 // set when the chunk may hold an exponent of 255 (Inf or NaN).
 template <typename Barrier>
-__device__ __forceinline__ bool decode_full_chunk(const uint8_t* buf, const ChunkHeader& h, uint32_t P[16],
-                                                  uint32_t* s_row_tot, bool& special) {
-    const uint32_t t = threadIdx.x, lane = t & 31, q = t >> 5;
+__device__ __forceinline__ bool decode_full_chunk(const Barrier& bar, const uint8_t* buf, const ChunkHeader& h,
+                                                  uint32_t P[16], uint32_t* s_row_tot, bool& special) {
+    const uint32_t t = threadIdx.x, lane = t & 31, q = (t >> 5) & 3;
     const uint8_t* body = buf + kChunkHeaderBytes;
     if (h.mode == kModeRaw) {
 #pragma unroll
@@ -86,10 +87,10 @@ __device__ __forceinline__ bool decode_full_chunk(const uint8_t* buf, const Chun
                 for (int b = 0; b < 4; ++b) bad |= ((c >> (8 * b)) & 0xFFu) + h.base > 255u;
                 E[m] = (c + base4) & ~ff;
             }
-            if (Barrier::any(bad)) return false;
+            if (bar.any(bad)) return false;
         }
         if (h.n_esc == 0) {
-            if (Barrier::any(sent != 0u)) return false;
+            if (bar.any(sent != 0u)) return false;
         } else {
             // escapes are listed in bit-plane order: plane word 32 q + l, then
             // bit; this thread's sentinel bits are exactly its word's escapes
@@ -101,7 +102,7 @@ __device__ __forceinline__ bool decode_full_chunk(const uint8_t* buf, const Chun
                 if (lane >= (uint32_t)d) incl += t2;
             }
             if (lane == 31) s_row_tot[q] = incl;
-            Barrier::sync();
+            bar.sync();
             uint32_t before = 0, total = 0;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {

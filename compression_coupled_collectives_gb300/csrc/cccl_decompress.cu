@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     uint32_t P[16];
     bool special = false;
-    if (!decode_full_chunk<CtaBarrier>(buf, h, P, row_tot, special)) {
+    if (!decode_full_chunk(CtaBarrier{}, buf, h, P, row_tot, special)) {
         if (t == 0) record_error(ws, kStatusCorrupt);
         return;
     }

@@ -133,22 +133,22 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Wait until the committed bulk stores of this thread have read their source.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
-// Barriers over the threads that decode one chunk together: the whole CTA,
-// or a named barrier over the first N threads (N a multiple of 32; every
+// Barriers over the threads that decode or encode one chunk together: the
+// whole CTA, or a named barrier over the 4 warps of a team (every
 // participating warp executes it as a whole).
 struct CtaBarrier {
-    __device__ static void sync() { __syncthreads(); }
-    __device__ static bool any(bool p) { return __syncthreads_or(p) != 0; }
+    __device__ void sync() const { __syncthreads(); }
+    __device__ bool any(bool p) const { return __syncthreads_or(p) != 0; }
 };
-template <int Id, int N>
-struct NamedBarrier {
-    __device__ static void sync() { asm volatile("bar.sync %0, %1;" ::"n"(Id), "n"(N) : "memory"); }
-    __device__ static bool any(bool p) {
+struct TeamBarrier {
+    uint32_t id;  // 1..15; barrier 0 is __syncthreads'
+    __device__ void sync() const { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+    __device__ bool any(bool p) const {
         uint32_t r;
         asm volatile(
-            "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, %2, %3, pi; selp.u32 %0, 1, 0, po; }"
+            "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, %2, 128, pi; selp.u32 %0, 1, 0, po; }"
             : "=r"(r)
-            : "r"((uint32_t)p), "n"(Id), "n"(N)
+            : "r"((uint32_t)p), "r"(id)
             : "memory");
         return r != 0;
     }
@@ -222,24 +222,28 @@ __device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funn
 
 // All 8 planes at once: 8 quads hold, per byte lane b, an 8x8 bit matrix
 // (row m = quad m, column p = bit p); transposing it turns codes into plane
-// words and back (plane p = row p).  Recursive block transpose by three
-// rounds of masked delta swaps (4x4, 2x2, 1x1 blocks), the same for every
-// byte lane since no swap crosses a byte.
-__device__ __forceinline__ void delta_swap(uint32_t& a, uint32_t& b, uint32_t s, uint32_t mask) {
-    const uint32_t t = ((a >> s) ^ b) & mask;
-    b ^= t;
-    a ^= t << s;
+// words and back (plane p = row p).  Recursive block transpose in three
+// rounds (4x4, 2x2, 1x1 blocks), the same for every byte lane since no
+// exchange crosses a byte.
+// Exchange the off-diagonal s x s blocks of rows a and b (a before b):
+// the bits of a selected by ~M move down by s into b's M bits and b's M bits
+// move up into a's ~M bits (each a single bit-select).
+__device__ __forceinline__ void block_swap(uint32_t& a, uint32_t& b, uint32_t s, uint32_t M) {
+    const uint32_t na = (a & M) | ((b << s) & ~M);
+    const uint32_t nb = ((a >> s) & M) | (b & ~M);
+    a = na;
+    b = nb;
 }
 __device__ __forceinline__ void transpose8x8x4(uint32_t* v) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) delta_swap(v[m], v[m + 4], 4, 0x0F0F0F0Fu);
+    for (int m = 0; m < 4; ++m) block_swap(v[m], v[m + 4], 4, 0x0F0F0F0Fu);
 #pragma unroll
     for (int m = 0; m < 8; m += 4) {
-        delta_swap(v[m], v[m + 2], 2, 0x33333333u);
-        delta_swap(v[m + 1], v[m + 3], 2, 0x33333333u);
+        block_swap(v[m], v[m + 2], 2, 0x33333333u);
+        block_swap(v[m + 1], v[m + 3], 2, 0x33333333u);
     }
 #pragma unroll
-    for (int m = 0; m < 8; m += 2) delta_swap(v[m], v[m + 1], 1, 0x55555555u);
+    for (int m = 0; m < 8; m += 2) block_swap(v[m], v[m + 1], 1, 0x55555555u);
 }
 
 // Plane p of 8 quads of codes (bits of codes above p are ignored).

@@ -228,6 +228,186 @@ __device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const Chunk
     if (lane < 16 && n_esc + lane < pad16(n_esc)) esc_out[n_esc + lane] = 0;
 }
 
+// ---------------------------------------------------------------------------
+// Team encoding: a full chunk held in registers by a team of four warps.
+// Thread (warp q of the team, lane l) holds rows 4 q .. 4 q + 3, elements
+// 8 l .. 8 l + 7 of each, as P[4 jj + x] = elements 2 x, 2 x + 1 of row
+// 4 q + jj (the layout decode_full_chunk produces): exactly the 32 elements
+// of bit-plane word 32 q + l, quad m = 2 jj + h being words P[2 m], P[2 m + 1].
+// The team meets twice per chunk (exponent extremes, escape counts); after
+// that every warp writes its own quarter.
+// ---------------------------------------------------------------------------
+struct TeamPlan {
+    uint32_t raw;         // 1: stored raw
+    uint32_t k;           // code width
+    uint32_t base;        // header base (0 when raw)
+    uint32_t n_esc;       // escapes at width k
+    uint32_t bytes;       // chunk size, header included
+    uint32_t esc_before;  // escapes of the quarters before this warp's, at width k
+};
+
+// Per-team exchange space in shared memory.
+struct TeamXch {
+    uint32_t mn[4], mx[4];  // per warp: smallest and largest exponent
+    uint32_t cnt[4][8];     // per warp: escapes at width k (k = 1..7)
+};
+
+// Exponent quad m of this thread's values (one byte per value).
+__device__ __forceinline__ uint32_t exponent_quad(const uint32_t P[16], int m) {
+    return __byte_perm(P[2 * m] << 1, P[2 * m + 1] << 1, 0x7531);
+}
+
+// Phase A for a team: exponent table and size of the chunk in P, leaving the
+// bit-planes of this thread's word (offsets e - base) in `planes`.  Every
+// thread of the team returns the same plan except esc_before.
+template <typename Barrier>
+__device__ __forceinline__ TeamPlan plan_chunk_team(const Barrier& bar, const uint32_t P[16], uint32_t planes[8],
+                                                    TeamXch& x) {
+    const uint32_t lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        // doubling puts each value's exponent in the high byte of its 16-bit lane
+        const uint32_t t0 = P[2 * m] << 1, t1 = P[2 * m + 1] << 1;
+        mn = vmin_u16x2(mn, vmin_u16x2(t0, t1));
+        mx = vmax_u16x2(mx, vmax_u16x2(t0, t1));
+        planes[m] = __byte_perm(t0, t1, 0x7531);
+    }
+    const uint32_t wmn = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
+    const uint32_t wmx = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
+    if (lane == 0) {
+        x.mn[q] = wmn;
+        x.mx[q] = wmx;
+    }
+    bar.sync();
+    const uint32_t emin = min(min(x.mn[0], x.mn[1]), min(x.mn[2], x.mn[3]));
+    const uint32_t emax = max(max(x.mx[0], x.mx[1]), max(x.mx[2], x.mx[3]));
+    const uint32_t base4 = emin * 0x01010101u;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) planes[m] -= base4;  // no borrow: every exponent >= emin
+    transpose8x8x4(planes);                          // quads of offsets -> planes
+    // escapes at width k are low_k | high_k (see plan_chunk_warp)
+    uint32_t high[8];
+    high[7] = planes[7];
+#pragma unroll
+    for (int k = 6; k >= 1; --k) high[k] = high[k + 1] | planes[k];
+    uint32_t low = planes[0];
+#pragma unroll
+    for (int k = 1; k <= 7; ++k) {
+        const uint32_t n = __reduce_add_sync(0xFFFFFFFFu, __popc(low | high[k]));
+        if (lane == 0) x.cnt[q][k] = n;
+        if (k < 7) low &= planes[k];
+    }
+    bar.sync();
+    TeamPlan pl{0u, 0u, emin, 0u, 0u, 0u};
+    uint32_t best = 0;
+    if (emax > emin) {
+        // lane k (1..7) sizes width k; the smallest (size, k) wins, so a tie
+        // keeps the smaller width
+        uint32_t n = 0, before = 0, key = 0xFFFFFFFFu;
+        if (lane >= 1 && lane <= 7) {
+            const uint32_t c0 = x.cnt[0][lane], c1 = x.cnt[1][lane], c2 = x.cnt[2][lane];
+            n = c0 + c1 + c2 + x.cnt[3][lane];
+            before = (q > 0 ? c0 : 0u) + (q > 1 ? c1 : 0u) + (q > 2 ? c2 : 0u);
+            key = ((kPlaneBytes * lane + (uint32_t)pad16(n)) << 3) | lane;
+        }
+        key = __reduce_min_sync(0xFFFFFFFFu, key);
+        pl.k = key & 7u;
+        best = key >> 3;
+        pl.n_esc = __shfl_sync(0xFFFFFFFFu, n, pl.k);
+        pl.esc_before = __shfl_sync(0xFFFFFFFFu, before, pl.k);
+    }
+    pl.raw = best >= kSmPlaneBytes ? 1u : 0u;
+    if (pl.raw) {
+        pl.k = 0;
+        pl.base = 0;
+        pl.n_esc = 0;
+        pl.esc_before = 0;
+        pl.bytes = kMaxChunkBytes;
+    } else {
+        pl.bytes = (uint32_t)(16 + kSmPlaneBytes + kPlaneBytes * pl.k + pad16(pl.n_esc));
+    }
+    return pl;
+}
+
+// Phase B for a team: write the chunk in P (planes from phase A) to `dst`
+// (global, 16-byte aligned).  No barrier: each warp writes the header (warp 0),
+// its four rows of the sign+fraction plane, its word of every bit-plane and
+// its escapes, whose place follows from esc_before.  `xq`: this thread's
+// 8-word scratch column in shared memory (word m at xq[128 m]), where the
+// exponent quads wait for the escape writer.
+__device__ __forceinline__ void write_chunk_team(const uint32_t P[16], const uint32_t planes[8], const TeamPlan& pl,
+                                                 uint8_t* dst, uint32_t* xq) {
+    const uint32_t lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+    uint8_t* body = dst + kChunkHeaderBytes;
+    if (q == 0 && lane == 0)
+        *reinterpret_cast<uint4*>(dst) =
+            make_uint4((pl.raw ? kModeRaw : kModePacked) | (pl.k << 8) | (pl.base << 16), kChunkElems | (pl.n_esc << 16),
+                       pl.bytes, 0u);
+    if (pl.raw) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+            *reinterpret_cast<uint4*>(body + 512 * (4 * q + jj) + 16 * lane) =
+                make_uint4(P[4 * jj], P[4 * jj + 1], P[4 * jj + 2], P[4 * jj + 3]);
+        return;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+        *reinterpret_cast<uint2*>(body + 256 * (4 * q + jj) + 8 * lane) =
+            make_uint2(sign_fraction_quad(P[4 * jj], P[4 * jj + 1]), sign_fraction_quad(P[4 * jj + 2], P[4 * jj + 3]));
+    const uint32_t k = pl.k;
+    if (k == 0) return;
+    uint32_t esc = escape_word(planes, k);
+    uint8_t* col = body + kSmPlaneBytes + 4 * (32 * q + lane);
+#pragma unroll
+    for (uint32_t p = 0; p < 8; ++p)
+        if (p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = planes[p] | esc;
+    const uint32_t n_esc = pl.n_esc;
+    if (n_esc == 0) return;
+    const uint32_t mine = __popc(esc);
+    uint32_t incl = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= (uint32_t)d) incl += t;
+    }
+    uint32_t idx = pl.esc_before + incl - mine;
+    uint8_t* esc_out = body + kSmPlaneBytes + kPlaneBytes * k;
+    if (esc) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) xq[128 * m] = exponent_quad(P, m);
+    }
+    const uint8_t* xb = reinterpret_cast<const uint8_t*>(xq);
+    while (__any_sync(0xFFFFFFFFu, esc != 0u)) {
+        if (esc) {
+            const uint32_t bit = __ffs(esc) - 1;  // element (m, b) = byte b of quad m
+            esc &= esc - 1;
+            if (idx < n_esc) esc_out[idx] = xb[512 * (bit & 7) + (bit >> 3)];
+            ++idx;
+        }
+    }
+    if (q == 0 && lane < 16 && n_esc + lane < pad16(n_esc)) esc_out[n_esc + lane] = 0;
+}
+
+// The partial last chunk held by a team (values past n_c ignored), raw.
+__device__ __forceinline__ void write_tail_chunk_team(const uint32_t P[16], uint32_t n_c, uint8_t* dst) {
+    const uint32_t lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+    const uint32_t bytes = (uint32_t)(16 + pad16(2 * n_c));
+    uint16_t* out = reinterpret_cast<uint16_t*>(dst + 16);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const uint32_t e = 256 * (4 * q + jj) + 8 * lane + 2 * x;
+            if (e < n_c) out[e] = (uint16_t)(P[4 * jj + x] & 0xFFFFu);
+            if (e + 1 < n_c) out[e + 1] = (uint16_t)(P[4 * jj + x] >> 16);
+        }
+    if (q == 0 && lane == 0) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(kModeRaw, n_c, bytes, 0u);
+        for (uint32_t b = 16 + 2 * n_c; b < bytes; ++b) dst[b] = 0;
+    }
+}
+
 // The partial last chunk (n_c < 4096 elements) is stored raw (section 5,
 // "Handling data alignment").  One warp; `vals` are its n_c values.
 template <typename Src>
