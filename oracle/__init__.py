@@ -61,8 +61,10 @@ def _bind(path: str):
     lib.oracle_sum_ranks.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, sz, u16p]
     lib.oracle_reduce.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(sz), ctypes.c_int, sz,
                                   u8p, sz, ctypes.POINTER(sz)]
+    lib.oracle_reduce_mixed.argtypes = [u16p, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(sz), ctypes.c_int,
+                                        sz, u8p, sz, ctypes.POINTER(sz)]
     for f in ("oracle_chunk_choice", "oracle_encode_chunk", "oracle_compress", "oracle_decompress",
-              "oracle_reduce"):
+              "oracle_reduce", "oracle_reduce_mixed"):
         getattr(lib, f).restype = ctypes.c_int
     lib.oracle_sum_ranks.restype = None
     lib.oracle_plane_position.restype = None
@@ -207,6 +209,25 @@ def sum_ranks(xs) -> np.ndarray:
     out = np.empty(n, np.uint16)
     _load().oracle_sum_ranks(ptrs, len(arrs), n, out.ctypes.data)
     return out
+
+
+def reduce_mixed(local, streams, n: int) -> np.ndarray:
+    """Local uncompressed operand (rank 0) and compressed streams (ranks 1..)
+    -> compressed stream of their rounded binary32 sum."""
+    loc = _u16(local).reshape(-1)
+    if loc.size != n:
+        raise ValueError("local operand must hold n values")
+    bs = [np.ascontiguousarray(s, dtype=np.uint8) for s in streams]
+    ptrs = (ctypes.c_void_p * max(len(bs), 1))(*[b.ctypes.data for b in bs])
+    sizes = (ctypes.c_size_t * max(len(bs), 1))(*[b.size for b in bs])
+    cap = compress_bound(n)
+    out = np.empty(cap, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_reduce_mixed(loc.ctypes.data, ptrs, sizes, len(bs), n, out.ctypes.data, cap,
+                                     ctypes.byref(nb))
+    if st != OK:
+        raise OracleError(st, "oracle_reduce_mixed")
+    return out[:nb.value]
 
 
 def reduce(streams, n: int) -> np.ndarray:

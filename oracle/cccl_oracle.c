@@ -547,3 +547,40 @@ int oracle_reduce(const uint8_t *const *ins, const size_t *in_bytes, int R, size
     free(sum);
     return st;
 }
+
+/* Selective-compression reduce (section 5, "Selective compression across
+ * collective stages"): an intermediate reduction step merges the local,
+ * uncompressed operand with received compressed partial results; only the
+ * remote data are decompressed.  The local operand is rank 0, the n_remote
+ * streams are ranks 1..n_remote, summed and compressed as oracle_reduce. */
+int oracle_reduce_mixed(const uint16_t *local, const uint8_t *const *ins, const size_t *in_bytes, int n_remote,
+                        size_t n, uint8_t *out, size_t capacity, size_t *out_bytes)
+{
+    if (local == NULL || n_remote < 0 || n_remote > 63 || n == 0 || out == NULL ||
+        (n_remote > 0 && (ins == NULL || in_bytes == NULL)))
+        return ORC_ERR_INVALID_ARG;
+    const int R = n_remote + 1;
+    const uint16_t **xs = (const uint16_t **)calloc((size_t)R, sizeof(uint16_t *));
+    uint16_t *sum = (uint16_t *)malloc(n * sizeof(uint16_t));
+    int st = (xs && sum) ? ORC_OK : ORC_ERR_INVALID_ARG;
+    if (xs)
+        xs[0] = local;
+    for (int r = 1; r < R && st == ORC_OK; r++) {
+        uint16_t *x = (uint16_t *)malloc(n * sizeof(uint16_t));
+        xs[r] = x;
+        if (!x)
+            st = ORC_ERR_INVALID_ARG;
+        else
+            st = oracle_decompress(ins[r - 1], in_bytes[r - 1], x, n);
+    }
+    if (st == ORC_OK) {
+        oracle_sum_ranks(xs, R, n, sum);
+        st = oracle_compress(sum, n, out, capacity, out_bytes);
+    }
+    if (xs)
+        for (int r = 1; r < R; r++)
+            free((void *)xs[r]);
+    free((void *)xs);
+    free(sum);
+    return st;
+}

@@ -39,6 +39,11 @@ MUTATIONS = [
     ("base_is_max", "best.base = emin;", "best.base = emax;"),
     ("offset_table_relative", "put_u64(out + STREAM_HEADER_BYTES + 8 * c, pos);",
      "put_u64(out + STREAM_HEADER_BYTES + 8 * c, pos - start);"),
+    ("mixed_remote_ranks_reversed", "st = oracle_decompress(ins[r - 1], in_bytes[r - 1], x, n);",
+     "st = oracle_decompress(ins[R - 1 - r], in_bytes[R - 1 - r], x, n);"),
+    ("mixed_local_added_last", "oracle_sum_ranks(xs, R, n, sum);",
+     "{ const uint16_t *t = xs[0]; for (int r = 0; r + 1 < R; r++) xs[r] = xs[r + 1]; xs[R - 1] = t; "
+     "oracle_sum_ranks(xs, R, n, sum); for (int r = R - 1; r > 0; r--) xs[r] = xs[r - 1]; xs[0] = t; }"),
 ]
 
 
@@ -98,6 +103,9 @@ def _battery(orc, wl):
     check("special_values", lambda: np.array_equal(orc.sum_ranks([sp_a, sp_b, sp_c]),
                                                    np.array([0x7FC0, 0x8000, 0x7FC0, 0x3F80], np.uint16)))
     check("rank_order", lambda: orc.sum_ranks([sp_b[3:], sp_c[3:], sp_a[3:]])[0] == 0)
+    # local 2^30, remote -2^30 then 1: (2^30 - 2^30) + 1 = 1 only in this order
+    check("mixed_rank_order", lambda: orc.decompress(
+        orc.reduce_mixed(sp_a[3:], [orc.compress(sp_b[3:]), orc.compress(sp_c[3:])], 1), 1)[0] == 0x3F80)
     return failed
 
 

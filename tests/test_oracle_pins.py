@@ -333,6 +333,39 @@ def test_reduce_equals_compress_of_rounded_sum(orc, wl):
     assert np.array_equal(dec, want)
 
 
+def test_reduce_mixed_is_reduce_with_the_local_operand_compressed(orc, wl):
+    """Compression is lossless, so merging the local uncompressed operand with
+    compressed remote ranks equals the plain reduce with the local operand
+    compressed first, as rank 0."""
+    for n, R in [(5 * CHUNK + 33, 3), (CHUNK, 2), (100, 4), (2 * CHUNK, 1)]:
+        xs = [wl.generate(5, r, count=n, start=(1 << 19) - 2 * CHUNK, n=1 << 20) for r in range(R)]
+        streams = [orc.compress(x) for x in xs]
+        assert np.array_equal(orc.reduce_mixed(xs[0], streams[1:], n), orc.reduce(streams, n))
+
+
+def test_reduce_mixed_matches_sequential_binary32_from_the_local_operand(orc, wl):
+    n = 6 * CHUNK + 5
+    xs = [wl.generate(1, r, count=n) for r in range(2)] + [wl.generate(2, 0, count=n)]
+    streams = [orc.compress(x) for x in xs[1:]]
+    dec = pf.decode_stream(orc.reduce_mixed(xs[0], streams, n).tobytes(), n)
+    acc = _f32(xs[0]).copy()
+    for x in xs[1:]:
+        acc = (acc + _f32(x)).astype(np.float32)
+    assert np.array_equal(dec, _torch_bf16(acc))
+
+
+def test_reduce_mixed_order_and_nan(orc):
+    big, one = 0x4E80, 0x3F80  # 2^30, 1
+    local = np.array([big | 0x8000, 0x7FC1, 0x0000], np.uint16)  # -2^30, NaN, +0
+    r1 = np.array([one, one, 0x8000], np.uint16)
+    r2 = np.array([big, one, 0x8000], np.uint16)
+    out = orc.decompress(orc.reduce_mixed(local, [orc.compress(r1), orc.compress(r2)], 3), 3)
+    # (-2^30 + 1) + 2^30 = 0 in binary32; NaN + 1 + 1 -> 0x7FC0; +0 + -0 + -0 = +0
+    assert np.array_equal(out, np.array([0x0000, 0x7FC0, 0x0000], np.uint16))
+    x = np.array([0x7FC1, 0x3F80, 0xFFFF], np.uint16)
+    assert np.array_equal(orc.decompress(orc.reduce_mixed(x, [], 3), 3), np.array([0x7FC0, 0x3F80, 0x7FC0], np.uint16))
+
+
 # ---------------------------------------------------------------- corrupt streams
 def _corrupt_cases(orc, wl):
     x = wl.generate(2, 0, count=3 * CHUNK + 10, n=1 << 20)
