@@ -46,6 +46,8 @@ _lib.cccl_decompress.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_decompress.restype = _i
 _lib.cccl_reduce_compressed.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_reduce_compressed.restype = _i
+_lib.cccl_reduce_mixed.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _vp, _sz, _vp, _sz, _vp]
+_lib.cccl_reduce_mixed.restype = _i
 _lib.cccl_get_result.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_i)]
 _lib.cccl_get_result.restype = _i
 _lib.cccl_status_string.argtypes = [_i]
@@ -128,6 +130,20 @@ def cccl_reduce_compressed(ins: Sequence[torch.Tensor], n_elems: int, out: torch
            "cccl_reduce_compressed")
 
 
+def cccl_reduce_mixed(local: torch.Tensor, remote: Sequence[torch.Tensor], out: torch.Tensor, ws: torch.Tensor,
+                      in_bytes: Sequence[int] | None = None, stream=None) -> None:
+    """Enqueue the selective-compression reduce: the uncompressed bf16 buffer
+    ``local`` (rank 0) plus the compressed streams ``remote`` (ranks 1..)."""
+    local = _bf16_bits(local)
+    n = len(remote)
+    ptrs = (_vp * max(n, 1))(*[t.data_ptr() for t in remote])
+    sizes = [t.numel() * t.element_size() for t in remote] if in_bytes is None else list(in_bytes)
+    szs = (_sz * max(n, 1))(*sizes)
+    _check(_lib.cccl_reduce_mixed(local.data_ptr(), ptrs, szs, n, local.numel(), out.data_ptr(),
+                                  out.numel() * out.element_size(), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "cccl_reduce_mixed")
+
+
 def cccl_get_result(ws: torch.Tensor, stream=None) -> tuple[int, int]:
     """Synchronise ``stream``; return (stream bytes of the last compress/reduce, device status)."""
     nbytes = ctypes.c_uint64(0)
@@ -165,6 +181,17 @@ def decompress(s: torch.Tensor, n_elems: int, stream=None) -> torch.Tensor:
     _, dev = cccl_get_result(ws, stream)
     _check(dev, "cccl_decompress (device)")
     return out
+
+
+def reduce_mixed(local: torch.Tensor, remote: Sequence[torch.Tensor], stream=None) -> torch.Tensor:
+    """Selective-compression reduce and wait; returns the output stream trimmed."""
+    n = local.numel()
+    out = empty_stream(n, local.device)
+    ws = empty_workspace(n, local.device)
+    cccl_reduce_mixed(local, remote, out, ws, stream=stream)
+    nbytes, dev = cccl_get_result(ws, stream)
+    _check(dev, "cccl_reduce_mixed (device)")
+    return out[:nbytes]
 
 
 def reduce_compressed(streams: Sequence[torch.Tensor], n_elems: int, stream=None) -> torch.Tensor:

@@ -132,6 +132,33 @@ cccl_status cccl_reduce_compressed(const void* const* h_ins, const size_t* h_in_
     return CCCL_OK;
 }
 
+cccl_status cccl_reduce_mixed(const uint16_t* d_local, const void* const* h_ins, const size_t* h_in_bytes,
+                              int n_remote, size_t n_elems, void* d_out, size_t out_capacity, void* d_ws,
+                              size_t ws_bytes, cccl_stream_t stream) {
+    if (n_remote < 0 || n_remote > cccl::kMaxRanks - 1) return CCCL_ERR_INVALID_ARG;
+    if (n_remote > 0 && (h_ins == nullptr || h_in_bytes == nullptr)) return CCCL_ERR_INVALID_ARG;
+    if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_local) || !aligned16(d_out) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < cccl_workspace_bytes(n_elems)) return CCCL_ERR_INVALID_ARG;
+    if (out_capacity < cccl_compress_bound(n_elems)) return CCCL_ERR_CAPACITY;
+    if (!device_range(d_local, 2 * n_elems) || !device_range(d_out, out_capacity) || !device_range(d_ws, ws_bytes))
+        return CCCL_ERR_INVALID_ARG;
+    cccl::ReduceInputs inputs{};
+    inputs.local = d_local;
+    for (int r = 0; r < n_remote; ++r) {
+        if (!aligned16(h_ins[r]) || h_in_bytes[r] == 0 || !device_range(h_ins[r], h_in_bytes[r]))
+            return CCCL_ERR_INVALID_ARG;
+        inputs.in[r + 1] = static_cast<const uint8_t*>(h_ins[r]);
+        inputs.in_bytes[r + 1] = h_in_bytes[r];
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    if (cccl::launch_reduce(inputs, n_remote + 1, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s) !=
+        cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
 cccl_status cccl_get_result(const void* d_ws, cccl_stream_t stream, uint64_t* out_bytes, cccl_status* dev_status) {
     if (d_ws == nullptr || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
     cccl::WsHeader h{};

@@ -9,9 +9,13 @@ namespace cccl {
 
 constexpr int kMaxRanks = 64;
 
+// Rank r's operand: the compressed stream in[r] of in_bytes[r] bytes, except
+// that rank 0 is the uncompressed bf16 buffer `local` when it is not null
+// (the selective-compression reduce).
 struct ReduceInputs {
     const uint8_t* in[kMaxRanks];
     uint64_t in_bytes[kMaxRanks];
+    const uint16_t* local;
 };
 
 // All pointers are device pointers already validated by the C ABI layer; the

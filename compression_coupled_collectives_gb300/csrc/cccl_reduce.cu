@@ -126,6 +126,12 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
         bool ok = true;
         for (uint32_t idx = lane; idx < n_out * (uint32_t)R; idx += 32) {
             const uint32_t t = idx / (uint32_t)R, r = idx % (uint32_t)R;
+            if (r == 0 && inputs.local != nullptr) {  // uncompressed: chunk c is values 4096 c ..
+                const uint64_t c = c0 + t, left = so.n_elems - c * kChunkElems;
+                m.off[t][r] = 2 * kChunkElems * c;
+                m.bytes[t][r] = 2 * (uint32_t)(left < kChunkElems ? left : kChunkElems);
+                continue;
+            }
             const ChunkView v = locate_chunk(inputs.in[r], inputs.in_bytes[r], so.n_elems, so.n_chunks, c0 + t);
             m.off[t][r] = v.offset;
             m.bytes[t][r] = v.bytes;
@@ -156,8 +162,14 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
                 }
                 if (lane == 0) {
                     fence_proxy_async_smem();
-                    bulk_load(ring + ((size_t)t * kRSlots + s) * kMaxChunkBytes, inputs.in[r] + m.off[t][r],
-                              m.bytes[t][r], &sm.full[t][s]);
+                    uint8_t* slot = ring + ((size_t)t * kRSlots + s) * kMaxChunkBytes;
+                    if (r != 0 || inputs.local == nullptr)
+                        bulk_load(slot, inputs.in[r] + m.off[t][r], m.bytes[t][r], &sm.full[t][s]);
+                    else if (m.bytes[t][r] == 2 * kChunkElems)  // a full local chunk, staged raw
+                        bulk_load(slot, reinterpret_cast<const uint8_t*>(inputs.local) + m.off[t][r],
+                                  2 * kChunkElems, &sm.full[t][s]);
+                    else  // the partial local chunk is read in place by the team
+                        mbar_arrive(&sm.full[t][s]);
                 }
                 __syncwarp();
                 ++ut[t];
@@ -205,8 +217,8 @@ __device__ __forceinline__ void reduce_placer(const StreamOut& so, ReduceSmem& s
 }
 
 // --------------------------------------------------------------------------- teams
-__device__ __forceinline__ void reduce_team(int R, const StreamOut& so, const uint8_t* ring_base, uint32_t* prev_base,
-                                            ReduceSmem& sm) {
+__device__ __forceinline__ void reduce_team(int R, const uint16_t* local, const StreamOut& so,
+                                            const uint8_t* ring_base, uint32_t* prev_base, ReduceSmem& sm) {
     const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127;
     const uint32_t wq = tt >> 5;  // warp within the team = quarter of the chunk
     const TeamBarrier bar{1u + team};
@@ -248,7 +260,34 @@ __device__ __forceinline__ void reduce_team(int R, const StreamOut& so, const ui
                         if (tt == 0) set_abort(so, sm);
                         return;  // the whole team
                     }
-                    if (fail == 0) {
+                    if (fail == 0 && r == 0 && local != nullptr) {
+                        // the uncompressed local operand: staged raw, or read in place
+                        uint32_t V[16];
+                        if (n_c == kChunkElems) {
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) {
+                                const uint4 v =
+                                    *reinterpret_cast<const uint4*>(buf + 512 * (4 * wq + jj) + 16 * lane);
+                                V[4 * jj] = v.x;
+                                V[4 * jj + 1] = v.y;
+                                V[4 * jj + 2] = v.z;
+                                V[4 * jj + 3] = v.w;
+                            }
+                        } else {
+                            const uint16_t* vals = local + c * kChunkElems;
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                                for (int x = 0; x < 4; ++x) {
+                                    const uint32_t e = 256 * (4 * wq + jj) + 8 * lane + 2 * x;
+                                    const uint32_t lo = e < n_c ? vals[e] : 0u, hi = e + 1 < n_c ? vals[e + 1] : 0u;
+                                    V[4 * jj + x] = lo | (hi << 16);
+                                }
+                        }
+                        special = true;
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) acc[x] = widen_pair(V[x]);
+                    } else if (fail == 0) {
                         const ChunkHeader h = read_chunk_header(buf);
                         bool good = chunk_header_valid(h, m.bytes[team][r], n_c);  // same for the team
                         uint32_t V[16];
@@ -388,7 +427,7 @@ __global__ void __launch_bounds__(kReduceThreads, 1) reduce_kernel(ReduceInputs 
     else if (w == kPlacerWarp)
         reduce_placer(so, sm);
     else
-        reduce_team(R, so, ring, prev, sm);
+        reduce_team(R, inputs.local, so, ring, prev, sm);
 }
 
 cudaError_t launch_reduce(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,

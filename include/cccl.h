@@ -166,6 +166,25 @@ cccl_status cccl_reduce_compressed(const void *const *h_ins, const size_t *h_in_
                                    void *d_out, size_t out_capacity, void *d_ws, size_t ws_bytes,
                                    cccl_stream_t stream);
 
+/* The selective-compression reduce step (section 5, "Selective compression
+ * across collective stages": an intermediate reduction merges the locally
+ * available, uncompressed data with received compressed partial results, and
+ * only the remote data are decompressed).
+ *   d_local       n_elems uint16 bf16 bit patterns, uncompressed: rank 0.
+ *   h_ins         host array of n_remote device pointers to compressed
+ *                 streams made for n_elems values (ranks 1..n_remote);
+ *                 h_in_bytes their readable sizes.  0 <= n_remote <= 63
+ *                 (both arrays may be NULL when n_remote is 0).
+ *   d_out, d_ws   as for cccl_reduce_compressed.
+ * The result is that of cccl_reduce_compressed on the R = n_remote + 1 ranks
+ * with rank 0's operand given uncompressed: acc = local[i] in binary32, then
+ * the remote ranks added in order, one rounding to bf16 (every NaN becomes
+ * 0x7FC0), compressed as cccl_compress would.
+ * Returns INVALID_ARG, CAPACITY, CUDA or OK synchronously. */
+cccl_status cccl_reduce_mixed(const uint16_t *d_local, const void *const *h_ins, const size_t *h_in_bytes,
+                              int n_remote, size_t n_elems, void *d_out, size_t out_capacity, void *d_ws,
+                              size_t ws_bytes, cccl_stream_t stream);
+
 /* Wait for the work enqueued on `stream` and read the outcome stored in the
  * workspace of the last call that used it.
  *   out_bytes     (may be NULL) the compressed stream size of a compress or

@@ -32,7 +32,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["cccl_compress_bound", "cccl_workspace_bytes", "cccl_compress", "cccl_compress_noalloc",
-                            "cccl_decompress", "cccl_reduce_compressed", "cccl_get_result",
+                            "cccl_decompress", "cccl_reduce_compressed", "cccl_reduce_mixed", "cccl_get_result",
                             "cccl_status_string"]), names
 
 
@@ -87,6 +87,14 @@ def test_host_side_argument_checks(cc):
     assert lib.cccl_reduce_compressed(ptrs, sizes, 2, n, B, bound - 1, W, wsb, None) == cc.CCCL_ERR_CAPACITY
     bad = (ctypes.c_void_p * 2)(A, A + 8)
     assert lib.cccl_reduce_compressed(bad, sizes, 2, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_mixed(A, ptrs, sizes, -1, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_mixed(A, ptrs, sizes, 64, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_mixed(A, None, sizes, 2, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_mixed(A + 2, ptrs, sizes, 2, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_mixed(None, None, None, 0, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_mixed(A, ptrs, sizes, 2, 0, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_mixed(A, ptrs, sizes, 2, n, B, bound - 1, W, wsb, None) == cc.CCCL_ERR_CAPACITY
+    assert lib.cccl_reduce_mixed(A, ptrs, sizes, 2, n, B, bound, W, wsb - 16, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_get_result(None, None, None, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_get_result(W + 4, None, None, None) == cc.CCCL_ERR_INVALID_ARG
 

@@ -311,6 +311,51 @@ def test_reduce_rejects_corrupt_input(cc, orc, wl):
         assert st == cc.CCCL_ERR_CORRUPT, name
 
 
+# ---------------------------------------------------------------- selective-compression reduce
+def check_reduce_mixed(cc, orc, local, xs, what=""):
+    n = local.size
+    refs = [orc.compress(x) for x in xs]
+    streams = [cc.compress(dev(x)) for x in xs]
+    got = cc.reduce_mixed(dev(local), streams).cpu().numpy()
+    want = orc.reduce_mixed(local, refs, n)
+    assert np.array_equal(got, want), "%s: reduced stream differs (%d vs %d bytes)" % (what, got.size, want.size)
+
+
+@pytest.mark.parametrize("n_remote", [0, 1, 2, 4, 9])
+@pytest.mark.parametrize("n", [100, CHUNK, 7 * CHUNK + 33, 40 * CHUNK])
+def test_reduce_mixed(cc, orc, wl, n_remote, n):
+    local = wl.generate(3, 7, count=n)
+    xs = [wl.generate(3, r, count=n) for r in range(n_remote)]
+    check_reduce_mixed(cc, orc, local, xs, "n=%d remote=%d" % (n, n_remote))
+
+
+def test_reduce_mixed_special_and_raw_chunks(cc, orc, wl):
+    n = 9 * CHUNK + 1001
+    start = (1 << 27) - 4 * CHUNK  # across the uniform / special-value boundary of workload 5
+    local = wl.generate(5, 0, start=start, count=n)
+    xs = [wl.generate(5, r, start=start, count=n) for r in range(1, 4)]
+    check_reduce_mixed(cc, orc, local, xs, "workload 5")
+
+
+def test_reduce_mixed_full_gradient_buffer(cc, orc, wl):
+    n = 1 << 22  # 128 chunk groups of the 64 MiB gradient-like workload
+    local = wl.generate(2, 0, count=n)
+    check_reduce_mixed(cc, orc, local, [wl.generate(3, 1, count=n)], "gradient")
+
+
+def test_reduce_mixed_rejects_corrupt_remote(cc, orc, wl):
+    n = 3 * CHUNK + 10
+    local = dev(wl.generate(2, 0, count=n, n=1 << 20))
+    good = torch.from_numpy(orc.compress(wl.generate(2, 0, count=n, n=1 << 20))).cuda()
+    for name, bad in _corrupt_variants(orc, wl):
+        d = torch.from_numpy(np.frombuffer(bad, np.uint8).copy()).cuda()
+        out = cc.empty_stream(n)
+        ws = cc.empty_workspace(n)
+        cc.cccl_reduce_mixed(local, [good, d], out, ws)
+        _, st = cc.cccl_get_result(ws)
+        assert st == cc.CCCL_ERR_CORRUPT, name
+
+
 def test_argument_errors(cc):
     n = 5 * CHUNK
     x = torch.zeros(n, dtype=torch.int16, device="cuda")
