@@ -1,72 +1,139 @@
-// cccl_decompress.cu -- the decompress kernel: one CTA per chunk; the chunk
-// is staged in shared memory by one bulk (TMA) copy, then each thread
-// rebuilds its 32 values ("CCCL: In-GPU Compression-Coupled Collective
-// Communication", section 4.1 inverted; the "Decomp." stage of Figure 2).
+// cccl_decompress.cu -- the decompress kernel ("CCCL: In-GPU
+// Compression-Coupled Collective Communication", section 4.1 inverted; the
+// "Decomp." stage of Figure 2).
+//
+// Persistent: several CTAs per SM, each taking every gridDim-th chunk.  A CTA
+// has a producer warp, which locates its next chunks through the offset table
+// and stages them by bulk (TMA) copies in a ring of kDSlots buffers, and a
+// team of 4 decode warps, which rebuild 32 values per thread from each staged
+// chunk and store them with 16-byte writes.  So the location and the copy of
+// later chunks overlap the decoding of the current one.
 #include "cccl_decode.cuh"
 #include "cccl_launch.h"
 
 namespace cccl {
 
-__global__ void __launch_bounds__(kThreads)
+constexpr int kDSlots = 4;
+constexpr int kDTeamThreads = 128;
+constexpr int kDProducerWarp = 4;
+constexpr int kDThreads = kDTeamThreads + 32;
+constexpr int kDCtasPerSm = 6;
+
+struct DecompressSmem {
+    uint64_t full[kDSlots];   // the slot's chunk landed, or its meta says there is none
+    uint64_t free_[kDSlots];  // the team is done with the slot (1 arrival)
+    uint32_t bytes[kDSlots];  // staged chunk size
+    uint32_t ok[kDSlots];     // the chunk was located
+    uint32_t row_tot[4];
+    volatile uint32_t abort;
+};
+
+__global__ void __launch_bounds__(kDThreads)
     decompress_kernel(const uint8_t* __restrict__ s, uint64_t in_bytes, uint16_t* __restrict__ out, uint64_t n_elems,
                       uint64_t n_chunks, WsHeader* ws) {
-    __shared__ __align__(128) uint8_t buf[kMaxChunkBytes];
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ uint32_t s_bytes, s_ok;
-    __shared__ uint32_t row_tot[16];
+    __shared__ __align__(128) uint8_t ring[kDSlots][kMaxChunkBytes];
+    __shared__ DecompressSmem sm;
     const uint32_t t = threadIdx.x, lane = t & 31, q = t >> 5;
-    const uint64_t c = blockIdx.x;
-    const uint64_t left = n_elems - c * kChunkElems;
-    const uint32_t n_c = left < kChunkElems ? (uint32_t)left : kChunkElems;
-
     if (t == 0) {
-        const ChunkView v = locate_chunk(s, in_bytes, n_elems, n_chunks, c);
-        s_ok = v.ok;
-        s_bytes = v.bytes;
-        if (v.ok) {
-            mbar_init(&bar, 1);
-            fence_mbar_init();
-            bulk_load(buf, s + v.offset, v.bytes, &bar);
+        for (int i = 0; i < kDSlots; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.free_[i], 1);
         }
+        sm.abort = 0;
+        fence_mbar_init();
     }
     __syncthreads();
-    if (!s_ok) {
-        if (t == 0) record_error(ws, kStatusCorrupt);
+    const uint64_t stride = gridDim.x;
+
+    if (q == kDProducerWarp) {
+        // ------------------------------------------------------------ producer
+        uint32_t i = 0;
+        for (uint64_t c = blockIdx.x; c < n_chunks; c += stride, ++i) {
+            const uint32_t slot = i % kDSlots;
+            if (i >= (uint32_t)kDSlots &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait(&sm.free_[slot], (i / kDSlots - 1) & 1u))) {
+                if (lane == 0) {
+                    record_error(ws, kStatusTimeout);
+                    sm.abort = 1;
+                }
+                break;
+            }
+            if (__any_sync(0xFFFFFFFFu, sm.abort != 0)) break;
+            if (lane == 0) {
+                const ChunkView v = locate_chunk(s, in_bytes, n_elems, n_chunks, c);
+                sm.ok[slot] = v.ok;
+                sm.bytes[slot] = v.bytes;
+                if (v.ok) {
+                    fence_proxy_async_smem();
+                    bulk_load(ring[slot], s + v.offset, v.bytes, &sm.full[slot]);
+                } else {
+                    mbar_arrive(&sm.full[slot]);  // nothing to stage; the team reports it
+                }
+            }
+            __syncwarp();
+        }
+        // no copy may still be landing when the CTA exits
+        for (uint32_t v = i > (uint32_t)kDSlots ? i - kDSlots : 0u; v < i; ++v)
+            mbar_wait(&sm.full[v % kDSlots], (v / kDSlots) & 1u);
         return;
     }
-    const bool arrived = mbar_wait(&bar, 0);
-    if (__syncthreads_or(!arrived)) {
-        if (t == 0) record_error(ws, kStatusTimeout);
-        return;
-    }
-    const ChunkHeader h = read_chunk_header(buf);
-    if (!chunk_header_valid(h, s_bytes, n_c)) {
-        if (t == 0) record_error(ws, kStatusCorrupt);
-        return;
-    }
-    uint16_t* dst = out + c * kChunkElems;
-    if (n_c < kChunkElems) {  // partial last chunk: raw by construction
-        const uint16_t* vals = reinterpret_cast<const uint16_t*>(buf + kChunkHeaderBytes);
-        for (uint32_t i = t; i < n_c; i += kThreads) dst[i] = vals[i];
-        return;
-    }
-    uint32_t P[16];
-    bool special = false;
-    if (!decode_full_chunk(CtaBarrier{}, buf, h, P, row_tot, special)) {
-        if (t == 0) record_error(ws, kStatusCorrupt);
-        return;
-    }
+
+    // ---------------------------------------------------------------- decode team
+    const TeamBarrier bar{1u};
+    uint32_t i = 0;
+    for (uint64_t c = blockIdx.x; c < n_chunks; c += stride, ++i) {
+        const uint32_t slot = i % kDSlots;
+        const uint8_t* buf = ring[slot];
+        const bool landed = !sm.abort && mbar_wait(&sm.full[slot], (i / kDSlots) & 1u);
+        if (bar.any(!landed)) {
+            if (t == 0) {
+                record_error(ws, kStatusTimeout);
+                sm.abort = 1;
+            }
+            return;  // the whole team
+        }
+        const uint64_t left = n_elems - c * kChunkElems;
+        const uint32_t n_c = left < kChunkElems ? (uint32_t)left : kChunkElems;
+        uint16_t* dst = out + c * kChunkElems;
+        bool good = sm.ok[slot] != 0;
+        ChunkHeader h{};
+        if (good) {
+            h = read_chunk_header(buf);
+            good = chunk_header_valid(h, sm.bytes[slot], n_c);  // the same verdict for every thread
+        }
+        if (good) {
+            if (n_c < kChunkElems) {  // partial last chunk: raw by construction
+                const uint16_t* vals = reinterpret_cast<const uint16_t*>(buf + kChunkHeaderBytes);
+                for (uint32_t e = t; e < n_c; e += kDTeamThreads) dst[e] = vals[e];
+            } else {
+                uint32_t P[16];
+                bool special = false;
+                good = decode_full_chunk(bar, buf, h, P, sm.row_tot, special);
+                if (good) {
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-        *reinterpret_cast<uint4*>(dst + 256 * (4 * q + jj) + 8 * lane) =
-            make_uint4(P[4 * jj], P[4 * jj + 1], P[4 * jj + 2], P[4 * jj + 3]);
+                    for (int jj = 0; jj < 4; ++jj)
+                        *reinterpret_cast<uint4*>(dst + 256 * (4 * q + jj) + 8 * lane) =
+                            make_uint4(P[4 * jj], P[4 * jj + 1], P[4 * jj + 2], P[4 * jj + 3]);
+                }
+            }
+        }
+        if (!good && t == 0) record_error(ws, kStatusCorrupt);
+        bar.sync();  // the team is done with the slot and row_tot
+        if (t == 0) mbar_arrive(&sm.free_[slot]);
+    }
 }
 
 cudaError_t launch_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t n_elems, void* ws,
                               cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     const uint64_t n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
-    decompress_kernel<<<(unsigned)n_chunks, kThreads, 0, stream>>>(in, in_bytes, out, n_elems, n_chunks,
-                                                                   static_cast<WsHeader*>(ws));
+    const uint64_t slots = (uint64_t)sms * kDCtasPerSm;
+    const unsigned grid = (unsigned)(n_chunks < slots ? n_chunks : slots);
+    decompress_kernel<<<grid, kDThreads, 0, stream>>>(in, in_bytes, out, n_elems, n_chunks,
+                                                      static_cast<WsHeader*>(ws));
     return cudaGetLastError();
 }
 
