@@ -13,11 +13,11 @@
 
 namespace cccl {
 
-constexpr int kDSlots = 4;
+constexpr int kDSlots = 3;
 constexpr int kDTeamThreads = 128;
 constexpr int kDProducerWarp = 4;
 constexpr int kDThreads = kDTeamThreads + 32;
-constexpr int kDCtasPerSm = 6;
+constexpr int kDCtasPerSm = 8;
 
 struct DecompressSmem {
     uint64_t full[kDSlots];   // the slot's chunk landed, or its meta says there is none
