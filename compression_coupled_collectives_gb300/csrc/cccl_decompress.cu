@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kDThreads)
     uint32_t i = 0;
     for (uint64_t c = blockIdx.x; c < n_chunks; c += stride, ++i) {
         const uint32_t slot = i % kDSlots;
-        const uint8_t* buf = ring[slot];
+        uint8_t* buf = ring[slot];
         const bool landed = !sm.abort && mbar_wait(&sm.full[slot], (i / kDSlots) & 1u);
         if (bar.any(!landed)) {
             if (t == 0) {

@@ -218,11 +218,11 @@ __device__ __forceinline__ void reduce_placer(const StreamOut& so, ReduceSmem& s
 
 // --------------------------------------------------------------------------- teams
 __device__ __forceinline__ void reduce_team(int R, const uint16_t* local, const StreamOut& so,
-                                            const uint8_t* ring_base, uint32_t* prev_base, ReduceSmem& sm) {
+                                            uint8_t* ring_base, uint32_t* prev_base, ReduceSmem& sm) {
     const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127;
     const uint32_t wq = tt >> 5;  // warp within the team = quarter of the chunk
     const TeamBarrier bar{1u + team};
-    const uint8_t* ring = ring_base + (size_t)team * kRSlots * kMaxChunkBytes;
+    uint8_t* ring = ring_base + (size_t)team * kRSlots * kMaxChunkBytes;
     uint32_t* prev_st = prev_base + (size_t)team * kPrevWords * kTeamThreads + tt;  // word w at prev_st[128 w]
     const uint64_t n_full = so.n_elems / kChunkElems;
     uint32_t u = 0;  // rank chunks consumed (the loader's order for this team)
@@ -254,7 +254,7 @@ __device__ __forceinline__ void reduce_team(int R, const uint16_t* local, const 
                 bool special = false;
                 for (int r = 0; r < R; ++r, ++u) {
                     const uint32_t s = u % kRSlots;
-                    const uint8_t* buf = ring + (size_t)s * kMaxChunkBytes;
+                    uint8_t* buf = ring + (size_t)s * kMaxChunkBytes;
                     const bool landed = !sm.abort && mbar_wait(&sm.full[team][s], (u / kRSlots) & 1u);
                     if (bar.any(!landed)) {
                         if (tt == 0) set_abort(so, sm);
