@@ -63,8 +63,10 @@ def _bind(path: str):
                                   u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_reduce_mixed.argtypes = [u16p, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(sz), ctypes.c_int,
                                         sz, u8p, sz, ctypes.POINTER(sz)]
+    lib.oracle_compress_paged.argtypes = [u16p, sz, ctypes.c_void_p, sz, u8p, sz, ctypes.POINTER(sz)]
+    lib.oracle_decompress_paged.argtypes = [u8p, sz, u16p, sz, ctypes.c_void_p, sz]
     for f in ("oracle_chunk_choice", "oracle_encode_chunk", "oracle_compress", "oracle_decompress",
-              "oracle_reduce", "oracle_reduce_mixed"):
+              "oracle_reduce", "oracle_reduce_mixed", "oracle_compress_paged", "oracle_decompress_paged"):
         getattr(lib, f).restype = ctypes.c_int
     lib.oracle_sum_ranks.restype = None
     lib.oracle_plane_position.restype = None
@@ -228,6 +230,32 @@ def reduce_mixed(local, streams, n: int) -> np.ndarray:
     if st != OK:
         raise OracleError(st, "oracle_reduce_mixed")
     return out[:nb.value]
+
+
+def compress_paged(pool, block_elems: int, table) -> np.ndarray:
+    """Stream of the blocks pool[table[i]] (block_elems values each), in order."""
+    pool = _u16(pool).reshape(-1)
+    tab = np.ascontiguousarray(table, dtype=np.int32)
+    n = tab.size * block_elems
+    cap = compress_bound(n)
+    out = np.empty(cap, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_compress_paged(pool.ctypes.data, block_elems, tab.ctypes.data, tab.size, out.ctypes.data,
+                                       cap, ctypes.byref(nb))
+    if st != OK:
+        raise OracleError(st, "oracle_compress_paged")
+    return out[:nb.value]
+
+
+def decompress_paged(s, pool, block_elems: int, table) -> np.ndarray:
+    """A copy of ``pool`` with the stream's blocks written where the table says."""
+    b = np.ascontiguousarray(s, dtype=np.uint8)
+    out = _u16(pool).reshape(-1).copy()
+    tab = np.ascontiguousarray(table, dtype=np.int32)
+    st = _load().oracle_decompress_paged(b.ctypes.data, b.size, out.ctypes.data, block_elems, tab.ctypes.data, tab.size)
+    if st != OK:
+        raise OracleError(st, "oracle_decompress_paged")
+    return out
 
 
 def reduce(streams, n: int) -> np.ndarray:

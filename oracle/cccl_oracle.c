@@ -584,3 +584,43 @@ int oracle_reduce_mixed(const uint16_t *local, const uint8_t *const *ins, const 
     free(sum);
     return st;
 }
+
+/* Paged payload (Figure 3 and section 6.2: KV-cache blocks sent between
+ * prefill and decode instances).  The logical buffer is the concatenation of
+ * n_blocks blocks of block_elems values, block i being pool block table[i];
+ * block_elems is a multiple of 4096, so no chunk straddles two blocks.
+ * compress_paged compresses the gathered buffer; decompress_paged writes the
+ * decompressed buffer back into the pool blocks named by the table (which
+ * must be distinct). */
+int oracle_compress_paged(const uint16_t *pool, size_t block_elems, const int32_t *table, size_t n_blocks,
+                          uint8_t *out, size_t capacity, size_t *out_bytes)
+{
+    if (pool == NULL || table == NULL || n_blocks == 0 || block_elems == 0 || block_elems % CHUNK_ELEMS != 0)
+        return ORC_ERR_INVALID_ARG;
+    const size_t n = n_blocks * block_elems;
+    uint16_t *x = (uint16_t *)malloc(n * sizeof(uint16_t));
+    if (!x)
+        return ORC_ERR_INVALID_ARG;
+    for (size_t i = 0; i < n_blocks; i++)
+        memcpy(x + i * block_elems, pool + (size_t)table[i] * block_elems, block_elems * sizeof(uint16_t));
+    int st = oracle_compress(x, n, out, capacity, out_bytes);
+    free(x);
+    return st;
+}
+
+int oracle_decompress_paged(const uint8_t *s, size_t s_bytes, uint16_t *pool, size_t block_elems, const int32_t *table,
+                            size_t n_blocks)
+{
+    if (pool == NULL || table == NULL || n_blocks == 0 || block_elems == 0 || block_elems % CHUNK_ELEMS != 0)
+        return ORC_ERR_INVALID_ARG;
+    const size_t n = n_blocks * block_elems;
+    uint16_t *x = (uint16_t *)malloc(n * sizeof(uint16_t));
+    if (!x)
+        return ORC_ERR_INVALID_ARG;
+    int st = oracle_decompress(s, s_bytes, x, n);
+    if (st == ORC_OK)
+        for (size_t i = 0; i < n_blocks; i++)
+            memcpy(pool + (size_t)table[i] * block_elems, x + i * block_elems, block_elems * sizeof(uint16_t));
+    free(x);
+    return st;
+}

@@ -41,6 +41,10 @@ MUTATIONS = [
      "put_u64(out + STREAM_HEADER_BYTES + 8 * c, pos - start);"),
     ("mixed_remote_ranks_reversed", "st = oracle_decompress(ins[r - 1], in_bytes[r - 1], x, n);",
      "st = oracle_decompress(ins[R - 1 - r], in_bytes[R - 1 - r], x, n);"),
+    ("paged_gather_ignores_table", "memcpy(x + i * block_elems, pool + (size_t)table[i] * block_elems,",
+     "memcpy(x + i * block_elems, pool + i * block_elems,"),
+    ("paged_scatter_ignores_table", "memcpy(pool + (size_t)table[i] * block_elems, x + i * block_elems,",
+     "memcpy(pool + i * block_elems, x + i * block_elems,"),
     ("mixed_local_added_last", "oracle_sum_ranks(xs, R, n, sum);",
      "{ const uint16_t *t = xs[0]; for (int r = 0; r + 1 < R; r++) xs[r] = xs[r + 1]; xs[R - 1] = t; "
      "oracle_sum_ranks(xs, R, n, sum); for (int r = R - 1; r > 0; r--) xs[r] = xs[r - 1]; xs[0] = t; }"),
@@ -106,6 +110,13 @@ def _battery(orc, wl):
     # local 2^30, remote -2^30 then 1: (2^30 - 2^30) + 1 = 1 only in this order
     check("mixed_rank_order", lambda: orc.decompress(
         orc.reduce_mixed(sp_a[3:], [orc.compress(sp_b[3:]), orc.compress(sp_c[3:])], 1), 1)[0] == 0x3F80)
+    pool = np.arange(6 * CHUNK, dtype=np.uint16) * 7 + 1
+    tab = np.array([4, 1, 3], np.int32)
+    check("paged_gather", lambda: np.array_equal(orc.compress_paged(pool, CHUNK, tab),
+                                                 orc.compress(pool.reshape(-1, CHUNK)[tab].reshape(-1))))
+    check("paged_scatter", lambda: np.array_equal(
+        orc.decompress_paged(orc.compress(pool[:3 * CHUNK]), np.zeros_like(pool), CHUNK, tab).reshape(-1, CHUNK)[tab],
+        pool[:3 * CHUNK].reshape(-1, CHUNK)))
     return failed
 
 

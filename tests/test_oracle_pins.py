@@ -366,6 +366,29 @@ def test_reduce_mixed_order_and_nan(orc):
     assert np.array_equal(orc.decompress(orc.reduce_mixed(x, [], 3), 3), np.array([0x7FC0, 0x3F80, 0x7FC0], np.uint16))
 
 
+def test_paged_compress_is_compress_of_the_gathered_blocks(orc, wl):
+    B = 4 * CHUNK  # 16 tokens x 8 heads x 128 dim of the KV-cache shape
+    pool = wl.generate(4, 0, count=9 * B)
+    for table in ([0, 1, 2], [7, 2, 2, 0, 8], list(range(9))[::-1]):
+        tab = np.array(table, np.int32)
+        gathered = pool.reshape(-1, B)[tab].reshape(-1)
+        assert np.array_equal(orc.compress_paged(pool, B, tab), orc.compress(gathered))
+    with pytest.raises(orc.OracleError):
+        orc.compress_paged(pool, B + 8, np.array([0], np.int32))
+
+
+def test_paged_round_trip_writes_only_the_named_blocks(orc, wl):
+    B = 2 * CHUNK
+    pool = wl.generate(4, 1, count=10 * B)
+    tab = np.array([6, 1, 9, 3], np.int32)
+    s = orc.compress_paged(pool, B, tab)
+    target = np.full(10 * B, 0x1234, np.uint16)
+    out = orc.decompress_paged(s, target, B, tab).reshape(-1, B)
+    want = target.reshape(-1, B).copy()
+    want[tab] = pool.reshape(-1, B)[tab]
+    assert np.array_equal(out, want)
+
+
 # ---------------------------------------------------------------- corrupt streams
 def _corrupt_cases(orc, wl):
     x = wl.generate(2, 0, count=3 * CHUNK + 10, n=1 << 20)
