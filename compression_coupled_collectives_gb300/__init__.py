@@ -46,6 +46,10 @@ _lib.cccl_decompress.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_decompress.restype = _i
 _lib.cccl_reduce_compressed.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_reduce_compressed.restype = _i
+_lib.cccl_compress_paged.argtypes = [_vp, _sz, _sz, _vp, _sz, _vp, _sz, _vp, _sz, _vp]
+_lib.cccl_compress_paged.restype = _i
+_lib.cccl_decompress_paged.argtypes = [_vp, _sz, _vp, _sz, _sz, _vp, _sz, _vp, _sz, _vp]
+_lib.cccl_decompress_paged.restype = _i
 _lib.cccl_reduce_mixed.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_reduce_mixed.restype = _i
 _lib.cccl_get_result.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_i)]
@@ -128,6 +132,30 @@ def cccl_reduce_compressed(ins: Sequence[torch.Tensor], n_elems: int, out: torch
     _check(_lib.cccl_reduce_compressed(ptrs, szs, R, n_elems, out.data_ptr(), out.numel() * out.element_size(),
                                        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
            "cccl_reduce_compressed")
+
+
+def cccl_compress_paged(pool: torch.Tensor, block_elems: int, table: torch.Tensor, out: torch.Tensor,
+                        ws: torch.Tensor, stream=None) -> None:
+    """Enqueue compression of the pool blocks named by ``table`` (int32, on the
+    device), in table order; ``pool`` holds whole blocks of block_elems values."""
+    pool = _bf16_bits(pool)
+    if table.dtype != torch.int32 or not table.is_contiguous():
+        raise TypeError("expected a contiguous int32 block table")
+    _check(_lib.cccl_compress_paged(pool.data_ptr(), pool.numel() // block_elems, block_elems, table.data_ptr(),
+                                    table.numel(), out.data_ptr(), out.numel() * out.element_size(), ws.data_ptr(),
+                                    ws.numel() * ws.element_size(), _stream(stream)), "cccl_compress_paged")
+
+
+def cccl_decompress_paged(s: torch.Tensor, pool: torch.Tensor, block_elems: int, table: torch.Tensor,
+                          ws: torch.Tensor, in_bytes: int | None = None, stream=None) -> None:
+    """Enqueue decompression of stream ``s`` into the pool blocks named by ``table``."""
+    pool = _bf16_bits(pool)
+    if table.dtype != torch.int32 or not table.is_contiguous():
+        raise TypeError("expected a contiguous int32 block table")
+    nbytes = s.numel() * s.element_size() if in_bytes is None else int(in_bytes)
+    _check(_lib.cccl_decompress_paged(s.data_ptr(), nbytes, pool.data_ptr(), pool.numel() // block_elems,
+                                      block_elems, table.data_ptr(), table.numel(), ws.data_ptr(),
+                                      ws.numel() * ws.element_size(), _stream(stream)), "cccl_decompress_paged")
 
 
 def cccl_reduce_mixed(local: torch.Tensor, remote: Sequence[torch.Tensor], out: torch.Tensor, ws: torch.Tensor,

@@ -78,7 +78,8 @@ cccl_status cccl_compress(const uint16_t* d_in, size_t n_elems, void* d_out, siz
         return CCCL_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
-    if (cccl::launch_compress(d_in, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s) != cudaSuccess)
+    if (cccl::launch_compress(d_in, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s,
+                              cccl::Paging{nullptr, 1, 0}) != cudaSuccess)
         return CCCL_ERR_CUDA;
     return CCCL_OK;
 }
@@ -104,7 +105,8 @@ cccl_status cccl_decompress(const void* d_in, size_t in_bytes, uint16_t* d_out, 
         return CCCL_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (clear_ws(d_ws, sizeof(cccl::WsHeader), s) != CCCL_OK) return CCCL_ERR_CUDA;
-    if (cccl::launch_decompress(static_cast<const uint8_t*>(d_in), in_bytes, d_out, n_elems, d_ws, s) != cudaSuccess)
+    if (cccl::launch_decompress(static_cast<const uint8_t*>(d_in), in_bytes, d_out, n_elems, d_ws, s,
+                                cccl::Paging{nullptr, 1, 0}) != cudaSuccess)
         return CCCL_ERR_CUDA;
     return CCCL_OK;
 }
@@ -128,6 +130,58 @@ cccl_status cccl_reduce_compressed(const void* const* h_ins, const size_t* h_in_
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
     if (cccl::launch_reduce(inputs, R, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
+// Checks shared by the paged entry points; sets n_elems.
+static cccl_status check_paged(const uint16_t* d_pool, size_t pool_blocks, size_t block_elems, const int32_t* d_table,
+                               size_t n_blocks, size_t* n_elems) {
+    if (block_elems == 0 || block_elems % kChunkElems != 0 || pool_blocks == 0 || n_blocks == 0)
+        return CCCL_ERR_INVALID_ARG;
+    if (pool_blocks > CCCL_MAX_ELEMS / block_elems || n_blocks > CCCL_MAX_ELEMS / block_elems ||
+        pool_blocks > (size_t)INT32_MAX + 1)
+        return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_pool) || d_table == nullptr || (reinterpret_cast<uintptr_t>(d_table) & 3) != 0)
+        return CCCL_ERR_INVALID_ARG;
+    if (!device_range(d_pool, 2 * pool_blocks * block_elems) || !device_range(d_table, 4 * n_blocks))
+        return CCCL_ERR_INVALID_ARG;
+    *n_elems = n_blocks * block_elems;
+    return CCCL_OK;
+}
+
+cccl_status cccl_compress_paged(const uint16_t* d_pool, size_t pool_blocks, size_t block_elems, const int32_t* d_table,
+                                size_t n_blocks, void* d_out, size_t out_capacity, void* d_ws, size_t ws_bytes,
+                                cccl_stream_t stream) {
+    size_t n_elems = 0;
+    const cccl_status st = check_paged(d_pool, pool_blocks, block_elems, d_table, n_blocks, &n_elems);
+    if (st != CCCL_OK) return st;
+    if (!aligned16(d_out) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < cccl_workspace_bytes(n_elems)) return CCCL_ERR_INVALID_ARG;
+    if (out_capacity < cccl_compress_bound(n_elems)) return CCCL_ERR_CAPACITY;
+    if (!device_range(d_out, out_capacity) || !device_range(d_ws, ws_bytes)) return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    const cccl::Paging pg{d_table, block_elems / kChunkElems, pool_blocks};
+    if (cccl::launch_compress(d_pool, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s, pg) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
+cccl_status cccl_decompress_paged(const void* d_in, size_t in_bytes, uint16_t* d_pool, size_t pool_blocks,
+                                  size_t block_elems, const int32_t* d_table, size_t n_blocks, void* d_ws,
+                                  size_t ws_bytes, cccl_stream_t stream) {
+    size_t n_elems = 0;
+    const cccl_status st = check_paged(d_pool, pool_blocks, block_elems, d_table, n_blocks, &n_elems);
+    if (st != CCCL_OK) return st;
+    if (in_bytes == 0 || !aligned16(d_in) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < sizeof(cccl::WsHeader)) return CCCL_ERR_INVALID_ARG;
+    if (!device_range(d_in, in_bytes) || !device_range(d_ws, ws_bytes)) return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, sizeof(cccl::WsHeader), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    const cccl::Paging pg{d_table, block_elems / kChunkElems, pool_blocks};
+    if (cccl::launch_decompress(static_cast<const uint8_t*>(d_in), in_bytes, d_pool, n_elems, d_ws, s, pg) !=
+        cudaSuccess)
         return CCCL_ERR_CUDA;
     return CCCL_OK;
 }

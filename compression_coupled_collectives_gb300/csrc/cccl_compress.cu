@@ -45,17 +45,20 @@ struct CompressSmem {
 };
 
 // Control lane: fill stage s with group g (or mark it empty).
-__device__ __forceinline__ void issue_group(const uint16_t* in, uint64_t g, uint64_t n_groups, uint64_t n_full,
-                                            uint8_t* stage, CompressSmem& sm, int s) {
+__device__ __forceinline__ void issue_group(const uint16_t* in, const Paging& pg, WsHeader* ws, uint64_t g,
+                                            uint64_t n_groups, uint64_t n_full, uint8_t* stage, CompressSmem& sm,
+                                            int s) {
     sm.group[s] = g;
     sm.tally[s] = 0;
     for (int w = 0; w < kGroup; ++w) {
         const uint64_t c = g * kGroup + w;
-        if (g < n_groups && c < n_full)
-            bulk_load(stage + ((size_t)s * kGroup + w) * kChunkBytesRaw, in + c * kChunkElems, kChunkBytesRaw,
-                      &sm.load[s][w]);
-        else
+        const uint64_t e = g < n_groups && c < n_full ? chunk_elem_offset(pg, c) : kBadChunk;
+        if (e != kBadChunk) {
+            bulk_load(stage + ((size_t)s * kGroup + w) * kChunkBytesRaw, in + e, kChunkBytesRaw, &sm.load[s][w]);
+        } else {
+            if (g < n_groups && c < n_full) record_error(ws, kStatusInvalidArg);  // a block outside the pool
             mbar_arrive(&sm.load[s][w]);  // nothing to copy: complete the phase at once
+        }
     }
 }
 
@@ -115,7 +118,7 @@ __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__
                         write_chunk_warp(prev.regs, prev.plan, stage + ((size_t)sp * kGroup + w) * kChunkBytesRaw,
                                          dst);
                     } else {
-                        const uint16_t* src = in + prev.c * kChunkElems;
+                        const uint16_t* src = in + prev.c * kChunkElems;  // a partial chunk is never paged
                         write_tail_chunk_warp([src](uint32_t e) { return src[e]; },
                                               (uint32_t)(so.n_elems - prev.c * kChunkElems), dst);
                     }
@@ -131,7 +134,8 @@ __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__
     return live;
 }
 
-__global__ void __launch_bounds__(kCompressThreads, 1) compress_kernel(const uint16_t* __restrict__ in, StreamOut so) {
+__global__ void __launch_bounds__(kCompressThreads, 1)
+    compress_kernel(const uint16_t* __restrict__ in, Paging pg, StreamOut so) {
     extern __shared__ __align__(128) uint8_t stage[];
     __shared__ CompressSmem sm;
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -157,12 +161,12 @@ __global__ void __launch_bounds__(kCompressThreads, 1) compress_kernel(const uin
         // stages free up.  (Taken all at once, every CTA's third ticket would
         // be sized two iterations later than its number says, and every
         // look-back behind it would wait for that.)
-        if (lane == 0) issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 0);
+        if (lane == 0) issue_group(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 0);
         __syncwarp();
         const bool first_landed = __all_sync(0xFFFFFFFFu, mbar_wait(&sm.load[0][0], 0u));
         if (lane == 0) {
             if (!first_landed) record_error(so.ws, kStatusTimeout);
-            issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 1);
+            issue_group(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 1);
         }
         __syncwarp();
         for (int i = 0;; ++i) {
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(kCompressThreads, 1) compress_kernel(const uin
                 break;
             }
             if (i == 0) {
-                if (lane == 0) issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 2);
+                if (lane == 0) issue_group(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 2);
                 __syncwarp();
             }
             const uint32_t mine = lane < (uint32_t)kGroup ? sm.size[s][lane] : 0u;
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(kCompressThreads, 1) compress_kernel(const uin
                 }
                 if (lane == 0) {
                     fence_proxy_async_smem();
-                    issue_group(in, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, sp);
+                    issue_group(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, sp);
                 }
                 __syncwarp();
             }
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kCompressThreads, 1) compress_kernel(const uin
 }
 
 cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const Paging& pg) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
@@ -238,7 +242,7 @@ cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, 
     so.n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
     const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
     const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
-    compress_kernel<<<grid, kCompressThreads, kCompressSmemBytes, stream>>>(in, so);
+    compress_kernel<<<grid, kCompressThreads, kCompressSmemBytes, stream>>>(in, pg, so);
     return cudaGetLastError();
 }
 
@@ -294,7 +298,7 @@ cudaError_t launch_compress_noalloc(const uint16_t* in, uint64_t n_elems, uint8_
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(out, 0, kStreamHeaderBytes, stream);
     if (e != cudaSuccess) return e;
-    return launch_compress(in, n_elems, out, capacity, scratch, stream);
+    return launch_compress(in, n_elems, out, capacity, scratch, stream, Paging{nullptr, 1, 0});
 }
 
 }  // namespace cccl

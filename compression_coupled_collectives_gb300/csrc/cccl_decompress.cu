@@ -29,8 +29,8 @@ struct DecompressSmem {
 };
 
 __global__ void __launch_bounds__(kDThreads)
-    decompress_kernel(const uint8_t* __restrict__ s, uint64_t in_bytes, uint16_t* __restrict__ out, uint64_t n_elems,
-                      uint64_t n_chunks, WsHeader* ws) {
+    decompress_kernel(const uint8_t* __restrict__ s, uint64_t in_bytes, uint16_t* __restrict__ out, Paging pg,
+                      uint64_t n_elems, uint64_t n_chunks, WsHeader* ws) {
     __shared__ __align__(128) uint8_t ring[kDSlots][kMaxChunkBytes];
     __shared__ DecompressSmem sm;
     const uint32_t t = threadIdx.x, lane = t & 31, q = t >> 5;
@@ -94,8 +94,10 @@ __global__ void __launch_bounds__(kDThreads)
         }
         const uint64_t left = n_elems - c * kChunkElems;
         const uint32_t n_c = left < kChunkElems ? (uint32_t)left : kChunkElems;
-        uint16_t* dst = out + c * kChunkElems;
-        bool good = sm.ok[slot] != 0;
+        const uint64_t e = chunk_elem_offset(pg, c);
+        uint16_t* dst = out + e;
+        if (e == kBadChunk && t == 0) record_error(ws, kStatusInvalidArg);  // a block outside the pool
+        bool good = sm.ok[slot] != 0 && e != kBadChunk;
         ChunkHeader h{};
         if (good) {
             h = read_chunk_header(buf);
@@ -117,14 +119,14 @@ __global__ void __launch_bounds__(kDThreads)
                 }
             }
         }
-        if (!good && t == 0) record_error(ws, kStatusCorrupt);
+        if (!good && e != kBadChunk && t == 0) record_error(ws, kStatusCorrupt);
         bar.sync();  // the team is done with the slot and row_tot
         if (t == 0) mbar_arrive(&sm.free_[slot]);
     }
 }
 
 cudaError_t launch_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t n_elems, void* ws,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const Paging& pg) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -132,7 +134,7 @@ cudaError_t launch_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* ou
     const uint64_t n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
     const uint64_t slots = (uint64_t)sms * kDCtasPerSm;
     const unsigned grid = (unsigned)(n_chunks < slots ? n_chunks : slots);
-    decompress_kernel<<<grid, kDThreads, 0, stream>>>(in, in_bytes, out, n_elems, n_chunks,
+    decompress_kernel<<<grid, kDThreads, 0, stream>>>(in, in_bytes, out, pg, n_elems, n_chunks,
                                                       static_cast<WsHeader*>(ws));
     return cudaGetLastError();
 }

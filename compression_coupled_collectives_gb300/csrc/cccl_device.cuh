@@ -34,6 +34,7 @@ constexpr uint32_t kModePacked = 0;
 constexpr uint32_t kModeRaw = 1;
 
 // device status codes (same values as cccl_status)
+constexpr uint32_t kStatusInvalidArg = 1;  // a block table entry outside its pool
 constexpr uint32_t kStatusCorrupt = 3;
 constexpr uint32_t kStatusTimeout = 4;
 
@@ -43,6 +44,24 @@ struct WsHeader {
     uint32_t error;        // 0 or the largest device status seen
     uint64_t total_bytes;  // stream size, written by the last chunk
 };
+
+// Where chunk c's 4096 values live: c * 4096 in a contiguous buffer (no
+// table), or in block table[c / chunks_per_block] of a pool of equal blocks
+// (a paged KV-cache payload).  Returns kBadChunk for a table entry outside
+// the pool.
+struct Paging {
+    const int32_t* table;       // device block table, or nullptr
+    uint64_t chunks_per_block;  // block_elems / 4096
+    uint64_t pool_blocks;
+};
+constexpr uint64_t kBadChunk = ~0ull;
+__device__ __forceinline__ uint64_t chunk_elem_offset(const Paging& pg, uint64_t c) {
+    if (pg.table == nullptr) return c * kChunkElems;
+    const uint64_t blk = c / pg.chunks_per_block, j = c - blk * pg.chunks_per_block;
+    const int32_t e = pg.table[blk];
+    if (e < 0 || (uint64_t)e >= pg.pool_blocks) return kBadChunk;
+    return ((uint64_t)e * pg.chunks_per_block + j) * kChunkElems;
+}
 
 // Placement word of the decoupled look-back: flag in bits 62..63.
 constexpr uint64_t kFlagAggregate = 1ull << 62;  // value = this chunk's bytes

@@ -364,14 +364,13 @@ __device__ __forceinline__ void write_chunk_team(const uint32_t P[16], const uin
         if (p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = planes[p] | esc;
     const uint32_t n_esc = pl.n_esc;
     if (n_esc == 0) return;
-    const uint32_t mine = __popc(esc);
-    uint32_t incl = mine;
+    // escapes of the lanes before this one, from six independent ballots of
+    // the count's bits (a count is at most 32)
+    const uint32_t mine = __popc(esc), below = (1u << lane) - 1u;
+    uint32_t excl = 0;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= (uint32_t)d) incl += t;
-    }
-    uint32_t idx = pl.esc_before + incl - mine;
+    for (int b = 0; b < 6; ++b) excl += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, (mine >> b) & 1u) & below) << b;
+    uint32_t idx = pl.esc_before + excl;
     uint8_t* esc_out = body + kSmPlaneBytes + kPlaneBytes * k;
     if (esc) {
 #pragma unroll

@@ -20,14 +20,16 @@ struct ReduceInputs {
 
 // All pointers are device pointers already validated by the C ABI layer; the
 // workspace header and placement words have been cleared on `stream`.
+// Paging (cccl_device.cuh): contiguous data when pg.table is null.
+struct Paging;
 cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const Paging& pg);
 // The same compression with its scratch in a static device array (no
 // workspace argument); n_elems <= CCCL_NOALLOC_MAX_ELEMS.
 cudaError_t launch_compress_noalloc(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity,
                                     cudaStream_t stream);
 cudaError_t launch_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t n_elems, void* ws,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const Paging& pg);
 cudaError_t launch_reduce(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
                           cudaStream_t stream);
 

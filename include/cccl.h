@@ -166,6 +166,30 @@ cccl_status cccl_reduce_compressed(const void *const *h_ins, const size_t *h_in_
                                    void *d_out, size_t out_capacity, void *d_ws, size_t ws_bytes,
                                    cccl_stream_t stream);
 
+/* Paged payload: the KV-cache blocks that prefill sends to decode ("CCCL:
+ * In-GPU Compression-Coupled Collective Communication", section 6.2 and
+ * Figure 3: PD disaggregation), compressed from where they lie in a paged
+ * cache and decompressed into the receiver's blocks; no transport here.
+ *   d_pool        pool_blocks blocks of block_elems bf16 values each,
+ *                 contiguous; block_elems is a multiple of 4096, so no chunk
+ *                 straddles two blocks.
+ *   d_table       device array of n_blocks int32 block indices: the logical
+ *                 buffer is blocks d_table[0], d_table[1], ... in that order
+ *                 (n_elems = n_blocks * block_elems).
+ * cccl_compress_paged produces exactly the stream cccl_compress produces for
+ * the gathered buffer (d_out, out_capacity, d_ws, ws_bytes as there).
+ * cccl_decompress_paged decompresses a stream made for n_elems values into the
+ * named blocks; the table's entries must then be distinct.
+ * A table entry outside 0..pool_blocks-1 is reported by cccl_get_result as
+ * CCCL_ERR_INVALID_ARG (its chunks are skipped; the output is unspecified).
+ * Returns INVALID_ARG, CAPACITY (compress), CUDA or OK synchronously. */
+cccl_status cccl_compress_paged(const uint16_t *d_pool, size_t pool_blocks, size_t block_elems, const int32_t *d_table,
+                                size_t n_blocks, void *d_out, size_t out_capacity, void *d_ws, size_t ws_bytes,
+                                cccl_stream_t stream);
+cccl_status cccl_decompress_paged(const void *d_in, size_t in_bytes, uint16_t *d_pool, size_t pool_blocks,
+                                  size_t block_elems, const int32_t *d_table, size_t n_blocks, void *d_ws,
+                                  size_t ws_bytes, cccl_stream_t stream);
+
 /* The selective-compression reduce step (section 5, "Selective compression
  * across collective stages": an intermediate reduction merges the locally
  * available, uncompressed data with received compressed partial results, and

@@ -356,6 +356,56 @@ def test_reduce_mixed_rejects_corrupt_remote(cc, orc, wl):
         assert st == cc.CCCL_ERR_CORRUPT, name
 
 
+# ---------------------------------------------------------------- paged payload
+KV_BLOCK = 16 * 8 * 128  # 16 tokens x 8 heads x 128 dim of the KV-cache shape = 4 chunks
+
+
+@pytest.mark.parametrize("n_pool,n_blocks,seed", [(8, 3, 0), (64, 40, 1), (2048, 1024, 2)])
+def test_paged_compress_and_decompress(cc, orc, wl, n_pool, n_blocks, seed):
+    rng = np.random.default_rng(seed)
+    pool = wl.generate(4, 0, count=n_pool * KV_BLOCK)
+    table = rng.permutation(n_pool)[:n_blocks].astype(np.int32)
+    if n_blocks > 2:
+        table[-1] = table[0]  # compress may read a block twice
+    dpool = dev(pool)
+    dtab = torch.from_numpy(table).cuda()
+    n = n_blocks * KV_BLOCK
+    out = cc.empty_stream(n)
+    ws = cc.empty_workspace(n)
+    cc.cccl_compress_paged(dpool, KV_BLOCK, dtab, out, ws)
+    nbytes, st = cc.cccl_get_result(ws)
+    assert st == 0
+    got = out[:nbytes].cpu().numpy()
+    want = orc.compress_paged(pool, KV_BLOCK, table)
+    assert np.array_equal(got, want)
+    # decompress into distinct blocks of another pool
+    dtab2 = torch.from_numpy(rng.permutation(n_pool)[:n_blocks].astype(np.int32)).cuda()
+    target = np.full(n_pool * KV_BLOCK, 0x3C00, np.uint16)
+    dtarget = dev(target)
+    cc.cccl_decompress_paged(out[:nbytes], dtarget, KV_BLOCK, dtab2, ws)
+    _, st = cc.cccl_get_result(ws)
+    assert st == 0
+    want_pool = orc.decompress_paged(want, target, KV_BLOCK, dtab2.cpu().numpy())
+    assert np.array_equal(host_u16(dtarget), want_pool)
+
+
+def test_paged_table_entry_outside_the_pool(cc, orc, wl):
+    pool = dev(wl.generate(4, 0, count=4 * KV_BLOCK))
+    n = 2 * KV_BLOCK
+    out = cc.empty_stream(n)
+    ws = cc.empty_workspace(n)
+    for bad in ([0, 4], [-1, 1]):
+        dtab = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        cc.cccl_compress_paged(pool, KV_BLOCK, dtab, out, ws)
+        _, st = cc.cccl_get_result(ws)
+        assert st == cc.CCCL_ERR_INVALID_ARG
+    good = cc.compress(pool[:n])
+    dtab = torch.tensor([1, 7], dtype=torch.int32, device="cuda")
+    cc.cccl_decompress_paged(good, pool, KV_BLOCK, dtab, ws)
+    _, st = cc.cccl_get_result(ws)
+    assert st == cc.CCCL_ERR_INVALID_ARG
+
+
 def test_argument_errors(cc):
     n = 5 * CHUNK
     x = torch.zeros(n, dtype=torch.int16, device="cuda")
