@@ -250,6 +250,68 @@ def workload_config() -> dict:
             "parallelism": "replicas (weak scaling, no cross-GPU traffic)"}
 
 
+# ---------------------------------------------------------------- rows beyond the step
+KV_BLOCK = 16 * 8 * 128  # 16 tokens x 8 heads x 128 dim
+
+
+def measure_extras(cc, torch, np, xs, streams, sizes, n, flush, peak, reps: int = 50) -> dict:
+    """The selective-compression reduce and the paged payload, each timed alone
+    (CUDA events on the current stream, L2 flushed before every repetition,
+    median), with their algorithmic HBM bytes."""
+    import workloads
+
+    stream = torch.cuda.current_stream()
+    out = {}
+
+    def timed(fn):
+        ts = []
+        for k in range(reps + 3):
+            flush.fill_(k & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if k >= 3:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    # local rank-0 buffer + one compressed remote rank, 64 MiB each
+    red = cc.empty_stream(n)
+    ws = cc.empty_workspace(n)
+    ms = timed(lambda: cc.cccl_reduce_mixed(xs[0], [streams[1][:sizes[1]]], red, ws, stream=stream))
+    out_bytes, st = cc.cccl_get_result(ws, stream)
+    algo = 2 * n + sizes[1] + out_bytes
+    out["reduce_mixed"] = {"ms": round(ms, 5), "workload": "local rank-0 buffer (uncompressed) + 1 compressed remote "
+                           "rank of the 64 MiB gradient-like buffer", "status": st,
+                           "uncompressed_gbs": round(2 * 2 * n / (ms * 1e-3) / 1e9, 1), "algorithmic_bytes": algo,
+                           "hbm_gbs": round(algo / (ms * 1e-3) / 1e9, 1),
+                           "frac_of_measured_copy": round(algo / (ms * 1e-3) / 1e9 / peak, 4)}
+    # KV-cache blocks of the [32, 2, 4096, 8, 128] shape: 4096 of a pool of 8192 blocks, shuffled
+    n_pool, n_blk = 8192, 4096
+    pool = torch.from_numpy(workloads.generate(4, 0, count=n_pool * KV_BLOCK).view(np.int16)).cuda()
+    table = torch.from_numpy(np.random.default_rng(7).permutation(n_pool)[:n_blk].astype(np.int32)).cuda()
+    npg = n_blk * KV_BLOCK
+    s_pg = cc.empty_stream(npg)
+    ws_pg = cc.empty_workspace(npg)
+    ms_c = timed(lambda: cc.cccl_compress_paged(pool, KV_BLOCK, table, s_pg, ws_pg, stream=stream))
+    pbytes, st_c = cc.cccl_get_result(ws_pg, stream)
+    target = torch.empty_like(pool)
+    ms_d = timed(lambda: cc.cccl_decompress_paged(s_pg[:pbytes], target, KV_BLOCK, table, ws_pg, stream=stream))
+    _, st_d = cc.cccl_get_result(ws_pg, stream)
+    ok = bool(torch.equal(target.view(n_pool, KV_BLOCK)[table.long()], pool.view(n_pool, KV_BLOCK)[table.long()]))
+    for name, ms_x, st_x in (("compress_paged", ms_c, st_c), ("decompress_paged", ms_d, st_d)):
+        algo = 2 * npg + pbytes
+        out[name] = {"ms": round(ms_x, 5), "workload": "4096 KV-cache blocks of 16 tokens x 8 heads x 128 dim "
+                     "(64 Mi values) gathered through a shuffled block table from a pool of 8192", "status": st_x,
+                     "uncompressed_gbs": round(2 * npg / (ms_x * 1e-3) / 1e9, 1), "algorithmic_bytes": algo,
+                     "hbm_gbs": round(algo / (ms_x * 1e-3) / 1e9, 1),
+                     "frac_of_measured_copy": round(algo / (ms_x * 1e-3) / 1e9 / peak, 4),
+                     "ratio": round(pbytes / (2 * npg), 5)}
+    out["decompress_paged"]["round_trip_exact"] = ok
+    return out
+
+
 # ---------------------------------------------------------------- the GPU arm
 def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     import numpy as np
@@ -400,6 +462,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                 "d2h_bytes_per_step": 2 * n, "steps": e2e_steps},
         "gpu_launches": (R + 2) * args.steps,
         "clocks": clocks, "check": check,
+        "extras": measure_extras(cc, torch, np, xs, streams, sizes, n, flush, peak) if not args.no_extras else None,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(xs_host)
@@ -439,6 +502,7 @@ def main(argv=None) -> int:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the rows timed outside the step")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
