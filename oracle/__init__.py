@@ -63,10 +63,12 @@ def _bind(path: str):
                                   u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_reduce_mixed.argtypes = [u16p, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(sz), ctypes.c_int,
                                         sz, u8p, sz, ctypes.POINTER(sz)]
+    lib.oracle_compress_window.argtypes = [u16p, sz, u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_compress_paged.argtypes = [u16p, sz, ctypes.c_void_p, sz, u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_decompress_paged.argtypes = [u8p, sz, u16p, sz, ctypes.c_void_p, sz]
     for f in ("oracle_chunk_choice", "oracle_encode_chunk", "oracle_compress", "oracle_decompress",
-              "oracle_reduce", "oracle_reduce_mixed", "oracle_compress_paged", "oracle_decompress_paged"):
+              "oracle_reduce", "oracle_reduce_mixed", "oracle_compress_paged", "oracle_decompress_paged",
+              "oracle_compress_window"):
         getattr(lib, f).restype = ctypes.c_int
     lib.oracle_sum_ranks.restype = None
     lib.oracle_plane_position.restype = None
@@ -229,6 +231,18 @@ def reduce_mixed(local, streams, n: int) -> np.ndarray:
                                      ctypes.byref(nb))
     if st != OK:
         raise OracleError(st, "oracle_reduce_mixed")
+    return out[:nb.value]
+
+
+def compress_window(x) -> np.ndarray:
+    """Window-base variant (stream version 2) of compress."""
+    x = _u16(x).reshape(-1)
+    cap = compress_bound(x.size)
+    out = np.empty(cap, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_compress_window(x.ctypes.data, x.size, out.ctypes.data, cap, ctypes.byref(nb))
+    if st != OK:
+        raise OracleError(st, "oracle_compress_window")
     return out[:nb.value]
 
 

@@ -54,6 +54,7 @@
 #define CHUNK_HEADER_BYTES 16u
 #define STREAM_MAGIC 0x31424343u /* "CCB1" */
 #define STREAM_VERSION 1u
+#define STREAM_VERSION_WINDOW 2u /* the window-base variant: same layout, other table choice */
 #define DTYPE_BF16 1u
 #define MODE_PACKED 0u
 #define MODE_RAW 1u
@@ -260,6 +261,81 @@ static chunk_choice choose_encoding(const uint16_t *x, size_t n_c)
     return best;
 }
 
+/* Window-base variant (stream version 2).  The chunk's table is again a
+ * fixed code width k and a base, but the base is the start of the window of
+ * S = 2^k - 1 exponents [base, base + S - 1] that leaves the fewest
+ * escapes: every exponent outside the window, below it included, is an
+ * escape.  This is section 4.3's per-block frequency table taken at its
+ * word: the codes go to the most frequent contiguous run of exponent
+ * symbols, so that rare low outliers (zeros, subnormals, tiny magnitudes)
+ * no longer stretch the range.  Ties: the smaller k, then the smaller base;
+ * raw when no k beats the 4096 bytes of exponents (ties too); k = 0 when all
+ * exponents are equal.  escapes(k, b) = #(e < b) + #(e >= b + S), from the
+ * exponent histogram and its prefix sums. */
+static chunk_choice choose_encoding_window(const uint16_t *x, size_t n_c)
+{
+    chunk_choice best;
+    best.raw = 1;
+    best.k = 0;
+    best.base = 0;
+    best.n_esc = 0;
+    best.bytes = raw_chunk_bytes(n_c);
+    if (n_c != CHUNK_ELEMS)
+        return best;
+
+    size_t hist[256] = {0};
+    unsigned emin = 255, emax = 0;
+    for (size_t i = 0; i < n_c; i++) {
+        unsigned e = exponent_of(x[i]);
+        hist[e]++;
+        if (e < emin)
+            emin = e;
+        if (e > emax)
+            emax = e;
+    }
+    size_t below[257]; /* below[v] = number of exponents < v */
+    below[0] = 0;
+    for (unsigned v = 0; v < 256; v++)
+        below[v + 1] = below[v] + hist[v];
+
+    int have = 0;
+    unsigned best_k = 0, best_base = emin;
+    size_t best_size = 0, best_esc = 0;
+    if (emax == emin) {
+        have = 1;
+    } else {
+        for (unsigned k = 1; k <= 7; k++) {
+            unsigned S = (1u << k) - 1;
+            size_t k_esc = 0;
+            unsigned k_base = 0;
+            for (unsigned b = 0; b < 256; b++) {
+                unsigned top = b + S < 256 ? b + S : 256; /* first exponent above the window */
+                size_t n_esc = below[b] + (n_c - below[top]);
+                if (b == 0 || n_esc < k_esc) { /* strict: ties keep the smaller base */
+                    k_esc = n_esc;
+                    k_base = b;
+                }
+            }
+            size_t size = (size_t)BIT_PLANE_BYTES * k + pad16(k_esc);
+            if (!have || size < best_size) {
+                have = 1;
+                best_k = k;
+                best_base = k_base;
+                best_size = size;
+                best_esc = k_esc;
+            }
+        }
+    }
+    if (best_size >= SM_PLANE_BYTES)
+        return best;
+    best.raw = 0;
+    best.k = best_k;
+    best.base = best_base;
+    best.n_esc = best_esc;
+    best.bytes = packed_chunk_bytes(best_k, best_esc);
+    return best;
+}
+
 /* Encoding statistics of one chunk without writing it (for tests). */
 int oracle_chunk_choice(const uint16_t *x, size_t n_c, unsigned *raw, unsigned *k, unsigned *base,
                         size_t *n_esc, size_t *bytes)
@@ -359,7 +435,8 @@ int oracle_encode_chunk(const uint16_t *x, size_t n_c, uint8_t *out, size_t *byt
 /* ------------------------------------------------------------------ */
 /* stream encoder                                                      */
 /* ------------------------------------------------------------------ */
-int oracle_compress(const uint16_t *x, size_t n, uint8_t *out, size_t capacity, size_t *out_bytes)
+static int compress_stream(const uint16_t *x, size_t n, uint8_t *out, size_t capacity, size_t *out_bytes,
+                           int window)
 {
     if (n == 0 || x == NULL || out == NULL)
         return ORC_ERR_INVALID_ARG;
@@ -373,7 +450,8 @@ int oracle_compress(const uint16_t *x, size_t n, uint8_t *out, size_t capacity, 
     memset(out, 0, start);
     for (size_t c = 0; c < n_chunks; c++) {
         size_t n_c = chunk_len(n, c);
-        chunk_choice ch = choose_encoding(x + c * CHUNK_ELEMS, n_c);
+        chunk_choice ch = window ? choose_encoding_window(x + c * CHUNK_ELEMS, n_c)
+                                 : choose_encoding(x + c * CHUNK_ELEMS, n_c);
         if (pos + ch.bytes > capacity)
             return ORC_ERR_CAPACITY;
         put_u64(out + STREAM_HEADER_BYTES + 8 * c, pos);
@@ -382,7 +460,7 @@ int oracle_compress(const uint16_t *x, size_t n, uint8_t *out, size_t capacity, 
     }
 
     put_u32(out + 0, STREAM_MAGIC);
-    put_u16(out + 4, STREAM_VERSION);
+    put_u16(out + 4, window ? STREAM_VERSION_WINDOW : STREAM_VERSION);
     put_u16(out + 6, DTYPE_BF16);
     put_u32(out + 8, CHUNK_ELEMS);
     put_u32(out + 12, 0);
@@ -392,6 +470,17 @@ int oracle_compress(const uint16_t *x, size_t n, uint8_t *out, size_t capacity, 
     /* bytes 40..63 stay zero */
     *out_bytes = pos;
     return ORC_OK;
+}
+
+int oracle_compress(const uint16_t *x, size_t n, uint8_t *out, size_t capacity, size_t *out_bytes)
+{
+    return compress_stream(x, n, out, capacity, out_bytes, 0);
+}
+
+/* The window-base variant: the same stream layout, version 2. */
+int oracle_compress_window(const uint16_t *x, size_t n, uint8_t *out, size_t capacity, size_t *out_bytes)
+{
+    return compress_stream(x, n, out, capacity, out_bytes, 1);
 }
 
 /* ------------------------------------------------------------------ */
@@ -466,7 +555,7 @@ int oracle_decompress(const uint8_t *s, size_t s_bytes, uint16_t *x, size_t n)
         return ORC_ERR_CORRUPT;
     size_t n_chunks = oracle_n_chunks(n);
     size_t start = oracle_data_start(n);
-    if (get_u32(s + 0) != STREAM_MAGIC || get_u16(s + 4) != STREAM_VERSION || get_u16(s + 6) != DTYPE_BF16 ||
+    if (get_u32(s + 0) != STREAM_MAGIC || (get_u16(s + 4) != STREAM_VERSION && get_u16(s + 4) != STREAM_VERSION_WINDOW) || get_u16(s + 6) != DTYPE_BF16 ||
         get_u32(s + 8) != CHUNK_ELEMS || get_u64(s + 16) != n || get_u64(s + 24) != n_chunks)
         return ORC_ERR_CORRUPT;
     size_t total = get_u64(s + 32);

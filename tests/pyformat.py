@@ -54,9 +54,11 @@ def split(x: np.ndarray):
     return expo, sm
 
 
-def encode_chunk_at(x: np.ndarray, k: int | None) -> bytes | None:
-    """Chunk bytes for a given width k (None = raw); None if k cannot
-    represent the chunk (k = 0 needs a single exponent)."""
+def encode_chunk_at(x: np.ndarray, k: int | None, base: int | None = None) -> bytes | None:
+    """Chunk bytes for a given width k (None = raw) and base (None: the
+    minimum exponent); None if k cannot represent the chunk (k = 0 needs a
+    single exponent, equal to the base).  Exponents outside
+    [base, base + 2^k - 2] escape."""
     n_c = x.size
     if k is None:
         body = x.astype("<u2").tobytes()
@@ -65,17 +67,17 @@ def encode_chunk_at(x: np.ndarray, k: int | None) -> bytes | None:
         return (hdr + body).ljust(size, b"\0")
     assert n_c == CHUNK
     expo, sm = split(x)
-    base = int(expo.min())
-    off = expo - base
+    base = int(expo.min()) if base is None else int(base)
+    off = expo.astype(np.int64) - base
     if k == 0:
-        if off.max() != 0:
+        if off.min() != 0 or off.max() != 0:
             return None
         esc = b""
         planes = b""
     else:
         sent = (1 << k) - 1
-        code = np.minimum(off, sent)
-        escaped = off >= sent
+        escaped = (off < 0) | (off >= sent)
+        code = np.where(escaped, sent, off).astype(np.uint32)
         order = np.argsort(32 * WORD_OF + BIT_OF)  # elements in bit-plane order
         esc = expo[order][escaped[order]].astype(np.uint8).tobytes()
         words = np.zeros((k, 128), np.uint64)
@@ -120,6 +122,46 @@ def encode_stream(x: np.ndarray) -> bytes:
     return hdr + table + b"".join(chunks)
 
 
+def window_table(x: np.ndarray):
+    """Window-base variant: for every k, the escape count of every base
+    (exponents outside [b, b + 2^k - 2]), counted directly; returns the
+    chosen (k, base, n_esc) or None for raw, with the variant's tie rules."""
+    e = split(x)[0].astype(np.int64)
+    if e.min() == e.max():
+        return 0, int(e.min()), 0
+    best = None
+    for k in range(1, 8):
+        S = (1 << k) - 1
+        b = np.arange(256)[:, None]
+        n_esc = ((e[None, :] < b) | (e[None, :] >= b + S)).sum(1)
+        bk = int(np.argmin(n_esc))  # first minimum: the smallest base
+        size = 512 * k + _rup16(int(n_esc[bk]))
+        if best is None or size < best[0]:
+            best = (size, k, bk, int(n_esc[bk]))
+    if best[0] >= 4096:
+        return None
+    return best[1], best[2], best[3]
+
+
+def encode_stream_window(x: np.ndarray) -> bytes:
+    """Whole version-2 stream from window_table's choices."""
+    n = x.size
+    nch = -(-n // CHUNK)
+    start = 64 + _rup16(8 * nch)
+    chunks = []
+    for c in range(nch):
+        xc = x[c * CHUNK:(c + 1) * CHUNK]
+        choice = window_table(xc) if xc.size == CHUNK else None
+        chunks.append(encode_chunk_at(xc, None) if choice is None else encode_chunk_at(xc, choice[0], choice[1]))
+    offs, pos = [], start
+    for ch in chunks:
+        offs.append(pos)
+        pos += len(ch)
+    hdr = struct.pack("<IHHIIQQQ", MAGIC, 2, 1, CHUNK, 0, n, nch, pos).ljust(64, b"\0")
+    table = struct.pack("<%dQ" % nch, *offs).ljust(start - 64, b"\0")
+    return hdr + table + b"".join(chunks)
+
+
 class Corrupt(ValueError):
     pass
 
@@ -154,7 +196,7 @@ def decode_chunk(buf: bytes, n_c: int) -> np.ndarray:
 def decode_stream(s: bytes, n: int) -> np.ndarray:
     s = bytes(s)
     magic, ver, dt, ce, _, n_el, nch, total = struct.unpack_from("<IHHIIQQQ", s, 0)
-    if (magic, ver, dt, ce, n_el, nch) != (MAGIC, 1, 1, CHUNK, n, -(-n // CHUNK)):
+    if (magic, dt, ce, n_el, nch) != (MAGIC, 1, CHUNK, n, -(-n // CHUNK)) or ver not in (1, 2):
         raise Corrupt("stream header")
     offs = list(struct.unpack_from("<%dQ" % nch, s, 64)) + [total]
     out = np.empty(n, np.uint16)

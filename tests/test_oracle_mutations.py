@@ -16,8 +16,10 @@ ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file
 CHUNK = 4096
 
 MUTATIONS = [
-    ("tie_keeps_larger_k", "if (!have || size < best_size)", "if (!have || size <= best_size)"),
-    ("raw_tie_goes_packed", "if (best_size >= SM_PLANE_BYTES)", "if (best_size > SM_PLANE_BYTES)"),
+    ("tie_keeps_larger_k", "if (!have || size < best_size) { /* strict: ties keep the smaller k */",
+     "if (!have || size <= best_size) { /* strict: ties keep the smaller k */"),
+    ("raw_tie_goes_packed", "if (best_size >= SM_PLANE_BYTES) /* no gain over 8-bit exponents: raw (ties too) */",
+     "if (best_size > SM_PLANE_BYTES) /* no gain over 8-bit exponents: raw (ties too) */"),
     ("sign_bit_dropped", "return ((b >> 8) & 0x80u) | (b & 0x7Fu);", "return (b & 0x7Fu);"),
     ("plane_bit_order_swapped", "*bit = 8 * (s % 4) + 2 * (j % 4) + s / 4;", "*bit = 8 * (s % 4) + 2 * (s / 4) + j % 4;"),
     ("plane_word_order_swapped", "*word = (j / 4) * 32 + l;", "*word = l * 4 + j / 4;"),
@@ -41,6 +43,8 @@ MUTATIONS = [
      "put_u64(out + STREAM_HEADER_BYTES + 8 * c, pos - start);"),
     ("mixed_remote_ranks_reversed", "st = oracle_decompress(ins[r - 1], in_bytes[r - 1], x, n);",
      "st = oracle_decompress(ins[R - 1 - r], in_bytes[R - 1 - r], x, n);"),
+    ("window_tie_keeps_larger_base", "if (b == 0 || n_esc < k_esc) {", "if (b == 0 || n_esc <= k_esc) {"),
+    ("window_one_too_narrow", "unsigned top = b + S < 256 ? b + S : 256;", "unsigned top = b + S - 1 < 256 ? b + S - 1 : 256;"),
     ("paged_gather_ignores_table", "memcpy(x + i * block_elems, pool + (size_t)table[i] * block_elems,",
      "memcpy(x + i * block_elems, pool + i * block_elems,"),
     ("paged_scatter_ignores_table", "memcpy(pool + (size_t)table[i] * block_elems, x + i * block_elems,",
@@ -110,6 +114,10 @@ def _battery(orc, wl):
     # local 2^30, remote -2^30 then 1: (2^30 - 2^30) + 1 = 1 only in this order
     check("mixed_rank_order", lambda: orc.decompress(
         orc.reduce_mixed(sp_a[3:], [orc.compress(sp_b[3:]), orc.compress(sp_c[3:])], 1), 1)[0] == 0x3F80)
+    wx = wl.generate(5, 0, start=(1 << 27) - 2 * CHUNK, count=4 * CHUNK)
+    check("window_variant", lambda: orc.compress_window(wx).tobytes() == pf.encode_stream_window(wx))
+    te = (np.arange(CHUNK) % 11 + 100).astype(np.uint16)  # exponents 100..110: k = 4 from any base 96..100
+    check("window_base_tie", lambda: pf.chunk_headers(orc.compress_window((te << 7) | 0x11).tobytes())[0][3] == 96)
     pool = np.arange(6 * CHUNK, dtype=np.uint16) * 7 + 1
     tab = np.array([4, 1, 3], np.int32)
     check("paged_gather", lambda: np.array_equal(orc.compress_paged(pool, CHUNK, tab),

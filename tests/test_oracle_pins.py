@@ -389,6 +389,50 @@ def test_paged_round_trip_writes_only_the_named_blocks(orc, wl):
     assert np.array_equal(out, want)
 
 
+# ---------------------------------------------------------------- window-base variant (version 2)
+def test_window_variant_matches_the_independent_encoder(orc, wl):
+    """Every (k, base) escape count is recounted in numpy (pyformat.window_table)
+    and the stream rebuilt from those choices, byte for byte."""
+    samples = [wl.generate(5, 0, start=(1 << 27) - 2 * CHUNK, count=6 * CHUNK),  # uniform | specials half
+               wl.generate(2, 0, count=5 * CHUNK + 77), wl.generate(4, 0, count=4 * CHUNK),
+               np.random.default_rng(3).permutation(65536).astype(np.uint16)[:8 * CHUNK]]
+    for x in samples:
+        assert orc.compress_window(x).tobytes() == pf.encode_stream_window(x)
+
+
+def test_window_variant_is_lossless_and_never_larger(orc, wl):
+    allp = np.random.default_rng(11).permutation(65536).astype(np.uint16)
+    assert np.array_equal(orc.decompress(orc.compress_window(allp), allp.size), allp)
+    for x in (wl.generate(5, 1, start=1 << 27, count=16 * CHUNK), wl.generate(2, 1, count=16 * CHUNK)):
+        v1, v2 = orc.compress(x), orc.compress_window(x)
+        assert np.array_equal(orc.decompress(v2, x.size), x)
+        s1, s2 = pf.chunk_headers(v1.tobytes()), pf.chunk_headers(v2.tobytes())
+        assert all(b[6] <= a[6] for a, b in zip(s1, s2))  # chunk by chunk
+        assert v2[4] == 2 and v1[4] == 1
+
+
+def test_window_variant_hand_case(orc):
+    """4090 exponents spread over 124..130 and 6 zeros: version 1 must take the
+    base 0 and goes raw (every offset >= 124 escapes even at k = 7); the window
+    [124, 130] at k = 3 leaves only the 6 zeros: 3 * 512 + pad16(6) = 1552."""
+    e = np.concatenate([np.arange(4090) % 7 + 124, np.zeros(6, np.int64)]).astype(np.uint16)
+    e = e[np.random.default_rng(5).permutation(e.size)]
+    x = ((e << 7) | 0x35).astype(np.uint16)
+    v1 = pf.chunk_headers(orc.compress(x).tobytes())[0]
+    v2 = pf.chunk_headers(orc.compress_window(x).tobytes())[0]
+    assert v1[1:3] == (1, 0)  # raw
+    assert v2[1:4] == (0, 3, 124) and v2[5:7] == (6, 16 + 4096 + 1552)
+
+
+def test_window_variant_base_tie_takes_the_smallest(orc):
+    """Exponents 100..110, evenly: at k = 4 (15 codes) every window starting at
+    96..100 holds them all (no escapes, 2048 bytes, the best size), and the
+    smallest start wins."""
+    e = (np.arange(CHUNK) % 11 + 100).astype(np.uint16)
+    h = pf.chunk_headers(orc.compress_window((e << 7) | 0x11).tobytes())[0]
+    assert h[1:4] == (0, 4, 96) and h[5] == 0
+
+
 # ---------------------------------------------------------------- corrupt streams
 def _corrupt_cases(orc, wl):
     x = wl.generate(2, 0, count=3 * CHUNK + 10, n=1 << 20)
@@ -403,7 +447,7 @@ def _corrupt_cases(orc, wl):
         return bytes(t)
 
     yield "magic", mut(lambda t: t.__setitem__(0, 0))
-    yield "version", mut(lambda t: t.__setitem__(4, 2))
+    yield "version", mut(lambda t: t.__setitem__(4, 3))
     yield "n_elems", mut(lambda t: struct.pack_into("<Q", t, 16, x.size + 1))
     yield "total_bytes", mut(lambda t: struct.pack_into("<Q", t, 32, len(s) + 16))
     yield "offset_misaligned", mut(lambda t: struct.pack_into("<Q", t, 64 + 8, hdrs[1][0] + 8))
