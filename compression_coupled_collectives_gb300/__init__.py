@@ -40,6 +40,8 @@ _lib.cccl_workspace_bytes.argtypes = [_sz]
 _lib.cccl_workspace_bytes.restype = _sz
 _lib.cccl_compress.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_compress.restype = _i
+_lib.cccl_compress_window.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp]
+_lib.cccl_compress_window.restype = _i
 _lib.cccl_compress_noalloc.argtypes = [_vp, _sz, _vp, _sz, _vp]
 _lib.cccl_compress_noalloc.restype = _i
 _lib.cccl_decompress.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp]
@@ -101,6 +103,14 @@ def cccl_compress(x: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, stream=N
     x = _bf16_bits(x)
     _check(_lib.cccl_compress(x.data_ptr(), x.numel(), out.data_ptr(), out.numel() * out.element_size(),
                               ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)), "cccl_compress")
+
+
+def cccl_compress_window(x: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    """Enqueue the window-base variant of compression (stream version 2)."""
+    x = _bf16_bits(x)
+    _check(_lib.cccl_compress_window(x.data_ptr(), x.numel(), out.data_ptr(), out.numel() * out.element_size(),
+                                     ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "cccl_compress_window")
 
 
 def cccl_compress_noalloc(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
@@ -198,6 +208,16 @@ def compress(x: torch.Tensor, stream=None) -> torch.Tensor:
     cccl_compress(x, out, ws, stream)
     nbytes, dev = cccl_get_result(ws, stream)
     _check(dev, "cccl_compress (device)")
+    return out[:nbytes]
+
+
+def compress_window(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """Window-base variant of compress; waits and returns the trimmed stream."""
+    out = empty_stream(x.numel(), x.device)
+    ws = empty_workspace(x.numel(), x.device)
+    cccl_compress_window(x, out, ws, stream)
+    nbytes, dev = cccl_get_result(ws, stream)
+    _check(dev, "cccl_compress_window (device)")
     return out[:nbytes]
 
 

@@ -84,6 +84,22 @@ cccl_status cccl_compress(const uint16_t* d_in, size_t n_elems, void* d_out, siz
     return CCCL_OK;
 }
 
+cccl_status cccl_compress_window(const uint16_t* d_in, size_t n_elems, void* d_out, size_t out_capacity, void* d_ws,
+                                 size_t ws_bytes, cccl_stream_t stream) {
+    if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_in) || !aligned16(d_out) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < cccl_workspace_bytes(n_elems)) return CCCL_ERR_INVALID_ARG;
+    if (out_capacity < cccl_compress_bound(n_elems)) return CCCL_ERR_CAPACITY;
+    if (!device_range(d_in, 2 * n_elems) || !device_range(d_out, out_capacity) || !device_range(d_ws, ws_bytes))
+        return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    if (cccl::launch_compress(d_in, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s,
+                              cccl::Paging{nullptr, 1, 0}, true) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
 cccl_status cccl_compress_noalloc(const uint16_t* d_in, size_t n_elems, void* d_out, size_t out_capacity,
                                   cccl_stream_t stream) {
     if (n_elems == 0 || n_elems > CCCL_NOALLOC_MAX_ELEMS) return CCCL_ERR_INVALID_ARG;

@@ -42,6 +42,7 @@ struct CompressSmem {
     unsigned long long tally[kRing];  // sized warps (high word) and their bytes (low word)
     uint32_t size[kRing][kGroup];
     uint64_t off[2][kGroup];       // chunk offsets, or kFlagPoison
+    uint32_t hist[kGroup][264];    // window-base variant: each compute warp's exponent histogram
 };
 
 // Control lane: fill stage s with group g (or mark it empty).
@@ -73,6 +74,7 @@ struct WarpChunk {
     uint64_t c;
 };
 
+template <bool kWindow>
 __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__ in, const StreamOut& so,
                                              uint8_t* stage, CompressSmem& sm, WarpChunk& cur, WarpChunk& prev) {
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -86,7 +88,8 @@ __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__
         cur.c = g * kGroup + w;
         cur.bytes = 0;
         if (cur.c < n_full) {
-            cur.plan = plan_chunk_warp(stage + ((size_t)s * kGroup + w) * kChunkBytesRaw, cur.regs);
+            const uint8_t* chunk = stage + ((size_t)s * kGroup + w) * kChunkBytesRaw;
+            cur.plan = kWindow ? plan_chunk_warp_window(chunk, cur.regs, sm.hist[w]) : plan_chunk_warp(chunk, cur.regs);
             cur.bytes = cur.plan.bytes;
         } else if (cur.c < so.n_chunks) {
             cur.bytes = tail_chunk_bytes((uint32_t)(so.n_elems - cur.c * kChunkElems));
@@ -134,6 +137,7 @@ __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__
     return live;
 }
 
+template <bool kWindow>
 __global__ void __launch_bounds__(kCompressThreads, 1)
     compress_kernel(const uint16_t* __restrict__ in, Paging pg, StreamOut so) {
     extern __shared__ __align__(128) uint8_t stage[];
@@ -215,18 +219,21 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
     cur.bytes = prev.bytes = 0;
     cur.c = prev.c = 0;
     for (int i = 0;; ++i) {
-        if (!compute_step(i, in, so, stage, sm, cur, prev)) break;
+        if (!compute_step<kWindow>(i, in, so, stage, sm, cur, prev)) break;
         prev = cur;
     }
 }
 
 cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
-                            cudaStream_t stream, const Paging& pg) {
+                            cudaStream_t stream, const Paging& pg, bool window) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr = cudaFuncSetAttribute(compress_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kCompressSmemBytes);
+        if (attr == cudaSuccess)
+            attr = cudaFuncSetAttribute(compress_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kCompressSmemBytes);
     });
     if (attr != cudaSuccess) return attr;
     int dev = 0, sms = 0;
@@ -240,9 +247,13 @@ cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, 
     so.status = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + sizeof(WsHeader));
     so.n_elems = n_elems;
     so.n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
+    so.version = window ? kVersionWindow : kVersion;
     const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
     const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
-    compress_kernel<<<grid, kCompressThreads, kCompressSmemBytes, stream>>>(in, pg, so);
+    if (window)
+        compress_kernel<true><<<grid, kCompressThreads, kCompressSmemBytes, stream>>>(in, pg, so);
+    else
+        compress_kernel<false><<<grid, kCompressThreads, kCompressSmemBytes, stream>>>(in, pg, so);
     return cudaGetLastError();
 }
 
@@ -298,7 +309,7 @@ cudaError_t launch_compress_noalloc(const uint16_t* in, uint64_t n_elems, uint8_
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(out, 0, kStreamHeaderBytes, stream);
     if (e != cudaSuccess) return e;
-    return launch_compress(in, n_elems, out, capacity, scratch, stream, Paging{nullptr, 1, 0});
+    return launch_compress(in, n_elems, out, capacity, scratch, stream, Paging{nullptr, 1, 0}, false);
 }
 
 }  // namespace cccl

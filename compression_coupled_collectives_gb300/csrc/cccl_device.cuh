@@ -29,7 +29,11 @@ constexpr uint32_t kPlaneBytes = 512;
 constexpr uint32_t kMaxChunkBytes = kChunkHeaderBytes + 2 * kChunkElems;  // 8208: a raw full chunk
 constexpr uint32_t kMagic = 0x31424343u;                                  // "CCB1"
 constexpr uint32_t kVersion = 1;
+constexpr uint32_t kVersionWindow = 2;  // window-base variant: same layout, other table choice
 constexpr uint32_t kDtypeBf16 = 1;
+__device__ __forceinline__ bool known_version_word(uint32_t w1) {
+    return w1 == (kVersion | (kDtypeBf16 << 16)) || w1 == (kVersionWindow | (kDtypeBf16 << 16));
+}
 constexpr uint32_t kModePacked = 0;
 constexpr uint32_t kModeRaw = 1;
 
@@ -384,7 +388,7 @@ __device__ __forceinline__ ChunkView locate_chunk(const uint8_t* s, uint64_t in_
     const uint64_t start = data_start(n_chunks);
     if (in_bytes < start) return v;
     const uint32_t w0 = ld_u32_aligned(s + 0), w1 = ld_u32_aligned(s + 4), w2 = ld_u32_aligned(s + 8);
-    if (w0 != kMagic || w1 != (kVersion | (kDtypeBf16 << 16)) || w2 != kChunkElems) return v;
+    if (w0 != kMagic || !known_version_word(w1) || w2 != kChunkElems) return v;
     if (ld_u64_aligned(s + 16) != n_elems || ld_u64_aligned(s + 24) != n_chunks) return v;
     const uint64_t total = ld_u64_aligned(s + 32);
     if (total > in_bytes || total < start) return v;
@@ -407,7 +411,7 @@ __device__ __forceinline__ uint64_t stream_total(const uint8_t* s, uint64_t in_b
     const uint64_t start = data_start(n_chunks);
     if (in_bytes < start) return 0;
     const uint32_t w0 = ld_u32_aligned(s + 0), w1 = ld_u32_aligned(s + 4), w2 = ld_u32_aligned(s + 8);
-    if (w0 != kMagic || w1 != (kVersion | (kDtypeBf16 << 16)) || w2 != kChunkElems) return 0;
+    if (w0 != kMagic || !known_version_word(w1) || w2 != kChunkElems) return 0;
     if (ld_u64_aligned(s + 16) != n_elems || ld_u64_aligned(s + 24) != n_chunks) return 0;
     const uint64_t total = ld_u64_aligned(s + 32);
     if (total > in_bytes || total < start) return 0;

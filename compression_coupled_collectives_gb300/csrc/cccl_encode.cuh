@@ -27,6 +27,7 @@ struct StreamOut {
     WsHeader* ws;
     uint64_t n_elems;
     uint64_t n_chunks;
+    uint32_t version;    // stream header version: kVersion, or kVersionWindow
 };
 
 // Encoding decision of one full chunk (warp-uniform).
@@ -142,6 +143,112 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk, Chunk
     } else {
         pl.bytes = (uint32_t)(16 + kSmPlaneBytes + kPlaneBytes * pl.k + pad16(pl.n_esc));
     }
+    return pl;
+}
+
+// Phase A of the window-base variant (stream version 2): for every width k
+// the base is the start of the window of 2^k - 1 exponents with the fewest
+// escapes (exponents outside it, below included), ties to the smaller base;
+// then the smallest size wins, ties to the smaller k.  `hist`: this warp's
+// 257 words of shared memory.  Leaves in `r` the bit-planes of the codes,
+// escaped elements carrying all ones, which is what write_chunk_warp's
+// escape test (low_k | high_k) and plane writes expect.
+__device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk, ChunkRegs& r, uint32_t* hist) {
+    const uint32_t lane = threadIdx.x & 31;
+    *reinterpret_cast<uint4*>(hist + 8 * lane) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(hist + 8 * lane + 4) = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint4 v = lds_row(chunk, j, lane);
+        const uint32_t t0 = v.x << 1, t1 = v.y << 1, t2 = v.z << 1, t3 = v.w << 1;
+        mn = vmin_u16x2(mn, vmin_u16x2(vmin_u16x2(t0, t1), vmin_u16x2(t2, t3)));
+        mx = vmax_u16x2(mx, vmax_u16x2(vmax_u16x2(t0, t1), vmax_u16x2(t2, t3)));
+        r.P[2 * j] = __byte_perm(t0, t1, 0x7531);
+        r.P[2 * j + 1] = __byte_perm(t2, t3, 0x7531);
+    }
+    const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
+    const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
+    __syncwarp();  // the histogram is cleared
+    // exponent histogram
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+        const uint32_t q = r.P[m];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) atomicAdd(hist + ((q >> (8 * b)) & 0xFFu), 1u);
+    }
+    __syncwarp();
+    // below[v] = exponents smaller than v; lane l holds v = 8 l .. 8 l + 7
+    const uint4 h0 = *reinterpret_cast<const uint4*>(hist + 8 * lane);
+    const uint4 h1 = *reinterpret_cast<const uint4*>(hist + 8 * lane + 4);
+    const uint32_t h[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    uint32_t below[8], run = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        below[i] = run;
+        run += h[i];
+    }
+    uint32_t incl = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= (uint32_t)d) incl += t;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) below[i] += incl - run;
+    __syncwarp();  // every lane has read its bins
+    *reinterpret_cast<uint4*>(hist + 8 * lane) = make_uint4(below[0], below[1], below[2], below[3]);
+    *reinterpret_cast<uint4*>(hist + 8 * lane + 4) = make_uint4(below[4], below[5], below[6], below[7]);
+    if (lane == 31) hist[256] = kChunkElems;
+    __syncwarp();
+    ChunkPlan pl{0u, 0u, emin, 0u, 0u};
+    uint32_t best = 0;
+    if (emax > emin) {
+        best = 0xFFFFFFFFu;
+#pragma unroll
+        for (uint32_t k = 1; k <= 7; ++k) {
+            const uint32_t S = (1u << k) - 1u;
+            uint32_t key = 0xFFFFFFFFu;  // (escapes, base): fewest escapes, then the smallest base
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t b = 8 * lane + i, top = min(b + S, 256u);
+                const uint32_t n = below[i] + (kChunkElems - hist[top]);
+                key = min(key, (n << 8) | b);
+            }
+            key = __reduce_min_sync(0xFFFFFFFFu, key);
+            const uint32_t n = key >> 8, size = kPlaneBytes * k + (uint32_t)pad16(n);
+            if (size < best) {  // ascending k: a tie keeps the smaller width
+                best = size;
+                pl.k = k;
+                pl.base = key & 0xFFu;
+                pl.n_esc = n;
+            }
+        }
+    }
+    pl.raw = best >= kSmPlaneBytes ? 1u : 0u;
+    if (pl.raw) {
+        pl.k = 0;
+        pl.base = 0;
+        pl.n_esc = 0;
+        pl.bytes = kMaxChunkBytes;
+        return pl;
+    }
+    pl.bytes = (uint32_t)(16 + kSmPlaneBytes + kPlaneBytes * pl.k + pad16(pl.n_esc));
+    if (pl.k == 0) return pl;
+    // codes: e - base inside the window, all ones outside (an escape).
+    // Byte-wise e - base with no borrow between bytes, and the bytes where
+    // e < base (the borrow out of each byte).
+    const uint32_t b4 = pl.base * 0x01010101u, kb = (128u - ((1u << pl.k) - 1u)) * 0x01010101u;
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+        const uint32_t e = r.P[m];
+        const uint32_t d = ((e | 0x80808080u) - (b4 & 0x7F7F7F7Fu)) ^ ((e ^ ~b4) & 0x80808080u);
+        const uint32_t lt = ((~e & b4) | (~(e ^ b4) & d)) & 0x80808080u;  // e < base
+        const uint32_t esc = flags_to_mask(lt | ge_flags(d, kb));
+        r.P[m] = d | esc;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) transpose8x8x4(r.P + 8 * q);
     return pl;
 }
 
@@ -459,7 +566,7 @@ __device__ __forceinline__ void finish_chunk(const StreamOut& so, uint64_t c, ui
     uint8_t* out = so.out;
     *reinterpret_cast<uint64_t*>(out + kStreamHeaderBytes + 8 * c) = offset;
     if (c == 0) {
-        *reinterpret_cast<uint4*>(out + 0) = make_uint4(kMagic, kVersion | (kDtypeBf16 << 16), kChunkElems, 0u);
+        *reinterpret_cast<uint4*>(out + 0) = make_uint4(kMagic, so.version | (kDtypeBf16 << 16), kChunkElems, 0u);
         *reinterpret_cast<uint4*>(out + 16) =
             make_uint4((uint32_t)so.n_elems, (uint32_t)(so.n_elems >> 32), (uint32_t)so.n_chunks,
                        (uint32_t)(so.n_chunks >> 32));

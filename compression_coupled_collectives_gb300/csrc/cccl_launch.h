@@ -22,8 +22,9 @@ struct ReduceInputs {
 // workspace header and placement words have been cleared on `stream`.
 // Paging (cccl_device.cuh): contiguous data when pg.table is null.
 struct Paging;
+// window: the window-base variant (stream version 2) instead of base = minimum.
 cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
-                            cudaStream_t stream, const Paging& pg);
+                            cudaStream_t stream, const Paging& pg, bool window = false);
 // The same compression with its scratch in a static device array (no
 // workspace argument); n_elems <= CCCL_NOALLOC_MAX_ELEMS.
 cudaError_t launch_compress_noalloc(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity,

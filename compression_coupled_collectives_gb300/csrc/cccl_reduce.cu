@@ -450,6 +450,7 @@ cudaError_t launch_reduce(const ReduceInputs& inputs, int R, uint64_t n_elems, u
     so.status = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + sizeof(WsHeader));
     so.n_elems = n_elems;
     so.n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
+    so.version = kVersion;
     const uint64_t n_groups = (so.n_chunks + kTeams - 1) / kTeams;
     const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
     reduce_kernel<<<grid, kReduceThreads, kReduceSmemBytes, stream>>>(inputs, R, so);

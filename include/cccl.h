@@ -106,6 +106,21 @@ size_t cccl_workspace_bytes(size_t n_elems);
 cccl_status cccl_compress(const uint16_t *d_in, size_t n_elems, void *d_out, size_t out_capacity, void *d_ws,
                           size_t ws_bytes, cccl_stream_t stream);
 
+/* The window-base variant of cccl_compress: the same stream layout with
+ * version 2 in its header.  For every code width k the chunk's base is the
+ * start of the window of 2^k - 1 exponents that leaves the fewest escapes
+ * (every exponent outside the window, below it included, is an escape; ties
+ * to the smaller base), instead of the minimum exponent; then the smallest
+ * size wins as in cccl_compress (ties to the smaller k, raw when not smaller
+ * than 4096 bytes of exponents).  Section 4.3's per-block frequency table
+ * taken at its word: the codes go to the most frequent run of exponent
+ * symbols, so rare low outliers (zeros, subnormals) become escapes instead
+ * of stretching the range.  Never larger than cccl_compress's stream, chunk
+ * by chunk.  Arguments and errors as for cccl_compress; cccl_decompress,
+ * cccl_reduce_compressed and cccl_reduce_mixed read both versions. */
+cccl_status cccl_compress_window(const uint16_t *d_in, size_t n_elems, void *d_out, size_t out_capacity, void *d_ws,
+                                 size_t ws_bytes, cccl_stream_t stream);
+
 /* Largest n_elems cccl_compress_noalloc accepts (2^30 values, 2 GiB). */
 #define CCCL_NOALLOC_MAX_ELEMS ((size_t)1 << 30)
 

@@ -356,6 +356,41 @@ def test_reduce_mixed_rejects_corrupt_remote(cc, orc, wl):
         assert st == cc.CCCL_ERR_CORRUPT, name
 
 
+# ---------------------------------------------------------------- window-base variant (version 2)
+@pytest.mark.parametrize("workload,start,count", [
+    (1, 0, 40 * CHUNK + 9), (2, 0, 64 * CHUNK), (4, 0, 32 * CHUNK),
+    (5, (1 << 27) - 16 * CHUNK, 48 * CHUNK),  # uniform patterns, then N(0, 1) with specials
+])
+def test_window_variant(cc, orc, wl, workload, start, count):
+    x = wl.generate(workload, 0, start=start, count=count)
+    got = cc.compress_window(dev(x)).cpu().numpy()
+    want = orc.compress_window(x)
+    assert np.array_equal(got, want)
+    assert np.array_equal(host_u16(cc.decompress(torch.from_numpy(got).cuda(), x.size)), x)
+
+
+def test_window_variant_every_pattern_and_crafted(cc, orc):
+    allp = np.random.default_rng(2).permutation(65536).astype(np.uint16)
+    assert np.array_equal(cc.compress_window(dev(allp)).cpu().numpy(), orc.compress_window(allp))
+    rng = np.random.default_rng(8)
+    chunks = []
+    for lo, hi, n_out in [(124, 130, 6), (100, 110, 0), (0, 3, 40), (250, 255, 7), (60, 70, 1000)]:
+        e = rng.integers(lo, hi + 1, CHUNK)
+        e[rng.choice(CHUNK, n_out, replace=False)] = rng.integers(0, 256, n_out)
+        sm = rng.integers(0, 256, CHUNK)
+        chunks.append((((sm & 0x80) << 8) | (e << 7) | (sm & 0x7F)).astype(np.uint16))
+    x = np.concatenate(chunks)
+    assert np.array_equal(cc.compress_window(dev(x)).cpu().numpy(), orc.compress_window(x))
+
+
+def test_reduce_reads_window_streams(cc, orc, wl):
+    n = 9 * CHUNK + 5
+    xs = [wl.generate(5, r, start=1 << 27, count=n) for r in range(3)]
+    ins = [cc.compress_window(dev(x)) for x in xs]
+    got = cc.reduce_compressed(ins, n).cpu().numpy()
+    assert np.array_equal(got, orc.reduce([orc.compress_window(x) for x in xs], n))
+
+
 # ---------------------------------------------------------------- paged payload
 KV_BLOCK = 16 * 8 * 128  # 16 tokens x 8 heads x 128 dim of the KV-cache shape = 4 chunks
 
