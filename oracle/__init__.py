@@ -63,12 +63,14 @@ def _bind(path: str):
                                   u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_reduce_mixed.argtypes = [u16p, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(sz), ctypes.c_int,
                                         sz, u8p, sz, ctypes.POINTER(sz)]
+    lib.oracle_reduce_op.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(sz), ctypes.c_int, sz,
+                                     ctypes.c_int, u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_compress_window.argtypes = [u16p, sz, u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_compress_paged.argtypes = [u16p, sz, ctypes.c_void_p, sz, u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_decompress_paged.argtypes = [u8p, sz, u16p, sz, ctypes.c_void_p, sz]
     for f in ("oracle_chunk_choice", "oracle_encode_chunk", "oracle_compress", "oracle_decompress",
               "oracle_reduce", "oracle_reduce_mixed", "oracle_compress_paged", "oracle_decompress_paged",
-              "oracle_compress_window"):
+              "oracle_compress_window", "oracle_reduce_op"):
         getattr(lib, f).restype = ctypes.c_int
     lib.oracle_sum_ranks.restype = None
     lib.oracle_plane_position.restype = None
@@ -270,6 +272,23 @@ def decompress_paged(s, pool, block_elems: int, table) -> np.ndarray:
     if st != OK:
         raise OracleError(st, "oracle_decompress_paged")
     return out
+
+
+OP_SUM, OP_MIN, OP_MAX = 0, 1, 2
+
+
+def reduce_op(streams, n: int, op: int) -> np.ndarray:
+    """reduce with op OP_SUM, OP_MIN or OP_MAX."""
+    bs = [np.ascontiguousarray(s, dtype=np.uint8) for s in streams]
+    ptrs = (ctypes.c_void_p * len(bs))(*[b.ctypes.data for b in bs])
+    sizes = (ctypes.c_size_t * len(bs))(*[b.size for b in bs])
+    cap = compress_bound(n)
+    out = np.empty(cap, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_reduce_op(ptrs, sizes, len(bs), n, op, out.ctypes.data, cap, ctypes.byref(nb))
+    if st != OK:
+        raise OracleError(st, "oracle_reduce_op")
+    return out[:nb.value]
 
 
 def reduce(streams, n: int) -> np.ndarray:

@@ -713,3 +713,55 @@ int oracle_decompress_paged(const uint8_t *s, size_t s_bytes, uint16_t *pool, si
     free(x);
     return st;
 }
+
+/* Min and max reduce ops (section 5: CopyReducePacks performs "the required
+ * collective operation (e.g., sum, min, max)").  Element-wise over the
+ * ranks, exact (the result is one of the inputs, so there is no binary32
+ * stage): a NaN in any rank gives 0x7FC0; otherwise the smallest (largest)
+ * value, with -0 below +0.  op: 1 min, 2 max (0 is the sum of oracle_reduce). */
+static int is_nan_bf16(uint16_t b)
+{
+    return (b & 0x7FFFu) > 0x7F80u;
+}
+static int less_bf16(uint16_t a, uint16_t b) /* a < b, neither NaN, -0 < +0 */
+{
+    int na = (a & 0x8000u) != 0, nb = (b & 0x8000u) != 0;
+    if (na != nb)
+        return na; /* negative (including -0) below positive (including +0) */
+    if (na)
+        return (a & 0x7FFFu) > (b & 0x7FFFu); /* larger magnitude is smaller */
+    return a < b;
+}
+
+int oracle_reduce_op(const uint8_t *const *ins, const size_t *in_bytes, int R, size_t n, int op, uint8_t *out,
+                     size_t capacity, size_t *out_bytes)
+{
+    if (op == 0)
+        return oracle_reduce(ins, in_bytes, R, n, out, capacity, out_bytes);
+    if ((op != 1 && op != 2) || R < 1 || R > 64 || n == 0 || ins == NULL || in_bytes == NULL || out == NULL)
+        return ORC_ERR_INVALID_ARG;
+    uint16_t *x = (uint16_t *)malloc(n * sizeof(uint16_t));
+    uint16_t *acc = (uint16_t *)malloc(n * sizeof(uint16_t));
+    int st = (x && acc) ? ORC_OK : ORC_ERR_INVALID_ARG;
+    for (int r = 0; r < R && st == ORC_OK; r++) {
+        st = oracle_decompress(ins[r], in_bytes[r], r == 0 ? acc : x, n);
+        if (st != ORC_OK || r == 0)
+            continue;
+        for (size_t i = 0; i < n; i++) {
+            uint16_t a = acc[i], b = x[i];
+            if (is_nan_bf16(a) || is_nan_bf16(b))
+                acc[i] = 0x7FC0;
+            else if (op == 1 ? less_bf16(b, a) : less_bf16(a, b))
+                acc[i] = b;
+        }
+    }
+    if (st == ORC_OK) {
+        for (size_t i = 0; i < n; i++)
+            if (is_nan_bf16(acc[i]))
+                acc[i] = 0x7FC0;
+        st = oracle_compress(acc, n, out, capacity, out_bytes);
+    }
+    free(x);
+    free(acc);
+    return st;
+}

@@ -45,6 +45,10 @@ MUTATIONS = [
      "st = oracle_decompress(ins[R - 1 - r], in_bytes[R - 1 - r], x, n);"),
     ("window_tie_keeps_larger_base", "if (b == 0 || n_esc < k_esc) {", "if (b == 0 || n_esc <= k_esc) {"),
     ("window_one_too_narrow", "unsigned top = b + S < 256 ? b + S : 256;", "unsigned top = b + S - 1 < 256 ? b + S - 1 : 256;"),
+    ("min_signed_zero_order", "        return na; /* negative (including -0) below positive (including +0) */",
+     "        return nb; /* negative (including -0) below positive (including +0) */"),
+    ("minmax_nan_dropped", "            if (is_nan_bf16(a) || is_nan_bf16(b))\n                acc[i] = 0x7FC0;\n            else if",
+     "            if (0)\n                acc[i] = 0x7FC0;\n            else if"),
     ("paged_gather_ignores_table", "memcpy(x + i * block_elems, pool + (size_t)table[i] * block_elems,",
      "memcpy(x + i * block_elems, pool + i * block_elems,"),
     ("paged_scatter_ignores_table", "memcpy(pool + (size_t)table[i] * block_elems, x + i * block_elems,",
@@ -114,6 +118,11 @@ def _battery(orc, wl):
     # local 2^30, remote -2^30 then 1: (2^30 - 2^30) + 1 = 1 only in this order
     check("mixed_rank_order", lambda: orc.decompress(
         orc.reduce_mixed(sp_a[3:], [orc.compress(sp_b[3:]), orc.compress(sp_c[3:])], 1), 1)[0] == 0x3F80)
+    mm = [np.array([0x0000, 0x3F80, 0x7FC1, 0x8000], np.uint16), np.array([0x8000, 0xBF80, 0x3F80, 0x0000], np.uint16)]
+    check("min_max", lambda: (lambda s: orc.decompress(orc.reduce_op(s, 4, 1), 4).tolist() ==
+                              [0x8000, 0xBF80, 0x7FC0, 0x8000] and
+                              orc.decompress(orc.reduce_op(s, 4, 2), 4).tolist() ==
+                              [0x0000, 0x3F80, 0x7FC0, 0x0000])([orc.compress(v) for v in mm]))
     wx = wl.generate(5, 0, start=(1 << 27) - 2 * CHUNK, count=4 * CHUNK)
     check("window_variant", lambda: orc.compress_window(wx).tobytes() == pf.encode_stream_window(wx))
     te = (np.arange(CHUNK) % 11 + 100).astype(np.uint16)  # exponents 100..110: k = 4 from any base 96..100

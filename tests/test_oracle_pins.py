@@ -389,6 +389,45 @@ def test_paged_round_trip_writes_only_the_named_blocks(orc, wl):
     assert np.array_equal(out, want)
 
 
+# ---------------------------------------------------------------- min / max reduce ops
+def _order_key(x):
+    """bf16 bits -> unsigned key in IEEE total order (-0 below +0)."""
+    x = x.astype(np.uint32)
+    return np.where(x & 0x8000, (~x) & 0xFFFF, x | 0x8000)
+
+
+def _minmax_numpy(xs, op):
+    keys = np.stack([_order_key(x) for x in xs])
+    pick = keys.argmin(0) if op == 1 else keys.argmax(0)
+    out = np.stack(xs)[pick, np.arange(xs[0].size)].astype(np.uint16)
+    nan = np.zeros(xs[0].size, bool)
+    for x in xs:
+        nan |= (x & 0x7FFF) > 0x7F80
+    out[nan] = 0x7FC0
+    return out
+
+
+@pytest.mark.parametrize("op", [1, 2])
+def test_reduce_min_max_match_an_independent_total_order(orc, wl, op):
+    n = 5 * CHUNK + 3
+    xs = [wl.generate(5, r, start=(1 << 27) - 2 * CHUNK, count=n) for r in range(3)]
+    rng = np.random.default_rng(op)
+    specials = np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC1, 0x0001, 0x8001, 0x3F80, 0xBF80], np.uint16)
+    xs.append(rng.choice(specials, n).astype(np.uint16))
+    got = orc.decompress(orc.reduce_op([orc.compress(x) for x in xs], n, op), n)
+    assert np.array_equal(got, _minmax_numpy(xs, op))
+
+
+def test_reduce_min_max_single_rank_and_signed_zero(orc):
+    x = np.array([0x8000, 0x0000, 0x7FC1, 0x3F80], np.uint16)
+    s = [orc.compress(x)]
+    for op in (1, 2):
+        assert np.array_equal(orc.decompress(orc.reduce_op(s, 4, op), 4), np.array([0x8000, 0x0000, 0x7FC0, 0x3F80]))
+    a, b = orc.compress(np.array([0x0000], np.uint16)), orc.compress(np.array([0x8000], np.uint16))
+    assert orc.decompress(orc.reduce_op([a, b], 1, 1), 1)[0] == 0x8000  # min(+0, -0) = -0
+    assert orc.decompress(orc.reduce_op([b, a], 1, 2), 1)[0] == 0x0000  # max(-0, +0) = +0
+
+
 # ---------------------------------------------------------------- window-base variant (version 2)
 def test_window_variant_matches_the_independent_encoder(orc, wl):
     """Every (k, base) escape count is recounted in numpy (pyformat.window_table)
