@@ -26,6 +26,7 @@ CCCL_ERR_TIMEOUT = 4
 CCCL_ERR_CUDA = 5
 CCCL_ERR_UNIMPLEMENTED = 6
 CHUNK_ELEMS = 4096
+CCCL_OP_SUM, CCCL_OP_MIN, CCCL_OP_MAX = 0, 1, 2
 MAX_RANKS = 64
 
 if not os.path.exists(LIB_PATH):
@@ -52,6 +53,8 @@ _lib.cccl_compress_paged.argtypes = [_vp, _sz, _sz, _vp, _sz, _vp, _sz, _vp, _sz
 _lib.cccl_compress_paged.restype = _i
 _lib.cccl_decompress_paged.argtypes = [_vp, _sz, _vp, _sz, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_decompress_paged.restype = _i
+_lib.cccl_reduce_op.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _i, _vp, _sz, _vp, _sz, _vp]
+_lib.cccl_reduce_op.restype = _i
 _lib.cccl_reduce_mixed.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_reduce_mixed.restype = _i
 _lib.cccl_get_result.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_i)]
@@ -166,6 +169,17 @@ def cccl_decompress_paged(s: torch.Tensor, pool: torch.Tensor, block_elems: int,
     _check(_lib.cccl_decompress_paged(s.data_ptr(), nbytes, pool.data_ptr(), pool.numel() // block_elems,
                                       block_elems, table.data_ptr(), table.numel(), ws.data_ptr(),
                                       ws.numel() * ws.element_size(), _stream(stream)), "cccl_decompress_paged")
+
+
+def cccl_reduce_op(ins: Sequence[torch.Tensor], n_elems: int, op: int, out: torch.Tensor, ws: torch.Tensor,
+                   in_bytes: Sequence[int] | None = None, stream=None) -> None:
+    """Enqueue the compressed reduce with operator ``op`` (CCCL_OP_SUM, _MIN or _MAX)."""
+    R = len(ins)
+    ptrs = (_vp * max(R, 1))(*[t.data_ptr() for t in ins])
+    sizes = [t.numel() * t.element_size() for t in ins] if in_bytes is None else list(in_bytes)
+    szs = (_sz * max(R, 1))(*sizes)
+    _check(_lib.cccl_reduce_op(ptrs, szs, R, n_elems, op, out.data_ptr(), out.numel() * out.element_size(),
+                               ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)), "cccl_reduce_op")
 
 
 def cccl_reduce_mixed(local: torch.Tensor, remote: Sequence[torch.Tensor], out: torch.Tensor, ws: torch.Tensor,

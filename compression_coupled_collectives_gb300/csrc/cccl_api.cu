@@ -202,6 +202,30 @@ cccl_status cccl_decompress_paged(const void* d_in, size_t in_bytes, uint16_t* d
     return CCCL_OK;
 }
 
+cccl_status cccl_reduce_op(const void* const* h_ins, const size_t* h_in_bytes, int R, size_t n_elems, int op,
+                           void* d_out, size_t out_capacity, void* d_ws, size_t ws_bytes, cccl_stream_t stream) {
+    if (op != CCCL_OP_SUM && op != CCCL_OP_MIN && op != CCCL_OP_MAX) return CCCL_ERR_INVALID_ARG;
+    if (h_ins == nullptr || h_in_bytes == nullptr || R < 1 || R > cccl::kMaxRanks) return CCCL_ERR_INVALID_ARG;
+    if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_out) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < cccl_workspace_bytes(n_elems)) return CCCL_ERR_INVALID_ARG;
+    if (out_capacity < cccl_compress_bound(n_elems)) return CCCL_ERR_CAPACITY;
+    if (!device_range(d_out, out_capacity) || !device_range(d_ws, ws_bytes)) return CCCL_ERR_INVALID_ARG;
+    cccl::ReduceInputs inputs{};
+    inputs.op = (uint32_t)op;
+    for (int r = 0; r < R; ++r) {
+        if (!aligned16(h_ins[r]) || h_in_bytes[r] == 0 || !device_range(h_ins[r], h_in_bytes[r]))
+            return CCCL_ERR_INVALID_ARG;
+        inputs.in[r] = static_cast<const uint8_t*>(h_ins[r]);
+        inputs.in_bytes[r] = h_in_bytes[r];
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    if (cccl::launch_reduce(inputs, R, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
 cccl_status cccl_reduce_mixed(const uint16_t* d_local, const void* const* h_ins, const size_t* h_in_bytes,
                               int n_remote, size_t n_elems, void* d_out, size_t out_capacity, void* d_ws,
                               size_t ws_bytes, cccl_stream_t stream) {

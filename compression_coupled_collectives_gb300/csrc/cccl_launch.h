@@ -16,6 +16,7 @@ struct ReduceInputs {
     const uint8_t* in[kMaxRanks];
     uint64_t in_bytes[kMaxRanks];
     const uint16_t* local;
+    uint32_t op;  // 0 sum (binary32, one rounding), 1 min, 2 max (exact)
 };
 
 // All pointers are device pointers already validated by the C ABI layer; the

@@ -58,6 +58,26 @@ __device__ __forceinline__ uint32_t canonical_nan_pair(uint32_t d) {
     return (d & ~mask) | (0x7FC07FC0u & mask);
 }
 
+// Element-wise min (op 1) or max (op 2) of two bf16 pairs, exact: a NaN in
+// either lane gives a NaN there (made canonical afterwards); otherwise the
+// IEEE total order, -0 below +0, through the usual sign-magnitude key
+// (negative: all bits flipped; positive: sign bit set), compared as u16.
+__device__ __forceinline__ uint32_t order_key_pair(uint32_t x) {
+    return x ^ ((((x >> 15) & 0x00010001u) * 0x7FFFu) | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t from_order_key_pair(uint32_t k) {
+    return k ^ ((((~k >> 15) & 0x00010001u) * 0x7FFFu) | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t nan_lanes_pair(uint32_t x) {  // 0xFFFF where x is a NaN
+    return ((((x & 0x7FFF7FFFu) + 0x007F007Fu) & 0x80008000u) >> 15) * 0xFFFFu;
+}
+__device__ __forceinline__ uint32_t minmax_pair(uint32_t a, uint32_t b, uint32_t op) {
+    const uint32_t ka = order_key_pair(a), kb = order_key_pair(b);
+    const uint32_t r = from_order_key_pair(op == 1 ? vmin_u16x2(ka, kb) : vmax_u16x2(ka, kb));
+    const uint32_t nan = nan_lanes_pair(a) | nan_lanes_pair(b);
+    return (r & ~nan) | (0x7FC07FC0u & nan);
+}
+
 // Warp-uniform reads of the abort flag and of a bounded wait's outcome.
 __device__ __forceinline__ bool warp_any(bool p) { return __any_sync(0xFFFFFFFFu, p); }
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
@@ -217,7 +237,7 @@ __device__ __forceinline__ void reduce_placer(const StreamOut& so, ReduceSmem& s
 }
 
 // --------------------------------------------------------------------------- teams
-__device__ __forceinline__ void reduce_team(int R, const uint16_t* local, const StreamOut& so,
+__device__ __forceinline__ void reduce_team(int R, const uint16_t* local, uint32_t op, const StreamOut& so,
                                             uint8_t* ring_base, uint32_t* prev_base, ReduceSmem& sm) {
     const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127;
     const uint32_t wq = tt >> 5;  // warp within the team = quarter of the chunk
@@ -286,7 +306,7 @@ __device__ __forceinline__ void reduce_team(int R, const uint16_t* local, const 
                         }
                         special = true;
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) acc[x] = widen_pair(V[x]);
+                        for (int x = 0; x < 16; ++x) acc[x] = op == 0 ? widen_pair(V[x]) : V[x];
                     } else if (fail == 0) {
                         const ChunkHeader h = read_chunk_header(buf);
                         bool good = chunk_header_valid(h, m.bytes[team][r], n_c);  // same for the team
@@ -311,6 +331,10 @@ __device__ __forceinline__ void reduce_team(int R, const uint16_t* local, const 
                         }
                         if (!good) {
                             fail = kStatusCorrupt;
+                        } else if (op != 0) {  // min / max: exact, on the bf16 pairs
+#pragma unroll
+                            for (int x = 0; x < 16; ++x)
+                                acc[x] = r == 0 ? V[x] : minmax_pair((uint32_t)acc[x], V[x], op);
                         } else if (r == 0) {
 #pragma unroll
                             for (int x = 0; x < 16; ++x) acc[x] = widen_pair(V[x]);
@@ -324,7 +348,7 @@ __device__ __forceinline__ void reduce_team(int R, const uint16_t* local, const 
                 }
                 if (fail == 0) {
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) P[x] = round_pair_bf16(acc[x]);
+                    for (int x = 0; x < 16; ++x) P[x] = op == 0 ? round_pair_bf16(acc[x]) : (uint32_t)acc[x];
                     if (bar.any(special)) {
 #pragma unroll
                         for (int x = 0; x < 16; ++x) P[x] = canonical_nan_pair(P[x]);
@@ -427,7 +451,7 @@ __global__ void __launch_bounds__(kReduceThreads, 1) reduce_kernel(ReduceInputs 
     else if (w == kPlacerWarp)
         reduce_placer(so, sm);
     else
-        reduce_team(R, inputs.local, so, ring, prev, sm);
+        reduce_team(R, inputs.local, inputs.op, so, ring, prev, sm);
 }
 
 cudaError_t launch_reduce(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,

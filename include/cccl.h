@@ -181,6 +181,19 @@ cccl_status cccl_reduce_compressed(const void *const *h_ins, const size_t *h_in_
                                    void *d_out, size_t out_capacity, void *d_ws, size_t ws_bytes,
                                    cccl_stream_t stream);
 
+/* Reduce operators of cccl_reduce_op ("CCCL: In-GPU Compression-Coupled
+ * Collective Communication", section 5: CopyReducePacks performs "the
+ * required collective operation (e.g., sum, min, max)"). */
+#define CCCL_OP_SUM 0 /* binary32 sum in rank order, one rounding: cccl_reduce_compressed */
+#define CCCL_OP_MIN 1 /* exact element-wise minimum: any NaN gives 0x7FC0; -0 below +0 */
+#define CCCL_OP_MAX 2 /* exact element-wise maximum: any NaN gives 0x7FC0; +0 above -0 */
+
+/* cccl_reduce_compressed with the operator `op` (CCCL_OP_*).  The result is
+ * compressed exactly as cccl_compress would.  An unknown op is INVALID_ARG;
+ * the other arguments and errors are those of cccl_reduce_compressed. */
+cccl_status cccl_reduce_op(const void *const *h_ins, const size_t *h_in_bytes, int R, size_t n_elems, int op,
+                           void *d_out, size_t out_capacity, void *d_ws, size_t ws_bytes, cccl_stream_t stream);
+
 /* Paged payload: the KV-cache blocks that prefill sends to decode ("CCCL:
  * In-GPU Compression-Coupled Collective Communication", section 6.2 and
  * Figure 3: PD disaggregation), compressed from where they lie in a paged

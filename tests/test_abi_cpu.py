@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     assert names == sorted(["cccl_compress_bound", "cccl_workspace_bytes", "cccl_compress", "cccl_compress_noalloc",
                             "cccl_decompress", "cccl_reduce_compressed", "cccl_reduce_mixed", "cccl_get_result",
                             "cccl_status_string", "cccl_compress_paged", "cccl_decompress_paged",
-                            "cccl_compress_window"]), names
+                            "cccl_compress_window", "cccl_reduce_op"]), names
 
 
 def test_library_exports_every_declared_symbol(cc):
@@ -110,6 +110,9 @@ def test_host_side_argument_checks(cc):
     assert lib.cccl_compress_window(A, 0, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_compress_window(A + 2, n, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_compress_window(A, n, B, bound - 1, W, wsb, None) == cc.CCCL_ERR_CAPACITY
+    assert lib.cccl_reduce_op(ptrs, sizes, 2, n, 3, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_op(ptrs, sizes, 2, n, -1, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_op(ptrs, sizes, 0, n, 1, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_get_result(None, None, None, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_get_result(W + 4, None, None, None) == cc.CCCL_ERR_INVALID_ARG
 

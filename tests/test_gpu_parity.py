@@ -311,6 +311,40 @@ def test_reduce_rejects_corrupt_input(cc, orc, wl):
         assert st == cc.CCCL_ERR_CORRUPT, name
 
 
+# ---------------------------------------------------------------- min / max reduce ops
+@pytest.mark.parametrize("op", [1, 2])
+@pytest.mark.parametrize("R", [1, 2, 3, 7])
+def test_reduce_min_max(cc, orc, wl, op, R):
+    n = 11 * CHUNK + 123
+    rng = np.random.default_rng(10 * op + R)
+    specials = np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC1, 0xFFFF, 0x0001, 0x8001, 0x3F80, 0xBF80], np.uint16)
+    xs = []
+    for r in range(R):
+        x = wl.generate(3, r, count=n)
+        idx = rng.choice(n, 300, replace=False)
+        x[idx] = rng.choice(specials, idx.size)
+        xs.append(x)
+    refs = [orc.compress(x) for x in xs]
+    streams = [torch.from_numpy(rf).cuda() for rf in refs]
+    out = cc.empty_stream(n)
+    ws = cc.empty_workspace(n)
+    cc.cccl_reduce_op(streams, n, op, out, ws)
+    nbytes, st = cc.cccl_get_result(ws)
+    assert st == 0
+    assert np.array_equal(out[:nbytes].cpu().numpy(), orc.reduce_op(refs, n, op))
+
+
+def test_reduce_op_sum_is_reduce_compressed(cc, orc, wl):
+    n = 7 * CHUNK + 1
+    refs = [orc.compress(wl.generate(2, r, count=n, n=1 << 20)) for r in range(2)]
+    streams = [torch.from_numpy(rf).cuda() for rf in refs]
+    out = cc.empty_stream(n)
+    ws = cc.empty_workspace(n)
+    cc.cccl_reduce_op(streams, n, cc.CCCL_OP_SUM, out, ws)
+    nbytes, _ = cc.cccl_get_result(ws)
+    assert np.array_equal(out[:nbytes].cpu().numpy(), orc.reduce(refs, n))
+
+
 # ---------------------------------------------------------------- selective-compression reduce
 def check_reduce_mixed(cc, orc, local, xs, what=""):
     n = local.size
