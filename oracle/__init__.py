@@ -1,4 +1,4 @@
-"""CPU oracle of the compressed bf16 stream and the fused compressed reduce.
+"""CPU oracle of the compressed stream (bf16, fp16, fp32) and the fused compressed reduce.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg (``bench.py``) may import this package.  The GPU
@@ -33,7 +33,7 @@ def build(force: bool = False) -> str:
         tmp = _LIB + ".tmp.%d" % os.getpid()
         subprocess.check_call(
             ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
-             "-Wall", "-Wextra", "-o", tmp, _SRC])
+             "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -68,7 +68,24 @@ def _bind(path: str):
     lib.oracle_compress_window.argtypes = [u16p, sz, u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_compress_paged.argtypes = [u16p, sz, ctypes.c_void_p, sz, u8p, sz, ctypes.POINTER(sz)]
     lib.oracle_decompress_paged.argtypes = [u8p, sz, u16p, sz, ctypes.c_void_p, sz]
-    for f in ("oracle_chunk_choice", "oracle_encode_chunk", "oracle_compress", "oracle_decompress",
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_compress_bound_typed.argtypes = [ip, sz]
+    lib.oracle_compress_bound_typed.restype = sz
+    lib.oracle_chunk_choice_typed.argtypes = [ip, vp, sz] + [ctypes.POINTER(ctypes.c_uint)] * 3 + \
+        [ctypes.POINTER(sz)] * 2
+    lib.oracle_encode_chunk_typed.argtypes = [ip, vp, sz, u8p, ctypes.POINTER(sz)]
+    lib.oracle_compress_typed.argtypes = [ip, vp, sz, u8p, sz, ctypes.POINTER(sz), ip]
+    lib.oracle_decompress_typed.argtypes = [ip, u8p, sz, vp, sz]
+    lib.oracle_sum_ranks_typed.argtypes = [ip, ctypes.POINTER(ctypes.c_void_p), ip, sz, vp]
+    lib.oracle_reduce_typed.argtypes = [ip, ip, vp, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(sz), ip, sz,
+                                        u8p, sz, ctypes.POINTER(sz)]
+    lib.oracle_round_fp16.argtypes = [ctypes.c_float]
+    lib.oracle_round_fp16.restype = ctypes.c_uint16
+    lib.oracle_fp16_to_float.argtypes = [ctypes.c_uint16]
+    lib.oracle_fp16_to_float.restype = ctypes.c_float
+    for f in ("oracle_chunk_choice_typed", "oracle_encode_chunk_typed", "oracle_compress_typed",
+              "oracle_decompress_typed", "oracle_sum_ranks_typed", "oracle_reduce_typed",
+              "oracle_chunk_choice", "oracle_encode_chunk", "oracle_compress", "oracle_decompress",
               "oracle_reduce", "oracle_reduce_mixed", "oracle_compress_paged", "oracle_decompress_paged",
               "oracle_compress_window", "oracle_reduce_op"):
         getattr(lib, f).restype = ctypes.c_int
@@ -110,7 +127,7 @@ class use_library:
 
 def build_from(src: str, out: str) -> str:
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
-                           "-w", "-o", out, src])
+                           "-w", "-o", out, src, "-lm"])
     return out
 
 
@@ -303,3 +320,115 @@ def reduce(streams, n: int) -> np.ndarray:
     if st != OK:
         raise OracleError(st, "oracle_reduce")
     return out[:nb.value]
+
+
+# ---------------------------------------------------------------------------
+# element types: bf16, fp16, fp32 (the same split with 8-, 5- and 8-bit
+# exponents).  Values travel as their bit patterns: uint16 for bf16 and fp16,
+# uint32 for fp32.
+# ---------------------------------------------------------------------------
+DTYPE_BF16, DTYPE_FP16, DTYPE_FP32 = 1, 2, 3
+_BITS = {DTYPE_BF16: np.uint16, DTYPE_FP16: np.uint16, DTYPE_FP32: np.uint32}
+
+
+def _bits(dtype: int, x) -> np.ndarray:
+    want = _BITS[dtype]
+    a = np.ascontiguousarray(x)
+    if a.dtype != want:
+        a = a.view(want) if a.dtype.itemsize == np.dtype(want).itemsize else a.astype(want)
+    return a.reshape(-1)
+
+
+def compress_bound_typed(dtype: int, n: int) -> int:
+    return _load().oracle_compress_bound_typed(dtype, n)
+
+
+def chunk_choice_typed(dtype: int, x) -> dict:
+    a = _bits(dtype, x)
+    raw, k, base = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+    n_esc, nbytes = ctypes.c_size_t(), ctypes.c_size_t()
+    st = _load().oracle_chunk_choice_typed(dtype, a.ctypes.data, a.size, ctypes.byref(raw), ctypes.byref(k),
+                                           ctypes.byref(base), ctypes.byref(n_esc), ctypes.byref(nbytes))
+    if st != OK:
+        raise OracleError(st, "oracle_chunk_choice_typed")
+    return dict(raw=raw.value, k=k.value, base=base.value, n_esc=n_esc.value, bytes=nbytes.value)
+
+
+def encode_chunk_typed(dtype: int, x) -> bytes:
+    a = _bits(dtype, x)
+    out = np.zeros(16 + 4 * CHUNK_ELEMS, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_encode_chunk_typed(dtype, a.ctypes.data, a.size, out.ctypes.data, ctypes.byref(nb))
+    if st != OK:
+        raise OracleError(st, "oracle_encode_chunk_typed")
+    return out[:nb.value].tobytes()
+
+
+def compress_typed(dtype: int, x, window: bool = False) -> np.ndarray:
+    """Bit patterns of one element type -> compressed stream (uint8 array)."""
+    a = _bits(dtype, x)
+    cap = compress_bound_typed(dtype, a.size)
+    out = np.empty(cap, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_compress_typed(dtype, a.ctypes.data, a.size, out.ctypes.data, cap, ctypes.byref(nb),
+                                       1 if window else 0)
+    if st != OK:
+        raise OracleError(st, "oracle_compress_typed")
+    return out[:nb.value]
+
+
+def decompress_typed(dtype: int, s, n: int) -> np.ndarray:
+    b = np.ascontiguousarray(np.frombuffer(bytes(s), np.uint8) if isinstance(s, (bytes, bytearray)) else s,
+                             dtype=np.uint8)
+    out = np.empty(n, _BITS[dtype])
+    st = _load().oracle_decompress_typed(dtype, b.ctypes.data, b.size, out.ctypes.data, n)
+    if st != OK:
+        raise OracleError(st, "oracle_decompress_typed")
+    return out
+
+
+def decompress_typed_status(dtype: int, s, n: int) -> int:
+    try:
+        decompress_typed(dtype, s, n)
+        return OK
+    except OracleError as e:
+        return e.status
+
+
+def sum_ranks_typed(dtype: int, xs) -> np.ndarray:
+    arrs = [_bits(dtype, x) for x in xs]
+    ptrs = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    out = np.empty(arrs[0].size, _BITS[dtype])
+    st = _load().oracle_sum_ranks_typed(dtype, ptrs, len(arrs), arrs[0].size, out.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "oracle_sum_ranks_typed")
+    return out
+
+
+def reduce_typed(dtype: int, streams, n: int, op: int = 0, local=None) -> np.ndarray:
+    """Reduce (op OP_SUM, OP_MIN, OP_MAX) of an optional local operand (rank
+    0) and compressed streams -> compressed stream of the result."""
+    bs = [np.ascontiguousarray(s, dtype=np.uint8) for s in streams]
+    ptrs = (ctypes.c_void_p * max(len(bs), 1))(*[b.ctypes.data for b in bs])
+    sizes = (ctypes.c_size_t * max(len(bs), 1))(*[b.size for b in bs])
+    loc = None
+    if local is not None:
+        loc = _bits(dtype, local)
+        if loc.size != n:
+            raise ValueError("local operand must hold n values")
+    cap = compress_bound_typed(dtype, n)
+    out = np.empty(cap, np.uint8)
+    nb = ctypes.c_size_t()
+    st = _load().oracle_reduce_typed(dtype, op, None if loc is None else loc.ctypes.data, ptrs, sizes, len(bs), n,
+                                     out.ctypes.data, cap, ctypes.byref(nb))
+    if st != OK:
+        raise OracleError(st, "oracle_reduce_typed")
+    return out[:nb.value]
+
+
+def round_fp16(f: float) -> int:
+    return int(_load().oracle_round_fp16(ctypes.c_float(f)))
+
+
+def fp16_to_float(h: int) -> float:
+    return float(_load().oracle_fp16_to_float(h))

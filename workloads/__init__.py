@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the five workloads (bf16 bit patterns as uint16).
+"""Seeded synthetic inputs for the five workloads (bf16 bit patterns as uint16;
+``generate_typed`` gives the same recipes as fp16 or fp32 bit patterns).
 
 Shared by the tests, the smoke check and the benchmark.  It holds none of the
 compression method's arithmetic: a counter-based SplitMix64 stream, uniforms,
@@ -112,6 +113,27 @@ def seed_of(workload: int, rank: int) -> int:
     return 1000 * workload + rank
 
 
+DTYPE_BF16, DTYPE_FP16, DTYPE_FP32 = 1, 2, 3
+# per element type: bit-pattern dtype, sign bit, exponent-all-ones pattern, fraction mask
+_TYPE = {DTYPE_BF16: (np.uint16, 0x8000, 0x7F80, 0x7F), DTYPE_FP16: (np.uint16, 0x8000, 0x7C00, 0x3FF),
+         DTYPE_FP32: (np.uint32, 0x80000000, 0x7F800000, 0x7FFFFF)}
+
+
+def to_fp16_bits(f32: np.ndarray) -> np.ndarray:
+    """binary32 -> IEEE fp16 bit patterns via torch's CPU conversion (RNE)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(f32, dtype=np.float32))
+    return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _to_bits(dtype: int, f32: np.ndarray) -> np.ndarray:
+    if dtype == DTYPE_BF16:
+        return to_bf16_bits(f32)
+    if dtype == DTYPE_FP16:
+        return to_fp16_bits(f32)
+    return np.ascontiguousarray(f32, dtype=np.float32).view(np.uint32)
+
+
 def generate(workload: int, rank: int = 0, start: int = 0, count: int | None = None,
              n: int | None = None) -> np.ndarray:
     """bf16 bits of ``workload``'s rank ``rank``, elements [start, start+count).
@@ -119,6 +141,18 @@ def generate(workload: int, rank: int = 0, start: int = 0, count: int | None = N
     ``n`` overrides the workload's element count (same recipe, other size);
     recipes that depend on the position (workloads 4 and 5) use it.
     """
+    return generate_typed(DTYPE_BF16, workload, rank, start, count, n)
+
+
+def generate_typed(dtype: int, workload: int, rank: int = 0, start: int = 0, count: int | None = None,
+                   n: int | None = None) -> np.ndarray:
+    """Bit patterns of ``workload``'s rank ``rank`` in element type ``dtype``
+    (1 bf16, 2 fp16: uint16; 3 fp32: uint32).  The same binary32 values as the
+    bf16 recipe, rounded by torch to the type (fp32: kept); workload 5's
+    incompressible half is random patterns of the type's width and its special
+    values use the type's fields (NaN payload, subnormal fraction: 1 .. all
+    fraction bits)."""
+    bits_t, sign_bit, exp_ones, frac_mask = _TYPE[dtype]
     total = SIZES[workload] if n is None else n
     if count is None:
         count = total - start
@@ -126,14 +160,14 @@ def generate(workload: int, rank: int = 0, start: int = 0, count: int | None = N
         raise ValueError("slice out of range")
     seed = seed_of(workload, rank)
     if count == 0:
-        return np.empty(0, np.uint16)
+        return np.empty(0, bits_t)
     if workload in (1, 3):
-        return to_bf16_bits((0.02 * normal(seed, _S_VALUE, start, count)).astype(np.float32))
+        return _to_bits(dtype, (0.02 * normal(seed, _S_VALUE, start, count)).astype(np.float32))
     if workload == 2:
         x = (1e-3 * normal(seed, _S_VALUE, start, count)).astype(np.float32)
         hot = uniform(seed, _S_AUX, start, count) <= 0.01
         x[hot] = x[hot] * np.float32(100.0)
-        return to_bf16_bits(x)
+        return _to_bits(dtype, x)
     if workload == 4:
         idx = np.arange(start, start + count, dtype=np.int64)
         head = (idx // KV_SHAPE[4]) % KV_SHAPE[3]
@@ -142,29 +176,31 @@ def generate(workload: int, rank: int = 0, start: int = 0, count: int | None = N
         slab_elems = KV_SHAPE[2] * KV_SHAPE[3] * KV_SHAPE[4]
         n_scales = -(-total // slab_elems) * KV_SHAPE[3]
         scales = 10.0 ** (-1.0 + 2.0 * uniform(seed, _S_AUX, 0, int(n_scales)))
-        return to_bf16_bits((normal(seed, _S_VALUE, start, count) * scales[scale_idx]).astype(np.float32))
+        return _to_bits(dtype, (normal(seed, _S_VALUE, start, count) * scales[scale_idx]).astype(np.float32))
     if workload == 5:
         half = total // 2
-        out = np.empty(count, np.uint16)
+        out = np.empty(count, bits_t)
+        width_mask = np.uint64(0xFFFF if bits_t == np.uint16 else 0xFFFFFFFF)
         lo = max(start, 0)
         a_end = min(start + count, half)
         if a_end > lo:  # incompressible half
-            out[:a_end - lo] = (u64(seed, _S_BITS, lo, a_end - lo) & np.uint64(0xFFFF)).astype(np.uint16)
+            out[:a_end - lo] = (u64(seed, _S_BITS, lo, a_end - lo) & width_mask).astype(bits_t)
         b_start = max(start, half)
         if start + count > b_start:
             m = start + count - b_start
             o = b_start - start
-            vals = to_bf16_bits(normal(seed, _S_VALUE, b_start, m).astype(np.float32))
+            vals = _to_bits(dtype, normal(seed, _S_VALUE, b_start, m).astype(np.float32))
             cat = uniform(seed, _S_CAT, b_start, m)
             bits = u64(seed, _S_AUX, b_start, m)
-            sign = ((bits >> np.uint64(63)) << np.uint64(15)).astype(np.uint16)
-            frac = ((bits & np.uint64(0x7F)) % np.uint64(127) + np.uint64(1)).astype(np.uint16)  # 1..127
+            sign = (((bits >> np.uint64(63)) * np.uint64(sign_bit))).astype(bits_t)
+            fm = np.uint64(frac_mask)
+            frac = ((bits & fm) % fm + np.uint64(1)).astype(bits_t)  # 1 .. frac_mask
             nan = cat <= 0.001
             inf = (cat > 0.001) & (cat <= 0.002)
             zero = (cat > 0.002) & (cat <= 0.003)
             sub = (cat > 0.003) & (cat <= 0.004)
-            vals[nan] = sign[nan] | np.uint16(0x7F80) | frac[nan]
-            vals[inf] = sign[inf] | np.uint16(0x7F80)
+            vals[nan] = sign[nan] | bits_t(exp_ones) | frac[nan]
+            vals[inf] = sign[inf] | bits_t(exp_ones)
             vals[zero] = sign[zero]
             vals[sub] = sign[sub] | frac[sub]
             out[o:] = vals
