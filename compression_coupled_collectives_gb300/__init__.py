@@ -1,5 +1,5 @@
-"""Python binding of libcccl: compressed bf16 communication buffers and the
-fused compressed reduce, on one GB300 GPU.
+"""Python binding of libcccl: compressed bf16 (and fp16, fp32) communication
+buffers and the fused compressed reduce, on one GB300 GPU.
 
 Every function here marshals arguments for the C ABI of ``include/cccl.h``
 (same names) and calls it; all compute runs in the library's sm_103a kernels.
@@ -27,6 +27,7 @@ CCCL_ERR_CUDA = 5
 CCCL_ERR_UNIMPLEMENTED = 6
 CHUNK_ELEMS = 4096
 CCCL_OP_SUM, CCCL_OP_MIN, CCCL_OP_MAX = 0, 1, 2
+CCCL_DTYPE_BF16, CCCL_DTYPE_FP16, CCCL_DTYPE_FP32 = 1, 2, 3
 MAX_RANKS = 64
 
 if not os.path.exists(LIB_PATH):
@@ -57,6 +58,15 @@ _lib.cccl_reduce_op.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _s
 _lib.cccl_reduce_op.restype = _i
 _lib.cccl_reduce_mixed.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _vp, _sz, _vp, _sz, _vp]
 _lib.cccl_reduce_mixed.restype = _i
+_lib.cccl_compress_bound_typed.argtypes = [_i, _sz]
+_lib.cccl_compress_bound_typed.restype = _sz
+_lib.cccl_compress_typed.argtypes = [_i, _vp, _sz, _vp, _sz, _vp, _sz, _i, _vp]
+_lib.cccl_compress_typed.restype = _i
+_lib.cccl_decompress_typed.argtypes = [_i, _vp, _sz, _vp, _sz, _vp, _sz, _vp]
+_lib.cccl_decompress_typed.restype = _i
+_lib.cccl_reduce_typed.argtypes = [_i, _i, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_sz), _i, _sz, _vp, _sz, _vp,
+                                   _sz, _vp]
+_lib.cccl_reduce_typed.restype = _i
 _lib.cccl_get_result.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_i)]
 _lib.cccl_get_result.restype = _i
 _lib.cccl_status_string.argtypes = [_i]
@@ -196,6 +206,60 @@ def cccl_reduce_mixed(local: torch.Tensor, remote: Sequence[torch.Tensor], out: 
                                   _stream(stream)), "cccl_reduce_mixed")
 
 
+# torch dtypes accepted for each element type (the values or their bit patterns)
+_TYPED = {CCCL_DTYPE_BF16: (torch.bfloat16, torch.int16, torch.uint16),
+          CCCL_DTYPE_FP16: (torch.float16, torch.int16, torch.uint16),
+          CCCL_DTYPE_FP32: (torch.float32, torch.int32, torch.uint32)}
+
+
+def _typed(dtype: int, x: torch.Tensor) -> torch.Tensor:
+    if dtype not in _TYPED:
+        raise ValueError("unknown element type %r" % (dtype,))
+    if x.dtype not in _TYPED[dtype]:
+        raise TypeError("expected values of element type %d or their bit patterns, got %s" % (dtype, x.dtype))
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x
+
+
+def cccl_compress_bound_typed(dtype: int, n_elems: int) -> int:
+    return int(_lib.cccl_compress_bound_typed(dtype, n_elems))
+
+
+def cccl_compress_typed(dtype: int, x: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, window: bool = False,
+                        stream=None) -> None:
+    """Enqueue compression of ``x`` (values of element type ``dtype``)."""
+    x = _typed(dtype, x)
+    _check(_lib.cccl_compress_typed(dtype, x.data_ptr(), x.numel(), out.data_ptr(), out.numel() * out.element_size(),
+                                    ws.data_ptr(), ws.numel() * ws.element_size(), 1 if window else 0,
+                                    _stream(stream)), "cccl_compress_typed")
+
+
+def cccl_decompress_typed(dtype: int, s: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                          in_bytes: int | None = None, stream=None) -> None:
+    """Enqueue decompression of stream ``s`` into ``out`` (out.numel() values of ``dtype``)."""
+    out = _typed(dtype, out)
+    nbytes = s.numel() * s.element_size() if in_bytes is None else int(in_bytes)
+    _check(_lib.cccl_decompress_typed(dtype, s.data_ptr(), nbytes, out.data_ptr(), out.numel(), ws.data_ptr(),
+                                      ws.numel() * ws.element_size(), _stream(stream)), "cccl_decompress_typed")
+
+
+def cccl_reduce_typed(dtype: int, op: int, local: torch.Tensor | None, ins: Sequence[torch.Tensor], n_elems: int,
+                      out: torch.Tensor, ws: torch.Tensor, in_bytes: Sequence[int] | None = None,
+                      stream=None) -> None:
+    """Enqueue the compressed reduce (op CCCL_OP_*) of the optional
+    uncompressed ``local`` operand (rank 0) and the streams ``ins``."""
+    if local is not None:
+        local = _typed(dtype, local)
+    n = len(ins)
+    ptrs = (_vp * max(n, 1))(*[t.data_ptr() for t in ins])
+    sizes = [t.numel() * t.element_size() for t in ins] if in_bytes is None else list(in_bytes)
+    szs = (_sz * max(n, 1))(*sizes)
+    _check(_lib.cccl_reduce_typed(dtype, op, None if local is None else local.data_ptr(), ptrs, szs, n, n_elems,
+                                  out.data_ptr(), out.numel() * out.element_size(), ws.data_ptr(),
+                                  ws.numel() * ws.element_size(), _stream(stream)), "cccl_reduce_typed")
+
+
 def cccl_get_result(ws: torch.Tensor, stream=None) -> tuple[int, int]:
     """Synchronise ``stream``; return (stream bytes of the last compress/reduce, device status)."""
     nbytes = ctypes.c_uint64(0)
@@ -264,4 +328,43 @@ def reduce_compressed(streams: Sequence[torch.Tensor], n_elems: int, stream=None
     cccl_reduce_compressed(streams, n_elems, out, ws, stream=stream)
     nbytes, dev = cccl_get_result(ws, stream)
     _check(dev, "cccl_reduce_compressed (device)")
+    return out[:nbytes]
+
+
+_BITS_OF = {CCCL_DTYPE_BF16: torch.int16, CCCL_DTYPE_FP16: torch.int16, CCCL_DTYPE_FP32: torch.int32}
+
+
+def empty_stream_typed(dtype: int, n_elems: int, device=None) -> torch.Tensor:
+    return torch.empty(cccl_compress_bound_typed(dtype, n_elems), dtype=torch.uint8, device=device or "cuda")
+
+
+def compress_typed(dtype: int, x: torch.Tensor, window: bool = False, stream=None) -> torch.Tensor:
+    """Compress values of element type ``dtype`` and wait; returns the trimmed stream."""
+    out = empty_stream_typed(dtype, x.numel(), x.device)
+    ws = empty_workspace(x.numel(), x.device)
+    cccl_compress_typed(dtype, x, out, ws, window, stream)
+    nbytes, dev = cccl_get_result(ws, stream)
+    _check(dev, "cccl_compress_typed (device)")
+    return out[:nbytes]
+
+
+def decompress_typed(dtype: int, s: torch.Tensor, n_elems: int, stream=None) -> torch.Tensor:
+    """Decompress and wait; returns n_elems bit patterns (int16, or int32 for fp32)."""
+    out = torch.empty(n_elems, dtype=_BITS_OF[dtype], device=s.device)
+    ws = empty_workspace(n_elems, s.device)
+    cccl_decompress_typed(dtype, s, out, ws, stream=stream)
+    _, dev = cccl_get_result(ws, stream)
+    _check(dev, "cccl_decompress_typed (device)")
+    return out
+
+
+def reduce_typed(dtype: int, streams: Sequence[torch.Tensor], n_elems: int, op: int = CCCL_OP_SUM,
+                 local: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Compressed reduce of any element type and wait; returns the trimmed stream."""
+    dev0 = local.device if local is not None else streams[0].device
+    out = empty_stream_typed(dtype, n_elems, dev0)
+    ws = empty_workspace(n_elems, dev0)
+    cccl_reduce_typed(dtype, op, local, streams, n_elems, out, ws, stream=stream)
+    nbytes, dev = cccl_get_result(ws, stream)
+    _check(dev, "cccl_reduce_typed (device)")
     return out[:nbytes]

@@ -51,6 +51,13 @@ cccl_status clear_ws(void* ws, size_t bytes, cudaStream_t s) {
 
 size_t ws_used(size_t n) { return sizeof(cccl::WsHeader) + 8 * n_chunks_of(n); }
 
+// bytes per value of a CCCL_DTYPE_*, 0 for an unknown type
+uint64_t elem_bytes(int dtype) {
+    if (dtype == CCCL_DTYPE_BF16 || dtype == CCCL_DTYPE_FP16) return 2;
+    if (dtype == CCCL_DTYPE_FP32) return 4;
+    return 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -249,6 +256,81 @@ cccl_status cccl_reduce_mixed(const uint16_t* d_local, const void* const* h_ins,
     if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
     if (cccl::launch_reduce(inputs, n_remote + 1, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws, s) !=
         cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
+size_t cccl_compress_bound_typed(int dtype, size_t n_elems) {
+    const uint64_t b = elem_bytes(dtype);
+    if (b == 0 || n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return 0;
+    const uint64_t full = n_elems / kChunkElems, tail = n_elems % kChunkElems;
+    uint64_t bytes = cccl::data_start(n_chunks_of(n_elems)) + full * (16 + b * kChunkElems);
+    if (tail) bytes += 16 + cccl::pad16(b * tail);
+    return (size_t)bytes;
+}
+
+cccl_status cccl_compress_typed(int dtype, const void* d_in, size_t n_elems, void* d_out, size_t out_capacity,
+                                void* d_ws, size_t ws_bytes, int window, cccl_stream_t stream) {
+    const uint64_t b = elem_bytes(dtype);
+    if (b == 0 || n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_in) || !aligned16(d_out) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < cccl_workspace_bytes(n_elems)) return CCCL_ERR_INVALID_ARG;
+    if (out_capacity < cccl_compress_bound_typed(dtype, n_elems)) return CCCL_ERR_CAPACITY;
+    if (!device_range(d_in, b * n_elems) || !device_range(d_out, out_capacity) || !device_range(d_ws, ws_bytes))
+        return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    if (cccl::launch_compress_typed((uint32_t)dtype, d_in, n_elems, static_cast<uint8_t*>(d_out), out_capacity, d_ws,
+                                    s, window != 0) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
+cccl_status cccl_decompress_typed(int dtype, const void* d_in, size_t in_bytes, void* d_out, size_t n_elems,
+                                  void* d_ws, size_t ws_bytes, cccl_stream_t stream) {
+    const uint64_t b = elem_bytes(dtype);
+    if (b == 0 || n_elems == 0 || n_elems > CCCL_MAX_ELEMS || in_bytes == 0) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_in) || !aligned16(d_out) || !aligned16(d_ws)) return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < sizeof(cccl::WsHeader)) return CCCL_ERR_INVALID_ARG;
+    if (!device_range(d_in, in_bytes) || !device_range(d_out, b * n_elems) || !device_range(d_ws, ws_bytes))
+        return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, sizeof(cccl::WsHeader), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    if (cccl::launch_decompress_typed((uint32_t)dtype, static_cast<const uint8_t*>(d_in), in_bytes, d_out, n_elems,
+                                      d_ws, s) != cudaSuccess)
+        return CCCL_ERR_CUDA;
+    return CCCL_OK;
+}
+
+cccl_status cccl_reduce_typed(int dtype, int op, const void* d_local, const void* const* h_ins,
+                              const size_t* h_in_bytes, int n_streams, size_t n_elems, void* d_out,
+                              size_t out_capacity, void* d_ws, size_t ws_bytes, cccl_stream_t stream) {
+    const uint64_t b = elem_bytes(dtype);
+    if (b == 0 || (op != CCCL_OP_SUM && op != CCCL_OP_MIN && op != CCCL_OP_MAX)) return CCCL_ERR_INVALID_ARG;
+    const int first = d_local != nullptr ? 1 : 0;
+    const int R = n_streams + first;
+    if (n_streams < 0 || R < 1 || R > cccl::kMaxRanks) return CCCL_ERR_INVALID_ARG;
+    if (n_streams > 0 && (h_ins == nullptr || h_in_bytes == nullptr)) return CCCL_ERR_INVALID_ARG;
+    if (n_elems == 0 || n_elems > CCCL_MAX_ELEMS) return CCCL_ERR_INVALID_ARG;
+    if (!aligned16(d_out) || !aligned16(d_ws) || (d_local != nullptr && !aligned16(d_local)))
+        return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < cccl_workspace_bytes(n_elems)) return CCCL_ERR_INVALID_ARG;
+    if (out_capacity < cccl_compress_bound_typed(dtype, n_elems)) return CCCL_ERR_CAPACITY;
+    if (!device_range(d_out, out_capacity) || !device_range(d_ws, ws_bytes)) return CCCL_ERR_INVALID_ARG;
+    if (d_local != nullptr && !device_range(d_local, b * n_elems)) return CCCL_ERR_INVALID_ARG;
+    cccl::ReduceInputs inputs{};
+    inputs.op = (uint32_t)op;
+    inputs.local = d_local;
+    for (int r = 0; r < n_streams; ++r) {
+        if (!aligned16(h_ins[r]) || h_in_bytes[r] == 0 || !device_range(h_ins[r], h_in_bytes[r]))
+            return CCCL_ERR_INVALID_ARG;
+        inputs.in[r + first] = static_cast<const uint8_t*>(h_ins[r]);
+        inputs.in_bytes[r + first] = h_in_bytes[r];
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, ws_used(n_elems), s) != CCCL_OK) return CCCL_ERR_CUDA;
+    if (cccl::launch_reduce_typed((uint32_t)dtype, inputs, R, n_elems, static_cast<uint8_t*>(d_out), out_capacity,
+                                  d_ws, s) != cudaSuccess)
         return CCCL_ERR_CUDA;
     return CCCL_OK;
 }

@@ -2,18 +2,19 @@
 // Collective Communication", sections 4.1, 4.3, 4.4; section 5 for the raw
 // partial chunk).
 //
-// Persistent and pipelined: one CTA per SM, kGroup compute warps plus one
-// control warp, and a ring of kRing stages, each holding one group of kGroup
-// consecutive chunks staged by bulk (TMA) copies.  Per group:
+// Persistent and pipelined: one CTA per SM, G compute warps plus one
+// control warp, and a ring of kRing stages, each holding one group of G
+// consecutive chunks staged by bulk (TMA) copies (G = 8 for the 16-bit
+// element types, 4 for fp32).  Per group:
 //   control warp  takes a ticket (the group index), issues the copies two
 //                 groups ahead, and once the compute warps have sized the
 //                 group, places it with one decoupled look-back;
 //   compute warp  sizes its chunk of group i+1 (exponent table, width,
-//                 escapes; the sign+fraction plane replaces the consumed
-//                 input in shared memory) while the control warp places
-//                 group i, then writes its chunk of group i at the final
-//                 offset: byte planes by bulk (TMA) stores, bit-planes and
-//                 escapes from registers.
+//                 escapes; the offset planes stay in registers) while the
+//                 control warp places group i, then writes its chunk of
+//                 group i at the final offset: the residual section and the
+//                 escapes read back from the staged input, the bit-planes
+//                 from registers, a raw chunk by one bulk (TMA) store.
 // So the look-back's wait for earlier groups overlaps with the sizing of the
 // next group, and the next copies are in flight during both.
 // Tickets hand out groups in order to CTAs that are already running, so every
@@ -26,36 +27,44 @@
 
 namespace cccl {
 
-constexpr int kGroup = 8;                     // chunks per group = compute warps
-constexpr int kRing = 3;                      // groups staged per CTA
-constexpr int kCtrl = kGroup;                 // warp index of the control warp
-constexpr int kCompressThreads = 32 * (kGroup + 1);
-constexpr size_t kChunkBytesRaw = 2 * kChunkElems;
-constexpr size_t kCompressSmemBytes = (size_t)kRing * kGroup * kChunkBytesRaw;
+// chunks per group = compute warps: 8 for the 16-bit types, 4 for fp32 (the
+// stage of a group is 64 KiB either way)
+template <class D>
+__host__ __device__ constexpr int group_of() { return D::kElemBytes == 4 ? 4 : 8; }
+constexpr int kRing = 3;  // groups staged per CTA
+template <class D>
+__host__ __device__ constexpr size_t raw_chunk_of() { return (size_t)D::kElemBytes * kChunkElems; }
+template <class D>
+__host__ __device__ constexpr int compress_threads() { return 32 * (group_of<D>() + 1); }
+template <class D>
+__host__ __device__ constexpr size_t compress_smem() { return (size_t)kRing * group_of<D>() * raw_chunk_of<D>(); }
 
+template <int G>
 struct CompressSmem {
-    uint64_t load[kRing][kGroup];  // stage filled (one per compute warp)
+    uint64_t load[kRing][G];       // stage filled (one per compute warp)
     uint64_t sized[kRing];         // all compute warps sized the stage's group
     uint64_t free_[kRing];         // all compute warps wrote the stage's group out
     uint64_t placed[2];            // control warp published the offsets
     uint64_t group[kRing];         // group index held by each stage (>= n_groups: none)
     unsigned long long tally[kRing];  // sized warps (high word) and their bytes (low word)
-    uint32_t size[kRing][kGroup];
-    uint64_t off[2][kGroup];       // chunk offsets, or kFlagPoison
-    uint32_t hist[kGroup][264];    // window-base variant: each compute warp's exponent histogram
+    uint32_t size[kRing][G];
+    uint64_t off[2][G];            // chunk offsets, or kFlagPoison
+    uint32_t hist[G][264];         // window-base variant: each compute warp's exponent histogram
 };
 
 // Control lane: fill stage s with group g (or mark it empty).
-__device__ __forceinline__ void issue_group(const uint16_t* in, const Paging& pg, WsHeader* ws, uint64_t g,
-                                            uint64_t n_groups, uint64_t n_full, uint8_t* stage, CompressSmem& sm,
+template <class D, int G>
+__device__ __forceinline__ void issue_group(const uint8_t* in, const Paging& pg, WsHeader* ws, uint64_t g,
+                                            uint64_t n_groups, uint64_t n_full, uint8_t* stage, CompressSmem<G>& sm,
                                             int s) {
+    constexpr size_t kRaw = raw_chunk_of<D>();
     sm.group[s] = g;
     sm.tally[s] = 0;
-    for (int w = 0; w < kGroup; ++w) {
-        const uint64_t c = g * kGroup + w;
+    for (int w = 0; w < G; ++w) {
+        const uint64_t c = g * G + w;
         const uint64_t e = g < n_groups && c < n_full ? chunk_elem_offset(pg, c) : kBadChunk;
         if (e != kBadChunk) {
-            bulk_load(stage + ((size_t)s * kGroup + w) * kChunkBytesRaw, in + e, kChunkBytesRaw, &sm.load[s][w]);
+            bulk_load(stage + ((size_t)s * G + w) * kRaw, in + e * D::kElemBytes, (uint32_t)kRaw, &sm.load[s][w]);
         } else {
             if (g < n_groups && c < n_full) record_error(ws, kStatusInvalidArg);  // a block outside the pool
             mbar_arrive(&sm.load[s][w]);  // nothing to copy: complete the phase at once
@@ -74,25 +83,30 @@ struct WarpChunk {
     uint64_t c;
 };
 
-template <bool kWindow>
-__device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__ in, const StreamOut& so,
-                                             uint8_t* stage, CompressSmem& sm, WarpChunk& cur, WarpChunk& prev) {
+template <class D, bool kWindow>
+__device__ __forceinline__ bool compute_step(int i, const uint8_t* __restrict__ in, const StreamOut& so,
+                                             uint8_t* stage, CompressSmem<group_of<D>()>& sm, WarpChunk& cur,
+                                             WarpChunk& prev) {
+    constexpr int G = group_of<D>();
+    constexpr size_t kRaw = raw_chunk_of<D>();
+    using Elem = typename std::conditional<D::kElemBytes == 4, uint32_t, uint16_t>::type;
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint64_t n_full = so.n_elems / kChunkElems;
-    const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
+    const uint64_t n_groups = (so.n_chunks + G - 1) / G;
     const int s = i % kRing;
     const bool filled = __all_sync(0xFFFFFFFFu, mbar_wait(&sm.load[s][w], (uint32_t)(i / kRing) & 1u));
     const uint64_t g = sm.group[s];
     const bool live = filled && g < n_groups;
     if (live) {
-        cur.c = g * kGroup + w;
+        cur.c = g * G + w;
         cur.bytes = 0;
         if (cur.c < n_full) {
-            const uint8_t* chunk = stage + ((size_t)s * kGroup + w) * kChunkBytesRaw;
-            cur.plan = kWindow ? plan_chunk_warp_window(chunk, cur.regs, sm.hist[w]) : plan_chunk_warp(chunk, cur.regs);
+            const uint8_t* chunk = stage + ((size_t)s * G + w) * kRaw;
+            cur.plan = kWindow ? plan_chunk_warp_window<D>(chunk, cur.regs, sm.hist[w])
+                               : plan_chunk_warp<D>(chunk, cur.regs);
             cur.bytes = cur.plan.bytes;
         } else if (cur.c < so.n_chunks) {
-            cur.bytes = tail_chunk_bytes((uint32_t)(so.n_elems - cur.c * kChunkElems));
+            cur.bytes = tail_chunk_bytes<D>((uint32_t)(so.n_elems - cur.c * kChunkElems));
         }
         __syncwarp();
         if (lane == 0) {
@@ -101,7 +115,7 @@ __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__
             // the look-backs of later groups need not wait for this CTA's
             // control warp
             const unsigned long long old = atomicAdd(&sm.tally[s], (1ull << 32) | cur.bytes);
-            if ((old >> 32) == kGroup - 1)
+            if ((old >> 32) == G - 1)
                 publish_unit_size(so.status, g, (uint32_t)old + cur.bytes, data_start(so.n_chunks));
             mbar_arrive(&sm.sized[s]);
         }
@@ -118,12 +132,12 @@ __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__
                 } else {
                     uint8_t* dst = so.out + off;
                     if (prev.c < n_full) {
-                        write_chunk_warp(prev.regs, prev.plan, stage + ((size_t)sp * kGroup + w) * kChunkBytesRaw,
-                                         dst);
+                        write_chunk_warp<D>(prev.regs, prev.plan, stage + ((size_t)sp * G + w) * kRaw, dst);
                     } else {
-                        const uint16_t* src = in + prev.c * kChunkElems;  // a partial chunk is never paged
-                        write_tail_chunk_warp([src](uint32_t e) { return src[e]; },
-                                              (uint32_t)(so.n_elems - prev.c * kChunkElems), dst);
+                        // a partial chunk is never paged
+                        const Elem* src = reinterpret_cast<const Elem*>(in) + prev.c * kChunkElems;
+                        write_tail_chunk_warp<D>([src](uint32_t e) { return src[e]; },
+                                                 (uint32_t)(so.n_elems - prev.c * kChunkElems), dst);
                     }
                     if (lane == 0) finish_chunk(so, prev.c, off, prev.bytes);
                 }
@@ -137,20 +151,22 @@ __device__ __forceinline__ bool compute_step(int i, const uint16_t* __restrict__
     return live;
 }
 
-template <bool kWindow>
-__global__ void __launch_bounds__(kCompressThreads, 1)
-    compress_kernel(const uint16_t* __restrict__ in, Paging pg, StreamOut so) {
+template <class D, bool kWindow>
+__global__ void __launch_bounds__(compress_threads<D>(), 1)
+    compress_kernel(const uint8_t* __restrict__ in, Paging pg, StreamOut so) {
+    constexpr int G = group_of<D>();
+    constexpr int kCtrl = G;  // warp index of the control warp
     extern __shared__ __align__(128) uint8_t stage[];
-    __shared__ CompressSmem sm;
+    __shared__ CompressSmem<G> sm;
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint64_t n_full = so.n_elems / kChunkElems;
-    const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
+    const uint64_t n_groups = (so.n_chunks + G - 1) / G;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) {
-            for (int i = 0; i < kGroup; ++i) mbar_init(&sm.load[s][i], 1);
-            mbar_init(&sm.sized[s], kGroup);
-            mbar_init(&sm.free_[s], kGroup);
+            for (int i = 0; i < G; ++i) mbar_init(&sm.load[s][i], 1);
+            mbar_init(&sm.sized[s], G);
+            mbar_init(&sm.free_[s], G);
         }
         for (int x = 0; x < 2; ++x) mbar_init(&sm.placed[x], 1);
         fence_mbar_init();
@@ -165,12 +181,12 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
         // stages free up.  (Taken all at once, every CTA's third ticket would
         // be sized two iterations later than its number says, and every
         // look-back behind it would wait for that.)
-        if (lane == 0) issue_group(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 0);
+        if (lane == 0) issue_group<D>(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 0);
         __syncwarp();
         const bool first_landed = __all_sync(0xFFFFFFFFu, mbar_wait(&sm.load[0][0], 0u));
         if (lane == 0) {
             if (!first_landed) record_error(so.ws, kStatusTimeout);
-            issue_group(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 1);
+            issue_group<D>(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 1);
         }
         __syncwarp();
         for (int i = 0;; ++i) {
@@ -182,19 +198,20 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
                 break;
             }
             if (i == 0) {
-                if (lane == 0) issue_group(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 2);
+                if (lane == 0)
+                    issue_group<D>(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, 2);
                 __syncwarp();
             }
-            const uint32_t mine = lane < (uint32_t)kGroup ? sm.size[s][lane] : 0u;
+            const uint32_t mine = lane < (uint32_t)G ? sm.size[s][lane] : 0u;
             uint32_t incl = mine;
 #pragma unroll
-            for (int d = 1; d < kGroup; d <<= 1) {
+            for (int d = 1; d < G; d <<= 1) {
                 const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
                 if (lane >= (uint32_t)d) incl += t;
             }
-            const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, kGroup - 1);
+            const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, G - 1);
             const uint64_t go = lookback_offset_wide(so.status, g, total, data_start(so.n_chunks), so.ws, true);
-            if (lane < (uint32_t)kGroup) sm.off[i & 1][lane] = go == kFlagPoison ? kFlagPoison : go + (incl - mine);
+            if (lane < (uint32_t)G) sm.off[i & 1][lane] = go == kFlagPoison ? kFlagPoison : go + (incl - mine);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.placed[i & 1]);
             // group i-1 is written out: refill its stage, for group i+2
@@ -206,7 +223,7 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
                 }
                 if (lane == 0) {
                     fence_proxy_async_smem();
-                    issue_group(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, sp);
+                    issue_group<D>(in, pg, so.ws, atomicAdd(&so.ws->ticket, 1u), n_groups, n_full, stage, sm, sp);
                 }
                 __syncwarp();
             }
@@ -219,21 +236,19 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
     cur.bytes = prev.bytes = 0;
     cur.c = prev.c = 0;
     for (int i = 0;; ++i) {
-        if (!compute_step<kWindow>(i, in, so, stage, sm, cur, prev)) break;
+        if (!compute_step<D, kWindow>(i, in, so, stage, sm, cur, prev)) break;
         prev = cur;
     }
 }
 
-cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
-                            cudaStream_t stream, const Paging& pg, bool window) {
+template <class D, bool kWindow>
+cudaError_t launch_compress_t(const uint8_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
+                              cudaStream_t stream, const Paging& pg) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(compress_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kCompressSmemBytes);
-        if (attr == cudaSuccess)
-            attr = cudaFuncSetAttribute(compress_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kCompressSmemBytes);
+        attr = cudaFuncSetAttribute(compress_kernel<D, kWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)compress_smem<D>());
     });
     if (attr != cudaSuccess) return attr;
     int dev = 0, sms = 0;
@@ -247,14 +262,33 @@ cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, 
     so.status = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + sizeof(WsHeader));
     so.n_elems = n_elems;
     so.n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
-    so.version = window ? kVersionWindow : kVersion;
-    const uint64_t n_groups = (so.n_chunks + kGroup - 1) / kGroup;
+    so.version = kWindow ? kVersionWindow : kVersion;
+    so.dtype = D::kCode;
+    const uint64_t n_groups = (so.n_chunks + group_of<D>() - 1) / group_of<D>();
     const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
-    if (window)
-        compress_kernel<true><<<grid, kCompressThreads, kCompressSmemBytes, stream>>>(in, pg, so);
-    else
-        compress_kernel<false><<<grid, kCompressThreads, kCompressSmemBytes, stream>>>(in, pg, so);
+    compress_kernel<D, kWindow><<<grid, compress_threads<D>(), compress_smem<D>(), stream>>>(in, pg, so);
     return cudaGetLastError();
+}
+
+cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
+                            cudaStream_t stream, const Paging& pg, bool window) {
+    const uint8_t* bytes = reinterpret_cast<const uint8_t*>(in);
+    return window ? launch_compress_t<Bf16, true>(bytes, n_elems, out, capacity, ws, stream, pg)
+                  : launch_compress_t<Bf16, false>(bytes, n_elems, out, capacity, ws, stream, pg);
+}
+
+cudaError_t launch_compress_typed(uint32_t dtype, const void* in, uint64_t n_elems, uint8_t* out, uint64_t capacity,
+                                  void* ws, cudaStream_t stream, bool window) {
+    const uint8_t* bytes = static_cast<const uint8_t*>(in);
+    const Paging pg{nullptr, 1, 0};
+    if (dtype == Fp16::kCode)
+        return window ? launch_compress_t<Fp16, true>(bytes, n_elems, out, capacity, ws, stream, pg)
+                      : launch_compress_t<Fp16, false>(bytes, n_elems, out, capacity, ws, stream, pg);
+    if (dtype == Fp32::kCode)
+        return window ? launch_compress_t<Fp32, true>(bytes, n_elems, out, capacity, ws, stream, pg)
+                      : launch_compress_t<Fp32, false>(bytes, n_elems, out, capacity, ws, stream, pg);
+    return window ? launch_compress_t<Bf16, true>(bytes, n_elems, out, capacity, ws, stream, pg)
+                  : launch_compress_t<Bf16, false>(bytes, n_elems, out, capacity, ws, stream, pg);
 }
 
 // ---------------------------------------------------------------------------
@@ -263,9 +297,9 @@ cudaError_t launch_compress(const uint16_t* in, uint64_t n_elems, uint8_t* out, 
 // group) lives in this file-scope device array instead.  Every GPU that loads
 // the library holds it until the process exits.
 // ---------------------------------------------------------------------------
-constexpr uint64_t kNoAllocMaxGroups = CCCL_NOALLOC_MAX_ELEMS / kChunkElems / kGroup;
+constexpr uint64_t kNoAllocMaxGroups = CCCL_NOALLOC_MAX_ELEMS / kChunkElems / group_of<Bf16>();
 constexpr size_t kNoAllocScratchBytes = sizeof(WsHeader) + 8 * kNoAllocMaxGroups;
-static_assert(CCCL_NOALLOC_MAX_ELEMS % ((uint64_t)kChunkElems * kGroup) == 0, "whole groups");
+static_assert(CCCL_NOALLOC_MAX_ELEMS % ((uint64_t)kChunkElems * group_of<Bf16>()) == 0, "whole groups");
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -301,7 +335,7 @@ cudaError_t launch_compress_noalloc(const uint16_t* in, uint64_t n_elems, uint8_
     cudaError_t e = noalloc_scratch(&scratch);
     if (e != cudaSuccess) return e;
     const uint64_t n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
-    const uint64_t n_groups = (n_chunks + kGroup - 1) / kGroup;
+    const uint64_t n_groups = (n_chunks + group_of<Bf16>() - 1) / group_of<Bf16>();
     // the scratch keeps the previous call's contents: clear what must start at
     // zero, and the stream header, whose size field then stays 0 unless the
     // whole stream was placed

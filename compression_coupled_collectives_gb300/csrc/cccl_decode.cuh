@@ -4,36 +4,57 @@
 // Inverse of the split of "CCCL: In-GPU Compression-Coupled Collective
 // Communication", section 4.1: each exponent is base + code, or, where the
 // code is the sentinel 2^k - 1, the next byte of the chunk's escape list
-// (bit-plane order); sign and fraction come back from their byte.
+// (bit-plane order); sign and fraction come back from the residual section.
 #pragma once
 
 #include "cccl_device.cuh"
 
 namespace cccl {
 
-// Decode the full chunk staged at `buf` (header already validated against
-// the stream) into this thread's 16 words of bf16 pairs: thread t (warp
-// q = t / 32, lane l) gets rows 4 q .. 4 q + 3, elements 8 l .. 8 l + 7 of
-// each, as P[4 jj + w] = elements 2 w, 2 w + 1 of row 4 q + jj.  The four
-// warps of a team (four consecutive warps starting at a multiple of four;
-// q = warp index mod 4) call it together and meet at `Barrier`; every branch
-// on the header is uniform over them.  Returns false if the chunk body is malformed (a sentinel
-// count that disagrees with n_esc, or base + code above 255).  `special` is
-// set when the chunk may hold an exponent of 255 (Inf or NaN).
-template <typename Barrier>
-__device__ __forceinline__ bool decode_full_chunk(const Barrier& bar, uint8_t* buf, const ChunkHeader& h,
-                                                  uint32_t P[16], uint32_t* s_row_tot, bool& special) {
-    const uint32_t t = threadIdx.x, lane = t & 31, q = (t >> 5) & 3;
-    const uint8_t* body = buf + kChunkHeaderBytes;
-    if (h.mode == kModeRaw) {
+// This thread's words (decode_full_chunk's layout, below) of 4096 raw values
+// at `vals` in shared memory.
+template <class D>
+__device__ __forceinline__ void load_raw_full(const uint8_t* vals, uint32_t* P) {
+    const uint32_t lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+    if constexpr (D::kElemBytes == 4) {
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            const uint4 v = *reinterpret_cast<const uint4*>(body + 512 * (4 * q + jj) + 16 * lane);
+            const uint8_t* row = vals + 1024 * (4 * q + jj) + 32 * lane;
+            const uint4 a = *reinterpret_cast<const uint4*>(row), b = *reinterpret_cast<const uint4*>(row + 16);
+            P[8 * jj] = a.x, P[8 * jj + 1] = a.y, P[8 * jj + 2] = a.z, P[8 * jj + 3] = a.w;
+            P[8 * jj + 4] = b.x, P[8 * jj + 5] = b.y, P[8 * jj + 6] = b.z, P[8 * jj + 7] = b.w;
+        }
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const uint4 v = *reinterpret_cast<const uint4*>(vals + 512 * (4 * q + jj) + 16 * lane);
             P[4 * jj] = v.x;
             P[4 * jj + 1] = v.y;
             P[4 * jj + 2] = v.z;
             P[4 * jj + 3] = v.w;
         }
+    }
+}
+
+// Decode the full chunk staged at `buf` (header already validated against
+// the stream) into this thread's words.  Thread t (warp q = t / 32, lane l)
+// gets rows 4 q .. 4 q + 3, elements 8 l .. 8 l + 7 of each: for the 16-bit
+// types P[4 jj + w] = elements 2 w, 2 w + 1 of row 4 q + jj (16 words), for
+// fp32 P[8 jj + s] = element s of row 4 q + jj (32 words).  The four warps of
+// a team (four consecutive warps starting at a multiple of four; q = warp
+// index mod 4) call it together and meet at `Barrier`; every branch on the
+// header is uniform over them.  Returns false if the chunk body is malformed
+// (a sentinel count that disagrees with n_esc, or an exponent the type cannot
+// hold).  `special` is set when the chunk may hold an all-ones exponent (Inf
+// or NaN).
+template <class D, typename Barrier>
+__device__ __forceinline__ bool decode_full_chunk(const Barrier& bar, uint8_t* buf, const ChunkHeader& h, uint32_t* P,
+                                                  uint32_t* s_row_tot, bool& special) {
+    constexpr uint32_t kTop = (1u << D::kExpBits) - 1;  // all-ones exponent
+    const uint32_t t = threadIdx.x, lane = t & 31, q = (t >> 5) & 3;
+    const uint8_t* body = buf + kChunkHeaderBytes;
+    if (h.mode == kModeRaw) {
+        load_raw_full<D>(body, P);
         special = true;
         return true;
     }
@@ -46,8 +67,21 @@ __device__ __forceinline__ bool decode_full_chunk(const Barrier& bar, uint8_t* b
         S[2 * jj + 1] = v.y;
     }
     uint32_t sent = 0xFFFFFFFFu;  // bit set where the code is the sentinel (all k bits set)
-    const uint8_t* col = body + kSmPlaneBytes + 4 * (32 * q + lane);
-    if (k >= 4) {  // one 8x8 bit transpose turns the planes into codes
+    const uint8_t* col = body + D::kResidBytes + 4 * (32 * q + lane);
+    if constexpr (D::kExpBits == 5) {
+        // codes (k <= 4) in slots 0..3 and the three residual planes in slots
+        // 5..7: one transpose gives per byte code | f8 << 5 | f9 << 6 | sign << 7
+        const uint8_t* rcol = body + kSmPlaneBytes + 4 * (32 * q + lane);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            code[p] = p < k ? *reinterpret_cast<const uint32_t*>(col + kPlaneBytes * p) : 0xFFFFFFFFu;
+            sent &= code[p];
+            if (p >= k) code[p] = 0u;
+        }
+#pragma unroll
+        for (int r = 0; r < 3; ++r) code[5 + r] = *reinterpret_cast<const uint32_t*>(rcol + kPlaneBytes * r);
+        transpose8x8x4(code);
+    } else if (k >= 4) {  // one 8x8 bit transpose turns the planes into codes
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             code[p] = p < k ? *reinterpret_cast<const uint32_t*>(col + kPlaneBytes * p) : 0xFFFFFFFFu;
@@ -63,18 +97,26 @@ __device__ __forceinline__ bool decode_full_chunk(const Barrier& bar, uint8_t* b
             sent &= w;
         }
     }
+    uint32_t R[8];  // fp16: the residual bits 5..7 of every byte
+    if constexpr (D::kExpBits == 5) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            R[m] = code[m] & 0xE0E0E0E0u;
+            code[m] &= 0x0F0F0F0Fu;
+        }
+    }
     const uint32_t base4 = h.base * 0x01010101u;
     uint32_t E[8];
     if (k == 0) {
 #pragma unroll
         for (int m = 0; m < 8; ++m) E[m] = base4;
-        special = (h.base == 255);
+        special = (h.base == kTop);
     } else {
         const uint32_t max_code = (1u << k) - 2u;  // largest non-sentinel code
-        special = (h.base + max_code >= 255u);
-        if (h.base + max_code + 1u <= 255u) {
-            // no code, the sentinel included, carries out of its byte;
-            // escaped bytes are overwritten below
+        special = (h.base + max_code >= kTop);
+        if (h.base + max_code + 1u <= kTop) {
+            // no code, the sentinel included, leaves the type's exponents (or
+            // carries out of its byte); escaped bytes are overwritten below
 #pragma unroll
             for (int m = 0; m < 8; ++m) E[m] = code[m] + base4;
         } else {  // only a malformed stream overflows here
@@ -84,7 +126,7 @@ __device__ __forceinline__ bool decode_full_chunk(const Barrier& bar, uint8_t* b
                 const uint32_t ff = ((sent >> m) & 0x01010101u) * 0xFFu;
                 const uint32_t c = code[m] & ~ff;
 #pragma unroll
-                for (int b = 0; b < 4; ++b) bad |= ((c >> (8 * b)) & 0xFFu) + h.base > 255u;
+                for (int b = 0; b < 4; ++b) bad |= ((c >> (8 * b)) & 0xFFu) + h.base > kTop;
                 E[m] = (c + base4) & ~ff;
             }
             if (bar.any(bad)) return false;
@@ -111,11 +153,11 @@ __device__ __forceinline__ bool decode_full_chunk(const Barrier& bar, uint8_t* b
                 total += v;
             }
             if (total != h.n_esc) return false;  // CTA-uniform
-            const uint8_t* esc = body + kSmPlaneBytes + kPlaneBytes * k;
-            bool inf_nan = false;
+            const uint8_t* esc = body + D::kResidBytes + kPlaneBytes * k;
+            bool inf_nan = false, esc_bad = false;
             if (sent) {
                 // patch the escaped exponents in shared memory: this thread's
-                // exponent quads go over its own sign+fraction bytes (already
+                // exponent quads go over its own byte-plane bytes (already
                 // in S), each escape byte lands in place, the quads come back
                 uint8_t* own = buf + kChunkHeaderBytes + 256 * 4 * q + 8 * lane;
 #pragma unroll
@@ -127,7 +169,8 @@ __device__ __forceinline__ bool decode_full_chunk(const Barrier& bar, uint8_t* b
                     rest &= rest - 1;
                     const uint32_t e = idx < h.n_esc ? esc[idx] : 0u;
                     ++idx;
-                    inf_nan |= (e == 255u);
+                    inf_nan |= (e == kTop);
+                    if constexpr (D::kExpBits < 8) esc_bad |= (e > kTop);
                     own[((bit & 6) << 7) | ((bit & 1) << 2) | (bit >> 3)] = (uint8_t)e;
                 }
 #pragma unroll
@@ -137,11 +180,37 @@ __device__ __forceinline__ bool decode_full_chunk(const Barrier& bar, uint8_t* b
                     E[2 * jj + 1] = v.y;
                 }
             }
+            if constexpr (D::kExpBits < 8) {
+                if (bar.any(esc_bad)) return false;
+            }
             special = special || inf_nan;
         }
     }
+    if constexpr (D::kExpBits == 5) {
 #pragma unroll
-    for (int m = 0; m < 8; ++m) join_quad(E[m], S[m], P[2 * m], P[2 * m + 1]);
+        for (int m = 0; m < 8; ++m) join_quad_fp16(E[m], R[m], S[m], P[2 * m], P[2 * m + 1]);
+    } else if constexpr (D::kElemBytes == 4) {
+        // upper halves from (E, S); lower halves from the section after the
+        // byte plane (row j of this thread: 16 bytes at 4096 + 512 j + 16 l)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const uint4 lo = *reinterpret_cast<const uint4*>(body + kSmPlaneBytes + 512 * (4 * q + jj) + 16 * lane);
+            const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t A, B;
+                join_quad(E[2 * jj + hh], S[2 * jj + hh], A, B);
+                uint32_t* o = P + 8 * jj + 4 * hh;
+                o[0] = join_first(L[2 * hh], A);
+                o[1] = join_second(L[2 * hh], A);
+                o[2] = join_first(L[2 * hh + 1], B);
+                o[3] = join_second(L[2 * hh + 1], B);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) join_quad(E[m], S[m], P[2 * m], P[2 * m + 1]);
+    }
     return true;
 }
 
@@ -152,6 +221,15 @@ namespace cccl {
 // bf16 pair -> binary32 pair (exact)
 __device__ __forceinline__ uint64_t widen_pair(uint32_t p) {
     return (uint64_t)(p << 16) | ((uint64_t)(p & 0xFFFF0000u) << 32);
+}
+// fp16 pair -> binary32 pair (exact)
+__device__ __forceinline__ uint64_t widen_pair_fp16(uint32_t p) {
+    uint32_t lo, hi;
+    asm("{ .reg .b16 l, h; .reg .f32 fl, fh; mov.b32 {l, h}, %2; cvt.f32.f16 fl, l; cvt.f32.f16 fh, h;"
+        " mov.b32 %0, fl; mov.b32 %1, fh; }"
+        : "=r"(lo), "=r"(hi)
+        : "r"(p));
+    return (uint64_t)lo | ((uint64_t)hi << 32);
 }
 __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
     uint64_t d;

@@ -4,34 +4,42 @@
 //
 // Persistent: several CTAs per SM, each taking every gridDim-th chunk.  A CTA
 // has a producer warp, which locates its next chunks through the offset table
-// and stages them by bulk (TMA) copies in a ring of kDSlots buffers, and a
+// and stages them by bulk (TMA) copies in a small ring of buffers, and a
 // team of 4 decode warps, which rebuild 32 values per thread from each staged
-// chunk and store them with 16-byte writes.  So the location and the copy of
+// chunk and store them with 16-byte writes.  One kernel per element type.  So the location and the copy of
 // later chunks overlap the decoding of the current one.
 #include "cccl_decode.cuh"
 #include "cccl_launch.h"
 
 namespace cccl {
 
-constexpr int kDSlots = 3;
 constexpr int kDTeamThreads = 128;
 constexpr int kDProducerWarp = 4;
 constexpr int kDThreads = kDTeamThreads + 32;
-constexpr int kDCtasPerSm = 8;
+// staged chunks per CTA and CTAs per SM: three 8.2 KB slots for the 16-bit
+// types, two 16.4 KB slots for fp32; 8 CTAs per SM for bf16, 7 for fp16 (its
+// decode holds 8 more words), 6 for fp32 (registers and shared memory)
+template <class D>
+__host__ __device__ constexpr int dslots() { return D::kElemBytes == 4 ? 2 : 3; }
+template <class D>
+__host__ __device__ constexpr int dctas_per_sm() { return D::kElemBytes == 4 ? 6 : (D::kExpBits == 5 ? 7 : 8); }
 
 struct DecompressSmem {
-    uint64_t full[kDSlots];   // the slot's chunk landed, or its meta says there is none
-    uint64_t free_[kDSlots];  // the team is done with the slot (1 arrival)
-    uint32_t bytes[kDSlots];  // staged chunk size
-    uint32_t ok[kDSlots];     // the chunk was located
+    uint64_t full[3];         // the slot's chunk landed, or its meta says there is none
+    uint64_t free_[3];        // the team is done with the slot (1 arrival)
+    uint32_t bytes[3];        // staged chunk size
+    uint32_t ok[3];           // the chunk was located
     uint32_t row_tot[4];
     volatile uint32_t abort;
 };
 
-__global__ void __launch_bounds__(kDThreads)
-    decompress_kernel(const uint8_t* __restrict__ s, uint64_t in_bytes, uint16_t* __restrict__ out, Paging pg,
+template <class D>
+__global__ void __launch_bounds__(kDThreads, dctas_per_sm<D>())
+    decompress_kernel(const uint8_t* __restrict__ s, uint64_t in_bytes, uint8_t* __restrict__ out, Paging pg,
                       uint64_t n_elems, uint64_t n_chunks, WsHeader* ws) {
-    __shared__ __align__(128) uint8_t ring[kDSlots][kMaxChunkBytes];
+    constexpr int kDSlots = dslots<D>();
+    using Elem = typename std::conditional<D::kElemBytes == 4, uint32_t, uint16_t>::type;
+    __shared__ __align__(128) uint8_t ring[kDSlots][max_chunk_bytes<D>()];
     __shared__ DecompressSmem sm;
     const uint32_t t = threadIdx.x, lane = t & 31, q = t >> 5;
     if (t == 0) {
@@ -60,7 +68,7 @@ __global__ void __launch_bounds__(kDThreads)
             }
             if (__any_sync(0xFFFFFFFFu, sm.abort != 0)) break;
             if (lane == 0) {
-                const ChunkView v = locate_chunk(s, in_bytes, n_elems, n_chunks, c);
+                const ChunkView v = locate_chunk<D>(s, in_bytes, n_elems, n_chunks, c);
                 sm.ok[slot] = v.ok;
                 sm.bytes[slot] = v.bytes;
                 if (v.ok) {
@@ -95,27 +103,36 @@ __global__ void __launch_bounds__(kDThreads)
         const uint64_t left = n_elems - c * kChunkElems;
         const uint32_t n_c = left < kChunkElems ? (uint32_t)left : kChunkElems;
         const uint64_t e = chunk_elem_offset(pg, c);
-        uint16_t* dst = out + e;
+        Elem* dst = reinterpret_cast<Elem*>(out) + e;
         if (e == kBadChunk && t == 0) record_error(ws, kStatusInvalidArg);  // a block outside the pool
         bool good = sm.ok[slot] != 0 && e != kBadChunk;
         ChunkHeader h{};
         if (good) {
             h = read_chunk_header(buf);
-            good = chunk_header_valid(h, sm.bytes[slot], n_c);  // the same verdict for every thread
+            good = chunk_header_valid<D>(h, sm.bytes[slot], n_c);  // the same verdict for every thread
         }
         if (good) {
             if (n_c < kChunkElems) {  // partial last chunk: raw by construction
-                const uint16_t* vals = reinterpret_cast<const uint16_t*>(buf + kChunkHeaderBytes);
-                for (uint32_t e = t; e < n_c; e += kDTeamThreads) dst[e] = vals[e];
+                const Elem* vals = reinterpret_cast<const Elem*>(buf + kChunkHeaderBytes);
+                for (uint32_t x = t; x < n_c; x += kDTeamThreads) dst[x] = vals[x];
             } else {
-                uint32_t P[16];
+                uint32_t P[thread_words<D>()];
                 bool special = false;
-                good = decode_full_chunk(bar, buf, h, P, sm.row_tot, special);
+                good = decode_full_chunk<D>(bar, buf, h, P, sm.row_tot, special);
                 if (good) {
+                    if constexpr (D::kElemBytes == 4) {
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        *reinterpret_cast<uint4*>(dst + 256 * (4 * q + jj) + 8 * lane) =
-                            make_uint4(P[4 * jj], P[4 * jj + 1], P[4 * jj + 2], P[4 * jj + 3]);
+                        for (int jj = 0; jj < 4; ++jj) {
+                            uint4* row = reinterpret_cast<uint4*>(dst + 256 * (4 * q + jj) + 8 * lane);
+                            row[0] = make_uint4(P[8 * jj], P[8 * jj + 1], P[8 * jj + 2], P[8 * jj + 3]);
+                            row[1] = make_uint4(P[8 * jj + 4], P[8 * jj + 5], P[8 * jj + 6], P[8 * jj + 7]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            *reinterpret_cast<uint4*>(dst + 256 * (4 * q + jj) + 8 * lane) =
+                                make_uint4(P[4 * jj], P[4 * jj + 1], P[4 * jj + 2], P[4 * jj + 3]);
+                    }
                 }
             }
         }
@@ -125,18 +142,32 @@ __global__ void __launch_bounds__(kDThreads)
     }
 }
 
-cudaError_t launch_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t n_elems, void* ws,
-                              cudaStream_t stream, const Paging& pg) {
+template <class D>
+cudaError_t launch_decompress_t(const uint8_t* in, uint64_t in_bytes, void* out, uint64_t n_elems, void* ws,
+                                cudaStream_t stream, const Paging& pg) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const uint64_t n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
-    const uint64_t slots = (uint64_t)sms * kDCtasPerSm;
+    const uint64_t slots = (uint64_t)sms * dctas_per_sm<D>();
     const unsigned grid = (unsigned)(n_chunks < slots ? n_chunks : slots);
-    decompress_kernel<<<grid, kDThreads, 0, stream>>>(in, in_bytes, out, pg, n_elems, n_chunks,
-                                                      static_cast<WsHeader*>(ws));
+    decompress_kernel<D><<<grid, kDThreads, 0, stream>>>(in, in_bytes, static_cast<uint8_t*>(out), pg, n_elems,
+                                                         n_chunks, static_cast<WsHeader*>(ws));
     return cudaGetLastError();
+}
+
+cudaError_t launch_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t n_elems, void* ws,
+                              cudaStream_t stream, const Paging& pg) {
+    return launch_decompress_t<Bf16>(in, in_bytes, out, n_elems, ws, stream, pg);
+}
+
+cudaError_t launch_decompress_typed(uint32_t dtype, const uint8_t* in, uint64_t in_bytes, void* out, uint64_t n_elems,
+                                    void* ws, cudaStream_t stream) {
+    const Paging pg{nullptr, 1, 0};
+    if (dtype == Fp16::kCode) return launch_decompress_t<Fp16>(in, in_bytes, out, n_elems, ws, stream, pg);
+    if (dtype == Fp32::kCode) return launch_decompress_t<Fp32>(in, in_bytes, out, n_elems, ws, stream, pg);
+    return launch_decompress_t<Bf16>(in, in_bytes, out, n_elems, ws, stream, pg);
 }
 
 }  // namespace cccl

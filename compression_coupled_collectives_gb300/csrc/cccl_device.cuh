@@ -30,9 +30,45 @@ constexpr uint32_t kMaxChunkBytes = kChunkHeaderBytes + 2 * kChunkElems;  // 820
 constexpr uint32_t kMagic = 0x31424343u;                                  // "CCB1"
 constexpr uint32_t kVersion = 1;
 constexpr uint32_t kVersionWindow = 2;  // window-base variant: same layout, other table choice
-constexpr uint32_t kDtypeBf16 = 1;
+
+// Element types: section 4.1's split (the exponent re-encoded, sign and
+// fraction kept verbatim), worked out for bf16 and taken with the field widths
+// of fp16 (5-bit exponent) and fp32 (8-bit exponent).  A packed chunk's body
+// is the type's residual section (kResidBytes: sign and fraction), then k
+// exponent planes, then the escapes.
+//   bf16: byte plane = sign << 7 | fraction bits 0..6;
+//   fp16: byte plane = fraction bits 0..7, then three bit-planes holding
+//         fraction bit 8, fraction bit 9 and the sign;
+//   fp32: the upper half is a bf16 pattern and is coded as one; the byte
+//         plane is its sign+fraction byte, followed by the 4096 lower halves.
+// Widths run 1..kExpBits - 1; a chunk is packed only when its exponent part
+// is smaller than the exponents stored verbatim (512 bytes per exponent bit).
+struct Bf16 {
+    static constexpr uint32_t kCode = 1, kElemBytes = 2, kExpBits = 8;
+    static constexpr uint32_t kResidBytes = kSmPlaneBytes;
+};
+struct Fp16 {
+    static constexpr uint32_t kCode = 2, kElemBytes = 2, kExpBits = 5;
+    static constexpr uint32_t kResidBytes = kSmPlaneBytes + 3 * kPlaneBytes;
+};
+struct Fp32 {
+    static constexpr uint32_t kCode = 3, kElemBytes = 4, kExpBits = 8;
+    static constexpr uint32_t kResidBytes = kSmPlaneBytes + 2 * kChunkElems;
+};
+constexpr uint32_t kDtypeBf16 = Bf16::kCode;
+template <class D>
+__host__ __device__ constexpr uint32_t max_width() { return D::kExpBits - 1; }
+template <class D>
+__host__ __device__ constexpr uint32_t raw_exponent_bytes() { return kPlaneBytes * D::kExpBits; }
+template <class D>
+__host__ __device__ constexpr uint32_t max_chunk_bytes() { return kChunkHeaderBytes + D::kElemBytes * kChunkElems; }
+// 32-bit words of one thread's 32 elements
+template <class D>
+__host__ __device__ constexpr int thread_words() { return (int)D::kElemBytes * 8; }
+
+template <class D>
 __device__ __forceinline__ bool known_version_word(uint32_t w1) {
-    return w1 == (kVersion | (kDtypeBf16 << 16)) || w1 == (kVersionWindow | (kDtypeBf16 << 16));
+    return w1 == (kVersion | (D::kCode << 16)) || w1 == (kVersionWindow | (D::kCode << 16));
 }
 constexpr uint32_t kModePacked = 0;
 constexpr uint32_t kModeRaw = 1;
@@ -220,6 +256,31 @@ __device__ __forceinline__ void join_quad(uint32_t e, uint32_t sm, uint32_t& A, 
     B = __byte_perm(lo, hi, 0x7362);
 }
 
+// fp16 quads.  A, B: two words of two fp16 each (elements 4h+0, 4h+1 in A;
+// 4h+2, 4h+3 in B).  Per value the high byte is sign | exponent (5 bits) |
+// fraction bits 9, 8; the quad moves the exponent to bits 0..4 and keeps the
+// other three bits above it: fraction bit 8 in bit 5, bit 9 in bit 6, the
+// sign in bit 7.  Subtracting a base <= every exponent leaves bits 5..7 alone.
+__device__ __forceinline__ uint32_t fp16_exponent_quad(uint32_t A, uint32_t B) {
+    const uint32_t H = __byte_perm(A, B, 0x7531);
+    return ((H >> 2) & 0x1F1F1F1Fu) | ((H & 0x03030303u) << 5) | (H & 0x80808080u);
+}
+// The two fp16 exponents of a pair-word in the high byte of each 16-bit lane.
+__device__ __forceinline__ uint32_t fp16_exponent_lanes(uint32_t A) { return (A >> 2) & 0x1F001F00u; }
+// Inverse: low fraction bytes L, exponents E (one per byte, <= 31) and the
+// quad bits 5..7 in R -> two pair-words.
+__device__ __forceinline__ void join_quad_fp16(uint32_t E, uint32_t R, uint32_t L, uint32_t& A, uint32_t& B) {
+    const uint32_t H = (R & 0x80808080u) | (E << 2) | ((R >> 5) & 0x03030303u);
+    A = __byte_perm(L, H, 0x5140);
+    B = __byte_perm(L, H, 0x7362);
+}
+// fp32 halves: the upper (bf16) halves, and the lower halves, of two values
+// as one pair-word each; and back.
+__device__ __forceinline__ uint32_t upper_halves(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
+__device__ __forceinline__ uint32_t lower_halves(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5410); }
+__device__ __forceinline__ uint32_t join_first(uint32_t lo, uint32_t hi) { return __byte_perm(lo, hi, 0x5410); }
+__device__ __forceinline__ uint32_t join_second(uint32_t lo, uint32_t hi) { return __byte_perm(lo, hi, 0x7632); }
+
 // Byte flags (0x80 per byte) of the bytes of `off` that are >= S, 1 <= S <= 127;
 // kb = (128 - S) * 0x01010101.  No carry crosses a byte.
 __device__ __forceinline__ uint32_t ge_flags(uint32_t off, uint32_t kb) {
@@ -373,7 +434,7 @@ __device__ __forceinline__ uint64_t lookback_offset_wide(uint64_t* status, uint6
 // ---------------------------------------------------------------------------
 struct ChunkView {
     uint64_t offset;  // byte offset of the chunk in its stream
-    uint32_t bytes;   // chunk size (<= kMaxChunkBytes once validated)
+    uint32_t bytes;   // chunk size (<= the type's raw full chunk once validated)
     uint32_t ok;      // 1 if the stream header and this chunk's table entries are valid
 };
 
@@ -382,13 +443,14 @@ __device__ __forceinline__ uint32_t ld_u32_aligned(const uint8_t* p) { return *r
 
 // One thread: check the stream header against (n_elems, in_bytes) and locate
 // chunk c through the offset table.  Every read stays inside in_bytes.
+template <class D>
 __device__ __forceinline__ ChunkView locate_chunk(const uint8_t* s, uint64_t in_bytes, uint64_t n_elems,
                                                   uint64_t n_chunks, uint64_t c) {
     ChunkView v{0, 0, 0};
     const uint64_t start = data_start(n_chunks);
     if (in_bytes < start) return v;
     const uint32_t w0 = ld_u32_aligned(s + 0), w1 = ld_u32_aligned(s + 4), w2 = ld_u32_aligned(s + 8);
-    if (w0 != kMagic || !known_version_word(w1) || w2 != kChunkElems) return v;
+    if (w0 != kMagic || !known_version_word<D>(w1) || w2 != kChunkElems) return v;
     if (ld_u64_aligned(s + 16) != n_elems || ld_u64_aligned(s + 24) != n_chunks) return v;
     const uint64_t total = ld_u64_aligned(s + 32);
     if (total > in_bytes || total < start) return v;
@@ -397,36 +459,7 @@ __device__ __forceinline__ ChunkView locate_chunk(const uint8_t* s, uint64_t in_
     if (c == 0 && off != start) return v;
     if ((off & 15) != 0 || end <= off || end > total || off < start) return v;
     // the bulk copy needs a size that is a multiple of 16; every valid chunk is
-    if (end - off > kMaxChunkBytes || ((end - off) & 15) != 0) return v;
-    v.offset = off;
-    v.bytes = (uint32_t)(end - off);
-    v.ok = 1;
-    return v;
-}
-
-// One thread: check a stream's header against (n_elems, in_bytes); returns
-// the stream's total_bytes, or 0 if the header is not valid.
-__device__ __forceinline__ uint64_t stream_total(const uint8_t* s, uint64_t in_bytes, uint64_t n_elems,
-                                                 uint64_t n_chunks) {
-    const uint64_t start = data_start(n_chunks);
-    if (in_bytes < start) return 0;
-    const uint32_t w0 = ld_u32_aligned(s + 0), w1 = ld_u32_aligned(s + 4), w2 = ld_u32_aligned(s + 8);
-    if (w0 != kMagic || !known_version_word(w1) || w2 != kChunkElems) return 0;
-    if (ld_u64_aligned(s + 16) != n_elems || ld_u64_aligned(s + 24) != n_chunks) return 0;
-    const uint64_t total = ld_u64_aligned(s + 32);
-    if (total > in_bytes || total < start) return 0;
-    return total;
-}
-// One thread: locate chunk c of a stream whose header passed stream_total.
-__device__ __forceinline__ ChunkView locate_in_stream(const uint8_t* s, uint64_t total, uint64_t n_chunks, uint64_t c) {
-    ChunkView v{0, 0, 0};
-    if (total == 0) return v;
-    const uint64_t start = data_start(n_chunks);
-    const uint64_t off = ld_u64_aligned(s + kStreamHeaderBytes + 8 * c);
-    const uint64_t end = (c + 1 < n_chunks) ? ld_u64_aligned(s + kStreamHeaderBytes + 8 * (c + 1)) : total;
-    if (c == 0 && off != start) return v;
-    if ((off & 15) != 0 || end <= off || end > total || off < start) return v;
-    if (end - off > kMaxChunkBytes || ((end - off) & 15) != 0) return v;
+    if (end - off > max_chunk_bytes<D>() || ((end - off) & 15) != 0) return v;
     v.offset = off;
     v.bytes = (uint32_t)(end - off);
     v.ok = 1;
@@ -449,14 +482,18 @@ __device__ __forceinline__ ChunkHeader read_chunk_header(const uint8_t* h) {
     return ch;
 }
 // Same rules as the format: raw chunks carry no table; a packed chunk is a
-// full chunk whose exponent part is smaller than 4096 bytes.
+// full chunk whose exponent part is smaller than its exponents stored
+// verbatim, and whose base is an exponent of the type.
+template <class D>
 __device__ __forceinline__ bool chunk_header_valid(const ChunkHeader& h, uint32_t staged_bytes, uint32_t n_c) {
     if (h.bytes != staged_bytes || h.n_c != n_c) return false;
-    if (h.mode == kModeRaw) return h.k == 0 && h.base == 0 && h.n_esc == 0 && h.bytes == 16 + pad16(2 * n_c);
-    if (h.mode != kModePacked || n_c != kChunkElems || h.k > 7) return false;
+    if (h.mode == kModeRaw)
+        return h.k == 0 && h.base == 0 && h.n_esc == 0 && h.bytes == 16 + pad16(D::kElemBytes * n_c);
+    if (h.mode != kModePacked || n_c != kChunkElems || h.k > max_width<D>() || h.base >= (1u << D::kExpBits))
+        return false;
     if (h.k == 0 && h.n_esc != 0) return false;
-    if (h.bytes != 16 + kSmPlaneBytes + kPlaneBytes * h.k + pad16(h.n_esc)) return false;
-    return kPlaneBytes * h.k + pad16(h.n_esc) < kSmPlaneBytes;
+    if (h.bytes != 16 + D::kResidBytes + kPlaneBytes * h.k + pad16(h.n_esc)) return false;
+    return kPlaneBytes * h.k + pad16(h.n_esc) < raw_exponent_bytes<D>();
 }
 
 }  // namespace cccl

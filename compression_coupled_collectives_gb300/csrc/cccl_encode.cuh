@@ -1,20 +1,23 @@
-// cccl_encode.cuh -- encoding chunks staged in shared memory and placing a
-// group of them in the output stream (shared by the compress and fused-reduce
-// kernels).
+// cccl_encode.cuh -- encoding chunks staged in shared memory or held in
+// registers (shared by the compress and fused-reduce kernels).
 //
 // Per chunk ("CCCL: In-GPU Compression-Coupled Collective Communication"):
-//   section 4.1  split every bf16 into its exponent and a sign+fraction byte;
+//   section 4.1  split every value into its exponent and the rest (sign and
+//                fraction, kept verbatim in the type's residual section);
 //   section 4.3  the chunk's own table: base = minimum exponent, width k that
 //                minimises 512 k + pad16(#escapes), fixed-length k-bit codes;
 //   section 4.4  the chunk is written once, straight into its final place;
 //   section 5    the partial last chunk is stored raw.
+// Element types (bf16, fp16, fp32) and their residual sections: see the
+// traits in cccl_device.cuh.
 //
 // Work split: one warp encodes one whole chunk (lane l owns the elements
 // 256 j + 8 l + s of all 16 rows j, i.e. bit-plane words 32 q + l for
-// q < 4), so a chunk needs only warp-level reductions.  A CTA of G warps
-// encodes G consecutive chunks and places them with ONE decoupled look-back
-// over groups; the chunks' offsets inside the group come from a local scan.
+// q < 4), so a chunk needs only warp-level reductions; or a team of four warps
+// encodes a chunk it holds in registers, a quarter per warp.
 #pragma once
+
+#include <type_traits>
 
 #include "cccl_device.cuh"
 
@@ -28,6 +31,7 @@ struct StreamOut {
     uint64_t n_elems;
     uint64_t n_chunks;
     uint32_t version;    // stream header version: kVersion, or kVersionWindow
+    uint32_t dtype;      // stream header element type (the trait's kCode)
 };
 
 // Encoding decision of one full chunk (warp-uniform).
@@ -43,29 +47,70 @@ struct ChunkPlan {
 // writing: the bit-planes of its four plane words.  P[8 q + p] is plane p of
 // word 32 q + l (lane l), i.e. bit p of the exponent offsets (e - base) of
 // the 32 elements that word covers: bit 8 b + m holds element 256 (4 q + m / 2)
-// + 8 l + 4 (m % 2) + b.  Sign and fraction stay in the staged chunk.
+// + 8 l + 4 (m % 2) + b.  For fp16, planes 5..7 hold fraction bit 8, fraction
+// bit 9 and the sign (the offsets need 5 bits at most).  The rest of sign and
+// fraction stays in the staged chunk.
 struct ChunkRegs {
     uint32_t P[32];
 };
 
-// This lane's 4 pair-words of row j (elements 256 j + 8 l .. + 7).
+// This lane's 4 pair-words of row j (elements 256 j + 8 l .. + 7) of a 16-bit
+// type.
 __device__ __forceinline__ uint4 lds_row(const uint8_t* chunk, uint32_t j, uint32_t lane) {
     return *reinterpret_cast<const uint4*>(chunk + 512 * j + 16 * lane);
 }
 
-// Sign+fraction bytes of 4 values held as two pair-words (section 4.1).
+// Sign+fraction bytes of 4 bf16 values held as two pair-words (section 4.1).
 __device__ __forceinline__ uint32_t sign_fraction_quad(uint32_t A, uint32_t B) {
     const uint32_t lo = __byte_perm(A, B, 0x6420), hi = __byte_perm(A, B, 0x7531);
     return (lo & 0x7F7F7F7Fu) | (hi & 0x80808080u);
 }
+// Low bytes of 4 fp16 values (fraction bits 0..7).
+__device__ __forceinline__ uint32_t low_byte_quad(uint32_t A, uint32_t B) { return __byte_perm(A, B, 0x6420); }
 
-// Escape bits at width k (1..7) of one plane word from its 8 planes: the
-// offset is at least 2^k - 1 when a bit at or above k is set (the offset
+// Row j of this lane's 8 staged values: two exponent quads (for fp16 with the
+// residual bits 5..7, see fp16_exponent_quad), and the running minimum and
+// maximum of the exponents held in the high bytes of 16-bit lanes.
+template <class D>
+__device__ __forceinline__ void row_exponents(const uint8_t* chunk, int j, uint32_t lane, uint32_t& q0, uint32_t& q1,
+                                              uint32_t& mn, uint32_t& mx) {
+    if constexpr (D::kExpBits == 5) {
+        const uint4 v = lds_row(chunk, j, lane);
+        const uint32_t u0 = fp16_exponent_lanes(v.x), u1 = fp16_exponent_lanes(v.y);
+        const uint32_t u2 = fp16_exponent_lanes(v.z), u3 = fp16_exponent_lanes(v.w);
+        mn = vmin_u16x2(mn, vmin_u16x2(vmin_u16x2(u0, u1), vmin_u16x2(u2, u3)));
+        mx = vmax_u16x2(mx, vmax_u16x2(vmax_u16x2(u0, u1), vmax_u16x2(u2, u3)));
+        q0 = fp16_exponent_quad(v.x, v.y);
+        q1 = fp16_exponent_quad(v.z, v.w);
+    } else {
+        uint32_t t0, t1, t2, t3;
+        if constexpr (D::kElemBytes == 4) {  // the upper halves are bf16 patterns
+            const uint8_t* row = chunk + 1024 * j + 32 * lane;
+            const uint4 a = *reinterpret_cast<const uint4*>(row), b = *reinterpret_cast<const uint4*>(row + 16);
+            t0 = upper_halves(a.x, a.y) << 1, t1 = upper_halves(a.z, a.w) << 1;
+            t2 = upper_halves(b.x, b.y) << 1, t3 = upper_halves(b.z, b.w) << 1;
+        } else {
+            const uint4 v = lds_row(chunk, j, lane);
+            t0 = v.x << 1, t1 = v.y << 1, t2 = v.z << 1, t3 = v.w << 1;
+        }
+        // doubling a pair-word puts each value's exponent in the high byte of
+        // its 16-bit lane (a low value's sign lands in the high lane's low
+        // byte, which cannot change its high byte)
+        mn = vmin_u16x2(mn, vmin_u16x2(vmin_u16x2(t0, t1), vmin_u16x2(t2, t3)));
+        mx = vmax_u16x2(mx, vmax_u16x2(vmax_u16x2(t0, t1), vmax_u16x2(t2, t3)));
+        q0 = __byte_perm(t0, t1, 0x7531);
+        q1 = __byte_perm(t2, t3, 0x7531);
+    }
+}
+
+// Escape bits at width k (1..kExpBits-1) of one plane word from its planes:
+// the offset is at least 2^k - 1 when a bit at or above k is set (the offset
 // reaches 2^k) or when bits 0..k-1 are all set.
+template <class D>
 __device__ __forceinline__ uint32_t escape_word(const uint32_t* P, uint32_t k) {
     uint32_t lowAnd = 0xFFFFFFFFu, highOr = 0u;
 #pragma unroll
-    for (uint32_t p = 0; p < 8; ++p) {
+    for (uint32_t p = 0; p < D::kExpBits; ++p) {
         if (p < k)
             lowAnd &= P[p];
         else
@@ -74,57 +119,59 @@ __device__ __forceinline__ uint32_t escape_word(const uint32_t* P, uint32_t k) {
     return lowAnd | highOr;
 }
 
-// Phase A: exponent table and size of the full chunk staged at `chunk` (8192
-// bytes of bf16 in shared memory, left untouched), leaving the bit-planes of
-// the exponent offsets in `r`.  One warp; every lane returns the same plan.
-//
-// The sizes of every width come from the planes at once: with
-// low_k = AND of planes 0..k-1 and high_k = OR of planes k..7, the escapes at
-// width k are exactly low_k | high_k, so seven popcounts per plane word give
-// the seven escape counts (section 4.3's per-block table, exact).
+// Escape counts of one plane word at every width: with low_k = AND of planes
+// 0..k-1 and high_k = OR of planes k..kExpBits-1, the escapes at width k are
+// exactly low_k | high_k (section 4.3's per-block table, exact).
+template <class D>
+__device__ __forceinline__ void add_escape_counts(const uint32_t* P, uint32_t* cnt) {
+    constexpr int kTop = (int)D::kExpBits - 1;
+    uint32_t high[8];
+    high[kTop] = P[kTop];
+#pragma unroll
+    for (int k = kTop - 1; k >= 1; --k) high[k] = high[k + 1] | P[k];
+    uint32_t low = P[0];
+#pragma unroll
+    for (int k = 1; k <= kTop; ++k) {
+        cnt[k] += __popc(low | high[k]);
+        if (k < kTop) low &= P[k];
+    }
+}
+
+// Size of a packed full chunk, header included.
+template <class D>
+__host__ __device__ constexpr uint32_t packed_chunk_bytes(uint32_t k, uint32_t n_esc) {
+    return (uint32_t)(16 + D::kResidBytes + kPlaneBytes * k + pad16(n_esc));
+}
+
+// Phase A: exponent table and size of the full chunk staged at `chunk` (left
+// untouched), leaving the bit-planes of the exponent offsets in `r`.  One
+// warp; every lane returns the same plan.
+template <class D>
 __device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk, ChunkRegs& r) {
     const uint32_t lane = threadIdx.x & 31;
     // exponent quads (r.P[2 j + h]: row j, elements 4 h .. 4 h + 3 of the
-    // lane's 8) and the exponent extremes.  Doubling a pair-word puts each
-    // value's exponent in the high byte of its 16-bit lane (a low value's sign
-    // lands in the high lane's low byte, which cannot change its high byte).
+    // lane's 8) and the exponent extremes
     uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const uint4 v = lds_row(chunk, j, lane);
-        const uint32_t t0 = v.x << 1, t1 = v.y << 1, t2 = v.z << 1, t3 = v.w << 1;
-        mn = vmin_u16x2(mn, vmin_u16x2(vmin_u16x2(t0, t1), vmin_u16x2(t2, t3)));
-        mx = vmax_u16x2(mx, vmax_u16x2(vmax_u16x2(t0, t1), vmax_u16x2(t2, t3)));
-        r.P[2 * j] = __byte_perm(t0, t1, 0x7531);
-        r.P[2 * j + 1] = __byte_perm(t2, t3, 0x7531);
-    }
+    for (int j = 0; j < 16; ++j) row_exponents<D>(chunk, j, lane, r.P[2 * j], r.P[2 * j + 1], mn, mx);
     const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
     const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
     const uint32_t base4 = emin * 0x01010101u;
-    uint32_t cnt[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // escapes at width k (k = 1..7)
+    uint32_t cnt[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // escapes at width k
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint32_t* P = r.P + 8 * q;
 #pragma unroll
         for (int m = 0; m < 8; ++m) P[m] -= base4;  // no borrow: every exponent >= emin
         transpose8x8x4(P);                          // quads of offsets -> planes
-        uint32_t high[8];
-        high[7] = P[7];
-#pragma unroll
-        for (int k = 6; k >= 1; --k) high[k] = high[k + 1] | P[k];
-        uint32_t low = P[0];
-#pragma unroll
-        for (int k = 1; k <= 7; ++k) {
-            cnt[k] += __popc(low | high[k]);
-            if (k < 7) low &= P[k];
-        }
+        add_escape_counts<D>(P, cnt);
     }
     ChunkPlan pl{0u, 0u, emin, 0u, 0u};
     uint32_t best = 0;
     if (emax > emin) {
         best = 0xFFFFFFFFu;
 #pragma unroll
-        for (int k = 1; k <= 7; ++k) {
+        for (int k = 1; k <= (int)max_width<D>(); ++k) {
             const uint32_t n = __reduce_add_sync(0xFFFFFFFFu, cnt[k]);
             const uint32_t size = kPlaneBytes * k + (uint32_t)pad16(n);
             if (size < best) {  // ascending k: a tie keeps the smaller width
@@ -134,14 +181,14 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk, Chunk
             }
         }
     }
-    pl.raw = best >= kSmPlaneBytes ? 1u : 0u;
+    pl.raw = best >= raw_exponent_bytes<D>() ? 1u : 0u;
     if (pl.raw) {
         pl.k = 0;
         pl.base = 0;
         pl.n_esc = 0;
-        pl.bytes = kMaxChunkBytes;
+        pl.bytes = max_chunk_bytes<D>();
     } else {
-        pl.bytes = (uint32_t)(16 + kSmPlaneBytes + kPlaneBytes * pl.k + pad16(pl.n_esc));
+        pl.bytes = packed_chunk_bytes<D>(pl.k, pl.n_esc);
     }
     return pl;
 }
@@ -153,27 +200,22 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk, Chunk
 // 257 words of shared memory.  Leaves in `r` the bit-planes of the codes,
 // escaped elements carrying all ones, which is what write_chunk_warp's
 // escape test (low_k | high_k) and plane writes expect.
+template <class D>
 __device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk, ChunkRegs& r, uint32_t* hist) {
+    constexpr uint32_t kExpMask4 = ((1u << D::kExpBits) - 1u) * 0x01010101u;  // the exponent bits of a quad
     const uint32_t lane = threadIdx.x & 31;
     *reinterpret_cast<uint4*>(hist + 8 * lane) = make_uint4(0u, 0u, 0u, 0u);
     *reinterpret_cast<uint4*>(hist + 8 * lane + 4) = make_uint4(0u, 0u, 0u, 0u);
     uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const uint4 v = lds_row(chunk, j, lane);
-        const uint32_t t0 = v.x << 1, t1 = v.y << 1, t2 = v.z << 1, t3 = v.w << 1;
-        mn = vmin_u16x2(mn, vmin_u16x2(vmin_u16x2(t0, t1), vmin_u16x2(t2, t3)));
-        mx = vmax_u16x2(mx, vmax_u16x2(vmax_u16x2(t0, t1), vmax_u16x2(t2, t3)));
-        r.P[2 * j] = __byte_perm(t0, t1, 0x7531);
-        r.P[2 * j + 1] = __byte_perm(t2, t3, 0x7531);
-    }
+    for (int j = 0; j < 16; ++j) row_exponents<D>(chunk, j, lane, r.P[2 * j], r.P[2 * j + 1], mn, mx);
     const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
     const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
     __syncwarp();  // the histogram is cleared
     // exponent histogram
 #pragma unroll
     for (int m = 0; m < 32; ++m) {
-        const uint32_t q = r.P[m];
+        const uint32_t q = r.P[m] & kExpMask4;
 #pragma unroll
         for (int b = 0; b < 4; ++b) atomicAdd(hist + ((q >> (8 * b)) & 0xFFu), 1u);
     }
@@ -204,9 +246,11 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk
     ChunkPlan pl{0u, 0u, emin, 0u, 0u};
     uint32_t best = 0;
     if (emax > emin) {
+        // a window starting above the type's exponents escapes everything, so
+        // scanning all 256 starts gives the same choice for narrower types
         best = 0xFFFFFFFFu;
 #pragma unroll
-        for (uint32_t k = 1; k <= 7; ++k) {
+        for (uint32_t k = 1; k <= max_width<D>(); ++k) {
             const uint32_t S = (1u << k) - 1u;
             uint32_t key = 0xFFFFFFFFu;  // (escapes, base): fewest escapes, then the smallest base
 #pragma unroll
@@ -225,31 +269,85 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk
             }
         }
     }
-    pl.raw = best >= kSmPlaneBytes ? 1u : 0u;
+    pl.raw = best >= raw_exponent_bytes<D>() ? 1u : 0u;
     if (pl.raw) {
         pl.k = 0;
         pl.base = 0;
         pl.n_esc = 0;
-        pl.bytes = kMaxChunkBytes;
+        pl.bytes = max_chunk_bytes<D>();
         return pl;
     }
-    pl.bytes = (uint32_t)(16 + kSmPlaneBytes + kPlaneBytes * pl.k + pad16(pl.n_esc));
-    if (pl.k == 0) return pl;
+    pl.bytes = packed_chunk_bytes<D>(pl.k, pl.n_esc);
+    // (fp16 goes on at k = 0 too: its residual planes 5..7 come from the
+    // transposes below; the codes, all escapes at width 0, are not written)
+    if (D::kExpBits != 5 && pl.k == 0) return pl;
     // codes: e - base inside the window, all ones outside (an escape).
     // Byte-wise e - base with no borrow between bytes, and the bytes where
     // e < base (the borrow out of each byte).
     const uint32_t b4 = pl.base * 0x01010101u, kb = (128u - ((1u << pl.k) - 1u)) * 0x01010101u;
 #pragma unroll
     for (int m = 0; m < 32; ++m) {
-        const uint32_t e = r.P[m];
+        const uint32_t e = r.P[m] & kExpMask4;
         const uint32_t d = ((e | 0x80808080u) - (b4 & 0x7F7F7F7Fu)) ^ ((e ^ ~b4) & 0x80808080u);
         const uint32_t lt = ((~e & b4) | (~(e ^ b4) & d)) & 0x80808080u;  // e < base
         const uint32_t esc = flags_to_mask(lt | ge_flags(d, kb));
-        r.P[m] = d | esc;
+        if constexpr (D::kExpBits == 5)
+            r.P[m] = ((d | esc) & kExpMask4) | (r.P[m] & ~kExpMask4);
+        else
+            r.P[m] = d | esc;
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) transpose8x8x4(r.P + 8 * q);
     return pl;
+}
+
+// The residual section of a packed full chunk staged at `chunk` (one warp):
+// the byte plane, then fp16's three bit-planes (from the lane's planes 5..7)
+// or fp32's lower halves.
+template <class D>
+__device__ __forceinline__ void write_residual_warp(const ChunkRegs& r, const uint8_t* chunk, uint8_t* body) {
+    const uint32_t lane = threadIdx.x & 31;
+    if constexpr (D::kElemBytes == 4) {
+#pragma unroll 4
+        for (int j = 0; j < 16; ++j) {
+            const uint8_t* row = chunk + 1024 * j + 32 * lane;
+            const uint4 a = *reinterpret_cast<const uint4*>(row), b = *reinterpret_cast<const uint4*>(row + 16);
+            *reinterpret_cast<uint2*>(body + 256 * j + 8 * lane) =
+                make_uint2(sign_fraction_quad(upper_halves(a.x, a.y), upper_halves(a.z, a.w)),
+                           sign_fraction_quad(upper_halves(b.x, b.y), upper_halves(b.z, b.w)));
+            *reinterpret_cast<uint4*>(body + kSmPlaneBytes + 512 * j + 16 * lane) =
+                make_uint4(lower_halves(a.x, a.y), lower_halves(a.z, a.w), lower_halves(b.x, b.y),
+                           lower_halves(b.z, b.w));
+        }
+    } else {
+#pragma unroll 4
+        for (int j = 0; j < 16; ++j) {
+            const uint4 v = lds_row(chunk, j, lane);
+            if constexpr (D::kExpBits == 5)
+                *reinterpret_cast<uint2*>(body + 256 * j + 8 * lane) =
+                    make_uint2(low_byte_quad(v.x, v.y), low_byte_quad(v.z, v.w));
+            else
+                *reinterpret_cast<uint2*>(body + 256 * j + 8 * lane) =
+                    make_uint2(sign_fraction_quad(v.x, v.y), sign_fraction_quad(v.z, v.w));
+        }
+        if constexpr (D::kExpBits == 5) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int t = 0; t < 3; ++t)
+                    *reinterpret_cast<uint32_t*>(body + kSmPlaneBytes + kPlaneBytes * t + 4 * (32 * q + lane)) =
+                        r.P[8 * q + 5 + t];
+        }
+    }
+}
+
+// Exponent of staged element i.
+template <class D>
+__device__ __forceinline__ uint32_t staged_exponent(const uint8_t* chunk, uint32_t i) {
+    if constexpr (D::kElemBytes == 4)
+        return (reinterpret_cast<const uint32_t*>(chunk)[i] >> 23) & 0xFFu;
+    else
+        return (reinterpret_cast<const uint16_t*>(chunk)[i] >> (15 - D::kExpBits)) & ((1u << D::kExpBits) - 1u);
 }
 
 // Phase B: write the full chunk staged at `chunk` (unchanged since phase A)
@@ -258,9 +356,10 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk
 // waits until the copy has read `chunk` before returning; the caller must
 // have ordered any generic writes of `chunk` before it with
 // fence.proxy.async.  A packed chunk is written by coalesced stores: the
-// sign+fraction plane, the k planes (escaped elements carry the sentinel,
+// residual section, the k planes (escaped elements carry the sentinel,
 // all k bits set), then the escape bytes in bit-plane order, read back from
 // the staged values.
+template <class D>
 __device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const ChunkPlan& pl, const uint8_t* chunk,
                                                  uint8_t* dst) {
     const uint32_t lane = threadIdx.x & 31;
@@ -271,29 +370,24 @@ __device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const Chunk
                        pl.bytes, 0u);
     if (pl.raw) {
         if (lane == 0) {
-            bulk_store(body, chunk, 2 * kChunkElems);
+            bulk_store(body, chunk, D::kElemBytes * kChunkElems);
             bulk_commit();
             bulk_wait_read();
         }
         __syncwarp();
         return;
     }
-#pragma unroll 4
-    for (int j = 0; j < 16; ++j) {
-        const uint4 v = lds_row(chunk, j, lane);
-        *reinterpret_cast<uint2*>(body + 256 * j + 8 * lane) =
-            make_uint2(sign_fraction_quad(v.x, v.y), sign_fraction_quad(v.z, v.w));
-    }
+    write_residual_warp<D>(r, chunk, body);
     const uint32_t k = pl.k;
     if (k == 0) return;
     uint32_t esc[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const uint32_t* P = r.P + 8 * q;
-        esc[q] = escape_word(P, k);
-        uint8_t* col = body + kSmPlaneBytes + 4 * (32 * q + lane);
+        esc[q] = escape_word<D>(P, k);
+        uint8_t* col = body + D::kResidBytes + 4 * (32 * q + lane);
 #pragma unroll
-        for (uint32_t p = 0; p < 8; ++p)
+        for (uint32_t p = 0; p < max_width<D>(); ++p)
             if (p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = P[p] | esc[q];
     }
     const uint32_t n_esc = pl.n_esc;
@@ -314,8 +408,7 @@ __device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const Chunk
     const uint32_t t0 = ta & 0xFFFFu, t1 = ta >> 16, t2 = tb & 0xFFFFu;
     const uint32_t ea = a - c01, eb = b - c23;  // exclusive over lanes
     const uint32_t first[4] = {ea & 0xFFFFu, t0 + (ea >> 16), t0 + t1 + (eb & 0xFFFFu), t0 + t1 + t2 + (eb >> 16)};
-    const uint16_t* vals = reinterpret_cast<const uint16_t*>(chunk);
-    uint8_t* esc_out = body + kSmPlaneBytes + kPlaneBytes * k;
+    uint8_t* esc_out = body + D::kResidBytes + kPlaneBytes * k;
     // one escape of every quarter per step: four independent load -> store
     // chains in flight per lane
     uint32_t idx[4] = {first[0], first[1], first[2], first[3]};
@@ -327,7 +420,7 @@ __device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const Chunk
                 esc[q] &= esc[q] - 1;
                 const uint32_t m = bit & 7, bb = bit >> 3;
                 const uint32_t i = 256 * (4 * q + (m >> 1)) + 8 * lane + 4 * (m & 1) + bb;
-                if (idx[q] < n_esc) esc_out[idx[q]] = (uint8_t)(vals[i] >> 7);
+                if (idx[q] < n_esc) esc_out[idx[q]] = (uint8_t)staged_exponent<D>(chunk, i);
                 ++idx[q];
             }
         }
@@ -338,9 +431,10 @@ __device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const Chunk
 // ---------------------------------------------------------------------------
 // Team encoding: a full chunk held in registers by a team of four warps.
 // Thread (warp q of the team, lane l) holds rows 4 q .. 4 q + 3, elements
-// 8 l .. 8 l + 7 of each, as P[4 jj + x] = elements 2 x, 2 x + 1 of row
-// 4 q + jj (the layout decode_full_chunk produces): exactly the 32 elements
-// of bit-plane word 32 q + l, quad m = 2 jj + h being words P[2 m], P[2 m + 1].
+// 8 l .. 8 l + 7 of each, in the layout decode_full_chunk produces (16-bit
+// types: P[4 jj + x] = elements 2 x, 2 x + 1 of row 4 q + jj; fp32:
+// P[8 jj + s] = element s): exactly the 32 elements of bit-plane word
+// 32 q + l, quad m = 2 jj + h being elements 4 h .. 4 h + 3 of row 4 q + jj.
 // The team meets twice per chunk (exponent extremes, escape counts); after
 // that every warp writes its own quarter.
 // ---------------------------------------------------------------------------
@@ -359,26 +453,50 @@ struct TeamXch {
     uint32_t cnt[4][8];     // per warp: escapes at width k (k = 1..7)
 };
 
-// Exponent quad m of this thread's values (one byte per value).
-__device__ __forceinline__ uint32_t exponent_quad(const uint32_t P[16], int m) {
-    return __byte_perm(P[2 * m] << 1, P[2 * m + 1] << 1, 0x7531);
+// The two upper-half pair-words (bf16 patterns) of quad m of an fp32 thread.
+__device__ __forceinline__ uint32_t upper_pair0(const uint32_t* P, int m) { return upper_halves(P[4 * m], P[4 * m + 1]); }
+__device__ __forceinline__ uint32_t upper_pair1(const uint32_t* P, int m) {
+    return upper_halves(P[4 * m + 2], P[4 * m + 3]);
+}
+
+// Exponent quad m of this thread's values (one exponent per byte).
+template <class D>
+__device__ __forceinline__ uint32_t exponent_quad(const uint32_t* P, int m) {
+    if constexpr (D::kElemBytes == 4)
+        return __byte_perm(upper_pair0(P, m) << 1, upper_pair1(P, m) << 1, 0x7531);
+    else if constexpr (D::kExpBits == 5)
+        return fp16_exponent_quad(P[2 * m], P[2 * m + 1]) & 0x1F1F1F1Fu;
+    else
+        return __byte_perm(P[2 * m] << 1, P[2 * m + 1] << 1, 0x7531);
 }
 
 // Phase A for a team: exponent table and size of the chunk in P, leaving the
-// bit-planes of this thread's word (offsets e - base) in `planes`.  Every
-// thread of the team returns the same plan except esc_before.
-template <typename Barrier>
-__device__ __forceinline__ TeamPlan plan_chunk_team(const Barrier& bar, const uint32_t P[16], uint32_t planes[8],
+// bit-planes of this thread's word (offsets e - base; fp16: residual bits in
+// planes 5..7) in `planes`.  Every thread of the team returns the same plan
+// except esc_before.
+template <class D, typename Barrier>
+__device__ __forceinline__ TeamPlan plan_chunk_team(const Barrier& bar, const uint32_t* P, uint32_t planes[8],
                                                     TeamXch& x) {
     const uint32_t lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
     uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-        // doubling puts each value's exponent in the high byte of its 16-bit lane
-        const uint32_t t0 = P[2 * m] << 1, t1 = P[2 * m + 1] << 1;
-        mn = vmin_u16x2(mn, vmin_u16x2(t0, t1));
-        mx = vmax_u16x2(mx, vmax_u16x2(t0, t1));
-        planes[m] = __byte_perm(t0, t1, 0x7531);
+        if constexpr (D::kExpBits == 5) {
+            const uint32_t u0 = fp16_exponent_lanes(P[2 * m]), u1 = fp16_exponent_lanes(P[2 * m + 1]);
+            mn = vmin_u16x2(mn, vmin_u16x2(u0, u1));
+            mx = vmax_u16x2(mx, vmax_u16x2(u0, u1));
+            planes[m] = fp16_exponent_quad(P[2 * m], P[2 * m + 1]);
+        } else {
+            // doubling puts each value's exponent in the high byte of its 16-bit lane
+            uint32_t t0, t1;
+            if constexpr (D::kElemBytes == 4)
+                t0 = upper_pair0(P, m) << 1, t1 = upper_pair1(P, m) << 1;
+            else
+                t0 = P[2 * m] << 1, t1 = P[2 * m + 1] << 1;
+            mn = vmin_u16x2(mn, vmin_u16x2(t0, t1));
+            mx = vmax_u16x2(mx, vmax_u16x2(t0, t1));
+            planes[m] = __byte_perm(t0, t1, 0x7531);
+        }
     }
     const uint32_t wmn = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
     const uint32_t wmx = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
@@ -393,26 +511,27 @@ __device__ __forceinline__ TeamPlan plan_chunk_team(const Barrier& bar, const ui
 #pragma unroll
     for (int m = 0; m < 8; ++m) planes[m] -= base4;  // no borrow: every exponent >= emin
     transpose8x8x4(planes);                          // quads of offsets -> planes
-    // escapes at width k are low_k | high_k (see plan_chunk_warp)
+    // escapes at width k are low_k | high_k (see add_escape_counts)
+    constexpr int kTop = (int)D::kExpBits - 1;
     uint32_t high[8];
-    high[7] = planes[7];
+    high[kTop] = planes[kTop];
 #pragma unroll
-    for (int k = 6; k >= 1; --k) high[k] = high[k + 1] | planes[k];
+    for (int k = kTop - 1; k >= 1; --k) high[k] = high[k + 1] | planes[k];
     uint32_t low = planes[0];
 #pragma unroll
-    for (int k = 1; k <= 7; ++k) {
+    for (int k = 1; k <= kTop; ++k) {
         const uint32_t n = __reduce_add_sync(0xFFFFFFFFu, __popc(low | high[k]));
         if (lane == 0) x.cnt[q][k] = n;
-        if (k < 7) low &= planes[k];
+        if (k < kTop) low &= planes[k];
     }
     bar.sync();
     TeamPlan pl{0u, 0u, emin, 0u, 0u, 0u};
     uint32_t best = 0;
     if (emax > emin) {
-        // lane k (1..7) sizes width k; the smallest (size, k) wins, so a tie
-        // keeps the smaller width
+        // lane k (1..kTop) sizes width k; the smallest (size, k) wins, so a
+        // tie keeps the smaller width
         uint32_t n = 0, before = 0, key = 0xFFFFFFFFu;
-        if (lane >= 1 && lane <= 7) {
+        if (lane >= 1 && lane <= (uint32_t)kTop) {
             const uint32_t c0 = x.cnt[0][lane], c1 = x.cnt[1][lane], c2 = x.cnt[2][lane];
             n = c0 + c1 + c2 + x.cnt[3][lane];
             before = (q > 0 ? c0 : 0u) + (q > 1 ? c1 : 0u) + (q > 2 ? c2 : 0u);
@@ -424,26 +543,27 @@ __device__ __forceinline__ TeamPlan plan_chunk_team(const Barrier& bar, const ui
         pl.n_esc = __shfl_sync(0xFFFFFFFFu, n, pl.k);
         pl.esc_before = __shfl_sync(0xFFFFFFFFu, before, pl.k);
     }
-    pl.raw = best >= kSmPlaneBytes ? 1u : 0u;
+    pl.raw = best >= raw_exponent_bytes<D>() ? 1u : 0u;
     if (pl.raw) {
         pl.k = 0;
         pl.base = 0;
         pl.n_esc = 0;
         pl.esc_before = 0;
-        pl.bytes = kMaxChunkBytes;
+        pl.bytes = max_chunk_bytes<D>();
     } else {
-        pl.bytes = (uint32_t)(16 + kSmPlaneBytes + kPlaneBytes * pl.k + pad16(pl.n_esc));
+        pl.bytes = packed_chunk_bytes<D>(pl.k, pl.n_esc);
     }
     return pl;
 }
 
 // Phase B for a team: write the chunk in P (planes from phase A) to `dst`
 // (global, 16-byte aligned).  No barrier: each warp writes the header (warp 0),
-// its four rows of the sign+fraction plane, its word of every bit-plane and
+// its four rows of the residual section, its word of every bit-plane and
 // its escapes, whose place follows from esc_before.  `xq`: this thread's
 // 8-word scratch column in shared memory (word m at xq[128 m]), where the
 // exponent quads wait for the escape writer.
-__device__ __forceinline__ void write_chunk_team(const uint32_t P[16], const uint32_t planes[8], const TeamPlan& pl,
+template <class D>
+__device__ __forceinline__ void write_chunk_team(const uint32_t* P, const uint32_t planes[8], const TeamPlan& pl,
                                                  uint8_t* dst, uint32_t* xq) {
     const uint32_t lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
     uint8_t* body = dst + kChunkHeaderBytes;
@@ -452,22 +572,52 @@ __device__ __forceinline__ void write_chunk_team(const uint32_t P[16], const uin
             make_uint4((pl.raw ? kModeRaw : kModePacked) | (pl.k << 8) | (pl.base << 16), kChunkElems | (pl.n_esc << 16),
                        pl.bytes, 0u);
     if (pl.raw) {
+        if constexpr (D::kElemBytes == 4) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-            *reinterpret_cast<uint4*>(body + 512 * (4 * q + jj) + 16 * lane) =
-                make_uint4(P[4 * jj], P[4 * jj + 1], P[4 * jj + 2], P[4 * jj + 3]);
+            for (int jj = 0; jj < 4; ++jj) {
+                uint8_t* row = body + 1024 * (4 * q + jj) + 32 * lane;
+                *reinterpret_cast<uint4*>(row) = make_uint4(P[8 * jj], P[8 * jj + 1], P[8 * jj + 2], P[8 * jj + 3]);
+                *reinterpret_cast<uint4*>(row + 16) =
+                    make_uint4(P[8 * jj + 4], P[8 * jj + 5], P[8 * jj + 6], P[8 * jj + 7]);
+            }
+        } else {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                *reinterpret_cast<uint4*>(body + 512 * (4 * q + jj) + 16 * lane) =
+                    make_uint4(P[4 * jj], P[4 * jj + 1], P[4 * jj + 2], P[4 * jj + 3]);
+        }
         return;
     }
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-        *reinterpret_cast<uint2*>(body + 256 * (4 * q + jj) + 8 * lane) =
-            make_uint2(sign_fraction_quad(P[4 * jj], P[4 * jj + 1]), sign_fraction_quad(P[4 * jj + 2], P[4 * jj + 3]));
+    for (int jj = 0; jj < 4; ++jj) {
+        uint8_t* plane_row = body + 256 * (4 * q + jj) + 8 * lane;
+        if constexpr (D::kElemBytes == 4) {
+            const uint32_t* R = P + 8 * jj;
+            *reinterpret_cast<uint2*>(plane_row) =
+                make_uint2(sign_fraction_quad(upper_halves(R[0], R[1]), upper_halves(R[2], R[3])),
+                           sign_fraction_quad(upper_halves(R[4], R[5]), upper_halves(R[6], R[7])));
+            *reinterpret_cast<uint4*>(body + kSmPlaneBytes + 512 * (4 * q + jj) + 16 * lane) =
+                make_uint4(lower_halves(R[0], R[1]), lower_halves(R[2], R[3]), lower_halves(R[4], R[5]),
+                           lower_halves(R[6], R[7]));
+        } else if constexpr (D::kExpBits == 5) {
+            *reinterpret_cast<uint2*>(plane_row) =
+                make_uint2(low_byte_quad(P[4 * jj], P[4 * jj + 1]), low_byte_quad(P[4 * jj + 2], P[4 * jj + 3]));
+        } else {
+            *reinterpret_cast<uint2*>(plane_row) = make_uint2(sign_fraction_quad(P[4 * jj], P[4 * jj + 1]),
+                                                              sign_fraction_quad(P[4 * jj + 2], P[4 * jj + 3]));
+        }
+    }
+    if constexpr (D::kExpBits == 5) {
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+            *reinterpret_cast<uint32_t*>(body + kSmPlaneBytes + kPlaneBytes * t + 4 * (32 * q + lane)) = planes[5 + t];
+    }
     const uint32_t k = pl.k;
     if (k == 0) return;
-    uint32_t esc = escape_word(planes, k);
-    uint8_t* col = body + kSmPlaneBytes + 4 * (32 * q + lane);
+    uint32_t esc = escape_word<D>(planes, k);
+    uint8_t* col = body + D::kResidBytes + 4 * (32 * q + lane);
 #pragma unroll
-    for (uint32_t p = 0; p < 8; ++p)
+    for (uint32_t p = 0; p < max_width<D>(); ++p)
         if (p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = planes[p] | esc;
     const uint32_t n_esc = pl.n_esc;
     if (n_esc == 0) return;
@@ -478,10 +628,10 @@ __device__ __forceinline__ void write_chunk_team(const uint32_t P[16], const uin
 #pragma unroll
     for (int b = 0; b < 6; ++b) excl += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, (mine >> b) & 1u) & below) << b;
     uint32_t idx = pl.esc_before + excl;
-    uint8_t* esc_out = body + kSmPlaneBytes + kPlaneBytes * k;
+    uint8_t* esc_out = body + D::kResidBytes + kPlaneBytes * k;
     if (esc) {
 #pragma unroll
-        for (int m = 0; m < 8; ++m) xq[128 * m] = exponent_quad(P, m);
+        for (int m = 0; m < 8; ++m) xq[128 * m] = exponent_quad<D>(P, m);
     }
     const uint8_t* xb = reinterpret_cast<const uint8_t*>(xq);
     while (__any_sync(0xFFFFFFFFu, esc != 0u)) {
@@ -495,69 +645,55 @@ __device__ __forceinline__ void write_chunk_team(const uint32_t P[16], const uin
     if (q == 0 && lane < 16 && n_esc + lane < pad16(n_esc)) esc_out[n_esc + lane] = 0;
 }
 
+template <class D>
+__host__ __device__ constexpr uint32_t tail_chunk_bytes(uint32_t n_c) {
+    return (uint32_t)(16 + pad16(D::kElemBytes * n_c));
+}
+
 // The partial last chunk held by a team (values past n_c ignored), raw.
-__device__ __forceinline__ void write_tail_chunk_team(const uint32_t P[16], uint32_t n_c, uint8_t* dst) {
+template <class D>
+__device__ __forceinline__ void write_tail_chunk_team(const uint32_t* P, uint32_t n_c, uint8_t* dst) {
     const uint32_t lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
-    const uint32_t bytes = (uint32_t)(16 + pad16(2 * n_c));
-    uint16_t* out = reinterpret_cast<uint16_t*>(dst + 16);
+    const uint32_t bytes = tail_chunk_bytes<D>(n_c);
+    if constexpr (D::kElemBytes == 4) {
+        uint32_t* out = reinterpret_cast<uint32_t*>(dst + 16);
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
+        for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const uint32_t e = 256 * (4 * q + jj) + 8 * lane + 2 * x;
-            if (e < n_c) out[e] = (uint16_t)(P[4 * jj + x] & 0xFFFFu);
-            if (e + 1 < n_c) out[e + 1] = (uint16_t)(P[4 * jj + x] >> 16);
-        }
+            for (int x = 0; x < 8; ++x) {
+                const uint32_t e = 256 * (4 * q + jj) + 8 * lane + x;
+                if (e < n_c) out[e] = P[8 * jj + x];
+            }
+    } else {
+        uint16_t* out = reinterpret_cast<uint16_t*>(dst + 16);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const uint32_t e = 256 * (4 * q + jj) + 8 * lane + 2 * x;
+                if (e < n_c) out[e] = (uint16_t)(P[4 * jj + x] & 0xFFFFu);
+                if (e + 1 < n_c) out[e + 1] = (uint16_t)(P[4 * jj + x] >> 16);
+            }
+    }
     if (q == 0 && lane == 0) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(kModeRaw, n_c, bytes, 0u);
-        for (uint32_t b = 16 + 2 * n_c; b < bytes; ++b) dst[b] = 0;
+        for (uint32_t b = 16 + D::kElemBytes * n_c; b < bytes; ++b) dst[b] = 0;
     }
 }
 
 // The partial last chunk (n_c < 4096 elements) is stored raw (section 5,
 // "Handling data alignment").  One warp; `vals` are its n_c values.
-template <typename Src>
+template <class D, typename Src>
 __device__ __forceinline__ void write_tail_chunk_warp(Src vals, uint32_t n_c, uint8_t* dst) {
+    using Elem = typename std::conditional<D::kElemBytes == 4, uint32_t, uint16_t>::type;
     const uint32_t lane = threadIdx.x & 31;
-    const uint32_t bytes = (uint32_t)(16 + pad16(2 * n_c));
-    uint16_t* out = reinterpret_cast<uint16_t*>(dst + 16);
+    const uint32_t bytes = tail_chunk_bytes<D>(n_c);
+    Elem* out = reinterpret_cast<Elem*>(dst + 16);
     for (uint32_t i = lane; i < n_c; i += 32) out[i] = vals(i);
     if (lane == 0) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(kModeRaw, n_c, bytes, 0u);
-        for (uint32_t b = 16 + 2 * n_c; b < bytes; ++b) dst[b] = 0;
+        for (uint32_t b = 16 + D::kElemBytes * n_c; b < bytes; ++b) dst[b] = 0;
     }
-}
-
-__host__ __device__ constexpr uint32_t tail_chunk_bytes(uint32_t n_c) { return (uint32_t)(16 + pad16(2 * n_c)); }
-
-// Group placement.  Every thread of the CTA calls it after each warp w has
-// stored its chunk's size (0 for a chunk past the end) in s_bytes[w].  Warp 0
-// scans the sizes and runs the look-back for group g; returns (to every
-// thread) the byte offset of warp w's chunk, or kFlagPoison.
-// A CTA whose chunks could not be sized (`failed`, CTA-uniform) publishes a
-// poisoned placement so that the groups after it give up at once.
-template <int G>
-__device__ __forceinline__ uint64_t place_group(const StreamOut& so, uint64_t g, const uint32_t* s_bytes,
-                                                uint64_t* s_offset, bool failed) {
-    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    if (__syncthreads_or(failed)) {
-        if (threadIdx.x == 0) st_relaxed_u64(&so.status[g], kFlagPoison);
-        return kFlagPoison;
-    }
-    if (w == 0) {
-        const uint32_t mine = lane < (uint32_t)G ? s_bytes[lane] : 0u;
-        uint32_t incl = mine;
-#pragma unroll
-        for (int d = 1; d < G; d <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-            if (lane >= (uint32_t)d) incl += t;
-        }
-        const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, G - 1);
-        const uint64_t go = lookback_offset_wide(so.status, g, total, data_start(so.n_chunks), so.ws);
-        if (lane < (uint32_t)G) s_offset[lane] = go == kFlagPoison ? kFlagPoison : go + (incl - mine);
-    }
-    __syncthreads();
-    return s_offset[w];
 }
 
 // Thread 0 of the warp that wrote chunk c: offset-table entry, the stream
@@ -566,7 +702,7 @@ __device__ __forceinline__ void finish_chunk(const StreamOut& so, uint64_t c, ui
     uint8_t* out = so.out;
     *reinterpret_cast<uint64_t*>(out + kStreamHeaderBytes + 8 * c) = offset;
     if (c == 0) {
-        *reinterpret_cast<uint4*>(out + 0) = make_uint4(kMagic, so.version | (kDtypeBf16 << 16), kChunkElems, 0u);
+        *reinterpret_cast<uint4*>(out + 0) = make_uint4(kMagic, so.version | (so.dtype << 16), kChunkElems, 0u);
         *reinterpret_cast<uint4*>(out + 16) =
             make_uint4((uint32_t)so.n_elems, (uint32_t)(so.n_elems >> 32), (uint32_t)so.n_chunks,
                        (uint32_t)(so.n_chunks >> 32));

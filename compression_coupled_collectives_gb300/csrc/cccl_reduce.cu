@@ -33,16 +33,22 @@
 namespace cccl {
 
 constexpr int kTeams = 3;                     // output chunks per group
-constexpr int kRSlots = 4;                    // staged rank chunks per team
 constexpr int kTeamThreads = 128;
 constexpr int kLoaderWarp = 4 * kTeams;
 constexpr int kPlacerWarp = kLoaderWarp + 1;
 constexpr int kReduceThreads = 32 * (kPlacerWarp + 1);
-constexpr int kPrevWords = 24;                // a team thread's chunk state: P[16], planes[8]
-constexpr size_t kRingBytes = (size_t)kTeams * kRSlots * kMaxChunkBytes;
-constexpr size_t kPrevBytes = (size_t)kTeams * kPrevWords * kTeamThreads * 4;
-constexpr size_t kReduceSmemBytes = kRingBytes + kPrevBytes;
 constexpr uint64_t kNoGroup = ~0ull;
+// staged rank chunks per team: 4 of 8.2 KB for the 16-bit types, 3 of 16.4 KB
+// for fp32
+template <class D>
+__host__ __device__ constexpr int rslots() { return D::kElemBytes == 4 ? 3 : 4; }
+// a team thread's chunk state between sizing and writing: its words, planes[8]
+template <class D>
+__host__ __device__ constexpr int prev_words() { return thread_words<D>() + 8; }
+template <class D>
+__host__ __device__ constexpr size_t ring_bytes() { return (size_t)kTeams * rslots<D>() * max_chunk_bytes<D>(); }
+template <class D>
+__host__ __device__ constexpr size_t reduce_smem() { return ring_bytes<D>() + (size_t)kTeams * prev_words<D>() * kTeamThreads * 4; }
 
 // binary32 pair -> bf16 pair, round to nearest even (hi lane from the upper word)
 __device__ __forceinline__ uint32_t round_pair_bf16(uint64_t v) {
@@ -50,32 +56,60 @@ __device__ __forceinline__ uint32_t round_pair_bf16(uint64_t v) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "r"((uint32_t)(v >> 32)), "r"((uint32_t)v));
     return d;
 }
-// every NaN lane -> 0x7FC0
-__device__ __forceinline__ uint32_t canonical_nan_pair(uint32_t d) {
-    const uint32_t mag = d & 0x7FFF7FFFu;
-    const uint32_t nan = (mag + 0x007F007Fu) & 0x80008000u;  // lanes with mag > 0x7F80
-    const uint32_t mask = (nan >> 15) * 0xFFFFu;
-    return (d & ~mask) | (0x7FC07FC0u & mask);
+// binary32 pair -> IEEE fp16 pair, round to nearest even, subnormal results
+// kept, overflow to Inf (hi lane from the upper word)
+__device__ __forceinline__ uint32_t round_pair_fp16(uint64_t v) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "r"((uint32_t)(v >> 32)), "r"((uint32_t)v));
+    return d;
 }
 
-// Element-wise min (op 1) or max (op 2) of two bf16 pairs, exact: a NaN in
-// either lane gives a NaN there (made canonical afterwards); otherwise the
-// IEEE total order, -0 below +0, through the usual sign-magnitude key
-// (negative: all bits flipped; positive: sign bit set), compared as u16.
+// 16-bit types: 0xFFFF in every lane that holds a NaN (magnitude above the
+// all-ones exponent with a zero fraction: 0x7F80 bf16, 0x7C00 fp16)
+template <class D>
+__device__ __forceinline__ uint32_t nan_lanes_pair(uint32_t x) {
+    constexpr uint32_t kAdd = (0x7FFFu - ((1u << D::kExpBits) - 1u) * (1u << (15 - D::kExpBits))) * 0x00010001u;
+    return ((((x & 0x7FFF7FFFu) + kAdd) & 0x80008000u) >> 15) * 0xFFFFu;
+}
+// the NaN every reduce writes: 0x7FC0 bf16, 0x7E00 fp16, 0x7FC00000 fp32
+template <class D>
+__host__ __device__ constexpr uint32_t canonical_nan() {
+    return D::kElemBytes == 4 ? 0x7FC00000u : (D::kExpBits == 5 ? 0x7E00u : 0x7FC0u);
+}
+// every NaN lane -> the canonical NaN
+template <class D>
+__device__ __forceinline__ uint32_t canonical_nan_pair(uint32_t d) {
+    const uint32_t mask = nan_lanes_pair<D>(d);
+    return (d & ~mask) | (canonical_nan<D>() * 0x00010001u & mask);
+}
+__device__ __forceinline__ uint32_t canonical_nan_word(uint32_t v) {
+    return (v & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : v;
+}
+
+// Element-wise min (op 1) or max (op 2), exact: a NaN in either operand gives
+// the canonical NaN; otherwise the IEEE total order, -0 below +0, through the
+// usual sign-magnitude key (negative: all bits flipped; positive: sign bit
+// set), compared as unsigned.
 __device__ __forceinline__ uint32_t order_key_pair(uint32_t x) {
     return x ^ ((((x >> 15) & 0x00010001u) * 0x7FFFu) | 0x80008000u);
 }
 __device__ __forceinline__ uint32_t from_order_key_pair(uint32_t k) {
     return k ^ ((((~k >> 15) & 0x00010001u) * 0x7FFFu) | 0x80008000u);
 }
-__device__ __forceinline__ uint32_t nan_lanes_pair(uint32_t x) {  // 0xFFFF where x is a NaN
-    return ((((x & 0x7FFF7FFFu) + 0x007F007Fu) & 0x80008000u) >> 15) * 0xFFFFu;
-}
+template <class D>
 __device__ __forceinline__ uint32_t minmax_pair(uint32_t a, uint32_t b, uint32_t op) {
     const uint32_t ka = order_key_pair(a), kb = order_key_pair(b);
     const uint32_t r = from_order_key_pair(op == 1 ? vmin_u16x2(ka, kb) : vmax_u16x2(ka, kb));
-    const uint32_t nan = nan_lanes_pair(a) | nan_lanes_pair(b);
-    return (r & ~nan) | (0x7FC07FC0u & nan);
+    const uint32_t nan = nan_lanes_pair<D>(a) | nan_lanes_pair<D>(b);
+    return (r & ~nan) | (canonical_nan<D>() * 0x00010001u & nan);
+}
+__device__ __forceinline__ uint32_t minmax_word(uint32_t a, uint32_t b, uint32_t op) {
+    const uint32_t ka = a ^ ((uint32_t)((int32_t)a >> 31) | 0x80000000u);
+    const uint32_t kb = b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+    const uint32_t k = op == 1 ? min(ka, kb) : max(ka, kb);
+    const uint32_t r = k ^ ((uint32_t)((int32_t)~k >> 31) | 0x80000000u);
+    const bool nan = (a & 0x7FFFFFFFu) > 0x7F800000u || (b & 0x7FFFFFFFu) > 0x7F800000u;
+    return nan ? 0x7FC00000u : r;
 }
 
 // Warp-uniform reads of the abort flag and of a bounded wait's outcome.
@@ -98,8 +132,8 @@ struct ReduceSmem {
     uint64_t decoded[2];                 // teams -> loader: meta[b] read (one arrival per team warp)
     uint64_t sized[2];                   // teams -> placer: sizes in size[b] (one arrival per team)
     uint64_t placed[2];                  // placer -> teams: offsets in off[b] (1 arrival)
-    uint64_t full[kTeams][kRSlots];      // a rank chunk landed in the slot (transaction count)
-    uint64_t free_[kTeams][kRSlots];     // the team is done with the slot (1 arrival)
+    uint64_t full[kTeams][4];            // a rank chunk landed in the slot (transaction count)
+    uint64_t free_[kTeams][4];           // the team is done with the slot (1 arrival)
     unsigned long long tally[2];         // sized teams (high word) and their bytes (low word)
     uint32_t size[2][kTeams];
     uint32_t failed[2][kTeams];          // the team's chunk could not be reduced
@@ -117,8 +151,11 @@ __device__ __forceinline__ void set_abort(const StreamOut& so, ReduceSmem& sm) {
 }
 
 // --------------------------------------------------------------------------- loader
+template <class D>
 __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R, const StreamOut& so, uint8_t* ring,
                                               ReduceSmem& sm) {
+    constexpr int kRSlots = rslots<D>();
+    constexpr uint32_t kRawBytes = D::kElemBytes * kChunkElems;
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t n_groups = (so.n_chunks + kTeams - 1) / kTeams;
     uint32_t ut[kTeams] = {};  // rank chunks issued to each team
@@ -148,11 +185,11 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
             const uint32_t t = idx / (uint32_t)R, r = idx % (uint32_t)R;
             if (r == 0 && inputs.local != nullptr) {  // uncompressed: chunk c is values 4096 c ..
                 const uint64_t c = c0 + t, left = so.n_elems - c * kChunkElems;
-                m.off[t][r] = 2 * kChunkElems * c;
-                m.bytes[t][r] = 2 * (uint32_t)(left < kChunkElems ? left : kChunkElems);
+                m.off[t][r] = (uint64_t)kRawBytes * c;
+                m.bytes[t][r] = D::kElemBytes * (uint32_t)(left < kChunkElems ? left : kChunkElems);
                 continue;
             }
-            const ChunkView v = locate_chunk(inputs.in[r], inputs.in_bytes[r], so.n_elems, so.n_chunks, c0 + t);
+            const ChunkView v = locate_chunk<D>(inputs.in[r], inputs.in_bytes[r], so.n_elems, so.n_chunks, c0 + t);
             m.off[t][r] = v.offset;
             m.bytes[t][r] = v.bytes;
             ok = ok && v.ok;
@@ -182,12 +219,12 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
                 }
                 if (lane == 0) {
                     fence_proxy_async_smem();
-                    uint8_t* slot = ring + ((size_t)t * kRSlots + s) * kMaxChunkBytes;
+                    uint8_t* slot = ring + ((size_t)t * kRSlots + s) * max_chunk_bytes<D>();
                     if (r != 0 || inputs.local == nullptr)
                         bulk_load(slot, inputs.in[r] + m.off[t][r], m.bytes[t][r], &sm.full[t][s]);
-                    else if (m.bytes[t][r] == 2 * kChunkElems)  // a full local chunk, staged raw
-                        bulk_load(slot, reinterpret_cast<const uint8_t*>(inputs.local) + m.off[t][r],
-                                  2 * kChunkElems, &sm.full[t][s]);
+                    else if (m.bytes[t][r] == kRawBytes)  // a full local chunk, staged raw
+                        bulk_load(slot, static_cast<const uint8_t*>(inputs.local) + m.off[t][r], kRawBytes,
+                                  &sm.full[t][s]);
                     else  // the partial local chunk is read in place by the team
                         mbar_arrive(&sm.full[t][s]);
                 }
@@ -237,12 +274,110 @@ __device__ __forceinline__ void reduce_placer(const StreamOut& so, ReduceSmem& s
 }
 
 // --------------------------------------------------------------------------- teams
-__device__ __forceinline__ void reduce_team(int R, const uint16_t* local, uint32_t op, const StreamOut& so,
+// One team's rank operand r of its chunk into V (decode_full_chunk's layout),
+// from the staged rank chunk or, for the partial local chunk, in place.
+template <class D>
+__device__ __forceinline__ void read_raw_partial(const uint8_t* vals_bytes, uint32_t n_c, uint32_t* V) {
+    const uint32_t lane = threadIdx.x & 31, wq = (threadIdx.x >> 5) & 3;
+    if constexpr (D::kElemBytes == 4) {
+        const uint32_t* vals = reinterpret_cast<const uint32_t*>(vals_bytes);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const uint32_t e = 256 * (4 * wq + jj) + 8 * lane + x;
+                V[8 * jj + x] = e < n_c ? vals[e] : 0u;
+            }
+    } else {
+        const uint16_t* vals = reinterpret_cast<const uint16_t*>(vals_bytes);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const uint32_t e = 256 * (4 * wq + jj) + 8 * lane + 2 * x;
+                const uint32_t lo = e < n_c ? vals[e] : 0u, hi = e + 1 < n_c ? vals[e + 1] : 0u;
+                V[4 * jj + x] = lo | (hi << 16);
+            }
+    }
+}
+
+// acc (16 binary32 pairs, or for min/max 16 words of raw values: the 16-bit
+// types keep a pair-word per entry, fp32 two words) op= V, in rank order.
+template <class D>
+__device__ __forceinline__ uint64_t widen(uint32_t v) {
+    if constexpr (D::kExpBits == 5)
+        return widen_pair_fp16(v);
+    else
+        return widen_pair(v);
+}
+template <class D>
+__device__ __forceinline__ void accumulate(uint64_t* acc, const uint32_t* V, uint32_t op, bool first) {
+    if constexpr (D::kElemBytes == 4) {
+        if (op != 0) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+                acc[x] = first ? ((uint64_t)V[2 * x] | ((uint64_t)V[2 * x + 1] << 32))
+                               : ((uint64_t)minmax_word((uint32_t)acc[x], V[2 * x], op) |
+                                  ((uint64_t)minmax_word((uint32_t)(acc[x] >> 32), V[2 * x + 1], op) << 32));
+        } else if (first) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = (uint64_t)V[2 * x] | ((uint64_t)V[2 * x + 1] << 32);
+        } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+                acc[x] = add_f32x2(acc[x], (uint64_t)V[2 * x] | ((uint64_t)V[2 * x + 1] << 32));
+        }
+    } else {
+        if (op != 0) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = first ? V[x] : minmax_pair<D>((uint32_t)acc[x], V[x], op);
+        } else if (first) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = widen<D>(V[x]);
+        } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = add_f32x2(acc[x], widen<D>(V[x]));
+        }
+    }
+}
+
+// The reduced chunk into P: one rounding of the binary32 sums to the type
+// (fp32: none), or the min / max values as they are; NaNs made canonical
+// when a rank may have held an Inf or a NaN.
+template <class D, typename Barrier>
+__device__ __forceinline__ void finish_values(const Barrier& bar, const uint64_t* acc, uint32_t op, bool special,
+                                              uint32_t* P) {
+    if constexpr (D::kElemBytes == 4) {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            P[2 * x] = (uint32_t)acc[x];
+            P[2 * x + 1] = (uint32_t)(acc[x] >> 32);
+        }
+        if (bar.any(special)) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) P[x] = canonical_nan_word(P[x]);
+        }
+    } else {
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+            P[x] = op != 0 ? (uint32_t)acc[x] : (D::kExpBits == 5 ? round_pair_fp16(acc[x]) : round_pair_bf16(acc[x]));
+        if (bar.any(special)) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) P[x] = canonical_nan_pair<D>(P[x]);
+        }
+    }
+}
+
+template <class D>
+__device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t op, const StreamOut& so,
                                             uint8_t* ring_base, uint32_t* prev_base, ReduceSmem& sm) {
+    constexpr int kRSlots = rslots<D>();
+    constexpr int kW = thread_words<D>();
+    constexpr int kPrevWords = prev_words<D>();
+    constexpr uint32_t kSlotBytes = max_chunk_bytes<D>();
     const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127;
-    const uint32_t wq = tt >> 5;  // warp within the team = quarter of the chunk
     const TeamBarrier bar{1u + team};
-    uint8_t* ring = ring_base + (size_t)team * kRSlots * kMaxChunkBytes;
+    uint8_t* ring = ring_base + (size_t)team * kRSlots * kSlotBytes;
     uint32_t* prev_st = prev_base + (size_t)team * kPrevWords * kTeamThreads + tt;  // word w at prev_st[128 w]
     const uint64_t n_full = so.n_elems / kChunkElems;
     uint32_t u = 0;  // rank chunks consumed (the loader's order for this team)
@@ -259,7 +394,7 @@ __device__ __forceinline__ void reduce_team(int R, const uint16_t* local, uint32
         const ReduceMeta& m = sm.meta[b];
         const uint64_t g = m.g;
         TeamPlan pl{};
-        uint32_t P[16], planes[8];
+        uint32_t P[kW], planes[8];
         uint32_t bytes = 0, fail = 0;
         uint64_t c = 0;
         uint32_t n_c = 0;
@@ -274,94 +409,54 @@ __device__ __forceinline__ void reduce_team(int R, const uint16_t* local, uint32
                 bool special = false;
                 for (int r = 0; r < R; ++r, ++u) {
                     const uint32_t s = u % kRSlots;
-                    uint8_t* buf = ring + (size_t)s * kMaxChunkBytes;
+                    uint8_t* buf = ring + (size_t)s * kSlotBytes;
                     const bool landed = !sm.abort && mbar_wait(&sm.full[team][s], (u / kRSlots) & 1u);
                     if (bar.any(!landed)) {
                         if (tt == 0) set_abort(so, sm);
                         return;  // the whole team
                     }
+                    uint32_t V[kW];
                     if (fail == 0 && r == 0 && local != nullptr) {
                         // the uncompressed local operand: staged raw, or read in place
-                        uint32_t V[16];
                         if (n_c == kChunkElems) {
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj) {
-                                const uint4 v =
-                                    *reinterpret_cast<const uint4*>(buf + 512 * (4 * wq + jj) + 16 * lane);
-                                V[4 * jj] = v.x;
-                                V[4 * jj + 1] = v.y;
-                                V[4 * jj + 2] = v.z;
-                                V[4 * jj + 3] = v.w;
-                            }
+                            load_raw_full<D>(buf, V);
                         } else {
-                            const uint16_t* vals = local + c * kChunkElems;
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                                for (int x = 0; x < 4; ++x) {
-                                    const uint32_t e = 256 * (4 * wq + jj) + 8 * lane + 2 * x;
-                                    const uint32_t lo = e < n_c ? vals[e] : 0u, hi = e + 1 < n_c ? vals[e + 1] : 0u;
-                                    V[4 * jj + x] = lo | (hi << 16);
-                                }
+                            read_raw_partial<D>(static_cast<const uint8_t*>(local) +
+                                                    (size_t)D::kElemBytes * c * kChunkElems,
+                                                n_c, V);
                         }
                         special = true;
-#pragma unroll
-                        for (int x = 0; x < 16; ++x) acc[x] = op == 0 ? widen_pair(V[x]) : V[x];
+                        accumulate<D>(acc, V, op, true);
                     } else if (fail == 0) {
                         const ChunkHeader h = read_chunk_header(buf);
-                        bool good = chunk_header_valid(h, m.bytes[team][r], n_c);  // same for the team
-                        uint32_t V[16];
+                        bool good = chunk_header_valid<D>(h, m.bytes[team][r], n_c);  // same for the team
                         if (good) {
                             if (n_c < kChunkElems) {  // partial last chunk: raw values, read those that exist
-                                const uint16_t* vals = reinterpret_cast<const uint16_t*>(buf + kChunkHeaderBytes);
-#pragma unroll
-                                for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                                    for (int x = 0; x < 4; ++x) {
-                                        const uint32_t e = 256 * (4 * wq + jj) + 8 * lane + 2 * x;
-                                        const uint32_t lo = e < n_c ? vals[e] : 0u, hi = e + 1 < n_c ? vals[e + 1] : 0u;
-                                        V[4 * jj + x] = lo | (hi << 16);
-                                    }
+                                read_raw_partial<D>(buf + kChunkHeaderBytes, n_c, V);
                                 special = true;
                             } else {
                                 bool sp = false;
-                                good = decode_full_chunk(bar, buf, h, V, sm.row_tot[team], sp);
+                                good = decode_full_chunk<D>(bar, buf, h, V, sm.row_tot[team], sp);
                                 special = special || sp;
                             }
                         }
-                        if (!good) {
+                        if (!good)
                             fail = kStatusCorrupt;
-                        } else if (op != 0) {  // min / max: exact, on the bf16 pairs
-#pragma unroll
-                            for (int x = 0; x < 16; ++x)
-                                acc[x] = r == 0 ? V[x] : minmax_pair((uint32_t)acc[x], V[x], op);
-                        } else if (r == 0) {
-#pragma unroll
-                            for (int x = 0; x < 16; ++x) acc[x] = widen_pair(V[x]);
-                        } else {
-#pragma unroll
-                            for (int x = 0; x < 16; ++x) acc[x] = add_f32x2(acc[x], widen_pair(V[x]));
-                        }
+                        else
+                            accumulate<D>(acc, V, op, r == 0);
                     }
                     bar.sync();  // the team is done with slot s and row_tot
                     if (tt == 0) mbar_arrive(&sm.free_[team][s]);
                 }
-                if (fail == 0) {
-#pragma unroll
-                    for (int x = 0; x < 16; ++x) P[x] = op == 0 ? round_pair_bf16(acc[x]) : (uint32_t)acc[x];
-                    if (bar.any(special)) {
-#pragma unroll
-                        for (int x = 0; x < 16; ++x) P[x] = canonical_nan_pair(P[x]);
-                    }
-                }
+                if (fail == 0) finish_values<D>(bar, acc, op, special, P);
             }
             if (lane == 0) mbar_arrive(&sm.decoded[b]);
             if (mine && fail == 0) {
                 if (c < n_full) {
-                    pl = plan_chunk_team(bar, P, planes, sm.xch[team]);
+                    pl = plan_chunk_team<D>(bar, P, planes, sm.xch[team]);
                     bytes = pl.bytes;
                 } else {
-                    bytes = tail_chunk_bytes(n_c);
+                    bytes = tail_chunk_bytes<D>(n_c);
                 }
             }
             if (tt == 0) {
@@ -392,16 +487,16 @@ __device__ __forceinline__ void reduce_team(int R, const uint16_t* local, uint32
                     if (off + prev_bytes > so.capacity) {  // cannot happen for a correct placement
                         if (tt == 0) record_error(so.ws, kStatusCorrupt);
                     } else {
-                        uint32_t Pp[16], Qp[8];
+                        uint32_t Pp[kW], Qp[8];
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) Pp[x] = prev_st[kTeamThreads * x];
+                        for (int x = 0; x < kW; ++x) Pp[x] = prev_st[kTeamThreads * x];
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) Qp[x] = prev_st[kTeamThreads * (16 + x)];
+                        for (int x = 0; x < 8; ++x) Qp[x] = prev_st[kTeamThreads * (kW + x)];
                         uint8_t* dst = so.out + off;
                         if (prev_c < n_full)
-                            write_chunk_team(Pp, Qp, prev_pl, dst, prev_st);
+                            write_chunk_team<D>(Pp, Qp, prev_pl, dst, prev_st);
                         else
-                            write_tail_chunk_team(Pp, (uint32_t)(so.n_elems - prev_c * kChunkElems), dst);
+                            write_tail_chunk_team<D>(Pp, (uint32_t)(so.n_elems - prev_c * kChunkElems), dst);
                         if (tt == 0) finish_chunk(so, prev_c, off, prev_bytes);
                     }
                 }
@@ -414,20 +509,21 @@ __device__ __forceinline__ void reduce_team(int R, const uint16_t* local, uint32
         prev_bytes = fail ? 0u : bytes;
         if (prev_bytes > 0) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) prev_st[kTeamThreads * x] = P[x];
+            for (int x = 0; x < kW; ++x) prev_st[kTeamThreads * x] = P[x];
 #pragma unroll
-            for (int x = 0; x < 8; ++x) prev_st[kTeamThreads * (16 + x)] = planes[x];
+            for (int x = 0; x < 8; ++x) prev_st[kTeamThreads * (kW + x)] = planes[x];
             prev_pl = pl;
             prev_c = c;
         }
     }
 }
 
+template <class D>
 __global__ void __launch_bounds__(kReduceThreads, 1) reduce_kernel(ReduceInputs inputs, int R, StreamOut so) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ ReduceSmem sm;
     uint8_t* ring = smem;
-    uint32_t* prev = reinterpret_cast<uint32_t*>(smem + kRingBytes);
+    uint32_t* prev = reinterpret_cast<uint32_t*>(smem + ring_bytes<D>());
     const uint32_t w = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -438,7 +534,7 @@ __global__ void __launch_bounds__(kReduceThreads, 1) reduce_kernel(ReduceInputs 
             sm.tally[b] = 0;
         }
         for (int t = 0; t < kTeams; ++t)
-            for (int s = 0; s < kRSlots; ++s) {
+            for (int s = 0; s < rslots<D>(); ++s) {
                 mbar_init(&sm.full[t][s], 1);
                 mbar_init(&sm.free_[t][s], 1);
             }
@@ -447,20 +543,21 @@ __global__ void __launch_bounds__(kReduceThreads, 1) reduce_kernel(ReduceInputs 
     }
     __syncthreads();
     if (w == kLoaderWarp)
-        reduce_loader(inputs, R, so, ring, sm);
+        reduce_loader<D>(inputs, R, so, ring, sm);
     else if (w == kPlacerWarp)
         reduce_placer(so, sm);
     else
-        reduce_team(R, inputs.local, inputs.op, so, ring, prev, sm);
+        reduce_team<D>(R, inputs.local, inputs.op, so, ring, prev, sm);
 }
 
-cudaError_t launch_reduce(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,
-                          void* ws, cudaStream_t stream) {
+template <class D>
+cudaError_t launch_reduce_t(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,
+                            void* ws, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kReduceSmemBytes);
+        attr = cudaFuncSetAttribute(reduce_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)reduce_smem<D>());
     });
     if (attr != cudaSuccess) return attr;
     int dev = 0, sms = 0;
@@ -475,10 +572,23 @@ cudaError_t launch_reduce(const ReduceInputs& inputs, int R, uint64_t n_elems, u
     so.n_elems = n_elems;
     so.n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
     so.version = kVersion;
+    so.dtype = D::kCode;
     const uint64_t n_groups = (so.n_chunks + kTeams - 1) / kTeams;
     const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
-    reduce_kernel<<<grid, kReduceThreads, kReduceSmemBytes, stream>>>(inputs, R, so);
+    reduce_kernel<D><<<grid, kReduceThreads, reduce_smem<D>(), stream>>>(inputs, R, so);
     return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,
+                          void* ws, cudaStream_t stream) {
+    return launch_reduce_t<Bf16>(inputs, R, n_elems, out, capacity, ws, stream);
+}
+
+cudaError_t launch_reduce_typed(uint32_t dtype, const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out,
+                                uint64_t capacity, void* ws, cudaStream_t stream) {
+    if (dtype == Fp16::kCode) return launch_reduce_t<Fp16>(inputs, R, n_elems, out, capacity, ws, stream);
+    if (dtype == Fp32::kCode) return launch_reduce_t<Fp32>(inputs, R, n_elems, out, capacity, ws, stream);
+    return launch_reduce_t<Bf16>(inputs, R, n_elems, out, capacity, ws, stream);
 }
 
 }  // namespace cccl

@@ -1,6 +1,7 @@
 /*
- * cccl.h -- C ABI of libcccl: lossless compression of bf16 communication
- * buffers and the compressed reduce step of an allreduce, on one GPU.
+ * cccl.h -- C ABI of libcccl: lossless compression of bf16 (and fp16, fp32)
+ * communication buffers and the compressed reduce step of an allreduce, on
+ * one GPU.
  *
  * Method: "CCCL: In-GPU Compression-Coupled Collective Communication"
  * (arXiv 2604.17172).
@@ -54,7 +55,8 @@
  *     anything is enqueued and return immediately.  Errors found on the
  *     device (corrupt input, a wait that ran out) and the compressed size
  *     land in the workspace; read them with cccl_get_result.
- *   - n_elems counts bf16 values (passed as their uint16 bit patterns).
+ *   - n_elems counts values: bf16 values (passed as their uint16 bit
+ *     patterns), except in the typed entry points below.
  */
 #ifndef CCCL_H
 #define CCCL_H
@@ -236,6 +238,72 @@ cccl_status cccl_decompress_paged(const void *d_in, size_t in_bytes, uint16_t *d
 cccl_status cccl_reduce_mixed(const uint16_t *d_local, const void *const *h_ins, const size_t *h_in_bytes,
                               int n_remote, size_t n_elems, void *d_out, size_t out_capacity, void *d_ws,
                               size_t ws_bytes, cccl_stream_t stream);
+
+/* Element types of the typed entry points: the stream header's dtype field.
+ * Section 4.1's split is stated for floating-point values and worked out for
+ * bf16; fp16 and fp32 take the same split with their own exponent field
+ * (this library's reading: the same scheme, other widths).  Values are
+ * passed as their bit patterns: uint16 for bf16 and fp16, uint32 for fp32.
+ *   bf16  exponent bits 7..14 (8 bits); packed body: 4096 bytes of
+ *         sign << 7 | fraction bits 0..6, then the exponent planes.
+ *   fp16  exponent bits 10..14 (5 bits); packed body: 4096 bytes of fraction
+ *         bits 0..7, three bit-planes (fraction bit 8, fraction bit 9, sign),
+ *         then the exponent planes; widths 1..4.
+ *   fp32  exponent bits 23..30 (8 bits); the upper 16 bits are coded as a
+ *         bf16 value: packed body: 4096 bytes of sign << 7 | fraction bits
+ *         16..22, the 4096 lower halves (fraction bits 0..15) as u16, then
+ *         the exponent planes.
+ * The other layers (header, offset table, chunk header, plane layout, escape
+ * bytes, raw chunks of n_c values) are as described at the top.  A full
+ * chunk is packed only when 512 k + pad16(n_esc) is below 512 * (exponent
+ * bits), else raw. */
+#define CCCL_DTYPE_BF16 1
+#define CCCL_DTYPE_FP16 2
+#define CCCL_DTYPE_FP32 3
+
+/* Worst-case stream size of n_elems values of `dtype` (every chunk raw):
+ * 64 + pad16(8 * n_chunks) + sum over chunks of 16 + pad16(bytes * n_c).
+ * 0 for n_elems 0 or above CCCL_MAX_ELEMS, or an unknown dtype.
+ * cccl_workspace_bytes(n_elems) serves every dtype. */
+size_t cccl_compress_bound_typed(int dtype, size_t n_elems);
+
+/* cccl_compress (window = 0) or cccl_compress_window (window != 0) for any
+ * element type.  d_in holds n_elems bit patterns of `dtype`;
+ * out_capacity >= cccl_compress_bound_typed(dtype, n_elems).  With
+ * CCCL_DTYPE_BF16 the stream is exactly cccl_compress's (or
+ * cccl_compress_window's).  Returns INVALID_ARG (also for an unknown dtype),
+ * CAPACITY, CUDA or OK. */
+cccl_status cccl_compress_typed(int dtype, const void *d_in, size_t n_elems, void *d_out, size_t out_capacity,
+                                void *d_ws, size_t ws_bytes, int window, cccl_stream_t stream);
+
+/* cccl_decompress for any element type: d_out receives n_elems bit patterns
+ * of `dtype`.  A stream whose header names another element type is CORRUPT
+ * (reported by cccl_get_result).  Returns INVALID_ARG, CUDA or OK. */
+cccl_status cccl_decompress_typed(int dtype, const void *d_in, size_t in_bytes, void *d_out, size_t n_elems,
+                                  void *d_ws, size_t ws_bytes, cccl_stream_t stream);
+
+/* The reduce step for any element type and operator (section 5,
+ * CopyReducePacks: sum, min, max), with an optional uncompressed local
+ * operand (section 5, selective compression).
+ *   d_local       NULL, or n_elems bit patterns of `dtype`: rank 0.
+ *   h_ins         host array of n_streams device pointers to compressed
+ *                 streams of `dtype` made for n_elems values, the next ranks
+ *                 in order; h_in_bytes their readable sizes.  The ranks
+ *                 R = n_streams + (d_local != NULL) must be 1..64.
+ *   op            CCCL_OP_SUM: acc = x_0[i] in binary32, acc = acc + x_r[i]
+ *                 in rank order (round to nearest even, subnormals kept),
+ *                 then one rounding to the type (bf16 and fp16: nearest
+ *                 even, with subnormals and overflow to Inf; fp32: none);
+ *                 CCCL_OP_MIN / CCCL_OP_MAX: exact, -0 below +0.  Any NaN
+ *                 becomes the type's NaN: 0x7FC0, 0x7E00, 0x7FC00000.
+ *   d_out, d_ws   out_capacity >= cccl_compress_bound_typed(dtype, n_elems),
+ *                 ws_bytes >= cccl_workspace_bytes(n_elems).
+ * The result is compressed exactly as cccl_compress_typed (window 0) would.
+ * Input errors are reported as CORRUPT by cccl_get_result.
+ * Returns INVALID_ARG, CAPACITY, CUDA or OK synchronously. */
+cccl_status cccl_reduce_typed(int dtype, int op, const void *d_local, const void *const *h_ins,
+                              const size_t *h_in_bytes, int n_streams, size_t n_elems, void *d_out,
+                              size_t out_capacity, void *d_ws, size_t ws_bytes, cccl_stream_t stream);
 
 /* Wait for the work enqueued on `stream` and read the outcome stored in the
  * workspace of the last call that used it.

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     assert names == sorted(["cccl_compress_bound", "cccl_workspace_bytes", "cccl_compress", "cccl_compress_noalloc",
                             "cccl_decompress", "cccl_reduce_compressed", "cccl_reduce_mixed", "cccl_get_result",
                             "cccl_status_string", "cccl_compress_paged", "cccl_decompress_paged",
-                            "cccl_compress_window", "cccl_reduce_op"]), names
+                            "cccl_compress_window", "cccl_reduce_op", "cccl_compress_bound_typed",
+                            "cccl_compress_typed", "cccl_decompress_typed", "cccl_reduce_typed"]), names
 
 
 def test_library_exports_every_declared_symbol(cc):
@@ -48,6 +49,20 @@ def test_bound_matches_oracle(cc, orc, n):
     assert cc.cccl_compress_bound(n) == orc.compress_bound(n)
     nch = -(-n // 4096)
     assert cc.cccl_workspace_bytes(n) == -(-(16 + 8 * nch) // 16) * 16
+
+
+@pytest.mark.parametrize("dtype", [1, 2, 3])
+@pytest.mark.parametrize("n", [1, 4095, 4096, 4097, 1 << 20, (1 << 26) + 5])
+def test_typed_bound_matches_oracle(cc, orc, dtype, n):
+    assert cc.cccl_compress_bound_typed(dtype, n) == orc.compress_bound_typed(dtype, n)
+
+
+def test_typed_bound_limits(cc):
+    assert cc.cccl_compress_bound_typed(1, 12345) == cc.cccl_compress_bound(12345)
+    assert cc.cccl_compress_bound_typed(0, 4096) == 0
+    assert cc.cccl_compress_bound_typed(4, 4096) == 0
+    assert cc.cccl_compress_bound_typed(3, 0) == 0
+    assert cc.cccl_compress_bound_typed(2, (1 << 40) + 1) == 0
 
 
 def test_bound_and_workspace_limits(cc):
@@ -113,6 +128,27 @@ def test_host_side_argument_checks(cc):
     assert lib.cccl_reduce_op(ptrs, sizes, 2, n, 3, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_reduce_op(ptrs, sizes, 2, n, -1, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_reduce_op(ptrs, sizes, 0, n, 1, B, bound, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    b32 = cc.cccl_compress_bound_typed(3, n)
+    assert lib.cccl_compress_typed(4, A, n, B, b32, W, wsb, 0, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress_typed(0, A, n, B, b32, W, wsb, 0, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress_typed(3, A, 0, B, b32, W, wsb, 0, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress_typed(3, A + 4, n, B, b32, W, wsb, 0, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress_typed(3, A, n, B, b32, W, wsb - 16, 0, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_compress_typed(3, A, n, B, bound, W, wsb, 0, None) == cc.CCCL_ERR_CAPACITY  # bf16's bound
+    assert lib.cccl_compress_typed(2, A, n, B, bound - 1, W, wsb, 1, None) == cc.CCCL_ERR_CAPACITY
+    assert lib.cccl_decompress_typed(5, A, 4096, B, n, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_decompress_typed(3, A, 0, B, n, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_decompress_typed(3, A, 4096, B + 8, n, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_decompress_typed(2, A, 4096, B, n, W, 8, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_typed(4, 0, None, ptrs, sizes, 2, n, B, b32, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_typed(3, 3, None, ptrs, sizes, 2, n, B, b32, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_typed(3, 0, None, ptrs, sizes, 0, n, B, b32, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_typed(3, 0, A, ptrs, sizes, 64, n, B, b32, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_typed(3, 0, None, ptrs, sizes, 65, n, B, b32, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_typed(3, 0, None, None, sizes, 2, n, B, b32, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_typed(3, 0, A + 4, ptrs, sizes, 2, n, B, b32, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_reduce_typed(3, 0, None, ptrs, sizes, 2, n, B, b32 - 1, W, wsb, None) == cc.CCCL_ERR_CAPACITY
+    assert lib.cccl_reduce_typed(3, 1, None, bad, sizes, 2, n, B, b32, W, wsb, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_get_result(None, None, None, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_get_result(W + 4, None, None, None) == cc.CCCL_ERR_INVALID_ARG
 
