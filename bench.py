@@ -326,6 +326,48 @@ def measure_extras(cc, torch, np, xs, streams, sizes, n, flush, peak, reps: int 
                      "algorithmic_bytes": algo, "hbm_gbs": round(algo / (ms_w * 1e-3) / 1e9, 1),
                      "frac_of_measured_copy": round(algo / (ms_w * 1e-3) / 1e9 / peak, 4),
                      "ratio": round(wbytes / (2 * n), 5), "ratio_min_base": round(v1bytes / (2 * n), 5)}
+    out.update(measure_dtypes(cc, torch, np, n, timed, stream, peak))
+    return out
+
+
+def measure_dtypes(cc, torch, np, n, timed, stream, peak) -> dict:
+    """The step (2 x compress, fused sum reduce, decompress of the result) on
+    the same gradient-like recipe in fp16 and fp32 (n values per rank), each
+    op timed alone, with its algorithmic HBM bytes."""
+    import workloads
+
+    out = {}
+    for name, dtype, bits in (("fp16", cc.CCCL_DTYPE_FP16, torch.int16), ("fp32", cc.CCCL_DTYPE_FP32, torch.int32)):
+        item = 2 if dtype == cc.CCCL_DTYPE_FP16 else 4
+        xs = [torch.from_numpy(workloads.generate_typed(dtype, WORKLOAD, r).view(np.int16 if item == 2 else np.int32))
+              .cuda() for r in range(2)]
+        cap = cc.cccl_compress_bound_typed(dtype, n)
+        ss = [torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in xs]
+        ws = cc.empty_workspace(n)
+        sizes = []
+        for x, s_ in zip(xs, ss):
+            cc.cccl_compress_typed(dtype, x, s_, ws, stream=stream)
+            sizes.append(cc.cccl_get_result(ws, stream)[0])
+        ms_c = timed(lambda: cc.cccl_compress_typed(dtype, xs[0], ss[0], ws, stream=stream))
+        red = torch.empty(cap, dtype=torch.uint8, device="cuda")
+        ins = [s_[:b] for s_, b in zip(ss, sizes)]
+        ms_r = timed(lambda: cc.cccl_reduce_typed(dtype, 0, None, ins, n, red, ws, stream=stream))
+        rbytes, st_r = cc.cccl_get_result(ws, stream)
+        y = torch.empty(n, dtype=bits, device="cuda")
+        ms_d = timed(lambda: cc.cccl_decompress_typed(dtype, red[:rbytes], y, ws, stream=stream))
+        _, st_d = cc.cccl_get_result(ws, stream)
+        rows = {"compress": (ms_c, item * n + sizes[0]), "reduce": (ms_r, sum(sizes) + rbytes),
+                "decompress": (ms_d, rbytes + item * n)}
+        entry = {"workload": "gradient-like buffer, %d values per rank (%d MiB of %s), 2 ranks"
+                             % (n, item * n >> 20, name), "ratio": round(sizes[0] / (item * n), 5),
+                 "status": max(st_r, st_d), "step_ms": round(2 * ms_c + ms_r + ms_d, 5),
+                 "step_uncompressed_gbs": round(2 * item * n / ((2 * ms_c + ms_r + ms_d) * 1e-3) / 1e9, 1)}
+        for op, (ms_x, algo) in rows.items():
+            entry[op] = {"ms": round(ms_x, 5), "algorithmic_bytes": int(algo),
+                         "hbm_gbs": round(algo / (ms_x * 1e-3) / 1e9, 1),
+                         "frac_of_measured_copy": round(algo / (ms_x * 1e-3) / 1e9 / peak, 4)}
+        out["dtype_" + name] = entry
+        del xs, ss, red, y
     return out
 
 
