@@ -27,29 +27,31 @@
 
 namespace cccl {
 
-// chunks per group = compute warps: 8 for the 16-bit types, 4 for fp32 (the
-// stage of a group is 64 KiB either way)
+// chunks per group: 8 for the 16-bit types, 4 for fp32 (the stage of a group
+// is 64 KiB either way); each chunk is encoded by a pair of compute warps
 template <class D>
 __host__ __device__ constexpr int group_of() { return D::kElemBytes == 4 ? 4 : 8; }
 constexpr int kRing = 3;  // groups staged per CTA
 template <class D>
 __host__ __device__ constexpr size_t raw_chunk_of() { return (size_t)D::kElemBytes * kChunkElems; }
 template <class D>
-__host__ __device__ constexpr int compress_threads() { return 32 * (group_of<D>() + 1); }
+__host__ __device__ constexpr int compress_threads() { return 32 * (2 * group_of<D>() + 1); }
 template <class D>
 __host__ __device__ constexpr size_t compress_smem() { return (size_t)kRing * group_of<D>() * raw_chunk_of<D>(); }
 
 template <int G>
 struct CompressSmem {
-    uint64_t load[kRing][G];       // stage filled (one per compute warp)
-    uint64_t sized[kRing];         // all compute warps sized the stage's group
-    uint64_t free_[kRing];         // all compute warps wrote the stage's group out
+    uint64_t load[kRing][G];       // a chunk of the stage landed (one per pair)
+    uint64_t sized[kRing];         // every pair sized its chunk of the stage's group
+    uint64_t free_[kRing];         // every compute warp wrote its part of the stage's group
     uint64_t placed[2];            // control warp published the offsets
     uint64_t group[kRing];         // group index held by each stage (>= n_groups: none)
-    unsigned long long tally[kRing];  // sized warps (high word) and their bytes (low word)
+    unsigned long long tally[kRing];  // sized pairs (high word) and their bytes (low word)
     uint32_t size[kRing][G];
     uint64_t off[2][G];            // chunk offsets, or kFlagPoison
-    uint32_t hist[G][264];         // window-base variant: each compute warp's exponent histogram
+    PairXch xch[G];                // each pair's exchange record
+    uint32_t hist[G][264];         // window-base variant: each pair's exponent histogram
+    uint32_t below[2 * G][264];    //   and each warp's prefix counts of it
 };
 
 // Control lane: fill stage s with group g (or mark it empty).
@@ -72,13 +74,14 @@ __device__ __forceinline__ void issue_group(const uint8_t* in, const Paging& pg,
     }
 }
 
-// Compute warp, one group: size this warp's chunk of group i (into cur) and
-// then write its chunk of group i - 1 (from prev).  Returns false once the
-// groups are exhausted (after writing group i - 1).  The loop keeps one copy
-// of it: instruction-cache space, not register moves, is the scarce resource.
+// Compute warp, one group: size this warp's half of its pair's chunk of
+// group i (into cur) and then write its half of the pair's chunk of group
+// i - 1 (from prev).  Returns false once the groups are exhausted (after
+// writing group i - 1).  The loop keeps one copy of it: instruction-cache
+// space, not register moves, is the scarce resource.
 struct WarpChunk {
-    ChunkRegs regs;
-    ChunkPlan plan;
+    HalfRegs regs;
+    PairPlan plan;
     uint32_t bytes;
     uint64_t c;
 };
@@ -90,28 +93,31 @@ __device__ __forceinline__ bool compute_step(int i, const uint8_t* __restrict__ 
     constexpr int G = group_of<D>();
     constexpr size_t kRaw = raw_chunk_of<D>();
     using Elem = typename std::conditional<D::kElemBytes == 4, uint32_t, uint16_t>::type;
-    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5, ci = w >> 1, h = w & 1;
+    const PairBarrier bar{1u + ci};
     const uint64_t n_full = so.n_elems / kChunkElems;
     const uint64_t n_groups = (so.n_chunks + G - 1) / G;
     const int s = i % kRing;
-    const bool filled = __all_sync(0xFFFFFFFFu, mbar_wait(&sm.load[s][w], (uint32_t)(i / kRing) & 1u));
+    // the pair decides together: a bounded wait that ran out for either warp
+    // fails both, so their barriers stay matched
+    const bool filled = !bar.any(!mbar_wait(&sm.load[s][ci], (uint32_t)(i / kRing) & 1u));
     const uint64_t g = sm.group[s];
     const bool live = filled && g < n_groups;
     if (live) {
-        cur.c = g * G + w;
+        cur.c = g * G + ci;
         cur.bytes = 0;
         if (cur.c < n_full) {
-            const uint8_t* chunk = stage + ((size_t)s * G + w) * kRaw;
-            cur.plan = kWindow ? plan_chunk_warp_window<D>(chunk, cur.regs, sm.hist[w])
-                               : plan_chunk_warp<D>(chunk, cur.regs);
-            cur.bytes = cur.plan.bytes;
+            const uint8_t* chunk = stage + ((size_t)s * G + ci) * kRaw;
+            cur.plan = kWindow ? plan_chunk_pair_window<D>(chunk, cur.regs, h, sm.xch[ci], sm.hist[ci], sm.below[w], bar)
+                               : plan_chunk_pair<D>(chunk, cur.regs, h, sm.xch[ci], bar);
+            cur.bytes = cur.plan.p.bytes;
         } else if (cur.c < so.n_chunks) {
             cur.bytes = tail_chunk_bytes<D>((uint32_t)(so.n_elems - cur.c * kChunkElems));
         }
         __syncwarp();
-        if (lane == 0) {
-            sm.size[s][w] = cur.bytes;
-            // the last warp to size the group publishes its size at once, so
+        if (h == 0 && lane == 0) {
+            sm.size[s][ci] = cur.bytes;
+            // the last pair to size the group publishes its size at once, so
             // the look-backs of later groups need not wait for this CTA's
             // control warp
             const unsigned long long old = atomicAdd(&sm.tally[s], (1ull << 32) | cur.bytes);
@@ -119,30 +125,30 @@ __device__ __forceinline__ bool compute_step(int i, const uint8_t* __restrict__ 
                 publish_unit_size(so.status, g, (uint32_t)old + cur.bytes, data_start(so.n_chunks));
             mbar_arrive(&sm.sized[s]);
         }
-    } else if (!filled && lane == 0) {
+    } else if (!filled && h == 0 && lane == 0) {
         record_error(so.ws, kStatusTimeout);
     }
     if (i > 0) {  // write group i - 1
         const int ip = i - 1, sp = ip % kRing;
         if (__all_sync(0xFFFFFFFFu, mbar_wait(&sm.placed[ip & 1], (uint32_t)(ip >> 1) & 1u))) {
-            const uint64_t off = sm.off[ip & 1][w];
+            const uint64_t off = sm.off[ip & 1][ci];
             if (off != kFlagPoison && prev.bytes > 0) {
                 if (off + prev.bytes > so.capacity) {  // cannot happen for a correct placement
-                    if (lane == 0) record_error(so.ws, kStatusCorrupt);
+                    if (h == 0 && lane == 0) record_error(so.ws, kStatusCorrupt);
                 } else {
                     uint8_t* dst = so.out + off;
                     if (prev.c < n_full) {
-                        write_chunk_warp<D>(prev.regs, prev.plan, stage + ((size_t)sp * G + w) * kRaw, dst);
-                    } else {
+                        write_chunk_pair<D>(prev.regs, prev.plan, h, stage + ((size_t)sp * G + ci) * kRaw, dst);
+                    } else if (h == 0) {
                         // a partial chunk is never paged
                         const Elem* src = reinterpret_cast<const Elem*>(in) + prev.c * kChunkElems;
                         write_tail_chunk_warp<D>([src](uint32_t e) { return src[e]; },
                                                  (uint32_t)(so.n_elems - prev.c * kChunkElems), dst);
                     }
-                    if (lane == 0) finish_chunk(so, prev.c, off, prev.bytes);
+                    if (h == 0 && lane == 0) finish_chunk(so, prev.c, off, prev.bytes);
                 }
             }
-        } else if (lane == 0) {
+        } else if (h == 0 && lane == 0) {
             record_error(so.ws, kStatusTimeout);
         }
         __syncwarp();
@@ -155,7 +161,7 @@ template <class D, bool kWindow>
 __global__ void __launch_bounds__(compress_threads<D>(), 1)
     compress_kernel(const uint8_t* __restrict__ in, Paging pg, StreamOut so) {
     constexpr int G = group_of<D>();
-    constexpr int kCtrl = G;  // warp index of the control warp
+    constexpr int kCtrl = 2 * G;  // warp index of the control warp
     extern __shared__ __align__(128) uint8_t stage[];
     __shared__ CompressSmem<G> sm;
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -166,7 +172,7 @@ __global__ void __launch_bounds__(compress_threads<D>(), 1)
         for (int s = 0; s < kRing; ++s) {
             for (int i = 0; i < G; ++i) mbar_init(&sm.load[s][i], 1);
             mbar_init(&sm.sized[s], G);
-            mbar_init(&sm.free_[s], G);
+            mbar_init(&sm.free_[s], 2 * G);
         }
         for (int x = 0; x < 2; ++x) mbar_init(&sm.placed[x], 1);
         fence_mbar_init();

@@ -11,10 +11,10 @@
 // Element types (bf16, fp16, fp32) and their residual sections: see the
 // traits in cccl_device.cuh.
 //
-// Work split: one warp encodes one whole chunk (lane l owns the elements
-// 256 j + 8 l + s of all 16 rows j, i.e. bit-plane words 32 q + l for
-// q < 4), so a chunk needs only warp-level reductions; or a team of four warps
-// encodes a chunk it holds in registers, a quarter per warp.
+// Work split: a pair of warps encodes a chunk staged in shared memory, half
+// the rows each (lane l owns elements 256 j + 8 l + s, i.e. bit-plane words
+// 32 q + l); or a team of four warps encodes a chunk it holds in registers, a
+// quarter per warp.
 #pragma once
 
 #include <type_traits>
@@ -41,17 +41,6 @@ struct ChunkPlan {
     uint32_t base;   // header base: minimum exponent (0 when raw)
     uint32_t n_esc;  // escapes at width k
     uint32_t bytes;  // chunk size, header included
-};
-
-// One lane's share of a full chunk, kept in registers between sizing and
-// writing: the bit-planes of its four plane words.  P[8 q + p] is plane p of
-// word 32 q + l (lane l), i.e. bit p of the exponent offsets (e - base) of
-// the 32 elements that word covers: bit 8 b + m holds element 256 (4 q + m / 2)
-// + 8 l + 4 (m % 2) + b.  For fp16, planes 5..7 hold fraction bit 8, fraction
-// bit 9 and the sign (the offsets need 5 bits at most).  The rest of sign and
-// fraction stays in the staged chunk.
-struct ChunkRegs {
-    uint32_t P[32];
 };
 
 // This lane's 4 pair-words of row j (elements 256 j + 8 l .. + 7) of a 16-bit
@@ -143,92 +132,157 @@ __host__ __device__ constexpr uint32_t packed_chunk_bytes(uint32_t k, uint32_t n
     return (uint32_t)(16 + D::kResidBytes + kPlaneBytes * k + pad16(n_esc));
 }
 
+// ---------------------------------------------------------------------------
+// Pair encoding: two warps encode one chunk staged in shared memory.  Warp h
+// (0 or 1) of the pair owns plane words 32 q + l for q = 2 h, 2 h + 1 (lane
+// l): rows 8 h .. 8 h + 7, elements 8 l .. 8 l + 7 of each.  The pair meets
+// twice per chunk (exponent extremes; escape counts) at a named barrier of 64
+// threads, through an exchange record in shared memory.
+// ---------------------------------------------------------------------------
+struct PairBarrier {
+    uint32_t id;  // 1..15; barrier 0 is __syncthreads'
+    __device__ void sync() const { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+    __device__ bool any(bool p) const {
+        uint32_t r;
+        asm volatile(
+            "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, %2, 64, pi; selp.u32 %0, 1, 0, po; }"
+            : "=r"(r)
+            : "r"((uint32_t)p), "r"(id)
+            : "memory");
+        return r != 0;
+    }
+};
+
+struct PairXch {
+    uint32_t mn[2], mx[2];  // per warp: smallest and largest exponent
+    uint32_t cnt[2][8];     // per warp: escapes at width k (window variant: [h][0] at the chosen table)
+};
+
+// One warp's half of a chunk, kept in registers between sizing and writing:
+// P[8 qq + p] is plane p of word 32 (2 h + qq) + l, i.e. bit p of the
+// exponent offsets (e - base) of the 32 elements that word covers (bit
+// 8 b + m: element 256 (4 q + m / 2) + 8 l + 4 (m % 2) + b).  For fp16,
+// planes 5..7 hold fraction bit 8, fraction bit 9 and the sign.
+struct HalfRegs {
+    uint32_t P[16];
+};
+
+// Plan of one full chunk: as ChunkPlan, plus the escapes of the pair's
+// first warp at the chosen table (where the second warp's escapes start).
+struct PairPlan {
+    ChunkPlan p;
+    uint32_t esc_before;  // 0 for warp 0
+};
+
 // Phase A: exponent table and size of the full chunk staged at `chunk` (left
-// untouched), leaving the bit-planes of the exponent offsets in `r`.  One
-// warp; every lane returns the same plan.
+// untouched), leaving this warp's bit-planes of the exponent offsets in `r`.
+// Both warps of the pair return the same plan (esc_before aside).
 template <class D>
-__device__ __forceinline__ ChunkPlan plan_chunk_warp(const uint8_t* chunk, ChunkRegs& r) {
+__device__ __forceinline__ PairPlan plan_chunk_pair(const uint8_t* chunk, HalfRegs& r, uint32_t h, PairXch& x,
+                                                    const PairBarrier& bar) {
+    constexpr uint32_t kTop = D::kExpBits - 1;
     const uint32_t lane = threadIdx.x & 31;
-    // exponent quads (r.P[2 j + h]: row j, elements 4 h .. 4 h + 3 of the
-    // lane's 8) and the exponent extremes
     uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) row_exponents<D>(chunk, j, lane, r.P[2 * j], r.P[2 * j + 1], mn, mx);
-    const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
-    const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
+    for (int jj = 0; jj < 8; ++jj) row_exponents<D>(chunk, 8 * h + jj, lane, r.P[2 * jj], r.P[2 * jj + 1], mn, mx);
+    const uint32_t wmn = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
+    const uint32_t wmx = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
+    if (lane == 0) {
+        x.mn[h] = wmn;
+        x.mx[h] = wmx;
+    }
+    bar.sync();
+    const uint32_t emin = min(x.mn[0], x.mn[1]), emax = max(x.mx[0], x.mx[1]);
     const uint32_t base4 = emin * 0x01010101u;
     uint32_t cnt[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // escapes at width k
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t* P = r.P + 8 * q;
+    for (int qq = 0; qq < 2; ++qq) {
+        uint32_t* P = r.P + 8 * qq;
 #pragma unroll
         for (int m = 0; m < 8; ++m) P[m] -= base4;  // no borrow: every exponent >= emin
         transpose8x8x4(P);                          // quads of offsets -> planes
         add_escape_counts<D>(P, cnt);
     }
-    ChunkPlan pl{0u, 0u, emin, 0u, 0u};
+#pragma unroll
+    for (uint32_t k = 1; k <= kTop; ++k) {
+        const uint32_t n = __reduce_add_sync(0xFFFFFFFFu, cnt[k]);
+        if (lane == 0) x.cnt[h][k] = n;
+    }
+    bar.sync();
+    PairPlan pp{{0u, 0u, emin, 0u, 0u}, 0u};
+    ChunkPlan& pl = pp.p;
     uint32_t best = 0;
     if (emax > emin) {
-        best = 0xFFFFFFFFu;
-#pragma unroll
-        for (int k = 1; k <= (int)max_width<D>(); ++k) {
-            const uint32_t n = __reduce_add_sync(0xFFFFFFFFu, cnt[k]);
-            const uint32_t size = kPlaneBytes * k + (uint32_t)pad16(n);
-            if (size < best) {  // ascending k: a tie keeps the smaller width
-                best = size;
-                pl.k = (uint32_t)k;
-                pl.n_esc = n;
-            }
+        // lane k (1..kTop) sizes width k; the smallest (size, k) wins, so a
+        // tie keeps the smaller width
+        uint32_t n = 0, before = 0, key = 0xFFFFFFFFu;
+        if (lane >= 1 && lane <= kTop) {
+            const uint32_t c0 = x.cnt[0][lane];
+            n = c0 + x.cnt[1][lane];
+            before = h ? c0 : 0u;
+            key = ((kPlaneBytes * lane + (uint32_t)pad16(n)) << 3) | lane;
         }
+        key = __reduce_min_sync(0xFFFFFFFFu, key);
+        pl.k = key & 7u;
+        best = key >> 3;
+        pl.n_esc = __shfl_sync(0xFFFFFFFFu, n, pl.k);
+        pp.esc_before = __shfl_sync(0xFFFFFFFFu, before, pl.k);
     }
     pl.raw = best >= raw_exponent_bytes<D>() ? 1u : 0u;
     if (pl.raw) {
         pl.k = 0;
         pl.base = 0;
         pl.n_esc = 0;
+        pp.esc_before = 0;
         pl.bytes = max_chunk_bytes<D>();
     } else {
         pl.bytes = packed_chunk_bytes<D>(pl.k, pl.n_esc);
     }
-    return pl;
+    return pp;
 }
 
 // Phase A of the window-base variant (stream version 2): for every width k
 // the base is the start of the window of 2^k - 1 exponents with the fewest
 // escapes (exponents outside it, below included), ties to the smaller base;
-// then the smallest size wins, ties to the smaller k.  `hist`: this warp's
-// 257 words of shared memory.  Leaves in `r` the bit-planes of the codes,
-// escaped elements carrying all ones, which is what write_chunk_warp's
-// escape test (low_k | high_k) and plane writes expect.
+// then the smallest size wins, ties to the smaller k.  `hist`: the pair's 264
+// words of shared memory; `below`: this warp's own 264 words.  Leaves in `r`
+// the bit-planes of the codes, escaped elements carrying all ones, which is
+// what write_chunk_pair's escape test (low_k | high_k) and plane writes
+// expect.
 template <class D>
-__device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk, ChunkRegs& r, uint32_t* hist) {
+__device__ __forceinline__ PairPlan plan_chunk_pair_window(const uint8_t* chunk, HalfRegs& r, uint32_t h, PairXch& x,
+                                                           uint32_t* hist, uint32_t* below_s,
+                                                           const PairBarrier& bar) {
     constexpr uint32_t kExpMask4 = ((1u << D::kExpBits) - 1u) * 0x01010101u;  // the exponent bits of a quad
     const uint32_t lane = threadIdx.x & 31;
-    *reinterpret_cast<uint4*>(hist + 8 * lane) = make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(hist + 8 * lane + 4) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(hist + 128 * h + 4 * lane) = make_uint4(0u, 0u, 0u, 0u);  // this warp's half
     uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) row_exponents<D>(chunk, j, lane, r.P[2 * j], r.P[2 * j + 1], mn, mx);
-    const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
-    const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
-    __syncwarp();  // the histogram is cleared
-    // exponent histogram
+    for (int jj = 0; jj < 8; ++jj) row_exponents<D>(chunk, 8 * h + jj, lane, r.P[2 * jj], r.P[2 * jj + 1], mn, mx);
+    const uint32_t wmn = __reduce_min_sync(0xFFFFFFFFu, min((mn >> 8) & 0xFFu, mn >> 24));
+    const uint32_t wmx = __reduce_max_sync(0xFFFFFFFFu, max((mx >> 8) & 0xFFu, mx >> 24));
+    if (lane == 0) {
+        x.mn[h] = wmn;
+        x.mx[h] = wmx;
+    }
+    bar.sync();  // the histogram is cleared, the extremes are in
+    const uint32_t emin = min(x.mn[0], x.mn[1]), emax = max(x.mx[0], x.mx[1]);
 #pragma unroll
-    for (int m = 0; m < 32; ++m) {
+    for (int m = 0; m < 16; ++m) {
         const uint32_t q = r.P[m] & kExpMask4;
 #pragma unroll
         for (int b = 0; b < 4; ++b) atomicAdd(hist + ((q >> (8 * b)) & 0xFFu), 1u);
     }
-    __syncwarp();
+    bar.sync();  // the histogram is complete
     // below[v] = exponents smaller than v; lane l holds v = 8 l .. 8 l + 7
     const uint4 h0 = *reinterpret_cast<const uint4*>(hist + 8 * lane);
     const uint4 h1 = *reinterpret_cast<const uint4*>(hist + 8 * lane + 4);
-    const uint32_t h[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
     uint32_t below[8], run = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         below[i] = run;
-        run += h[i];
+        run += hv[i];
     }
     uint32_t incl = run;
 #pragma unroll
@@ -238,12 +292,12 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) below[i] += incl - run;
-    __syncwarp();  // every lane has read its bins
-    *reinterpret_cast<uint4*>(hist + 8 * lane) = make_uint4(below[0], below[1], below[2], below[3]);
-    *reinterpret_cast<uint4*>(hist + 8 * lane + 4) = make_uint4(below[4], below[5], below[6], below[7]);
-    if (lane == 31) hist[256] = kChunkElems;
+    *reinterpret_cast<uint4*>(below_s + 8 * lane) = make_uint4(below[0], below[1], below[2], below[3]);
+    *reinterpret_cast<uint4*>(below_s + 8 * lane + 4) = make_uint4(below[4], below[5], below[6], below[7]);
+    if (lane == 31) below_s[256] = kChunkElems;
     __syncwarp();
-    ChunkPlan pl{0u, 0u, emin, 0u, 0u};
+    PairPlan pp{{0u, 0u, emin, 0u, 0u}, 0u};
+    ChunkPlan& pl = pp.p;
     uint32_t best = 0;
     if (emax > emin) {
         // a window starting above the type's exponents escapes everything, so
@@ -256,7 +310,7 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint32_t b = 8 * lane + i, top = min(b + S, 256u);
-                const uint32_t n = below[i] + (kChunkElems - hist[top]);
+                const uint32_t n = below[i] + (kChunkElems - below_s[top]);
                 key = min(key, (n << 8) | b);
             }
             key = __reduce_min_sync(0xFFFFFFFFu, key);
@@ -275,18 +329,18 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk
         pl.base = 0;
         pl.n_esc = 0;
         pl.bytes = max_chunk_bytes<D>();
-        return pl;
+        return pp;
     }
     pl.bytes = packed_chunk_bytes<D>(pl.k, pl.n_esc);
     // (fp16 goes on at k = 0 too: its residual planes 5..7 come from the
     // transposes below; the codes, all escapes at width 0, are not written)
-    if (D::kExpBits != 5 && pl.k == 0) return pl;
+    if (D::kExpBits != 5 && pl.k == 0) return pp;
     // codes: e - base inside the window, all ones outside (an escape).
     // Byte-wise e - base with no borrow between bytes, and the bytes where
     // e < base (the borrow out of each byte).
     const uint32_t b4 = pl.base * 0x01010101u, kb = (128u - ((1u << pl.k) - 1u)) * 0x01010101u;
 #pragma unroll
-    for (int m = 0; m < 32; ++m) {
+    for (int m = 0; m < 16; ++m) {
         const uint32_t e = r.P[m] & kExpMask4;
         const uint32_t d = ((e | 0x80808080u) - (b4 & 0x7F7F7F7Fu)) ^ ((e ^ ~b4) & 0x80808080u);
         const uint32_t lt = ((~e & b4) | (~(e ^ b4) & d)) & 0x80808080u;  // e < base
@@ -296,20 +350,29 @@ __device__ __forceinline__ ChunkPlan plan_chunk_warp_window(const uint8_t* chunk
         else
             r.P[m] = d | esc;
     }
+    uint32_t mine = 0;  // this warp's escapes at the chosen table
 #pragma unroll
-    for (int q = 0; q < 4; ++q) transpose8x8x4(r.P + 8 * q);
-    return pl;
+    for (int qq = 0; qq < 2; ++qq) {
+        transpose8x8x4(r.P + 8 * qq);
+        if (pl.k > 0) mine += __popc(escape_word<D>(r.P + 8 * qq, pl.k));
+    }
+    mine = __reduce_add_sync(0xFFFFFFFFu, mine);
+    if (lane == 0) x.cnt[h][0] = mine;
+    bar.sync();
+    pp.esc_before = h ? x.cnt[0][0] : 0u;
+    return pp;
 }
 
-// The residual section of a packed full chunk staged at `chunk` (one warp):
-// the byte plane, then fp16's three bit-planes (from the lane's planes 5..7)
-// or fp32's lower halves.
+// The residual section of this warp's rows (8 h .. 8 h + 7) of a packed full
+// chunk staged at `chunk`: the byte plane, then fp16's three bit-planes (from
+// the warp's planes 5..7) or fp32's lower halves.
 template <class D>
-__device__ __forceinline__ void write_residual_warp(const ChunkRegs& r, const uint8_t* chunk, uint8_t* body) {
+__device__ __forceinline__ void write_residual_pair(const HalfRegs& r, uint32_t h, const uint8_t* chunk, uint8_t* body) {
     const uint32_t lane = threadIdx.x & 31;
-    if constexpr (D::kElemBytes == 4) {
 #pragma unroll 4
-        for (int j = 0; j < 16; ++j) {
+    for (int jj = 0; jj < 8; ++jj) {
+        const uint32_t j = 8 * h + jj;
+        if constexpr (D::kElemBytes == 4) {
             const uint8_t* row = chunk + 1024 * j + 32 * lane;
             const uint4 a = *reinterpret_cast<const uint4*>(row), b = *reinterpret_cast<const uint4*>(row + 16);
             *reinterpret_cast<uint2*>(body + 256 * j + 8 * lane) =
@@ -318,10 +381,7 @@ __device__ __forceinline__ void write_residual_warp(const ChunkRegs& r, const ui
             *reinterpret_cast<uint4*>(body + kSmPlaneBytes + 512 * j + 16 * lane) =
                 make_uint4(lower_halves(a.x, a.y), lower_halves(a.z, a.w), lower_halves(b.x, b.y),
                            lower_halves(b.z, b.w));
-        }
-    } else {
-#pragma unroll 4
-        for (int j = 0; j < 16; ++j) {
+        } else {
             const uint4 v = lds_row(chunk, j, lane);
             if constexpr (D::kExpBits == 5)
                 *reinterpret_cast<uint2*>(body + 256 * j + 8 * lane) =
@@ -330,14 +390,14 @@ __device__ __forceinline__ void write_residual_warp(const ChunkRegs& r, const ui
                 *reinterpret_cast<uint2*>(body + 256 * j + 8 * lane) =
                     make_uint2(sign_fraction_quad(v.x, v.y), sign_fraction_quad(v.z, v.w));
         }
-        if constexpr (D::kExpBits == 5) {
+    }
+    if constexpr (D::kExpBits == 5) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+        for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
-                for (int t = 0; t < 3; ++t)
-                    *reinterpret_cast<uint32_t*>(body + kSmPlaneBytes + kPlaneBytes * t + 4 * (32 * q + lane)) =
-                        r.P[8 * q + 5 + t];
-        }
+            for (int t = 0; t < 3; ++t)
+                *reinterpret_cast<uint32_t*>(body + kSmPlaneBytes + kPlaneBytes * t + 4 * (32 * (2 * h + qq) + lane)) =
+                    r.P[8 * qq + 5 + t];
     }
 }
 
@@ -350,82 +410,82 @@ __device__ __forceinline__ uint32_t staged_exponent(const uint8_t* chunk, uint32
         return (reinterpret_cast<const uint16_t*>(chunk)[i] >> (15 - D::kExpBits)) & ((1u << D::kExpBits) - 1u);
 }
 
-// Phase B: write the full chunk staged at `chunk` (unchanged since phase A)
-// with its planes `r` to `dst` (global, 16-byte aligned) following `pl`.  One
-// warp.  A raw chunk leaves by one bulk (TMA) store issued by lane 0, which
-// waits until the copy has read `chunk` before returning; the caller must
-// have ordered any generic writes of `chunk` before it with
-// fence.proxy.async.  A packed chunk is written by coalesced stores: the
-// residual section, the k planes (escaped elements carry the sentinel,
-// all k bits set), then the escape bytes in bit-plane order, read back from
-// the staged values.
+// Phase B: this warp's share of writing the full chunk staged at `chunk`
+// (unchanged since phase A) with its planes `r` to `dst` (global, 16-byte
+// aligned) following `pp`.  No barrier.  A raw chunk leaves by one bulk (TMA)
+// store issued by lane 0 of warp 0, which waits until the copy has read
+// `chunk` before returning; the caller must have ordered any generic writes of
+// `chunk` before it with fence.proxy.async.  A packed chunk is written by
+// coalesced stores: the residual section (warp h: rows 8 h .. 8 h + 7), the
+// warp's words of the k planes (escaped elements carry the sentinel, all k
+// bits set), then its escape bytes in bit-plane order, read back from the
+// staged values, starting after esc_before.
 template <class D>
-__device__ __forceinline__ void write_chunk_warp(const ChunkRegs& r, const ChunkPlan& pl, const uint8_t* chunk,
-                                                 uint8_t* dst) {
+__device__ __forceinline__ void write_chunk_pair(const HalfRegs& r, const PairPlan& pp, uint32_t h,
+                                                 const uint8_t* chunk, uint8_t* dst) {
+    const ChunkPlan& pl = pp.p;
     const uint32_t lane = threadIdx.x & 31;
     uint8_t* body = dst + kChunkHeaderBytes;
-    if (lane == 0)
+    if (h == 0 && lane == 0)
         *reinterpret_cast<uint4*>(dst) =
             make_uint4((pl.raw ? kModeRaw : kModePacked) | (pl.k << 8) | (pl.base << 16), kChunkElems | (pl.n_esc << 16),
                        pl.bytes, 0u);
     if (pl.raw) {
-        if (lane == 0) {
-            bulk_store(body, chunk, D::kElemBytes * kChunkElems);
-            bulk_commit();
-            bulk_wait_read();
+        if (h == 0) {
+            if (lane == 0) {
+                bulk_store(body, chunk, D::kElemBytes * kChunkElems);
+                bulk_commit();
+                bulk_wait_read();
+            }
+            __syncwarp();
         }
-        __syncwarp();
         return;
     }
-    write_residual_warp<D>(r, chunk, body);
+    write_residual_pair<D>(r, h, chunk, body);
     const uint32_t k = pl.k;
     if (k == 0) return;
-    uint32_t esc[4];
+    uint32_t esc[2];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t* P = r.P + 8 * q;
-        esc[q] = escape_word<D>(P, k);
-        uint8_t* col = body + D::kResidBytes + 4 * (32 * q + lane);
+    for (int qq = 0; qq < 2; ++qq) {
+        const uint32_t* P = r.P + 8 * qq;
+        esc[qq] = escape_word<D>(P, k);
+        uint8_t* col = body + D::kResidBytes + 4 * (32 * (2 * h + qq) + lane);
 #pragma unroll
         for (uint32_t p = 0; p < max_width<D>(); ++p)
-            if (p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = P[p] | esc[q];
+            if (p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = P[p] | esc[qq];
     }
     const uint32_t n_esc = pl.n_esc;
     if (n_esc == 0) return;
-    // escapes before word (q, lane): all of quarters < q, then lanes < lane of
-    // quarter q (16-bit fields: at most 1024 per quarter)
-    const uint32_t c01 = __popc(esc[0]) | (__popc(esc[1]) << 16), c23 = __popc(esc[2]) | (__popc(esc[3]) << 16);
-    uint32_t a = c01, b = c23;
+    // escapes before word (q, lane): the first warp's (esc_before), then all
+    // of this warp's first quarter, then lanes < lane of quarter q (16-bit
+    // fields: at most 1024 per quarter)
+    const uint32_t c01 = __popc(esc[0]) | (__popc(esc[1]) << 16);
+    uint32_t a = c01;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t ta = __shfl_up_sync(0xFFFFFFFFu, a, d), tb = __shfl_up_sync(0xFFFFFFFFu, b, d);
-        if (lane >= (uint32_t)d) {
-            a += ta;
-            b += tb;
-        }
+        const uint32_t ta = __shfl_up_sync(0xFFFFFFFFu, a, d);
+        if (lane >= (uint32_t)d) a += ta;
     }
-    const uint32_t ta = __shfl_sync(0xFFFFFFFFu, a, 31), tb = __shfl_sync(0xFFFFFFFFu, b, 31);
-    const uint32_t t0 = ta & 0xFFFFu, t1 = ta >> 16, t2 = tb & 0xFFFFu;
-    const uint32_t ea = a - c01, eb = b - c23;  // exclusive over lanes
-    const uint32_t first[4] = {ea & 0xFFFFu, t0 + (ea >> 16), t0 + t1 + (eb & 0xFFFFu), t0 + t1 + t2 + (eb >> 16)};
+    const uint32_t t0 = __shfl_sync(0xFFFFFFFFu, a, 31) & 0xFFFFu;
+    const uint32_t ea = a - c01;  // exclusive over lanes
+    uint32_t idx[2] = {pp.esc_before + (ea & 0xFFFFu), pp.esc_before + t0 + (ea >> 16)};
     uint8_t* esc_out = body + D::kResidBytes + kPlaneBytes * k;
-    // one escape of every quarter per step: four independent load -> store
+    // one escape of each quarter per step: two independent load -> store
     // chains in flight per lane
-    uint32_t idx[4] = {first[0], first[1], first[2], first[3]};
-    while (__any_sync(0xFFFFFFFFu, (esc[0] | esc[1] | esc[2] | esc[3]) != 0u)) {
+    while (__any_sync(0xFFFFFFFFu, (esc[0] | esc[1]) != 0u)) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (esc[q]) {
-                const uint32_t bit = __ffs(esc[q]) - 1;
-                esc[q] &= esc[q] - 1;
-                const uint32_t m = bit & 7, bb = bit >> 3;
+        for (int qq = 0; qq < 2; ++qq) {
+            if (esc[qq]) {
+                const uint32_t bit = __ffs(esc[qq]) - 1;
+                esc[qq] &= esc[qq] - 1;
+                const uint32_t m = bit & 7, bb = bit >> 3, q = 2 * h + qq;
                 const uint32_t i = 256 * (4 * q + (m >> 1)) + 8 * lane + 4 * (m & 1) + bb;
-                if (idx[q] < n_esc) esc_out[idx[q]] = (uint8_t)staged_exponent<D>(chunk, i);
-                ++idx[q];
+                if (idx[qq] < n_esc) esc_out[idx[qq]] = (uint8_t)staged_exponent<D>(chunk, i);
+                ++idx[qq];
             }
         }
     }
-    if (lane < 16 && n_esc + lane < pad16(n_esc)) esc_out[n_esc + lane] = 0;
+    if (h == 1 && lane < 16 && n_esc + lane < pad16(n_esc)) esc_out[n_esc + lane] = 0;
 }
 
 // ---------------------------------------------------------------------------

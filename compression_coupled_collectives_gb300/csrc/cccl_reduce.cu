@@ -11,16 +11,16 @@
 //                        a quarter per warp, keeping 32 binary32 sums per
 //                        thread in registers; rounds once to bf16 and keeps
 //                        the chunk in registers; sizes it (the team meets
-//                        twice); then writes its chunk of the PREVIOUS group,
-//                        whose state waited in shared memory while the
-//                        placer placed it;
+//                        twice); then writes its chunk of the group two
+//                        iterations back (one for fp32), whose state waited
+//                        in shared memory while the placer placed it;
 //   loader (warp 12)     takes a ticket per group, locates every rank's
 //                        chunks through their offset tables and streams them
 //                        to the teams through one ring of staged rank chunks
 //                        per team, by bulk (TMA) copies;
 //   placer (warp 13)     places each sized group with one decoupled look-back.
-// So the look-back of group i overlaps the decode of group i + 1, and the
-// copies of later rank chunks are in flight during both.  The output chunk
+// So the look-back of group i overlaps the decode of groups i + 1 and i + 2,
+// and the copies of later rank chunks are in flight meanwhile.  The output chunk
 // never goes through shared memory.
 // Tickets hand out groups in order to CTAs that are already running, and a
 // group is sized without waiting on any later group: every look-back ends.
@@ -47,8 +47,20 @@ template <class D>
 __host__ __device__ constexpr int prev_words() { return thread_words<D>() + 8; }
 template <class D>
 __host__ __device__ constexpr size_t ring_bytes() { return (size_t)kTeams * rslots<D>() * max_chunk_bytes<D>(); }
+// sized chunks a team keeps in shared memory while the placer places them:
+// a team writes group i - pend_depth at iteration i, so the look-back of a
+// group overlaps the decoding of the next pend_depth groups (2 for the 16-bit
+// types; 1 for fp32, whose chunk state fills the space)
 template <class D>
-__host__ __device__ constexpr size_t reduce_smem() { return ring_bytes<D>() + (size_t)kTeams * prev_words<D>() * kTeamThreads * 4; }
+__host__ __device__ constexpr int pend_depth() { return D::kElemBytes == 4 ? 1 : 2; }
+// placement buffers (sizes -> offsets), cycled by group: one more than the depth
+template <class D>
+__host__ __device__ constexpr int place_bufs() { return pend_depth<D>() + 1; }
+constexpr int kMaxPlaceBufs = 3;
+template <class D>
+__host__ __device__ constexpr size_t reduce_smem() {
+    return ring_bytes<D>() + (size_t)kTeams * pend_depth<D>() * prev_words<D>() * kTeamThreads * 4;
+}
 
 // binary32 pair -> bf16 pair, round to nearest even (hi lane from the upper word)
 __device__ __forceinline__ uint32_t round_pair_bf16(uint64_t v) {
@@ -130,15 +142,18 @@ struct ReduceMeta {
 struct ReduceSmem {
     uint64_t meta_ready[2];              // loader -> teams: meta[b] describes the next group (1 arrival)
     uint64_t decoded[2];                 // teams -> loader: meta[b] read (one arrival per team warp)
-    uint64_t sized[2];                   // teams -> placer: sizes in size[b] (one arrival per team)
-    uint64_t placed[2];                  // placer -> teams: offsets in off[b] (1 arrival)
+    uint64_t sized[kMaxPlaceBufs];       // teams -> placer: sizes in size[p] (one arrival per team)
+    uint64_t placed[kMaxPlaceBufs];      // placer -> teams: offsets in off[p] (1 arrival)
     uint64_t full[kTeams][4];            // a rank chunk landed in the slot (transaction count)
     uint64_t free_[kTeams][4];           // the team is done with the slot (1 arrival)
-    unsigned long long tally[2];         // sized teams (high word) and their bytes (low word)
-    uint32_t size[2][kTeams];
-    uint32_t failed[2][kTeams];          // the team's chunk could not be reduced
-    uint64_t gid[2];                     // group sized in slot b, or kNoGroup
-    uint64_t off[2][kTeams];             // chunk offsets, or kFlagPoison
+    unsigned long long tally[kMaxPlaceBufs];  // sized teams (high word) and their bytes (low word)
+    uint32_t size[kMaxPlaceBufs][kTeams];
+    uint32_t failed[kMaxPlaceBufs][kTeams];   // the team's chunk could not be reduced
+    uint64_t gid[kMaxPlaceBufs];         // group sized in buffer p, or kNoGroup
+    uint64_t off[kMaxPlaceBufs][kTeams];      // chunk offsets, or kFlagPoison
+    TeamPlan pend_pl[kTeams][2][4];      // a pending chunk's plan, per team, slot and warp
+    uint64_t pend_c[kTeams][2];          //   its chunk index
+    uint32_t pend_bytes[kTeams][2];      //   and size (0: nothing to write)
     uint32_t row_tot[kTeams][4];         // the decoder's per-quarter escape totals
     TeamXch xch[kTeams];                 // the encoder's exchange space
     volatile uint32_t abort;             // a bounded wait ran out: every role stops
@@ -240,11 +255,13 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
 }
 
 // --------------------------------------------------------------------------- placer
+template <class D>
 __device__ __forceinline__ void reduce_placer(const StreamOut& so, ReduceSmem& sm) {
+    constexpr int kPB = place_bufs<D>();
     const uint32_t lane = threadIdx.x & 31;
     for (int i = 0; !warp_any(sm.abort); ++i) {
-        const int b = i & 1;
-        if (!warp_wait(&sm.sized[b], (uint32_t)(i >> 1) & 1u)) {
+        const int b = i % kPB;
+        if (!warp_wait(&sm.sized[b], (uint32_t)(i / kPB) & 1u)) {
             if (lane == 0) set_abort(so, sm);
             break;
         }
@@ -267,7 +284,7 @@ __device__ __forceinline__ void reduce_placer(const StreamOut& so, ReduceSmem& s
             go = lookback_offset_wide(so.status, g, total, data_start(so.n_chunks), so.ws, true);
         }
         if (lane < (uint32_t)kTeams) sm.off[b][lane] = go == kFlagPoison ? kFlagPoison : go + (incl - mine);
-        if (lane == 0) sm.tally[b] = 0;  // next used for group i + 2, after its writers saw placed[b]
+        if (lane == 0) sm.tally[b] = 0;  // next used for group i + kPB, sized after group i is written
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.placed[b]);
     }
@@ -368,24 +385,63 @@ __device__ __forceinline__ void finish_values(const Barrier& bar, const uint64_t
     }
 }
 
+// Write this team's pending chunk of group j (sized pend_depth iterations
+// earlier) once the placer has placed group j.  `st`: the chunk's state slot.
+template <class D>
+__device__ __forceinline__ void write_pending(const StreamOut& so, ReduceSmem& sm, int j, uint32_t* st) {
+    constexpr int kW = thread_words<D>();
+    constexpr int kPB = place_bufs<D>();
+    const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127, wq = tt >> 5;
+    const int slot = j % pend_depth<D>();
+    const uint32_t bytes = sm.pend_bytes[team][slot];
+    if (bytes == 0) return;
+    const int pb = j % kPB;
+    if (!warp_wait(&sm.placed[pb], (uint32_t)(j / kPB) & 1u)) {
+        if (lane == 0) set_abort(so, sm);
+        return;
+    }
+    const uint64_t off = sm.off[pb][team];
+    if (off == kFlagPoison) return;
+    if (off + bytes > so.capacity) {  // cannot happen for a correct placement
+        if (tt == 0) record_error(so.ws, kStatusCorrupt);
+        return;
+    }
+    const uint64_t c = sm.pend_c[team][slot];
+    const uint64_t n_full = so.n_elems / kChunkElems;
+    uint32_t Pp[kW], Qp[8];
+#pragma unroll
+    for (int x = 0; x < kW; ++x) Pp[x] = st[kTeamThreads * x];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) Qp[x] = st[kTeamThreads * (kW + x)];
+    uint8_t* dst = so.out + off;
+    if (c < n_full)
+        write_chunk_team<D>(Pp, Qp, sm.pend_pl[team][slot][wq], dst, st);
+    else
+        write_tail_chunk_team<D>(Pp, (uint32_t)(so.n_elems - c * kChunkElems), dst);
+    if (tt == 0) finish_chunk(so, c, off, bytes);
+}
+
 template <class D>
 __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t op, const StreamOut& so,
                                             uint8_t* ring_base, uint32_t* prev_base, ReduceSmem& sm) {
     constexpr int kRSlots = rslots<D>();
     constexpr int kW = thread_words<D>();
     constexpr int kPrevWords = prev_words<D>();
+    constexpr int kPend = pend_depth<D>();
+    constexpr int kPB = place_bufs<D>();
     constexpr uint32_t kSlotBytes = max_chunk_bytes<D>();
-    const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127;
+    const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127, wq = tt >> 5;
     const TeamBarrier bar{1u + team};
     uint8_t* ring = ring_base + (size_t)team * kRSlots * kSlotBytes;
-    uint32_t* prev_st = prev_base + (size_t)team * kPrevWords * kTeamThreads + tt;  // word w at prev_st[128 w]
+    // pending chunk slot s of this team: word w at st(s)[128 w]
+    auto st_of = [&](int s) { return prev_base + ((size_t)team * kPend + s) * kPrevWords * kTeamThreads + tt; };
     const uint64_t n_full = so.n_elems / kChunkElems;
+    if (tt == 0)
+        for (int s = 0; s < kPend; ++s) sm.pend_bytes[team][s] = 0;
+    bar.sync();
     uint32_t u = 0;  // rank chunks consumed (the loader's order for this team)
-    TeamPlan prev_pl{};
-    uint64_t prev_c = 0;
-    uint32_t prev_bytes = 0;  // 0: no previous chunk to write
     for (int i = 0;; ++i) {
-        const int b = i & 1;
+        const int b = i & 1, pb = i % kPB;
         const bool ready = mbar_wait(&sm.meta_ready[b], (uint32_t)(i >> 1) & 1u);
         if (bar.any(!ready || sm.abort)) {
             if (tt == 0) set_abort(so, sm);
@@ -460,61 +516,48 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
                 }
             }
             if (tt == 0) {
-                sm.size[b][team] = bytes;
-                sm.failed[b][team] = fail;
-                if (team == 0) sm.gid[b] = g;
+                sm.size[pb][team] = bytes;
+                sm.failed[pb][team] = fail;
+                if (team == 0) sm.gid[pb] = g;
                 if (fail) {
                     record_error(so.ws, fail);
                 } else {
                     // the last team to size the group publishes its size at once,
                     // so later groups' look-backs need not wait for the placer
-                    const unsigned long long old = atomicAdd(&sm.tally[b], (1ull << 32) | bytes);
+                    const unsigned long long old = atomicAdd(&sm.tally[pb], (1ull << 32) | bytes);
                     if ((old >> 32) == kTeams - 1)
                         publish_unit_size(so.status, g, (uint32_t)old + bytes, data_start(so.n_chunks));
                 }
-                mbar_arrive(&sm.sized[b]);
+                mbar_arrive(&sm.sized[pb]);
             }
         } else if (tt == 0) {
-            if (team == 0) sm.gid[b] = kNoGroup;
-            mbar_arrive(&sm.sized[b]);
+            if (team == 0) sm.gid[pb] = kNoGroup;
+            mbar_arrive(&sm.sized[pb]);
         }
-        // write this team's chunk of the previous group
-        if (i > 0 && prev_bytes > 0) {
-            const int pb = b ^ 1;
-            if (warp_wait(&sm.placed[pb], (uint32_t)((i - 1) >> 1) & 1u)) {
-                const uint64_t off = sm.off[pb][team];
-                if (off != kFlagPoison) {
-                    if (off + prev_bytes > so.capacity) {  // cannot happen for a correct placement
-                        if (tt == 0) record_error(so.ws, kStatusCorrupt);
-                    } else {
-                        uint32_t Pp[kW], Qp[8];
-#pragma unroll
-                        for (int x = 0; x < kW; ++x) Pp[x] = prev_st[kTeamThreads * x];
-#pragma unroll
-                        for (int x = 0; x < 8; ++x) Qp[x] = prev_st[kTeamThreads * (kW + x)];
-                        uint8_t* dst = so.out + off;
-                        if (prev_c < n_full)
-                            write_chunk_team<D>(Pp, Qp, prev_pl, dst, prev_st);
-                        else
-                            write_tail_chunk_team<D>(Pp, (uint32_t)(so.n_elems - prev_c * kChunkElems), dst);
-                        if (tt == 0) finish_chunk(so, prev_c, off, prev_bytes);
-                    }
-                }
-            } else if (lane == 0) {
-                set_abort(so, sm);
-            }
+        // write this team's chunk of group i - kPend; at the end, every
+        // chunk still pending
+        if (i >= kPend) write_pending<D>(so, sm, i - kPend, st_of((i - kPend) % kPend));
+        if (g == kNoGroup) {
+            for (int j = i - kPend + 1; j < i; ++j)
+                if (j >= 0) write_pending<D>(so, sm, j, st_of(j % kPend));
+            return;
         }
-        if (g == kNoGroup) return;
         // this chunk waits in shared memory for its placement
-        prev_bytes = fail ? 0u : bytes;
-        if (prev_bytes > 0) {
+        const int slot = i % kPend;
+        uint32_t* st = st_of(slot);
+        const uint32_t keep = fail ? 0u : bytes;
+        if (keep > 0) {
 #pragma unroll
-            for (int x = 0; x < kW; ++x) prev_st[kTeamThreads * x] = P[x];
+            for (int x = 0; x < kW; ++x) st[kTeamThreads * x] = P[x];
 #pragma unroll
-            for (int x = 0; x < 8; ++x) prev_st[kTeamThreads * (kW + x)] = planes[x];
-            prev_pl = pl;
-            prev_c = c;
+            for (int x = 0; x < 8; ++x) st[kTeamThreads * (kW + x)] = planes[x];
         }
+        if (lane == 0) sm.pend_pl[team][slot][wq] = pl;
+        if (tt == 0) {
+            sm.pend_c[team][slot] = c;
+            sm.pend_bytes[team][slot] = keep;
+        }
+        // (the next iteration's team barrier orders these writes before any read)
     }
 }
 
@@ -529,6 +572,8 @@ __global__ void __launch_bounds__(kReduceThreads, 1) reduce_kernel(ReduceInputs 
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.meta_ready[b], 1);
             mbar_init(&sm.decoded[b], 4 * kTeams);
+        }
+        for (int b = 0; b < place_bufs<D>(); ++b) {
             mbar_init(&sm.sized[b], kTeams);
             mbar_init(&sm.placed[b], 1);
             sm.tally[b] = 0;
@@ -545,7 +590,7 @@ __global__ void __launch_bounds__(kReduceThreads, 1) reduce_kernel(ReduceInputs 
     if (w == kLoaderWarp)
         reduce_loader<D>(inputs, R, so, ring, sm);
     else if (w == kPlacerWarp)
-        reduce_placer(so, sm);
+        reduce_placer<D>(so, sm);
     else
         reduce_team<D>(R, inputs.local, inputs.op, so, ring, prev, sm);
 }
