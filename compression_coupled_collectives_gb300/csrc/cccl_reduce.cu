@@ -32,11 +32,19 @@
 
 namespace cccl {
 
-constexpr int kTeams = 3;                     // output chunks per group
+constexpr int kMaxTeams = 4;
 constexpr int kTeamThreads = 128;
-constexpr int kLoaderWarp = 4 * kTeams;
-constexpr int kPlacerWarp = kLoaderWarp + 1;
-constexpr int kReduceThreads = 32 * (kPlacerWarp + 1);
+// decode teams per CTA = output chunks per group: 3, whose 14 warps leave
+// 128 registers per thread (a fourth team would leave 96, and the team code
+// spills there)
+template <class D>
+__host__ __device__ constexpr int teams() { return 3; }
+template <class D>
+__host__ __device__ constexpr int loader_warp() { return 4 * teams<D>(); }
+template <class D>
+__host__ __device__ constexpr int placer_warp() { return loader_warp<D>() + 1; }
+template <class D>
+__host__ __device__ constexpr int reduce_threads() { return 32 * (placer_warp<D>() + 1); }
 constexpr uint64_t kNoGroup = ~0ull;
 // staged rank chunks per team: 4 of 8.2 KB for the 16-bit types, 3 of 16.4 KB
 // for fp32
@@ -46,20 +54,25 @@ __host__ __device__ constexpr int rslots() { return D::kElemBytes == 4 ? 3 : 4; 
 template <class D>
 __host__ __device__ constexpr int prev_words() { return thread_words<D>() + 8; }
 template <class D>
-__host__ __device__ constexpr size_t ring_bytes() { return (size_t)kTeams * rslots<D>() * max_chunk_bytes<D>(); }
+__host__ __device__ constexpr size_t ring_bytes() { return (size_t)teams<D>() * rslots<D>() * max_chunk_bytes<D>(); }
 // sized chunks a team keeps in shared memory while the placer places them:
 // a team writes group i - pend_depth at iteration i, so the look-back of a
-// group overlaps the decoding of the next pend_depth groups (2 for the 16-bit
-// types; 1 for fp32, whose chunk state fills the space)
+// group overlaps the decoding of the next group
 template <class D>
-__host__ __device__ constexpr int pend_depth() { return D::kElemBytes == 4 ? 1 : 2; }
+__host__ __device__ constexpr int pend_depth() { return 1; }
 // placement buffers (sizes -> offsets), cycled by group: one more than the depth
 template <class D>
 __host__ __device__ constexpr int place_bufs() { return pend_depth<D>() + 1; }
 constexpr int kMaxPlaceBufs = 3;
+// chunk-state slots per team.  The 16-bit types keep one more than the
+// pending chunks: the chunk just sized is saved before a pending one is
+// written, so their states never share registers.  fp32, short of shared
+// memory, writes the pending chunk first and then saves into its slot.
+template <class D>
+__host__ __device__ constexpr int state_slots() { return D::kElemBytes == 4 ? pend_depth<D>() : pend_depth<D>() + 1; }
 template <class D>
 __host__ __device__ constexpr size_t reduce_smem() {
-    return ring_bytes<D>() + (size_t)kTeams * pend_depth<D>() * prev_words<D>() * kTeamThreads * 4;
+    return ring_bytes<D>() + (size_t)teams<D>() * state_slots<D>() * prev_words<D>() * kTeamThreads * 4;
 }
 
 // binary32 pair -> bf16 pair, round to nearest even (hi lane from the upper word)
@@ -135,8 +148,8 @@ struct ReduceMeta {
     uint64_t g;                          // group index, or kNoGroup: no more groups
     uint32_t ok;                         // every (chunk, rank) was located
     uint32_t n_out;                      // output chunks in the group
-    uint64_t off[kTeams][kMaxRanks];     // rank r's chunk kTeams g + t: offset in its stream
-    uint32_t bytes[kTeams][kMaxRanks];   //   and size
+    uint64_t off[kMaxTeams][kMaxRanks];  // rank r's chunk teams * g + t: offset in its stream
+    uint32_t bytes[kMaxTeams][kMaxRanks];  //   and size
 };
 
 struct ReduceSmem {
@@ -144,18 +157,18 @@ struct ReduceSmem {
     uint64_t decoded[2];                 // teams -> loader: meta[b] read (one arrival per team warp)
     uint64_t sized[kMaxPlaceBufs];       // teams -> placer: sizes in size[p] (one arrival per team)
     uint64_t placed[kMaxPlaceBufs];      // placer -> teams: offsets in off[p] (1 arrival)
-    uint64_t full[kTeams][4];            // a rank chunk landed in the slot (transaction count)
-    uint64_t free_[kTeams][4];           // the team is done with the slot (1 arrival)
+    uint64_t full[kMaxTeams][4];            // a rank chunk landed in the slot (transaction count)
+    uint64_t free_[kMaxTeams][4];           // the team is done with the slot (1 arrival)
     unsigned long long tally[kMaxPlaceBufs];  // sized teams (high word) and their bytes (low word)
-    uint32_t size[kMaxPlaceBufs][kTeams];
-    uint32_t failed[kMaxPlaceBufs][kTeams];   // the team's chunk could not be reduced
+    uint32_t size[kMaxPlaceBufs][kMaxTeams];
+    uint32_t failed[kMaxPlaceBufs][kMaxTeams];   // the team's chunk could not be reduced
     uint64_t gid[kMaxPlaceBufs];         // group sized in buffer p, or kNoGroup
-    uint64_t off[kMaxPlaceBufs][kTeams];      // chunk offsets, or kFlagPoison
-    TeamPlan pend_pl[kTeams][2][4];      // a pending chunk's plan, per team, slot and warp
-    uint64_t pend_c[kTeams][2];          //   its chunk index
-    uint32_t pend_bytes[kTeams][2];      //   and size (0: nothing to write)
-    uint32_t row_tot[kTeams][4];         // the decoder's per-quarter escape totals
-    TeamXch xch[kTeams];                 // the encoder's exchange space
+    uint64_t off[kMaxPlaceBufs][kMaxTeams];      // chunk offsets, or kFlagPoison
+    TeamPlan pend_pl[kMaxTeams][3][4];   // a pending chunk's plan, per team, slot and warp
+    uint64_t pend_c[kMaxTeams][3];       //   its chunk index
+    uint32_t pend_bytes[kMaxTeams][3];   //   and size (0: nothing to write)
+    uint32_t row_tot[kMaxTeams][4];         // the decoder's per-quarter escape totals
+    TeamXch xch[kMaxTeams];                 // the encoder's exchange space
     volatile uint32_t abort;             // a bounded wait ran out: every role stops
     ReduceMeta meta[2];
 };
@@ -170,6 +183,7 @@ template <class D>
 __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R, const StreamOut& so, uint8_t* ring,
                                               ReduceSmem& sm) {
     constexpr int kRSlots = rslots<D>();
+    constexpr int kTeams = teams<D>();
     constexpr uint32_t kRawBytes = D::kElemBytes * kChunkElems;
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t n_groups = (so.n_chunks + kTeams - 1) / kTeams;
@@ -258,6 +272,7 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
 template <class D>
 __device__ __forceinline__ void reduce_placer(const StreamOut& so, ReduceSmem& sm) {
     constexpr int kPB = place_bufs<D>();
+    constexpr int kTeams = teams<D>();
     const uint32_t lane = threadIdx.x & 31;
     for (int i = 0; !warp_any(sm.abort); ++i) {
         const int b = i % kPB;
@@ -392,7 +407,7 @@ __device__ __forceinline__ void write_pending(const StreamOut& so, ReduceSmem& s
     constexpr int kW = thread_words<D>();
     constexpr int kPB = place_bufs<D>();
     const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127, wq = tt >> 5;
-    const int slot = j % pend_depth<D>();
+    const int slot = j % state_slots<D>();
     const uint32_t bytes = sm.pend_bytes[team][slot];
     if (bytes == 0) return;
     const int pb = j % kPB;
@@ -428,16 +443,18 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
     constexpr int kW = thread_words<D>();
     constexpr int kPrevWords = prev_words<D>();
     constexpr int kPend = pend_depth<D>();
+    constexpr int kSlots = state_slots<D>();
     constexpr int kPB = place_bufs<D>();
     constexpr uint32_t kSlotBytes = max_chunk_bytes<D>();
+    constexpr int kTeams = teams<D>();
     const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127, wq = tt >> 5;
     const TeamBarrier bar{1u + team};
     uint8_t* ring = ring_base + (size_t)team * kRSlots * kSlotBytes;
     // pending chunk slot s of this team: word w at st(s)[128 w]
-    auto st_of = [&](int s) { return prev_base + ((size_t)team * kPend + s) * kPrevWords * kTeamThreads + tt; };
+    auto st_of = [&](int s) { return prev_base + ((size_t)team * kSlots + s) * kPrevWords * kTeamThreads + tt; };
     const uint64_t n_full = so.n_elems / kChunkElems;
     if (tt == 0)
-        for (int s = 0; s < kPend; ++s) sm.pend_bytes[team][s] = 0;
+        for (int s = 0; s < kSlots; ++s) sm.pend_bytes[team][s] = 0;
     bar.sync();
     uint32_t u = 0;  // rank chunks consumed (the loader's order for this team)
     for (int i = 0;; ++i) {
@@ -534,35 +551,39 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
             if (team == 0) sm.gid[pb] = kNoGroup;
             mbar_arrive(&sm.sized[pb]);
         }
-        // write this team's chunk of group i - kPend; at the end, every
-        // chunk still pending
-        if (i >= kPend) write_pending<D>(so, sm, i - kPend, st_of((i - kPend) % kPend));
+        // this chunk waits in shared memory for its placement; the chunk of
+        // group i - kPend is written (at the end, every chunk still pending)
+        auto save = [&]() {
+            const int slot = i % kSlots;
+            uint32_t* st = st_of(slot);
+            const uint32_t keep = fail ? 0u : bytes;
+            if (keep > 0) {
+#pragma unroll
+                for (int x = 0; x < kW; ++x) st[kTeamThreads * x] = P[x];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) st[kTeamThreads * (kW + x)] = planes[x];
+            }
+            if (lane == 0) sm.pend_pl[team][slot][wq] = pl;
+            if (tt == 0) {
+                sm.pend_c[team][slot] = c;
+                sm.pend_bytes[team][slot] = keep;
+            }
+        };
+        if (kSlots > kPend && g != kNoGroup) save();
+        if (i >= kPend) write_pending<D>(so, sm, i - kPend, st_of((i - kPend) % kSlots));
         if (g == kNoGroup) {
             for (int j = i - kPend + 1; j < i; ++j)
-                if (j >= 0) write_pending<D>(so, sm, j, st_of(j % kPend));
+                if (j >= 0) write_pending<D>(so, sm, j, st_of(j % kSlots));
             return;
         }
-        // this chunk waits in shared memory for its placement
-        const int slot = i % kPend;
-        uint32_t* st = st_of(slot);
-        const uint32_t keep = fail ? 0u : bytes;
-        if (keep > 0) {
-#pragma unroll
-            for (int x = 0; x < kW; ++x) st[kTeamThreads * x] = P[x];
-#pragma unroll
-            for (int x = 0; x < 8; ++x) st[kTeamThreads * (kW + x)] = planes[x];
-        }
-        if (lane == 0) sm.pend_pl[team][slot][wq] = pl;
-        if (tt == 0) {
-            sm.pend_c[team][slot] = c;
-            sm.pend_bytes[team][slot] = keep;
-        }
+        if (kSlots == kPend) save();
         // (the next iteration's team barrier orders these writes before any read)
     }
 }
 
 template <class D>
-__global__ void __launch_bounds__(kReduceThreads, 1) reduce_kernel(ReduceInputs inputs, int R, StreamOut so) {
+__global__ void __launch_bounds__(reduce_threads<D>(), 1) reduce_kernel(ReduceInputs inputs, int R, StreamOut so) {
+    constexpr int kTeams = teams<D>();
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ ReduceSmem sm;
     uint8_t* ring = smem;
@@ -587,9 +608,9 @@ __global__ void __launch_bounds__(kReduceThreads, 1) reduce_kernel(ReduceInputs 
         fence_mbar_init();
     }
     __syncthreads();
-    if (w == kLoaderWarp)
+    if (w == loader_warp<D>())
         reduce_loader<D>(inputs, R, so, ring, sm);
-    else if (w == kPlacerWarp)
+    else if (w == placer_warp<D>())
         reduce_placer<D>(so, sm);
     else
         reduce_team<D>(R, inputs.local, inputs.op, so, ring, prev, sm);
@@ -618,9 +639,9 @@ cudaError_t launch_reduce_t(const ReduceInputs& inputs, int R, uint64_t n_elems,
     so.n_chunks = (n_elems + kChunkElems - 1) / kChunkElems;
     so.version = kVersion;
     so.dtype = D::kCode;
-    const uint64_t n_groups = (so.n_chunks + kTeams - 1) / kTeams;
+    const uint64_t n_groups = (so.n_chunks + teams<D>() - 1) / teams<D>();
     const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
-    reduce_kernel<D><<<grid, kReduceThreads, reduce_smem<D>(), stream>>>(inputs, R, so);
+    reduce_kernel<D><<<grid, reduce_threads<D>(), reduce_smem<D>(), stream>>>(inputs, R, so);
     return cudaGetLastError();
 }
 
