@@ -512,3 +512,48 @@ def test_argument_errors(cc):
     cc.cccl_compress(x, out, ws)
     nbytes, st = cc.cccl_get_result(ws)
     assert st == 0 and nbytes > 0
+
+
+# ---------------------------------------------------------------- CUDA graphs
+def test_step_captured_in_a_cuda_graph(cc, orc, wl):
+    """The C ABI calls only enqueue work on the given stream (no host sync, no
+    allocation), so a whole step (two compressions, the fused reduce and the
+    decompression, each with its workspace clear) can be captured in a CUDA
+    graph and replayed; every replay reproduces the oracle's streams."""
+    n = 23 * CHUNK + 5
+    xs_host = [wl.generate(2, r, count=n, n=1 << 20) for r in range(2)]
+    xs = [dev(x) for x in xs_host]
+    outs = [cc.empty_stream(n) for _ in xs]
+    red = cc.empty_stream(n)
+    y = torch.empty(n, dtype=torch.int16, device="cuda")
+    wss = [cc.empty_workspace(n) for _ in range(4)]
+    sizes = []
+    for x, o, w in zip(xs, outs, wss):  # a first, uncaptured call of each entry point
+        cc.cccl_compress(x, o, w)
+        sizes.append(cc.cccl_get_result(w)[0])
+    cc.cccl_reduce_compressed(outs, n, red, wss[2])
+    cc.cccl_get_result(wss[2])
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=side):
+        s = torch.cuda.current_stream()
+        for x, o, w in zip(xs, outs, wss):
+            cc.cccl_compress(x, o, w, stream=s)
+        cc.cccl_reduce_compressed(outs, n, red, wss[2], stream=s)
+        cc.cccl_decompress(red, y, wss[3], stream=s)
+    refs = [orc.compress(x) for x in xs_host]
+    want_red = orc.reduce(refs, n)
+    for rep in range(3):
+        for o in outs:
+            o.zero_()
+        red.zero_()
+        y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for o, w, ref in zip(outs, wss, refs):
+            nb, st = cc.cccl_get_result(w)
+            assert st == 0 and np.array_equal(o[:nb].cpu().numpy(), ref), rep
+        nb, st = cc.cccl_get_result(wss[2])
+        assert st == 0 and np.array_equal(red[:nb].cpu().numpy(), want_red), rep
+        assert np.array_equal(host_u16(y), orc.decompress(want_red, n)), rep
