@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import platform
 import json
 import os
 import statistics
@@ -176,6 +177,61 @@ def oracle_step_seconds(xs, chunks: int) -> tuple[float, int]:
     return time.perf_counter() - t, n
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, else implementer/part)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model", "Hardware"):
+        for line in text.splitlines():
+            if line.split(":")[0].strip() == key:
+                return line.split(":", 1)[1].strip()
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line:
+            k, v = (t.strip() for t in line.split(":", 1))
+            fields.setdefault(k, v)
+    return "%s CPU implementer %s part %s" % (platform.machine(), fields.get("CPU implementer", "?"),
+                                              fields.get("CPU part", "?"))
+
+
+def cpu_baseline_all_cores(xs, budget_s: float = 6.0) -> dict:
+    """The oracle, as it stands, on every host core at once: each thread runs
+    the step on its own slice of chunks (the oracle is single-threaded C; the
+    threads share nothing)."""
+    import concurrent.futures as cf
+
+    import oracle
+
+    oracle.build()
+    cores = max(1, os.cpu_count() or 1)
+    n_chunks = xs[0].size // 4096
+    per = max(1, n_chunks // cores)
+    probe_t, _ = oracle_step_seconds(xs, 16)
+    # chunks per thread so that one round takes about budget_s / 2
+    take = max(1, min(per, int(budget_s / 2 / (probe_t / 16))))
+
+    def one(i):
+        a = (i * per) * 4096
+        part = [x[a:a + take * 4096] for x in xs]
+        return oracle_step_seconds(part, take)
+
+    total_n, t0 = 0, time.perf_counter()
+    rounds = 0
+    with cf.ThreadPoolExecutor(cores) as ex:
+        while time.perf_counter() - t0 < budget_s and rounds < 4:
+            total_n += sum(n for _, n in ex.map(one, range(cores)))
+            rounds += 1
+    total_t = time.perf_counter() - t0
+    gbs = len(xs) * 2 * total_n / total_t / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu": cpu_model(),
+            "sample": "%d threads, each the full step on its own %d-chunk slice of every rank, %d round(s), %.1f s"
+                      % (cores, take, rounds, total_t)}
+
+
 def cpu_baseline(xs, budget_s: float = 12.0) -> dict:
     import oracle
 
@@ -189,7 +245,7 @@ def cpu_baseline(xs, budget_s: float = 12.0) -> dict:
         total_n += n
         reps += 1
     gbs = len(xs) * 2 * total_n / total_t / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
             "sample": "the full step on the whole workload (%d ranks x %d values), %d repetition(s), "
                       "%.1f s, single-threaded C oracle" % (len(xs), n_full, reps, total_t)}
 
@@ -547,7 +603,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8+f32", "data": "synthetic",
-        "config": workload_config(),
+        "config": dict(workload_config(), input_sha256=[hashlib.sha256(x.tobytes()).hexdigest()[:16]
+                                                        for x in xs_host]),
         "ratio": {"compress": round(mean(sizes) / (2 * n), 5), "reduce_out": round(red_bytes / (2 * n), 5)},
         "ops": ops, "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": R * 2 * n,
@@ -562,6 +619,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(xs_host)
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(xs_host)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
