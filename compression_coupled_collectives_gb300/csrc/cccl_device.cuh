@@ -1,14 +1,15 @@
 // cccl_device.cuh -- device building blocks shared by the compress, decompress
 // and fused-reduce kernels (sm_103a).
 //
-// Thread layout of every kernel: one CTA of 128 threads per 4096-element
-// chunk.  Thread t = 32 q + l (warp q, lane l) owns the 32 elements
+// Thread layout of a 4096-element chunk: 4 quarters q of 32 lanes l; lane l
+// of quarter q owns the 32 elements
 //   i = 256 j + 8 l + s,   j = 4 q + jj (jj < 4),  s < 8,
-// i.e. four 16-byte rows of the chunk; a warp's 32 lanes cover 512
-// contiguous bytes per row, so every global load and store is a fully
-// coalesced 16-byte access.  The stream's bit-plane word 32 q + l holds
-// exactly these 32 elements (bit 8 (s % 4) + 2 jj + s / 4), so packing and
-// unpacking the exponent codes never leaves the thread.
+// i.e. four 16-byte rows of the chunk (bf16); a warp's 32 lanes cover 512
+// contiguous bytes per row, so global loads and stores are fully coalesced
+// 16-byte accesses.  The stream's bit-plane word 32 q + l holds exactly these
+// 32 elements (bit 8 (s % 4) + 2 jj + s / 4), so packing and unpacking the
+// exponent codes never leaves the thread.  A decode or encode team is four
+// warps, one quarter each; a compress pair is two warps, two quarters each.
 //
 // Inside a thread, 4 elements travel in one 32-bit word, one byte each
 // ("quads", element s = 4 h + b in byte b): m = 2 jj + h indexes the 8
@@ -21,7 +22,6 @@
 namespace cccl {
 
 constexpr uint32_t kChunkElems = 4096;
-constexpr uint32_t kThreads = 128;
 constexpr uint32_t kStreamHeaderBytes = 64;
 constexpr uint32_t kChunkHeaderBytes = 16;
 constexpr uint32_t kSmPlaneBytes = 4096;
@@ -138,13 +138,6 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 __device__ __forceinline__ void record_error(WsHeader* ws, uint32_t status) { atomicMax(&ws->error, status); }
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
@@ -240,15 +233,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // bf16 split / join on quads (section 4.1: sign and fraction travel raw,
 // only the 8-bit exponent is re-encoded)
 // ---------------------------------------------------------------------------
-// A, B: two words of two bf16 each (elements 4h+0, 4h+1 in A; 4h+2, 4h+3 in B).
-// e:  the four exponents, one per byte.
-// sm: the four sign+fraction bytes ((b >> 8) & 0x80 | b & 0x7F).
-__device__ __forceinline__ void split_quad(uint32_t A, uint32_t B, uint32_t& e, uint32_t& sm) {
-    const uint32_t lo = __byte_perm(A, B, 0x6420);  // low bytes of the 4 values
-    const uint32_t hi = __byte_perm(A, B, 0x7531);  // high bytes
-    sm = (lo & 0x7F7F7F7Fu) | (hi & 0x80808080u);
-    e = ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
-}
+// e: four exponents, one per byte; sm: the four sign+fraction bytes
+// ((b >> 8) & 0x80 | b & 0x7F).  Joined into two words of two bf16 each
+// (elements 4h+0, 4h+1 in A; 4h+2, 4h+3 in B).
 __device__ __forceinline__ void join_quad(uint32_t e, uint32_t sm, uint32_t& A, uint32_t& B) {
     const uint32_t lo = (sm & 0x7F7F7F7Fu) | ((e << 7) & 0x80808080u);
     const uint32_t hi = (sm & 0x80808080u) | ((e >> 1) & 0x7F7F7F7Fu);
@@ -288,13 +275,6 @@ __device__ __forceinline__ uint32_t ge_flags(uint32_t off, uint32_t kb) {
 }
 // 0x80 flags -> 0xFF byte masks
 __device__ __forceinline__ uint32_t flags_to_mask(uint32_t f) { return f | (f - (f >> 7)); }
-// Count of 0x80 flags over 8 quads (one popc).
-__device__ __forceinline__ uint32_t count_flags8(const uint32_t f[8]) {
-    uint32_t acc = 0;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) acc |= f[m] >> (7 - m);
-    return __popc(acc & 0xFFFFFFFFu);
-}
 
 // ---------------------------------------------------------------------------
 // bit-planes: plane p word = over quads m and bytes b, bit p of code(m, b) at
@@ -330,13 +310,6 @@ __device__ __forceinline__ void transpose8x8x4(uint32_t* v) {
     for (int m = 0; m < 8; m += 2) block_swap(v[m], v[m + 1], 1, 0x55555555u);
 }
 
-// Plane p of 8 quads of codes (bits of codes above p are ignored).
-__device__ __forceinline__ uint32_t pack_plane(const uint32_t* code, uint32_t p) {
-    uint32_t acc = 0;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) acc |= rotr(code[m], (p - (uint32_t)m) & 31u) & (0x01010101u << m);
-    return acc;
-}
 // OR plane word w (plane p) into 8 quads of codes.
 __device__ __forceinline__ void unpack_plane(uint32_t w, uint32_t p, uint32_t* code) {
     const uint32_t mask = 0x01010101u << p;
