@@ -155,7 +155,8 @@ struct PairBarrier {
 
 struct PairXch {
     uint32_t mn[2], mx[2];  // per warp: smallest and largest exponent
-    uint32_t cnt[2][8];     // per warp: escapes at width k (window variant: [h][0] at the chosen table)
+    uint32_t cnt[2][8];     // per warp: escapes at width k (window variant: [h][0] the escapes at the
+                            // chosen table, [h][1..4] the warp's best size, k, base, escapes)
 };
 
 // One warp's half of a chunk, kept in registers between sizing and writing:
@@ -244,7 +245,8 @@ __device__ __forceinline__ PairPlan plan_chunk_pair(const uint8_t* chunk, HalfRe
 // Phase A of the window-base variant (stream version 2): for every width k
 // the base is the start of the window of 2^k - 1 exponents with the fewest
 // escapes (exponents outside it, below included), ties to the smaller base;
-// then the smallest size wins, ties to the smaller k.  `hist`: the pair's 264
+// then the smallest size wins, ties to the smaller k.  The pair shares one
+// histogram and splits the widths between its warps.  `hist`: the pair's 264
 // words of shared memory; `below`: this warp's own 264 words.  Leaves in `r`
 // the bit-planes of the codes, escaped elements carrying all ones, which is
 // what write_chunk_pair's escape test (low_k | high_k) and plane writes
@@ -301,10 +303,14 @@ __device__ __forceinline__ PairPlan plan_chunk_pair_window(const uint8_t* chunk,
     uint32_t best = 0;
     if (emax > emin) {
         // a window starting above the type's exponents escapes everything, so
-        // scanning all 256 starts gives the same choice for narrower types
+        // scanning all 256 starts gives the same choice for narrower types.
+        // Warp 0 sizes the widths 1..kSplit, warp 1 the rest; each keeps its
+        // best (size, k, base, escapes) and the pair then takes the smaller
+        // size, warp 0's on a tie (its widths are the smaller ones).
+        constexpr uint32_t kSplit = (max_width<D>() + 1) / 2;
+        const uint32_t k_lo = h == 0 ? 1u : kSplit + 1, k_hi = h == 0 ? kSplit : max_width<D>();
         best = 0xFFFFFFFFu;
-#pragma unroll
-        for (uint32_t k = 1; k <= max_width<D>(); ++k) {
+        for (uint32_t k = k_lo; k <= k_hi; ++k) {
             const uint32_t S = (1u << k) - 1u;
             uint32_t key = 0xFFFFFFFFu;  // (escapes, base): fewest escapes, then the smallest base
 #pragma unroll
@@ -322,6 +328,18 @@ __device__ __forceinline__ PairPlan plan_chunk_pair_window(const uint8_t* chunk,
                 pl.n_esc = n;
             }
         }
+        if (lane == 0) {
+            x.cnt[h][1] = best;
+            x.cnt[h][2] = pl.k;
+            x.cnt[h][3] = pl.base;
+            x.cnt[h][4] = pl.n_esc;
+        }
+        bar.sync();
+        const uint32_t w = x.cnt[0][1] <= x.cnt[1][1] ? 0u : 1u;
+        best = x.cnt[w][1];
+        pl.k = x.cnt[w][2];
+        pl.base = x.cnt[w][3];
+        pl.n_esc = x.cnt[w][4];
     }
     pl.raw = best >= raw_exponent_bytes<D>() ? 1u : 0u;
     if (pl.raw) {
