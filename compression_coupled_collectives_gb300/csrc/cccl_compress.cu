@@ -2,19 +2,20 @@
 // Collective Communication", sections 4.1, 4.3, 4.4; section 5 for the raw
 // partial chunk).
 //
-// Persistent and pipelined: one CTA per SM, G compute warps plus one
-// control warp, and a ring of kRing stages, each holding one group of G
-// consecutive chunks staged by bulk (TMA) copies (G = 8 for the 16-bit
-// element types, 4 for fp32).  Per group:
+// Persistent and pipelined: one CTA per SM, 2 G compute warps (a pair per
+// chunk) plus one control warp, and a ring of kRing stages, each holding one
+// group of G consecutive chunks staged by bulk (TMA) copies (G = 8 for the
+// 16-bit element types, 4 for fp32).  Per group:
 //   control warp  takes a ticket (the group index), issues the copies two
-//                 groups ahead, and once the compute warps have sized the
-//                 group, places it with one decoupled look-back;
-//   compute warp  sizes its chunk of group i+1 (exponent table, width,
-//                 escapes; the offset planes stay in registers) while the
-//                 control warp places group i, then writes its chunk of
-//                 group i at the final offset: the residual section and the
-//                 escapes read back from the staged input, the bit-planes
-//                 from registers, a raw chunk by one bulk (TMA) store.
+//                 groups ahead, and once the pairs have sized the group,
+//                 places it with one decoupled look-back;
+//   compute pair  sizes its chunk of group i+1 (exponent table, width,
+//                 escapes; each warp keeps its half of the offset planes in
+//                 registers) while the control warp places group i, then
+//                 writes its chunk of group i at the final offset, a half per
+//                 warp: the residual section and the escapes read back from
+//                 the staged input, the bit-planes from registers, a raw chunk
+//                 by one bulk (TMA) store.
 // So the look-back's wait for earlier groups overlaps with the sizing of the
 // next group, and the next copies are in flight during both.
 // Tickets hand out groups in order to CTAs that are already running, so every

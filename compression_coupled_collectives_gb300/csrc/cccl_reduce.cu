@@ -1,27 +1,28 @@
 // cccl_reduce.cu -- the fused reduce kernel: the reduce step of a compressed
 // allreduce as one pass, decompress -> binary32 accumulate in rank order ->
-// one rounding to bf16 -> compress ("CCCL: In-GPU Compression-Coupled
-// Collective Communication", section 5, "Integration into the NCCL data
-// path" (CopyReducePacks); Figure 2).
+// one rounding to the element type -> compress ("CCCL: In-GPU
+// Compression-Coupled Collective Communication", section 5, "Integration into
+// the NCCL data path" (CopyReducePacks); Figure 2).  Also min and max.
 //
 // Persistent and pipelined, one CTA per SM with three roles:
 //   teams (warps 0..11)  three independent teams of 4 warps.  Per group of
-//                        kTeams consecutive output chunks, team t takes chunk
+//                        three consecutive output chunks, team t takes chunk
 //                        t: it decodes chunk c of every rank, in rank order,
 //                        a quarter per warp, keeping 32 binary32 sums per
-//                        thread in registers; rounds once to bf16 and keeps
-//                        the chunk in registers; sizes it (the team meets
-//                        twice); then writes its chunk of the group two
-//                        iterations back (one for fp32), whose state waited
-//                        in shared memory while the placer placed it;
+//                        thread in registers; rounds once to the element type
+//                        (bf16, fp16; fp32 needs none) and keeps the chunk in
+//                        registers; sizes it (the team meets twice); saves its
+//                        state to shared memory and writes its chunk of the
+//                        previous group, which the placer has placed meanwhile;
 //   loader (warp 12)     takes a ticket per group, locates every rank's
 //                        chunks through their offset tables and streams them
 //                        to the teams through one ring of staged rank chunks
 //                        per team, by bulk (TMA) copies;
 //   placer (warp 13)     places each sized group with one decoupled look-back.
-// So the look-back of group i overlaps the decode of groups i + 1 and i + 2,
-// and the copies of later rank chunks are in flight meanwhile.  The output chunk
-// never goes through shared memory.
+// So the look-back of group i overlaps the decode of group i + 1, and the
+// copies of later rank chunks are in flight meanwhile.  The output chunk
+// reaches shared memory only as its saved state (a column of words per
+// thread), never as staged output.
 // Tickets hand out groups in order to CTAs that are already running, and a
 // group is sized without waiting on any later group: every look-back ends.
 #include <mutex>
