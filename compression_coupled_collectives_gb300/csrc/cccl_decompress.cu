@@ -6,8 +6,9 @@
 // has a producer warp, which locates its next chunks through the offset table
 // and stages them by bulk (TMA) copies in a small ring of buffers, and a
 // team of 4 decode warps, which rebuild 32 values per thread from each staged
-// chunk and store them with 16-byte writes.  One kernel per element type.  So the location and the copy of
-// later chunks overlap the decoding of the current one.
+// chunk and store them with 16-byte writes.  So the location and the copy of
+// later chunks overlap the decoding of the current one.  One kernel per
+// element type.
 #include "cccl_decode.cuh"
 #include "cccl_launch.h"
 
