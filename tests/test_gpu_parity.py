@@ -557,3 +557,51 @@ def test_step_captured_in_a_cuda_graph(cc, orc, wl):
         nb, st = cc.cccl_get_result(wss[2])
         assert st == 0 and np.array_equal(red[:nb].cpu().numpy(), want_red), rep
         assert np.array_equal(host_u16(y), orc.decompress(want_red, n)), rep
+
+
+# ---------------------------------------------------------------- streams past 4 GiB
+def test_streams_past_4_gib(cc, orc, wl):
+    """3 x 2^30 + 3 chunks + 5 values per rank (about 6 GiB of bf16; the
+    streams, about 5 GB, pass 2^32 bytes): the offset table, compress,
+    decompress and the fused reduce must carry 64-bit offsets and element
+    indices.  The input tiles one
+    seeded 2^20-value block; every chunk's bytes depend only on its own
+    values, so sampled chunks are checked against the oracle chunk by chunk,
+    the offset table against the chunk sizes, and the round trip in full on
+    the device."""
+    import struct
+
+    tile = 1 << 20
+    n = 3 * (1 << 30) + 3 * CHUNK + 5
+    base = [wl.generate(2, r, count=tile, n=tile) for r in range(2)]
+    reps = -(-n // tile)
+    xs = [dev(b).repeat(reps)[:n].contiguous() for b in base]
+    streams = [cc.compress(x) for x in xs]
+    red = cc.reduce_compressed(streams, n)
+    nch = -(-n // CHUNK)
+    samples = [0, 1, 255, 256, nch // 2, nch - 3, nch - 2, nch - 1]
+    for s_dev, b in zip(streams + [red], base + [None]):
+        total = int(s_dev.numel())
+        head = s_dev[:64].cpu().numpy().tobytes()
+        assert struct.unpack_from("<QQQ", head, 16) == (n, nch, total)
+        assert total > (1 << 32)
+        offs = s_dev[64:64 + 8 * nch].cpu().numpy().view(np.uint64).astype(np.int64)
+        ends = np.append(offs[1:], total)
+        sizes = ends - offs
+        assert (sizes > 0).all() and (sizes % 16 == 0).all() and offs[0] == 64 + -(-8 * nch // 16) * 16
+        for c in samples:
+            got = s_dev[int(offs[c]):int(ends[c])].cpu().numpy().tobytes()
+            lo = c * CHUNK
+            n_c = min(CHUNK, n - lo)
+            if b is not None:
+                want = orc.encode_chunk(b[lo % tile:lo % tile + n_c])
+            else:  # the reduce: chunk c of the sum of chunk c of both ranks
+                parts = [orc.compress(bb[lo % tile:lo % tile + n_c]) for bb in base]
+                one = orc.reduce(parts, n_c)
+                o0 = struct.unpack_from("<Q", one.tobytes(), 64)[0]
+                want = one.tobytes()[o0:]
+            assert got == want, "chunk %d" % c
+    for x, s_dev in zip(xs, streams):
+        assert torch.equal(cc.decompress(s_dev, n), x)
+    del xs, streams, red
+    torch.cuda.empty_cache()
