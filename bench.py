@@ -7,8 +7,10 @@ x100) of R = 2 simulated data-parallel ranks held in this GPU's memory:
     fused reduce(stream 0, stream 1)              decompress -> binary32 sum -> bf16 -> compress
     decompress(reduced stream)                    the receiver's decode
 `value` = uncompressed gradient bytes entering the step (R * 2n) / step time,
-timed on the device with CUDA events, L2 flushed (256 MiB write) before every
-step, max over ranks.  N GPUs under torchrun run N independent replicas
+timed on the device with CUDA events around each step, the step replayed as
+one captured CUDA graph of the four library calls, L2 flushed (256 MiB write,
+untimed) before every step, max over ranks.  The ops are timed one by one in
+a second pass of plain launches.  N GPUs under torchrun run N independent replicas
 (weak scaling); nothing crosses GPUs.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
@@ -383,6 +385,89 @@ def measure_extras(cc, torch, np, xs, streams, sizes, n, flush, peak, reps: int 
                      "frac_of_measured_copy": round(algo / (ms_w * 1e-3) / 1e9 / peak, 4),
                      "ratio": round(wbytes / (2 * n), 5), "ratio_min_base": round(v1bytes / (2 * n), 5)}
     out.update(measure_dtypes(cc, torch, np, n, timed, stream, peak))
+    out.update(measure_workloads(cc, torch, np, timed, stream, peak))
+    return out
+
+
+def measure_workloads(cc, torch, np, timed, stream, peak) -> dict:
+    """The larger bf16 workloads at their full sizes, each op timed alone:
+    the R=8 fused reduce over 8 x 256 MiB pre-compressed ranks; the 512 MiB
+    KV-cache tensor round trip; the 512 MiB worst case (half incompressible)
+    round trip and its R=4 fused reduce.  Inputs are far larger than the L2."""
+    import workloads
+
+    out = {}
+    n_chunks = lambda n: -(-n // 4096)
+
+    def row(ms_x, algo, uncompressed, **kw):
+        d = {"ms": round(ms_x, 5), "algorithmic_bytes": int(algo),
+             "uncompressed_gbs": round(uncompressed / (ms_x * 1e-3) / 1e9, 1),
+             "hbm_gbs": round(algo / (ms_x * 1e-3) / 1e9, 1),
+             "frac_of_measured_copy": round(algo / (ms_x * 1e-3) / 1e9 / peak, 4)}
+        d.update(kw)
+        return d
+
+    def compressed(w, ranks):
+        n = workloads.SIZES[w]
+        ss, sizes = [], []
+        ws = cc.empty_workspace(n)
+        for r in range(ranks):
+            x = torch.from_numpy(workloads.generate(w, r).view(np.int16)).cuda()
+            s_ = cc.empty_stream(n)
+            cc.cccl_compress(x, s_, ws, stream=stream)
+            b, st = cc.cccl_get_result(ws, stream)
+            if st != 0:
+                raise RuntimeError("compress of workload %d rank %d: status %d" % (w, r, st))
+            ss.append(s_)
+            sizes.append(b)
+            if r > 0:
+                del x
+            else:
+                x0 = x
+        return n, x0, ss, sizes, ws
+
+    def reduce_row(n, ss, sizes, ws, R):
+        red = cc.empty_stream(n)
+        ins = [s_[:b] for s_, b in zip(ss[:R], sizes[:R])]
+        ms_r = timed(lambda: cc.cccl_reduce_compressed(ins, n, red, ws, stream=stream))
+        rbytes, st = cc.cccl_get_result(ws, stream)
+        tab = 8 * n_chunks(n)
+        return row(ms_r, sum(sizes[:R]) + R * tab + rbytes + tab, R * 2 * n, status=st,
+                   ratio_out=round(rbytes / (2 * n), 5))
+
+    def round_trip_rows(n, x, s_, b, ws):
+        ms_c = timed(lambda: cc.cccl_compress(x, s_, ws, stream=stream))
+        _, st_c = cc.cccl_get_result(ws, stream)
+        y = torch.empty_like(x)
+        ms_d = timed(lambda: cc.cccl_decompress(s_[:b], y, ws, stream=stream))
+        _, st_d = cc.cccl_get_result(ws, stream)
+        tab = 8 * n_chunks(n)
+        return (row(ms_c, 2 * n + b + tab, 2 * n, status=st_c, ratio=round(b / (2 * n), 5)),
+                row(ms_d, b + tab + 2 * n, 2 * n, status=st_d, round_trip_exact=bool(torch.equal(x, y))))
+
+    # R = 8 ranks of 134,217,728 values ~ N(0, 0.02)
+    n, x0, ss, sizes, ws = compressed(3, 8)
+    out["workload3_reduce_r8"] = reduce_row(n, ss, sizes, ws, 8)
+    out["workload3_reduce_r8"]["workload"] = "8 pre-compressed ranks of 134,217,728 bf16 values (256 MiB each) " \
+                                             "~ N(0, 0.02), fused reduce in rank order 0..7"
+    del x0, ss, ws
+    # KV-cache tensor [32, 2, 4096, 8, 128]
+    n, x0, ss, sizes, ws = compressed(4, 1)
+    c_row, d_row = round_trip_rows(n, x0, ss[0], sizes[0], ws)
+    kv = "KV-cache tensor [32, 2, 4096, 8, 128] = 268,435,456 bf16 values (512 MiB), per-head log-uniform scales"
+    out["workload4_compress"] = dict(c_row, workload=kv)
+    out["workload4_decompress"] = dict(d_row, workload=kv)
+    del x0, ss, ws
+    # worst case: half uniform 16-bit patterns, half N(0, 1) with specials; 4 ranks
+    n, x0, ss, sizes, ws = compressed(5, 4)
+    c_row, d_row = round_trip_rows(n, x0, ss[0], sizes[0], ws)
+    wc = "worst case, 268,435,456 bf16 values (512 MiB): half uniform 16-bit patterns, half N(0, 1) with 0.1% " \
+         "each NaN, +-Inf, +-0, subnormals"
+    out["workload5_compress"] = dict(c_row, workload=wc)
+    out["workload5_decompress"] = dict(d_row, workload=wc)
+    out["workload5_reduce_r4"] = dict(reduce_row(n, ss, sizes, ws, 4), workload=wc + "; 4 ranks, fused reduce")
+    del x0, ss, ws
+    torch.cuda.empty_cache()
     return out
 
 
@@ -461,23 +546,23 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def step(ev=None):
+    def step(ev=None, s=stream):
         # ev: list of (start, end) event pairs, one per op
         for r in range(R):
             if ev is not None:
-                ev[r][0].record(stream)
-            cc.cccl_compress(xs[r], streams[r], ws[r], stream)
+                ev[r][0].record(s)
+            cc.cccl_compress(xs[r], streams[r], ws[r], s)
             if ev is not None:
-                ev[r][1].record(stream)
+                ev[r][1].record(s)
         if ev is not None:
-            ev[R][0].record(stream)
-        cc.cccl_reduce_compressed(streams, n, red, ws[R], stream=stream)
+            ev[R][0].record(s)
+        cc.cccl_reduce_compressed(streams, n, red, ws[R], stream=s)
         if ev is not None:
-            ev[R][1].record(stream)
-            ev[R + 1][0].record(stream)
-        cc.cccl_decompress(red, y, ws[R + 1], stream=stream)
+            ev[R][1].record(s)
+            ev[R + 1][0].record(s)
+        cc.cccl_decompress(red, y, ws[R + 1], stream=s)
         if ev is not None:
-            ev[R + 1][1].record(stream)
+            ev[R + 1][1].record(s)
 
     # one untimed pass: sizes, ratios and a sampled check against the oracle
     step()
@@ -493,6 +578,27 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         flush.fill_(1)
         step()
     torch.cuda.synchronize()
+    y_plain = y.clone()
+
+    # The timed step is one CUDA graph: the same four library calls captured
+    # once (each call's workspace clear and kernel become graph nodes) and
+    # replayed every step.
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step(s=side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        step(s=torch.cuda.current_stream(device))
+    y.zero_()
+    for _ in range(warmup):
+        flush.fill_(1)
+        graph.replay()
+    torch.cuda.synchronize()
+    graph_ok = bool(torch.equal(y, y_plain))
+    del y_plain
 
     sampler = ClockSampler(device.index if device.index is not None else 0)
     sampler.start()
@@ -500,9 +606,23 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    op_ms = [[] for _ in range(R + 2)]
-    step_ms = []
+    # timed region: K graph replays, the L2 flushed before each (untimed)
     t_wall0 = time.time()
+    evg = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        evg[k][0].record(stream)
+        graph.replay()
+        evg[k][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evg]
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+    # the ops one by one: K more steps of plain launches with an event pair
+    # around every call (the call's workspace clear included), same flush
+    op_ms = [[] for _ in range(R + 2)]
+    plain_ms = []
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R + 2)] for _ in range(args.steps)]
     for k in range(args.steps):
         flush.fill_(k & 0xFF)
@@ -513,10 +633,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         e = evs[k]
         for i in range(R + 2):
             op_ms[i].append(e[i][0].elapsed_time(e[i][1]))
-        step_ms.append(e[0][0].elapsed_time(e[R + 1][1]))
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = max_over_ranks(sum(step_ms), world, device)
+        plain_ms.append(e[0][0].elapsed_time(e[R + 1][1]))
 
     # end to end through the same calls: pinned host inputs in, decoded result
     # out, every step.  Pipelined over three streams with two device buffer
@@ -606,6 +723,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "config": dict(workload_config(), input_sha256=[hashlib.sha256(x.tobytes()).hexdigest()[:16]
                                                         for x in xs_host]),
         "ratio": {"compress": round(mean(sizes) / (2 * n), 5), "reduce_out": round(red_bytes / (2 * n), 5)},
+        "launch": {"step": "one CUDA graph replay per step (the 4 library calls, each a workspace clear and a "
+                           "kernel)", "graph_result_matches_plain": graph_ok,
+                   "ops": "timed in a second pass of %d plain-launch steps, one event pair around each call "
+                          "(its workspace clear included)" % args.steps,
+                   "ms_per_step_plain": round(sum(plain_ms) / len(plain_ms), 5)},
         "ops": ops, "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": R * 2 * n,
                 "d2h_bytes_per_step": 2 * n, "steps": e2e_steps,

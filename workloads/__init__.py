@@ -161,6 +161,19 @@ def generate_typed(dtype: int, workload: int, rank: int = 0, start: int = 0, cou
     seed = seed_of(workload, rank)
     if count == 0:
         return np.empty(0, bits_t)
+    if count > 2 * _BLOCK:
+        # large requests: slices of one block each, on host threads (numpy and
+        # torch release the GIL); every recipe is counter-based, so the slices
+        # join into exactly the same bits
+        out = np.empty(count, bits_t)
+
+        def part(o):
+            m = min(_BLOCK, count - o)
+            out[o:o + m] = generate_typed(dtype, workload, rank, start + o, m, total)
+
+        with _cf.ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(part, range(0, count, _BLOCK)))
+        return out
     if workload in (1, 3):
         return _to_bits(dtype, (0.02 * normal(seed, _S_VALUE, start, count)).astype(np.float32))
     if workload == 2:
