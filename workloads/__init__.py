@@ -32,6 +32,7 @@ import concurrent.futures as _cf
 import ctypes
 import os
 import subprocess
+import threading
 
 import numpy as np
 
@@ -58,11 +59,14 @@ def build(force: bool = False) -> str:
 
 
 _lib = None
+_lib_lock = threading.Lock()
 
 
 def _load():
     global _lib
-    if _lib is None:
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
         lib = ctypes.CDLL(build())
         u64 = ctypes.c_uint64
         for f in ("wl_u64", "wl_uniform", "wl_normal"):
