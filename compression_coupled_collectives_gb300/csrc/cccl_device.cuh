@@ -206,6 +206,17 @@ struct TeamBarrier {
     }
 };
 
+// Non-blocking: has phase `parity` of `bar` completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for phase `parity` of `bar`; false if kWaitLimitNs ran out.
 // Each try suspends the warp in hardware (up to kSuspendHintNs) until the
 // phase completes, so a waiting warp costs no issue slots.
@@ -414,19 +425,29 @@ struct ChunkView {
 __device__ __forceinline__ uint64_t ld_u64_aligned(const uint8_t* p) { return *reinterpret_cast<const uint64_t*>(p); }
 __device__ __forceinline__ uint32_t ld_u32_aligned(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
-// One thread: check the stream header against (n_elems, in_bytes) and locate
-// chunk c through the offset table.  Every read stays inside in_bytes.
+// One thread: check the stream header against (n_elems, in_bytes); returns
+// the stream's total size, or 0 if the header is unusable.  Every read stays
+// inside in_bytes.
 template <class D>
-__device__ __forceinline__ ChunkView locate_chunk(const uint8_t* s, uint64_t in_bytes, uint64_t n_elems,
-                                                  uint64_t n_chunks, uint64_t c) {
+__device__ __forceinline__ uint64_t stream_total(const uint8_t* s, uint64_t in_bytes, uint64_t n_elems,
+                                                 uint64_t n_chunks) {
+    const uint64_t start = data_start(n_chunks);
+    if (in_bytes < start) return 0;
+    const uint32_t w0 = ld_u32_aligned(s + 0), w1 = ld_u32_aligned(s + 4), w2 = ld_u32_aligned(s + 8);
+    if (w0 != kMagic || !known_version_word<D>(w1) || w2 != kChunkElems) return 0;
+    if (ld_u64_aligned(s + 16) != n_elems || ld_u64_aligned(s + 24) != n_chunks) return 0;
+    const uint64_t total = ld_u64_aligned(s + 32);
+    if (total > in_bytes || total < start) return 0;
+    return total;
+}
+
+// One thread: locate chunk c through the offset table of a stream whose
+// header stream_total accepted (`total` its result, nonzero).  Every read
+// stays inside total.
+template <class D>
+__device__ __forceinline__ ChunkView locate_chunk_at(const uint8_t* s, uint64_t total, uint64_t n_chunks, uint64_t c) {
     ChunkView v{0, 0, 0};
     const uint64_t start = data_start(n_chunks);
-    if (in_bytes < start) return v;
-    const uint32_t w0 = ld_u32_aligned(s + 0), w1 = ld_u32_aligned(s + 4), w2 = ld_u32_aligned(s + 8);
-    if (w0 != kMagic || !known_version_word<D>(w1) || w2 != kChunkElems) return v;
-    if (ld_u64_aligned(s + 16) != n_elems || ld_u64_aligned(s + 24) != n_chunks) return v;
-    const uint64_t total = ld_u64_aligned(s + 32);
-    if (total > in_bytes || total < start) return v;
     const uint64_t off = ld_u64_aligned(s + kStreamHeaderBytes + 8 * c);
     const uint64_t end = (c + 1 < n_chunks) ? ld_u64_aligned(s + kStreamHeaderBytes + 8 * (c + 1)) : total;
     if (c == 0 && off != start) return v;
@@ -437,6 +458,15 @@ __device__ __forceinline__ ChunkView locate_chunk(const uint8_t* s, uint64_t in_
     v.bytes = (uint32_t)(end - off);
     v.ok = 1;
     return v;
+}
+
+// Both: check the header, then locate chunk c.
+template <class D>
+__device__ __forceinline__ ChunkView locate_chunk(const uint8_t* s, uint64_t in_bytes, uint64_t n_elems,
+                                                  uint64_t n_chunks, uint64_t c) {
+    const uint64_t total = stream_total<D>(s, in_bytes, n_elems, n_chunks);
+    if (total == 0) return ChunkView{0, 0, 0};
+    return locate_chunk_at<D>(s, total, n_chunks, c);
 }
 
 // Decoded chunk header (16 bytes at the start of a staged chunk).

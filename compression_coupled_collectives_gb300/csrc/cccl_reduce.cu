@@ -172,6 +172,7 @@ struct ReduceSmem {
     TeamXch xch[kMaxTeams];                 // the encoder's exchange space
     volatile uint32_t abort;             // a bounded wait ran out: every role stops
     ReduceMeta meta[2];
+    uint64_t total[kMaxRanks];           // rank r's stream size from its checked header (0: unusable)
 };
 
 __device__ __forceinline__ void set_abort(const StreamOut& so, ReduceSmem& sm) {
@@ -188,8 +189,18 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
     constexpr uint32_t kRawBytes = D::kElemBytes * kChunkElems;
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t n_groups = (so.n_chunks + kTeams - 1) / kTeams;
+    // every rank's stream header, checked once
+    for (int r = (int)lane; r < R; r += 32)
+        sm.total[r] = (r == 0 && inputs.local != nullptr)
+                          ? 1u
+                          : stream_total<D>(inputs.in[r], inputs.in_bytes[r], so.n_elems, so.n_chunks);
+    __syncwarp();
     uint32_t ut[kTeams] = {};  // rank chunks issued to each team
     bool stop = false;
+    // lane 0: the ticket for the next group, taken one group ahead so that
+    // its latency hides behind this group's work
+    uint64_t next = 0;
+    if (lane == 0) next = atomicAdd(&so.ws->ticket, 1u);
     for (int i = 0; !stop && !warp_any(sm.abort); ++i) {
         const int b = i & 1;
         // meta[b] was last read by the teams for group i - 2
@@ -197,9 +208,8 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
             if (lane == 0) set_abort(so, sm);
             break;
         }
-        uint64_t g = 0;
-        if (lane == 0) g = atomicAdd(&so.ws->ticket, 1u);
-        g = __shfl_sync(0xFFFFFFFFu, g, 0);
+        const uint64_t g = __shfl_sync(0xFFFFFFFFu, next, 0);
+        if (lane == 0 && g < n_groups) next = atomicAdd(&so.ws->ticket, 1u);
         ReduceMeta& m = sm.meta[b];
         if (g >= n_groups) {
             if (lane == 0) {
@@ -219,7 +229,9 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
                 m.bytes[t][r] = D::kElemBytes * (uint32_t)(left < kChunkElems ? left : kChunkElems);
                 continue;
             }
-            const ChunkView v = locate_chunk<D>(inputs.in[r], inputs.in_bytes[r], so.n_elems, so.n_chunks, c0 + t);
+            const uint64_t total = sm.total[r];
+            ChunkView v{0, 0, 0};
+            if (total != 0) v = locate_chunk_at<D>(inputs.in[r], total, so.n_chunks, c0 + t);
             m.off[t][r] = v.offset;
             m.bytes[t][r] = v.bytes;
             ok = ok && v.ok;
@@ -233,34 +245,60 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.meta_ready[b]);
         if (!ok) continue;  // nothing to stream: the teams poison the group
-        // rank-major, so that every team gets its next rank chunk in turn
-        for (int r = 0; r < R && !stop; ++r) {
-            for (uint32_t t = 0; t < n_out; ++t) {
-                const uint32_t s = ut[t] % kRSlots;
-                // the slot's previous rank chunk is consumed
-                if (ut[t] >= (uint32_t)kRSlots && !warp_wait(&sm.free_[t][s], (ut[t] / kRSlots - 1) & 1u)) {
-                    if (lane == 0) set_abort(so, sm);
-                    stop = true;
-                    break;
+        // Every team gets its rank chunks in rank order; a team whose next
+        // slot is still busy does not hold up the others.
+        uint32_t issued[kTeams] = {};  // this group's rank chunks issued to each team
+        uint32_t left = n_out * (uint32_t)R;
+        uint64_t t_blocked = 0;
+        uint32_t nap = 32;
+        while (left > 0) {
+            bool progress = false;
+#pragma unroll
+            for (int t = 0; t < kTeams; ++t) {
+                if (t >= (int)n_out) break;
+                while (issued[t] < (uint32_t)R) {
+                    const uint32_t s = ut[t] % kRSlots;
+                    // the slot's previous rank chunk is consumed
+                    if (ut[t] >= (uint32_t)kRSlots && !mbar_test(&sm.free_[t][s], (ut[t] / kRSlots - 1) & 1u)) break;
+                    const uint32_t r = issued[t];
+                    if (lane == 0) {
+                        fence_proxy_async_smem();
+                        uint8_t* slot = ring + ((size_t)t * kRSlots + s) * max_chunk_bytes<D>();
+                        if (r != 0 || inputs.local == nullptr)
+                            bulk_load(slot, inputs.in[r] + m.off[t][r], m.bytes[t][r], &sm.full[t][s]);
+                        else if (m.bytes[t][r] == kRawBytes)  // a full local chunk, staged raw
+                            bulk_load(slot, static_cast<const uint8_t*>(inputs.local) + m.off[t][r], kRawBytes,
+                                      &sm.full[t][s]);
+                        else  // the partial local chunk is read in place by the team
+                            mbar_arrive(&sm.full[t][s]);
+                    }
+                    __syncwarp();
+                    ++ut[t];
+                    ++issued[t];
+                    --left;
+                    progress = true;
                 }
-                if (warp_any(sm.abort)) {
-                    stop = true;
-                    break;
-                }
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    uint8_t* slot = ring + ((size_t)t * kRSlots + s) * max_chunk_bytes<D>();
-                    if (r != 0 || inputs.local == nullptr)
-                        bulk_load(slot, inputs.in[r] + m.off[t][r], m.bytes[t][r], &sm.full[t][s]);
-                    else if (m.bytes[t][r] == kRawBytes)  // a full local chunk, staged raw
-                        bulk_load(slot, static_cast<const uint8_t*>(inputs.local) + m.off[t][r], kRawBytes,
-                                  &sm.full[t][s]);
-                    else  // the partial local chunk is read in place by the team
-                        mbar_arrive(&sm.full[t][s]);
-                }
-                __syncwarp();
-                ++ut[t];
             }
+            if (progress) {
+                t_blocked = 0;
+                nap = 32;
+                continue;
+            }
+            // every team with chunks left waits for a slot: back off, bounded
+            if (warp_any(sm.abort)) {
+                stop = true;
+                break;
+            }
+            const uint64_t now = __shfl_sync(0xFFFFFFFFu, globaltimer_ns(), 0);
+            if (t_blocked == 0) {
+                t_blocked = now;
+            } else if (now - t_blocked > kWaitLimitNs) {
+                if (lane == 0) set_abort(so, sm);
+                stop = true;
+                break;
+            }
+            __nanosleep(nap);
+            if (nap < 256) nap <<= 1;
         }
     }
     // no copy may still be landing when the CTA exits
