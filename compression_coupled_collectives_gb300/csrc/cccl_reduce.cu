@@ -472,7 +472,7 @@ __device__ __forceinline__ void write_pending(const StreamOut& so, ReduceSmem& s
         write_chunk_team<D>(Pp, Qp, sm.pend_pl[team][slot][wq], dst, st);
     else
         write_tail_chunk_team<D>(Pp, (uint32_t)(so.n_elems - c * kChunkElems), dst);
-    if (tt == 0) finish_chunk(so, c, off, bytes);
+    if (tt == 64) finish_chunk(so, c, off, bytes);  // warp 0 wrote the chunk header
 }
 
 template <class D>
@@ -558,7 +558,7 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
                             accumulate<D>(acc, V, op, r == 0);
                     }
                     bar.sync();  // the team is done with slot s and row_tot
-                    if (tt == 0) mbar_arrive(&sm.free_[team][s]);
+                    if (tt == 32) mbar_arrive(&sm.free_[team][s]);
                 }
                 if (fail == 0) finish_values<D>(bar, acc, op, special, P);
             }
@@ -571,7 +571,7 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
                     bytes = tail_chunk_bytes<D>(n_c);
                 }
             }
-            if (tt == 0) {
+            if (tt == 96) {  // lane 0 of warp 3: warp 0 writes headers, warp 2 the table
                 sm.size[pb][team] = bytes;
                 sm.failed[pb][team] = fail;
                 if (team == 0) sm.gid[pb] = g;
@@ -586,7 +586,7 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
                 }
                 mbar_arrive(&sm.sized[pb]);
             }
-        } else if (tt == 0) {
+        } else if (tt == 96) {
             if (team == 0) sm.gid[pb] = kNoGroup;
             mbar_arrive(&sm.sized[pb]);
         }
