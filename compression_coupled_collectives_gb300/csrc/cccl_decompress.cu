@@ -3,12 +3,12 @@
 // "Decomp." stage of Figure 2).
 //
 // Persistent: several CTAs per SM, each taking every gridDim-th chunk.  A CTA
-// has a producer warp, which locates its next chunks through the offset table
-// and stages them by bulk (TMA) copies in a small ring of buffers, and a
-// team of 4 decode warps, which rebuild 32 values per thread from each staged
-// chunk and store them with 16-byte writes.  So the location and the copy of
-// later chunks overlap the decoding of the current one.  One kernel per
-// element type.
+// has a producer warp, which locates its chunks through the offset table (32
+// at a time, one per lane) and stages them by bulk (TMA) copies in a small
+// ring of buffers, and a team of 4 decode warps, which rebuild 32 values per
+// thread from each staged chunk and store them with 16-byte writes.  So the
+// location and the copy of later chunks overlap the decoding of the current
+// one.  One kernel per element type.
 #include "cccl_decode.cuh"
 #include "cccl_launch.h"
 
@@ -56,30 +56,47 @@ __global__ void __launch_bounds__(kDThreads, dctas_per_sm<D>())
 
     if (q == kDProducerWarp) {
         // ------------------------------------------------------------ producer
+        // The stream header is checked once; this CTA's chunks are located 32
+        // at a time, one per lane, so a copy waits only for its slot.
+        const uint64_t total = stream_total<D>(s, in_bytes, n_elems, n_chunks);
         uint32_t i = 0;
-        for (uint64_t c = blockIdx.x; c < n_chunks; c += stride, ++i) {
-            const uint32_t slot = i % kDSlots;
-            if (i >= (uint32_t)kDSlots &&
-                !__all_sync(0xFFFFFFFFu, mbar_wait(&sm.free_[slot], (i / kDSlots - 1) & 1u))) {
+        bool stop = false;
+        for (uint64_t c0 = blockIdx.x; c0 < n_chunks && !stop; c0 += 32 * stride) {
+            const uint64_t mine = c0 + lane * stride;
+            ChunkView v{0, 0, 0};
+            if (mine < n_chunks && total != 0) v = locate_chunk_at<D>(s, total, n_chunks, mine);
+            const uint64_t here = (n_chunks - c0 + stride - 1) / stride;
+            const uint32_t n_here = here < 32 ? (uint32_t)here : 32u;
+            for (uint32_t j = 0; j < n_here; ++j, ++i) {
+                const uint32_t slot = i % kDSlots;
+                if (i >= (uint32_t)kDSlots &&
+                    !__all_sync(0xFFFFFFFFu, mbar_wait(&sm.free_[slot], (i / kDSlots - 1) & 1u))) {
+                    if (lane == 0) {
+                        record_error(ws, kStatusTimeout);
+                        sm.abort = 1;
+                    }
+                    stop = true;
+                    break;
+                }
+                if (__any_sync(0xFFFFFFFFu, sm.abort != 0)) {
+                    stop = true;
+                    break;
+                }
+                const uint64_t off = __shfl_sync(0xFFFFFFFFu, v.offset, j);
+                const uint32_t bytes = __shfl_sync(0xFFFFFFFFu, v.bytes, j);
+                const uint32_t ok = __shfl_sync(0xFFFFFFFFu, v.ok, j);
                 if (lane == 0) {
-                    record_error(ws, kStatusTimeout);
-                    sm.abort = 1;
+                    sm.ok[slot] = ok;
+                    sm.bytes[slot] = bytes;
+                    if (ok) {
+                        fence_proxy_async_smem();
+                        bulk_load(ring[slot], s + off, bytes, &sm.full[slot]);
+                    } else {
+                        mbar_arrive(&sm.full[slot]);  // nothing to stage; the team reports it
+                    }
                 }
-                break;
+                __syncwarp();
             }
-            if (__any_sync(0xFFFFFFFFu, sm.abort != 0)) break;
-            if (lane == 0) {
-                const ChunkView v = locate_chunk<D>(s, in_bytes, n_elems, n_chunks, c);
-                sm.ok[slot] = v.ok;
-                sm.bytes[slot] = v.bytes;
-                if (v.ok) {
-                    fence_proxy_async_smem();
-                    bulk_load(ring[slot], s + v.offset, v.bytes, &sm.full[slot]);
-                } else {
-                    mbar_arrive(&sm.full[slot]);  // nothing to stage; the team reports it
-                }
-            }
-            __syncwarp();
         }
         // no copy may still be landing when the CTA exits
         for (uint32_t v = i > (uint32_t)kDSlots ? i - kDSlots : 0u; v < i; ++v)
