@@ -25,11 +25,12 @@ __host__ __device__ constexpr int dslots() { return D::kElemBytes == 4 ? 2 : 3; 
 template <class D>
 __host__ __device__ constexpr int dctas_per_sm() { return D::kElemBytes == 4 ? 6 : (D::kExpBits == 5 ? 7 : 8); }
 
+constexpr int kMaxDSlots = 3;
 struct DecompressSmem {
-    uint64_t full[3];         // the slot's chunk landed, or its meta says there is none
-    uint64_t free_[3];        // the team is done with the slot (1 arrival)
-    uint32_t bytes[3];        // staged chunk size
-    uint32_t ok[3];           // the chunk was located
+    uint64_t full[kMaxDSlots];   // the slot's chunk landed, or its meta says there is none
+    uint64_t free_[kMaxDSlots];  // the team is done with the slot (1 arrival)
+    uint32_t bytes[kMaxDSlots];  // staged chunk size
+    uint32_t ok[kMaxDSlots];     // the chunk was located
     uint32_t row_tot[4];
     volatile uint32_t abort;
 };
@@ -39,6 +40,7 @@ __global__ void __launch_bounds__(kDThreads, dctas_per_sm<D>())
     decompress_kernel(const uint8_t* __restrict__ s, uint64_t in_bytes, uint8_t* __restrict__ out, Paging pg,
                       uint64_t n_elems, uint64_t n_chunks, WsHeader* ws) {
     constexpr int kDSlots = dslots<D>();
+    static_assert(kDSlots <= kMaxDSlots, "DecompressSmem holds kMaxDSlots slots");
     using Elem = typename std::conditional<D::kElemBytes == 4, uint32_t, uint16_t>::type;
     __shared__ __align__(128) uint8_t ring[kDSlots][max_chunk_bytes<D>()];
     __shared__ DecompressSmem sm;

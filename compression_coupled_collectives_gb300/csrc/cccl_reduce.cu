@@ -51,6 +51,7 @@ constexpr uint64_t kNoGroup = ~0ull;
 // for fp32
 template <class D>
 __host__ __device__ constexpr int rslots() { return D::kElemBytes == 4 ? 3 : 4; }
+constexpr int kMaxRSlots = 4;
 // a team thread's chunk state between sizing and writing: its words, planes[8]
 template <class D>
 __host__ __device__ constexpr int prev_words() { return thread_words<D>() + 8; }
@@ -158,8 +159,8 @@ struct ReduceSmem {
     uint64_t decoded[2];                 // teams -> loader: meta[b] read (one arrival per team warp)
     uint64_t sized[kMaxPlaceBufs];       // teams -> placer: sizes in size[p] (one arrival per team)
     uint64_t placed[kMaxPlaceBufs];      // placer -> teams: offsets in off[p] (1 arrival)
-    uint64_t full[kMaxTeams][4];            // a rank chunk landed in the slot (transaction count)
-    uint64_t free_[kMaxTeams][4];           // the team is done with the slot (1 arrival)
+    uint64_t full[kMaxTeams][kMaxRSlots];   // a rank chunk landed in the slot (transaction count)
+    uint64_t free_[kMaxTeams][kMaxRSlots];  // the team is done with the slot (1 arrival)
     unsigned long long tally[kMaxPlaceBufs];  // sized teams (high word) and their bytes (low word)
     uint32_t size[kMaxPlaceBufs][kMaxTeams];
     uint32_t failed[kMaxPlaceBufs][kMaxTeams];   // the team's chunk could not be reduced
@@ -623,6 +624,9 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
 template <class D>
 __global__ void __launch_bounds__(reduce_threads<D>(), 1) reduce_kernel(ReduceInputs inputs, int R, StreamOut so) {
     constexpr int kTeams = teams<D>();
+    static_assert(kTeams <= kMaxTeams && rslots<D>() <= kMaxRSlots && state_slots<D>() <= 3 &&
+                      place_bufs<D>() <= kMaxPlaceBufs,
+                  "the shared-memory bookkeeping arrays are sized for these bounds");
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ ReduceSmem sm;
     uint8_t* ring = smem;
