@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(kDThreads, dctas_per_sm<D>())
         const uint32_t slot = i % kDSlots;
         uint8_t* buf = ring[slot];
         const bool landed = !sm.abort && mbar_wait(&sm.full[slot], (i / kDSlots) & 1u);
+        // one meeting per chunk: it has landed for every warp, and every warp
+        // is done with the previous chunk's slot and row_tot
         if (bar.any(!landed)) {
             if (t == 0) {
                 record_error(ws, kStatusTimeout);
@@ -120,6 +122,7 @@ __global__ void __launch_bounds__(kDThreads, dctas_per_sm<D>())
             }
             return;  // the whole team
         }
+        if (i > 0 && t == 32) mbar_arrive(&sm.free_[(i - 1) % kDSlots]);
         const uint64_t left = n_elems - c * kChunkElems;
         const uint32_t n_c = left < kChunkElems ? (uint32_t)left : kChunkElems;
         const uint64_t e = chunk_elem_offset(pg, c);
@@ -157,8 +160,6 @@ __global__ void __launch_bounds__(kDThreads, dctas_per_sm<D>())
             }
         }
         if (!good && e != kBadChunk && t == 0) record_error(ws, kStatusCorrupt);
-        bar.sync();  // the team is done with the slot and row_tot
-        if (t == 0) mbar_arrive(&sm.free_[slot]);
     }
 }
 

@@ -415,17 +415,16 @@ __device__ __forceinline__ void accumulate(uint64_t* acc, const uint32_t* V, uin
 
 // The reduced chunk into P: one rounding of the binary32 sums to the type
 // (fp32: none), or the min / max values as they are; NaNs made canonical
-// when a rank may have held an Inf or a NaN.
-template <class D, typename Barrier>
-__device__ __forceinline__ void finish_values(const Barrier& bar, const uint64_t* acc, uint32_t op, bool special,
-                                              uint32_t* P) {
+// when a rank may have held an Inf or a NaN (`special`: the team's verdict).
+template <class D>
+__device__ __forceinline__ void finish_values(const uint64_t* acc, uint32_t op, bool special, uint32_t* P) {
     if constexpr (D::kElemBytes == 4) {
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
             P[2 * x] = (uint32_t)acc[x];
             P[2 * x + 1] = (uint32_t)(acc[x] >> 32);
         }
-        if (bar.any(special)) {
+        if (special) {
 #pragma unroll
             for (int x = 0; x < 32; ++x) P[x] = canonical_nan_word(P[x]);
         }
@@ -433,7 +432,7 @@ __device__ __forceinline__ void finish_values(const Barrier& bar, const uint64_t
 #pragma unroll
         for (int x = 0; x < 16; ++x)
             P[x] = op != 0 ? (uint32_t)acc[x] : (D::kExpBits == 5 ? round_pair_fp16(acc[x]) : round_pair_bf16(acc[x]));
-        if (bar.any(special)) {
+        if (special) {
 #pragma unroll
             for (int x = 0; x < 16; ++x) P[x] = canonical_nan_pair<D>(P[x]);
         }
@@ -524,10 +523,14 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
                     const uint32_t s = u % kRSlots;
                     uint8_t* buf = ring + (size_t)s * kSlotBytes;
                     const bool landed = !sm.abort && mbar_wait(&sm.full[team][s], (u / kRSlots) & 1u);
+                    // one meeting per rank: slot s has landed for every warp,
+                    // and every warp is done with the previous rank's slot and
+                    // row_tot
                     if (bar.any(!landed)) {
                         if (tt == 0) set_abort(so, sm);
                         return;  // the whole team
                     }
+                    if (r > 0 && tt == 32) mbar_arrive(&sm.free_[team][(u - 1) % kRSlots]);
                     uint32_t V[kW];
                     if (fail == 0 && r == 0 && local != nullptr) {
                         // the uncompressed local operand: staged raw, or read in place
@@ -558,10 +561,11 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
                         else
                             accumulate<D>(acc, V, op, r == 0);
                     }
-                    bar.sync();  // the team is done with slot s and row_tot
-                    if (tt == 32) mbar_arrive(&sm.free_[team][s]);
                 }
-                if (fail == 0) finish_values<D>(bar, acc, op, special, P);
+                // the last rank's slot is released once the team meets again
+                const bool any_special = bar.any(special);
+                if (tt == 32) mbar_arrive(&sm.free_[team][(u - 1) % kRSlots]);
+                if (fail == 0) finish_values<D>(acc, op, any_special, P);
             }
             if (lane == 0) mbar_arrive(&sm.decoded[b]);
             if (mine && fail == 0) {
