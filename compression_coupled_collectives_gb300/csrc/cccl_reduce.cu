@@ -14,13 +14,18 @@
 //                        registers; sizes it (the team meets twice); saves its
 //                        state to shared memory and writes its chunk of the
 //                        previous group, which the placer has placed meanwhile;
-//   loader (warp 12)     takes a ticket per group, locates every rank's
-//                        chunks through their offset tables and streams them
-//                        to the teams through one ring of staged rank chunks
-//                        per team, by bulk (TMA) copies;
+//   loader (warp 12)     checks every rank's stream header once; takes a
+//                        ticket per group, one group ahead; locates every
+//                        rank's chunks through their offset tables and
+//                        streams them to the teams through one ring of staged
+//                        rank chunks per team, by bulk (TMA) copies, to
+//                        whichever team has a slot free;
 //   placer (warp 13)     places each sized group with one decoupled look-back.
 // So the look-back of group i overlaps the decode of group i + 1, and the
-// copies of later rank chunks are in flight meanwhile.  The output chunk
+// copies of later rank chunks are in flight meanwhile.  A team meets once per
+// rank chunk (its copy has landed, and every warp is done with the previous
+// one, whose slot is then released), and its per-chunk bookkeeping is spread
+// over its warps.  The output chunk
 // reaches shared memory only as its saved state (a column of words per
 // thread), never as staged output.
 // Tickets hand out groups in order to CTAs that are already running, and a
