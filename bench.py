@@ -76,11 +76,26 @@ def sum_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def code_lines(text: str) -> list[str]:
+    """The lines of a kernel source that the compiler sees as code: `//`
+    comments, trailing blanks and empty lines dropped (no string literal in
+    these sources holds `//`)."""
+    out = []
+    for line in text.splitlines():
+        line = line.split("//", 1)[0].rstrip()
+        if line:
+            out.append(line)
+    return out
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code, so that a comment edit does not
+    invalidate counters taken on the same code."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "compression_coupled_collectives_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "compression_coupled_collectives_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update("\n".join(code_lines(fh.read())).encode())
+            h.update(b"\0")
     return h.hexdigest()[:16]
 
 
