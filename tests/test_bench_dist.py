@@ -63,3 +63,29 @@ def test_single_process_defaults(monkeypatch):
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.simulated_ranks(0) == [0, 1]
     assert bench.simulated_ranks(3) == [6, 7]
+
+
+def test_kernel_source_hash_ignores_comments():
+    import bench
+
+    code = "int f(int x) {  // doubles\n    return 2 * x;\n}\n"
+    assert bench.code_lines(code) == ["int f(int x) {", "    return 2 * x;", "}"]
+    assert bench.code_lines("// only a comment\n\n   \n") == []
+    assert bench.code_lines(code) == bench.code_lines("// header\n" + code.replace("doubles", "twice"))
+    assert bench.code_lines(code) != bench.code_lines(code.replace("2 * x", "3 * x"))
+
+
+def test_recorded_traffic_is_consistent():
+    import json
+    import os
+
+    import bench
+
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        recs = json.load(f)
+    for k in ("compress_kernel", "reduce_kernel", "decompress_kernel"):
+        rec = recs[k]
+        assert rec["bytes_per_launch_scaled"] == rec["dram_read_bytes"] + rec["dram_write_bytes"]
+        assert len(rec["source_hash"]) == 16
+        # used only while it names the current kernel code
+        assert (bench.recorded_traffic(k) is not None) == (rec["source_hash"] == bench.kernel_source_hash())
