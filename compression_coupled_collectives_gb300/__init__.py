@@ -69,6 +69,8 @@ _lib.cccl_reduce_typed.argtypes = [_i, _i, _vp, ctypes.POINTER(_vp), ctypes.POIN
 _lib.cccl_reduce_typed.restype = _i
 _lib.cccl_get_result.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_i)]
 _lib.cccl_get_result.restype = _i
+_lib.cccl_selftest_timeouts.argtypes = [_vp, _sz, _vp]
+_lib.cccl_selftest_timeouts.restype = _i
 _lib.cccl_status_string.argtypes = [_i]
 _lib.cccl_status_string.restype = ctypes.c_char_p
 
@@ -267,6 +269,13 @@ def cccl_get_result(ws: torch.Tensor, stream=None) -> tuple[int, int]:
     _check(_lib.cccl_get_result(ws.data_ptr(), _stream(stream), ctypes.byref(nbytes), ctypes.byref(dev)),
            "cccl_get_result")
     return int(nbytes.value), int(dev.value)
+
+
+def cccl_selftest_timeouts(ws: torch.Tensor, stream=None) -> None:
+    """Enqueue the bounded-wait self test (an mbarrier wait and a look-back
+    that never complete); cccl_get_result then reports CCCL_ERR_TIMEOUT."""
+    _check(_lib.cccl_selftest_timeouts(ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "cccl_selftest_timeouts")
 
 
 # ---------------------------------------------------------------- conveniences

@@ -9,6 +9,29 @@
 #include "cccl_device.cuh"
 #include "cccl_launch.h"
 
+namespace cccl {
+
+// cccl_selftest_timeouts: warp 0 waits on an mbarrier that no thread arrives
+// on; warp 1 runs the look-back of unit 1, whose predecessor (unit 0) never
+// publishes.  Both waits give up after kWaitLimitNs; each records TIMEOUT.
+__global__ void selftest_timeouts_kernel(WsHeader* ws) {
+    __shared__ uint64_t never;
+    if (threadIdx.x == 0) {
+        mbar_init(&never, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    uint64_t* status = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + sizeof(WsHeader));
+    if (threadIdx.x < 32) {
+        const bool done = mbar_wait(&never, 0);
+        if (!done && threadIdx.x == 0) record_error(ws, kStatusTimeout);
+    } else {
+        lookback_offset_wide(status, 1, 16, data_start(2), ws);
+    }
+}
+
+}  // namespace cccl
+
 namespace {
 
 using cccl::kChunkElems;
@@ -344,6 +367,16 @@ cccl_status cccl_get_result(const void* d_ws, cccl_stream_t stream, uint64_t* ou
     if (out_bytes) *out_bytes = h.error ? 0 : h.total_bytes;
     if (dev_status) *dev_status = static_cast<cccl_status>(h.error);
     return CCCL_OK;
+}
+
+cccl_status cccl_selftest_timeouts(void* d_ws, size_t ws_bytes, cccl_stream_t stream) {
+    const size_t need = cccl_workspace_bytes(8192);
+    if (d_ws == nullptr || !aligned16(d_ws) || ws_bytes < need || !device_range(d_ws, need))
+        return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, need, s) != CCCL_OK) return CCCL_ERR_CUDA;
+    cccl::selftest_timeouts_kernel<<<1, 64, 0, s>>>(static_cast<cccl::WsHeader*>(d_ws));
+    return cudaGetLastError() == cudaSuccess ? CCCL_OK : CCCL_ERR_CUDA;
 }
 
 const char* cccl_status_string(cccl_status status) {

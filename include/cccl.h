@@ -314,6 +314,23 @@ cccl_status cccl_reduce_typed(int dtype, int op, const void *d_local, const void
  * workspace, CUDA if the copy or the synchronisation failed, else OK. */
 cccl_status cccl_get_result(const void *d_ws, cccl_stream_t stream, uint64_t *out_bytes, cccl_status *dev_status);
 
+/* Failure-detection self test of the library's bounded waits ("CCCL: In-GPU
+ * Compression-Coupled Collective Communication" gives no failure model; every
+ * device wait here gives up after 2 s of GPU time rather than spin forever).
+ * One small kernel runs both kinds of wait against a condition that never
+ * completes: an mbarrier no thread arrives on, and a decoupled look-back
+ * whose predecessor never publishes its size.  Each gives up after the
+ * library's wait limit (2 s) and records TIMEOUT in the workspace, as a
+ * stalled compress, decompress or reduce would; nothing faults, and the
+ * context stays usable.
+ *   d_ws          device workspace of at least cccl_workspace_bytes(8192)
+ *                 bytes, 16-byte aligned; cleared here first.
+ *   stream        the stream to run on.
+ * Returns INVALID_ARG for a null, misaligned, too small or non-device
+ * workspace, CUDA if the clear or the launch failed, else OK; then
+ * cccl_get_result reports TIMEOUT (after about 2 s). */
+cccl_status cccl_selftest_timeouts(void *d_ws, size_t ws_bytes, cccl_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char *cccl_status_string(cccl_status status);
 

@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
                             "cccl_decompress", "cccl_reduce_compressed", "cccl_reduce_mixed", "cccl_get_result",
                             "cccl_status_string", "cccl_compress_paged", "cccl_decompress_paged",
                             "cccl_compress_window", "cccl_reduce_op", "cccl_compress_bound_typed",
-                            "cccl_compress_typed", "cccl_decompress_typed", "cccl_reduce_typed"]), names
+                            "cccl_compress_typed", "cccl_decompress_typed", "cccl_reduce_typed",
+                            "cccl_selftest_timeouts"]), names
 
 
 def test_library_exports_every_declared_symbol(cc):
@@ -163,3 +164,14 @@ def test_host_pointers_are_refused(cc):
     al = lambda a: (a.ctypes.data + 15) // 16 * 16
     r = cc._lib.cccl_compress(al(x), n, al(out), cc.cccl_compress_bound(n), al(ws), cc.cccl_workspace_bytes(n), None)
     assert r == cc.CCCL_ERR_INVALID_ARG
+
+
+def test_selftest_timeouts_argument_checks(cc):
+    lib = cc._lib
+    need = cc.cccl_workspace_bytes(8192)
+    ws = np.zeros(need + 16, np.uint8)
+    base = (ws.ctypes.data + 15) // 16 * 16
+    assert lib.cccl_selftest_timeouts(None, need, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_selftest_timeouts(base + 4, need, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_selftest_timeouts(base, need - 16, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_selftest_timeouts(base, need, None) == cc.CCCL_ERR_INVALID_ARG  # host memory

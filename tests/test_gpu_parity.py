@@ -605,3 +605,25 @@ def test_streams_past_4_gib(cc, orc, wl):
         assert torch.equal(cc.decompress(s_dev, n), x)
     del xs, streams, red
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- bounded waits
+def test_bounded_waits_time_out_and_the_context_survives(cc, orc, wl):
+    """An mbarrier no thread arrives on and a look-back whose predecessor never
+    publishes: both waits give up after the 2 s limit and report TIMEOUT on the
+    host; the context stays usable for the next call."""
+    import time
+
+    ws = cc.empty_workspace(8192)
+    t0 = time.time()
+    cc.cccl_selftest_timeouts(ws)
+    nbytes, st = cc.cccl_get_result(ws)
+    took = time.time() - t0
+    assert st == cc.CCCL_ERR_TIMEOUT
+    assert nbytes == 0
+    assert 1.5 < took < 30.0
+    # the look-back poisoned its own unit for its successors
+    status = ws[16:32].cpu().numpy().view(np.uint64)
+    assert int(status[1]) >> 62 == 3
+    x = wl.generate(2, 0, count=3 * CHUNK + 7, n=1 << 20)
+    assert np.array_equal(cc.compress(dev(x)).cpu().numpy(), orc.compress(x))
