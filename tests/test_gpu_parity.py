@@ -559,6 +559,54 @@ def test_step_captured_in_a_cuda_graph(cc, orc, wl):
         assert np.array_equal(host_u16(y), orc.decompress(want_red, n)), rep
 
 
+def test_full_size_step_in_a_cuda_graph(cc, orc, wl):
+    """The benchmark's step as it times it: workload 2 at full size on two
+    simulated ranks, captured once as a CUDA graph and replayed.  Every replay
+    gives the same bytes as the plain calls (whose streams the full-size
+    workload test checks against the oracle), and sampled chunks match the
+    oracle directly."""
+    n = wl.SIZES[2]
+    xs_host = [wl.generate(2, r) for r in range(2)]
+    xs = [dev(x) for x in xs_host]
+    outs = [cc.empty_stream(n) for _ in xs]
+    red = cc.empty_stream(n)
+    y = torch.empty(n, dtype=torch.int16, device="cuda")
+    wss = [cc.empty_workspace(n) for _ in range(4)]
+
+    def step(s=None):
+        for x, o, w in zip(xs, outs, wss):
+            cc.cccl_compress(x, o, w, stream=s)
+        cc.cccl_reduce_compressed(outs, n, red, wss[2], stream=s)
+        cc.cccl_decompress(red, y, wss[3], stream=s)
+
+    step()
+    plain = [o[:cc.cccl_get_result(w)[0]].clone() for o, w in zip(outs + [red], wss[:3])]
+    y_plain = y.clone()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=side):
+        step(torch.cuda.current_stream())
+    for rep in range(2):
+        for t in outs + [red, y]:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for o, w, p in zip(outs + [red], wss[:3], plain):
+            nb, st = cc.cccl_get_result(w)
+            assert st == 0 and nb == p.numel() and torch.equal(o[:nb], p), rep
+        assert torch.equal(y, y_plain), rep
+    # sampled chunks of the replayed streams against the oracle
+    head = outs[0][:64 + 8 * (n // CHUNK)].cpu().numpy().tobytes()
+    for c in (0, 1, 4095, n // CHUNK - 1):
+        o0, o1 = struct.unpack_from("<QQ", head, 64 + 8 * c) if c + 1 < n // CHUNK else (
+            struct.unpack_from("<Q", head, 64 + 8 * c)[0], plain[0].numel())
+        got = outs[0][o0:o1].cpu().numpy().tobytes()
+        assert got == bytes(orc.encode_chunk(xs_host[0][c * CHUNK:(c + 1) * CHUNK])), c
+    want = orc.sum_ranks([x[:8 * CHUNK] for x in xs_host])
+    assert np.array_equal(host_u16(y[:8 * CHUNK]), want)
+
+
 # ---------------------------------------------------------------- streams past 4 GiB
 def test_streams_past_4_gib(cc, orc, wl):
     """3 x 2^30 + 3 chunks + 5 values per rank (about 6 GiB of bf16; the
