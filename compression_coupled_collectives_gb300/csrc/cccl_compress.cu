@@ -248,19 +248,23 @@ __global__ void __launch_bounds__(compress_threads<D>(), 1)
     }
 }
 
+// Per-device record of the shared-memory limit set for compress_kernel<D, W>,
+// by element type code and table choice (a plain static array, so that each
+// copy of this library loaded into a process keeps its own).
+static PerDeviceOnce g_compress_smem_limit[4][2];
+
 template <class D, bool kWindow>
 cudaError_t launch_compress_t(const uint8_t* in, uint64_t n_elems, uint8_t* out, uint64_t capacity, void* ws,
                               cudaStream_t stream, const Paging& pg) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(compress_kernel<D, kWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)compress_smem<D>());
-    });
-    if (attr != cudaSuccess) return attr;
+    PerDeviceOnce& smem_limit = g_compress_smem_limit[D::kCode][kWindow ? 1 : 0];
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = smem_limit.run(dev, [] {
+            return cudaFuncSetAttribute(compress_kernel<D, kWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)compress_smem<D>());
+        });
     if (e != cudaSuccess) return e;
     StreamOut so;
     so.out = out;

@@ -184,6 +184,8 @@ __device__ __forceinline__ void bulk_store(void* dst_gmem, const void* src_smem,
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the committed bulk stores of this thread have read their source.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until the committed bulk stores of this thread have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Barriers over the threads that decode or encode one chunk together: the
 // whole CTA, or a named barrier over the 4 warps of a team (every
@@ -347,8 +349,12 @@ __device__ __forceinline__ void publish_unit_size(uint64_t* status, uint64_t g, 
 }
 
 // `published`: the unit's size was already published with publish_unit_size.
+// `max_nap_ns`: the longest back-off between polls of an unfinished window
+// (a caller off the critical path polls less often, leaving issue slots to
+// the warps that share its SM sub-partition).
 __device__ __forceinline__ uint64_t lookback_offset_wide(uint64_t* status, uint64_t g, uint32_t bytes, uint64_t start,
-                                                         WsHeader* ws, bool published = false) {
+                                                         WsHeader* ws, bool published = false,
+                                                         uint32_t max_nap_ns = 512) {
     const uint32_t lane = threadIdx.x & 31;
     if (!published && lane == 0) publish_unit_size(status, g, bytes, start);
     if (g == 0) return start;
@@ -385,7 +391,7 @@ __device__ __forceinline__ uint64_t lookback_offset_wide(uint64_t* status, uint6
                 return kFlagPoison;
             }
             __nanosleep(ns);
-            if (ns < 512) ns <<= 1;
+            if (ns < max_nap_ns) ns <<= 1;
             continue;
         }
         uint32_t part = 0;  // aggregates are unit sizes (< 2^17 each)

@@ -634,15 +634,17 @@ __device__ __forceinline__ TeamPlan plan_chunk_team(const Barrier& bar, const ui
     return pl;
 }
 
-// Phase B for a team: write the chunk in P (planes from phase A) to `dst`
-// (global, 16-byte aligned).  No barrier: each warp writes the header (warp 0),
-// its four rows of the residual section, its word of every bit-plane and
-// its escapes, whose place follows from esc_before.  `xq`: this thread's
-// 8-word scratch column in shared memory (word m at xq[128 m]), where the
-// exponent quads wait for the escape writer.
+// Phase B for a team: the chunk in P (planes from phase A), in its final
+// byte layout, into `dst`, a staging buffer in shared memory (16-byte
+// aligned) whose first pl.bytes bytes are all written.  No barrier: each warp
+// writes the header (warp 0), its four rows of the residual section, its word
+// of every bit-plane and its escapes, whose place follows from esc_before.  A
+// thread with escapes first parks its exponent quads in its own 32 bytes of
+// the residual section, reads the escaped bytes back from there, then
+// overwrites them with the residual values.
 template <class D>
-__device__ __forceinline__ void write_chunk_team(const uint32_t* P, const uint32_t planes[8], const TeamPlan& pl,
-                                                 uint8_t* dst, uint32_t* xq) {
+__device__ __forceinline__ void stage_chunk_team(const uint32_t* P, const uint32_t planes[8], const TeamPlan& pl,
+                                                 uint8_t* dst) {
     const uint32_t lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
     uint8_t* body = dst + kChunkHeaderBytes;
     if (q == 0 && lane == 0)
@@ -666,9 +668,35 @@ __device__ __forceinline__ void write_chunk_team(const uint32_t* P, const uint32
         }
         return;
     }
+    const uint32_t k = pl.k, n_esc = pl.n_esc;
+    uint8_t* own = body + 256 * 4 * q + 8 * lane;  // this thread's bytes of rows 4 q .. 4 q + 3
+    const uint32_t esc = k ? escape_word<D>(planes, k) : 0u;
+    if (n_esc != 0) {
+        // escapes of the lanes before this one, from six independent ballots
+        // of the count's bits (a count is at most 32)
+        const uint32_t mine = __popc(esc), below = (1u << lane) - 1u;
+        uint32_t idx = pl.esc_before;
+#pragma unroll
+        for (int b = 0; b < 6; ++b) idx += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, (mine >> b) & 1u) & below) << b;
+        uint8_t* esc_out = body + D::kResidBytes + kPlaneBytes * k;
+        if (esc) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                *reinterpret_cast<uint2*>(own + 256 * jj) =
+                    make_uint2(exponent_quad<D>(P, 2 * jj), exponent_quad<D>(P, 2 * jj + 1));
+            uint32_t rest = esc;
+            while (rest) {
+                const uint32_t bit = __ffs(rest) - 1;  // element (m, b) = byte b of quad m
+                rest &= rest - 1;
+                if (idx < n_esc) esc_out[idx] = own[((bit & 6) << 7) | ((bit & 1) << 2) | (bit >> 3)];
+                ++idx;
+            }
+        }
+        if (q == 0 && lane < 16 && n_esc + lane < pad16(n_esc)) esc_out[n_esc + lane] = 0;
+    }
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-        uint8_t* plane_row = body + 256 * (4 * q + jj) + 8 * lane;
+        uint8_t* plane_row = own + 256 * jj;
         if constexpr (D::kElemBytes == 4) {
             const uint32_t* R = P + 8 * jj;
             *reinterpret_cast<uint2*>(plane_row) =
@@ -690,37 +718,10 @@ __device__ __forceinline__ void write_chunk_team(const uint32_t* P, const uint32
         for (int t = 0; t < 3; ++t)
             *reinterpret_cast<uint32_t*>(body + kSmPlaneBytes + kPlaneBytes * t + 4 * (32 * q + lane)) = planes[5 + t];
     }
-    const uint32_t k = pl.k;
-    if (k == 0) return;
-    uint32_t esc = escape_word<D>(planes, k);
     uint8_t* col = body + D::kResidBytes + 4 * (32 * q + lane);
 #pragma unroll
     for (uint32_t p = 0; p < max_width<D>(); ++p)
         if (p < k) *reinterpret_cast<uint32_t*>(col + kPlaneBytes * p) = planes[p] | esc;
-    const uint32_t n_esc = pl.n_esc;
-    if (n_esc == 0) return;
-    // escapes of the lanes before this one, from six independent ballots of
-    // the count's bits (a count is at most 32)
-    const uint32_t mine = __popc(esc), below = (1u << lane) - 1u;
-    uint32_t excl = 0;
-#pragma unroll
-    for (int b = 0; b < 6; ++b) excl += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, (mine >> b) & 1u) & below) << b;
-    uint32_t idx = pl.esc_before + excl;
-    uint8_t* esc_out = body + D::kResidBytes + kPlaneBytes * k;
-    if (esc) {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) xq[128 * m] = exponent_quad<D>(P, m);
-    }
-    const uint8_t* xb = reinterpret_cast<const uint8_t*>(xq);
-    while (__any_sync(0xFFFFFFFFu, esc != 0u)) {
-        if (esc) {
-            const uint32_t bit = __ffs(esc) - 1;  // element (m, b) = byte b of quad m
-            esc &= esc - 1;
-            if (idx < n_esc) esc_out[idx] = xb[512 * (bit & 7) + (bit >> 3)];
-            ++idx;
-        }
-    }
-    if (q == 0 && lane < 16 && n_esc + lane < pad16(n_esc)) esc_out[n_esc + lane] = 0;
 }
 
 template <class D>

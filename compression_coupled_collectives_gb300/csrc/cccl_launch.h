@@ -1,11 +1,33 @@
 // cccl_launch.h -- launchers of the three kernels (host side, internal).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace cccl {
+
+// Runs a per-device set-up step (a kernel attribute, which belongs to the
+// current device's context) the first time it is asked for on each device:
+// run(dev, fn) calls fn() until it has succeeded once for `dev`, then returns
+// cudaSuccess without calling it.  Devices 0..63 are remembered; for others
+// fn() runs every time.  Concurrent first calls may both run fn(), which is
+// harmless for an attribute.
+class PerDeviceOnce {
+  public:
+    template <typename Fn>
+    cudaError_t run(int dev, Fn fn) {
+        const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+        if (bit != 0 && (done_.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+        const cudaError_t e = fn();
+        if (e == cudaSuccess && bit != 0) done_.fetch_or(bit, std::memory_order_acq_rel);
+        return e;
+    }
+
+  private:
+    std::atomic<uint64_t> done_{0};
+};
 
 constexpr int kMaxRanks = 64;
 

@@ -5,33 +5,38 @@
 // the NCCL data path" (CopyReducePacks); Figure 2).  Also min and max.
 //
 // Persistent and pipelined, one CTA per SM with three roles:
-//   teams (warps 0..11)  three independent teams of 4 warps.  Per group of
-//                        three consecutive output chunks, team t takes chunk
-//                        t: it decodes chunk c of every rank, in rank order,
-//                        a quarter per warp, keeping 32 binary32 sums per
-//                        thread in registers; rounds once to the element type
-//                        (bf16, fp16; fp32 needs none) and keeps the chunk in
-//                        registers; sizes it (the team meets twice); saves its
-//                        state to shared memory and writes its chunk of the
-//                        previous group, which the placer has placed meanwhile;
-//   loader (warp 12)     checks every rank's stream header once; takes a
+//   teams (warps 0..4T-1)  T independent teams of 4 warps.  Per group of T
+//                        consecutive output chunks, team t takes chunk t.
+//                        Each warp of the team decodes its quarter of chunk c
+//                        of every rank, in rank order, on its own (no team
+//                        barrier per rank: the warp counts the escapes of the
+//                        quarters before its own itself), keeping 32 binary32
+//                        sums per thread in registers.  The team then meets,
+//                        rounds once to the element type (bf16, fp16; fp32
+//                        needs none), sizes the chunk (two more meetings) and
+//                        writes it, in its final byte layout, into one of its
+//                        staging buffers in shared memory;
+//   loader (warp 4T)     checks every rank's stream header once; takes a
 //                        ticket per group, one group ahead; locates every
-//                        rank's chunks through their offset tables and
-//                        streams them to the teams through one ring of staged
-//                        rank chunks per team, by bulk (TMA) copies, to
-//                        whichever team has a slot free;
-//   placer (warp 13)     places each sized group with one decoupled look-back.
-// So the look-back of group i overlaps the decode of group i + 1, and the
-// copies of later rank chunks are in flight meanwhile.  A team meets once per
-// rank chunk (its copy has landed, and every warp is done with the previous
-// one, whose slot is then released), and its per-chunk bookkeeping is spread
-// over its warps.  The output chunk
-// reaches shared memory only as its saved state (a column of words per
-// thread), never as staged output.
+//                        rank's chunk through its offset table and reads and
+//                        checks its header; streams the chunks to the teams
+//                        by bulk (TMA) copies, through one ring of staged rank
+//                        chunks per team, each team's in rank order, to
+//                        whichever team has a slot free; and while the
+//                        copies of a group wait for slots, locates the next
+//                        group;
+//   placer (warp 4T+1)   places each sized group with one decoupled
+//                        look-back, then copies the group's staged chunks to
+//                        their final places with one bulk (TMA) store each
+//                        and writes their offset-table entries.
+// So the teams never wait for a placement: the look-back of group i and the
+// copies out overlap the decoding of group i + 1, and the copies of later
+// rank chunks are in flight meanwhile.  A team meets four times per output
+// chunk whatever the number of ranks: after the group's description, after
+// its decodes (to agree on timeouts and on Inf/NaN), and twice to size the
+// chunk.
 // Tickets hand out groups in order to CTAs that are already running, and a
 // group is sized without waiting on any later group: every look-back ends.
-#include <mutex>
-
 #include "cccl_decode.cuh"
 #include "cccl_encode.cuh"
 #include "cccl_launch.h"
@@ -39,48 +44,41 @@
 namespace cccl {
 
 constexpr int kMaxTeams = 4;
-constexpr int kTeamThreads = 128;
-// decode teams per CTA = output chunks per group: 3, whose 14 warps leave
-// 128 registers per thread (a fourth team would leave 96, and the team code
-// spills there)
+// decode teams per CTA = output chunks per group: 3, so that the CTA's 14
+// warps (at most 4 per SM sub-partition) get 128 registers per thread
 template <class D>
 __host__ __device__ constexpr int teams() { return 3; }
 template <class D>
-__host__ __device__ constexpr int loader_warp() { return 4 * teams<D>(); }
+__host__ __device__ constexpr int loader_warp() { return 4 * teams<D>(); }   // also the locator
 template <class D>
-__host__ __device__ constexpr int placer_warp() { return loader_warp<D>() + 1; }
+__host__ __device__ constexpr int copier_warp() { return loader_warp<D>() + 1; }  // idle with one loader warp
+template <class D>
+__host__ __device__ constexpr int placer_warp() { return copier_warp<D>() + 1; }
+// group descriptions in flight: the loader describes group i + 1 while the
+// teams may still read those of groups i - 1 and i
+constexpr int kMetaBufs = 3;
 template <class D>
 __host__ __device__ constexpr int reduce_threads() { return 32 * (placer_warp<D>() + 1); }
 constexpr uint64_t kNoGroup = ~0ull;
-// staged rank chunks per team: 4 of 8.2 KB for the 16-bit types, 3 of 16.4 KB
-// for fp32
+// staged rank chunks per team: 6 of 8.2 KB for the 16-bit types (the copies
+// for the next output chunk are in flight while the team decodes this one),
+// 2 of 16.4 KB for fp32
 template <class D>
-__host__ __device__ constexpr int rslots() { return D::kElemBytes == 4 ? 3 : 4; }
-constexpr int kMaxRSlots = 4;
-// a team thread's chunk state between sizing and writing: its words, planes[8]
+__host__ __device__ constexpr int rslots() { return D::kElemBytes == 4 ? 2 : 6; }
+constexpr int kMaxRSlots = 6;
+// output staging buffers per team, cycled by group: a team stages the chunk
+// of group i while the placer still copies out the one of group i - 1
 template <class D>
-__host__ __device__ constexpr int prev_words() { return thread_words<D>() + 8; }
+__host__ __device__ constexpr int sbufs() { return 2; }
+constexpr int kMaxSBufs = 2;
 template <class D>
 __host__ __device__ constexpr size_t ring_bytes() { return (size_t)teams<D>() * rslots<D>() * max_chunk_bytes<D>(); }
-// sized chunks a team keeps in shared memory while the placer places them:
-// a team writes group i - pend_depth at iteration i, so the look-back of a
-// group overlaps the decoding of the next group
 template <class D>
-__host__ __device__ constexpr int pend_depth() { return 1; }
-// placement buffers (sizes -> offsets), cycled by group: one more than the depth
-template <class D>
-__host__ __device__ constexpr int place_bufs() { return pend_depth<D>() + 1; }
-constexpr int kMaxPlaceBufs = 3;
-// chunk-state slots per team.  The 16-bit types keep one more than the
-// pending chunks: the chunk just sized is saved before a pending one is
-// written, so their states never share registers.  fp32, short of shared
-// memory, writes the pending chunk first and then saves into its slot.
-template <class D>
-__host__ __device__ constexpr int state_slots() { return D::kElemBytes == 4 ? pend_depth<D>() : pend_depth<D>() + 1; }
-template <class D>
-__host__ __device__ constexpr size_t reduce_smem() {
-    return ring_bytes<D>() + (size_t)teams<D>() * state_slots<D>() * prev_words<D>() * kTeamThreads * 4;
+__host__ __device__ constexpr size_t staging_bytes() {
+    return (size_t)teams<D>() * sbufs<D>() * max_chunk_bytes<D>();
 }
+template <class D>
+__host__ __device__ constexpr size_t reduce_smem() { return ring_bytes<D>() + staging_bytes<D>(); }
 
 // binary32 pair -> bf16 pair, round to nearest even (hi lane from the upper word)
 __device__ __forceinline__ uint32_t round_pair_bf16(uint64_t v) {
@@ -150,35 +148,52 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity));
 }
 
+// A rank chunk's header, checked by the loader, packed for the teams: base
+// in bits 0..7, k in 8..10, raw in bit 11 (also for the uncompressed local
+// operand), n_esc in bits 16..31.
+__device__ __forceinline__ uint32_t pack_desc(const ChunkHeader& h) {
+    return h.base | (h.k << 8) | ((h.mode == kModeRaw ? 1u : 0u) << 11) | (h.n_esc << 16);
+}
+constexpr uint32_t kDescRaw = 1u << 11;
+__device__ __forceinline__ ChunkHeader unpack_desc(uint32_t d) {
+    ChunkHeader h;
+    h.base = d & 0xFFu;
+    h.k = (d >> 8) & 7u;
+    h.mode = (d & kDescRaw) ? kModeRaw : kModePacked;
+    h.n_esc = d >> 16;
+    h.n_c = 0;
+    h.bytes = 0;
+    return h;
+}
+
 // What the loader hands the teams for one group.
 struct ReduceMeta {
     uint64_t g;                          // group index, or kNoGroup: no more groups
-    uint32_t ok;                         // every (chunk, rank) was located
+    uint32_t ok;                         // every (chunk, rank) was located and its header is valid
     uint32_t n_out;                      // output chunks in the group
     uint64_t off[kMaxTeams][kMaxRanks];  // rank r's chunk teams * g + t: offset in its stream
-    uint32_t bytes[kMaxTeams][kMaxRanks];  //   and size
+    uint32_t bytes[kMaxTeams][kMaxRanks];  //   its size
+    uint32_t desc[kMaxTeams][kMaxRanks];   //   and its header (pack_desc)
 };
 
 struct ReduceSmem {
-    uint64_t meta_ready[2];              // loader -> teams: meta[b] describes the next group (1 arrival)
-    uint64_t decoded[2];                 // teams -> loader: meta[b] read (one arrival per team warp)
-    uint64_t sized[kMaxPlaceBufs];       // teams -> placer: sizes in size[p] (one arrival per team)
-    uint64_t placed[kMaxPlaceBufs];      // placer -> teams: offsets in off[p] (1 arrival)
+    uint64_t meta_ready[kMetaBufs];      // loader -> teams: meta[b] describes the next group (1 arrival)
+    uint64_t decoded[kMetaBufs];         // teams, loader -> loader: meta[b] read (each team warp and the loader)
+    uint64_t sized[kMaxSBufs];           // teams -> placer: the group's sizes are in (one arrival per team)
+    uint64_t staged[kMaxSBufs];          // teams -> placer: the group's chunks are staged (one per team warp)
+    uint64_t stored[kMaxSBufs];          // placer -> teams: the group's staging buffers were read (1 arrival)
     uint64_t full[kMaxTeams][kMaxRSlots];   // a rank chunk landed in the slot (transaction count)
-    uint64_t free_[kMaxTeams][kMaxRSlots];  // the team is done with the slot (1 arrival)
-    unsigned long long tally[kMaxPlaceBufs];  // sized teams (high word) and their bytes (low word)
-    uint32_t size[kMaxPlaceBufs][kMaxTeams];
-    uint32_t failed[kMaxPlaceBufs][kMaxTeams];   // the team's chunk could not be reduced
-    uint64_t gid[kMaxPlaceBufs];         // group sized in buffer p, or kNoGroup
-    uint64_t off[kMaxPlaceBufs][kMaxTeams];      // chunk offsets, or kFlagPoison
-    TeamPlan pend_pl[kMaxTeams][3][4];   // a pending chunk's plan, per team, slot and warp
-    uint64_t pend_c[kMaxTeams][3];       //   its chunk index
-    uint32_t pend_bytes[kMaxTeams][3];   //   and size (0: nothing to write)
-    uint32_t row_tot[kMaxTeams][4];         // the decoder's per-quarter escape totals
+    uint64_t free_[kMaxTeams][kMaxRSlots];  // every warp of the team is done with the slot (4 arrivals)
+    unsigned long long tally[kMaxSBufs];    // sized teams (high word) and their bytes (low word)
+    uint32_t size[kMaxSBufs][kMaxTeams];
+    uint32_t failed[kMaxSBufs][kMaxTeams];  // the team's chunk could not be reduced
+    uint64_t gid[kMaxSBufs];                // group sized in buffer p, or kNoGroup
+    int32_t esc_diff[kMaxTeams][kMaxRanks]; // per rank: sentinel codes found minus the header's escapes
+    uint32_t corrupt[kMaxTeams][2];         // a rank chunk body is malformed (by iteration parity)
     TeamXch xch[kMaxTeams];                 // the encoder's exchange space
-    volatile uint32_t abort;             // a bounded wait ran out: every role stops
-    ReduceMeta meta[2];
-    uint64_t total[kMaxRanks];           // rank r's stream size from its checked header (0: unusable)
+    volatile uint32_t abort;                // a bounded wait ran out: every role stops
+    ReduceMeta meta[kMetaBufs];
+    uint64_t total[kMaxRanks];              // rank r's stream size from its checked header (0: unusable)
 };
 
 __device__ __forceinline__ void set_abort(const StreamOut& so, ReduceSmem& sm) {
@@ -187,6 +202,86 @@ __device__ __forceinline__ void set_abort(const StreamOut& so, ReduceSmem& sm) {
 }
 
 // --------------------------------------------------------------------------- loader
+// Group j's description, into meta[j % kMetaBufs]: every rank's chunk located
+// through its offset table, its header read once and checked.  `next` holds
+// (lane 0) the ticket taken one group ahead; `last` is set once the tickets
+// run out (the description then says kNoGroup).  False if a bounded wait ran
+// out.
+template <class D>
+__device__ __forceinline__ bool locate_group(const ReduceInputs& inputs, int R, const StreamOut& so, ReduceSmem& sm,
+                                             int j, uint64_t& next, bool& last) {
+    constexpr int kTeams = teams<D>();
+    constexpr uint32_t kRawBytes = D::kElemBytes * kChunkElems;
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t n_groups = (so.n_chunks + kTeams - 1) / kTeams;
+    const int b = j % kMetaBufs;
+    // meta[b] was last read, by the teams and the loader, for group j - kMetaBufs
+    if (j >= kMetaBufs && !warp_wait(&sm.decoded[b], (uint32_t)((j - kMetaBufs) / kMetaBufs) & 1u)) {
+        if (lane == 0) set_abort(so, sm);
+        return false;
+    }
+    const uint64_t g = __shfl_sync(0xFFFFFFFFu, next, 0);
+    if (lane == 0 && g < n_groups) next = atomicAdd(&so.ws->ticket, 1u);
+    ReduceMeta& m = sm.meta[b];
+    if (g >= n_groups) {
+        if (lane == 0) {
+            m.g = kNoGroup;
+            mbar_arrive(&sm.meta_ready[b]);
+        }
+        last = true;
+        return true;
+    }
+    const uint64_t c0 = g * kTeams;
+    const uint32_t n_out = (uint32_t)min((uint64_t)kTeams, so.n_chunks - c0);
+    bool ok = true;
+    for (uint32_t idx = lane; idx < n_out * (uint32_t)R; idx += 32) {
+        const uint32_t t = idx / (uint32_t)R, r = idx % (uint32_t)R;
+        if (r == 0 && inputs.local != nullptr) {  // uncompressed: chunk c is values 4096 c ..
+            const uint64_t c = c0 + t, left = so.n_elems - c * kChunkElems;
+            m.off[t][r] = (uint64_t)kRawBytes * c;
+            m.bytes[t][r] = D::kElemBytes * (uint32_t)(left < kChunkElems ? left : kChunkElems);
+            m.desc[t][r] = kDescRaw;
+            continue;
+        }
+        const uint64_t total = sm.total[r];
+        ChunkView v{0, 0, 0};
+        if (total != 0) v = locate_chunk_at<D>(inputs.in[r], total, so.n_chunks, c0 + t);
+        // the chunk header, read here once (the same bytes the bulk copy
+        // stages) and checked against the offset table and the chunk's
+        // element count
+        if (v.ok) {
+            const uint64_t left = so.n_elems - (c0 + t) * kChunkElems;
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(inputs.in[r] + v.offset));
+            ChunkHeader h;
+            h.mode = w.x & 0xFF;
+            h.k = (w.x >> 8) & 0xFF;
+            h.base = (w.x >> 16) & 0xFF;
+            h.n_c = w.y & 0xFFFF;
+            h.n_esc = w.y >> 16;
+            h.bytes = w.z;
+            if (!chunk_header_valid<D>(h, v.bytes, left < kChunkElems ? (uint32_t)left : kChunkElems)) v.ok = 0;
+            m.desc[t][r] = pack_desc(h);
+        }
+        m.off[t][r] = v.offset;
+        m.bytes[t][r] = v.bytes;
+        ok = ok && v.ok;
+    }
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (lane == 0) {
+        m.g = g;
+        m.ok = ok ? 1u : 0u;
+        m.n_out = n_out;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.meta_ready[b]);
+    return true;
+}
+
+// The loader warp: per group, in ticket order, its description (locate_group)
+// and the bulk (TMA) copies of its rank chunks into the teams' rings, each
+// team's in rank order, to whichever team has a slot free.  While the copies
+// of group i wait for ring slots, it locates group i + 1, so the description
+// of the next group is ready before its slots are.
 template <class D>
 __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R, const StreamOut& so, uint8_t* ring,
                                               ReduceSmem& sm) {
@@ -194,67 +289,28 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
     constexpr int kTeams = teams<D>();
     constexpr uint32_t kRawBytes = D::kElemBytes * kChunkElems;
     const uint32_t lane = threadIdx.x & 31;
-    const uint64_t n_groups = (so.n_chunks + kTeams - 1) / kTeams;
     // every rank's stream header, checked once
     for (int r = (int)lane; r < R; r += 32)
         sm.total[r] = (r == 0 && inputs.local != nullptr)
                           ? 1u
                           : stream_total<D>(inputs.in[r], inputs.in_bytes[r], so.n_elems, so.n_chunks);
     __syncwarp();
-    uint32_t ut[kTeams] = {};  // rank chunks issued to each team
-    bool stop = false;
     // lane 0: the ticket for the next group, taken one group ahead so that
     // its latency hides behind this group's work
     uint64_t next = 0;
     if (lane == 0) next = atomicAdd(&so.ws->ticket, 1u);
+    bool last = false;                        // the tickets have run out
+    int located = locate_group<D>(inputs, R, so, sm, 0, next, last) ? 0 : -1;  // last group described
+    uint32_t ut[kTeams] = {};  // rank chunks issued to each team
+    bool stop = located < 0;
     for (int i = 0; !stop && !warp_any(sm.abort); ++i) {
-        const int b = i & 1;
-        // meta[b] was last read by the teams for group i - 2
-        if (i >= 2 && !warp_wait(&sm.decoded[b], (uint32_t)((i - 2) >> 1) & 1u)) {
-            if (lane == 0) set_abort(so, sm);
-            break;
-        }
-        const uint64_t g = __shfl_sync(0xFFFFFFFFu, next, 0);
-        if (lane == 0 && g < n_groups) next = atomicAdd(&so.ws->ticket, 1u);
-        ReduceMeta& m = sm.meta[b];
-        if (g >= n_groups) {
-            if (lane == 0) {
-                m.g = kNoGroup;
-                mbar_arrive(&sm.meta_ready[b]);
-            }
-            break;
-        }
-        const uint64_t c0 = g * kTeams;
-        const uint32_t n_out = (uint32_t)min((uint64_t)kTeams, so.n_chunks - c0);
-        bool ok = true;
-        for (uint32_t idx = lane; idx < n_out * (uint32_t)R; idx += 32) {
-            const uint32_t t = idx / (uint32_t)R, r = idx % (uint32_t)R;
-            if (r == 0 && inputs.local != nullptr) {  // uncompressed: chunk c is values 4096 c ..
-                const uint64_t c = c0 + t, left = so.n_elems - c * kChunkElems;
-                m.off[t][r] = (uint64_t)kRawBytes * c;
-                m.bytes[t][r] = D::kElemBytes * (uint32_t)(left < kChunkElems ? left : kChunkElems);
-                continue;
-            }
-            const uint64_t total = sm.total[r];
-            ChunkView v{0, 0, 0};
-            if (total != 0) v = locate_chunk_at<D>(inputs.in[r], total, so.n_chunks, c0 + t);
-            m.off[t][r] = v.offset;
-            m.bytes[t][r] = v.bytes;
-            ok = ok && v.ok;
-        }
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (lane == 0) {
-            m.g = g;
-            m.ok = ok ? 1u : 0u;
-            m.n_out = n_out;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.meta_ready[b]);
-        if (!ok) continue;  // nothing to stream: the teams poison the group
-        // Every team gets its rank chunks in rank order; a team whose next
-        // slot is still busy does not hold up the others.
+        const int b = i % kMetaBufs;
+        const ReduceMeta& m = sm.meta[b];
+        if (m.g == kNoGroup) break;
+        const uint32_t n_out = m.n_out;
+        // nothing to stream for a group that could not be located: the teams poison it
+        uint32_t left = m.ok ? n_out * (uint32_t)R : 0u;
         uint32_t issued[kTeams] = {};  // this group's rank chunks issued to each team
-        uint32_t left = n_out * (uint32_t)R;
         uint64_t t_blocked = 0;
         uint32_t nap = 32;
         while (left > 0) {
@@ -290,7 +346,16 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
                 nap = 32;
                 continue;
             }
-            // every team with chunks left waits for a slot: back off, bounded
+            // every team with chunks left waits for a slot: describe the next
+            // group meanwhile, else back off, bounded
+            if (!last && located == i) {
+                if (!locate_group<D>(inputs, R, so, sm, i + 1, next, last)) {
+                    stop = true;
+                    break;
+                }
+                located = i + 1;
+                continue;
+            }
             if (warp_any(sm.abort)) {
                 stop = true;
                 break;
@@ -306,6 +371,12 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
             __nanosleep(nap);
             if (nap < 256) nap <<= 1;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.decoded[b]);  // the loader is done with meta[b]
+        if (!stop && !last && located == i) {
+            if (!locate_group<D>(inputs, R, so, sm, i + 1, next, last)) break;
+            located = i + 1;
+        }
     }
     // no copy may still be landing when the CTA exits
     for (int t = 0; t < kTeams; ++t)
@@ -313,41 +384,80 @@ __device__ __forceinline__ void reduce_loader(const ReduceInputs& inputs, int R,
             mbar_wait(&sm.full[t][v % kRSlots], (v / kRSlots) & 1u);
 }
 
-// --------------------------------------------------------------------------- placer
+// --------------------------------------------------------------------------- locator and copier
+// The loader's work split over two warps, for inputs that are nearly
+// incompressible: their raw rank chunks decode so fast that the teams wait
+// for data whenever the copies stop while a group is being located.  The
+// locator describes each group (locate_group), up to two groups ahead of the
+// teams; the copier issues the bulk copies, rank by rank over the teams, each
+// copy once its slot is free (a suspending wait, no polling).
 template <class D>
-__device__ __forceinline__ void reduce_placer(const StreamOut& so, ReduceSmem& sm) {
-    constexpr int kPB = place_bufs<D>();
-    constexpr int kTeams = teams<D>();
+__device__ __forceinline__ void reduce_locator(const ReduceInputs& inputs, int R, const StreamOut& so,
+                                               ReduceSmem& sm) {
     const uint32_t lane = threadIdx.x & 31;
-    for (int i = 0; !warp_any(sm.abort); ++i) {
-        const int b = i % kPB;
-        if (!warp_wait(&sm.sized[b], (uint32_t)(i / kPB) & 1u)) {
+    for (int r = (int)lane; r < R; r += 32)
+        sm.total[r] = (r == 0 && inputs.local != nullptr)
+                          ? 1u
+                          : stream_total<D>(inputs.in[r], inputs.in_bytes[r], so.n_elems, so.n_chunks);
+    __syncwarp();
+    uint64_t next = 0;
+    if (lane == 0) next = atomicAdd(&so.ws->ticket, 1u);
+    bool last = false;
+    for (int i = 0; !last && !warp_any(sm.abort); ++i)
+        if (!locate_group<D>(inputs, R, so, sm, i, next, last)) break;
+}
+
+template <class D>
+__device__ __forceinline__ void reduce_copier(const ReduceInputs& inputs, int R, const StreamOut& so, uint8_t* ring,
+                                              ReduceSmem& sm) {
+    constexpr int kRSlots = rslots<D>();
+    constexpr int kTeams = teams<D>();
+    constexpr uint32_t kRawBytes = D::kElemBytes * kChunkElems;
+    const uint32_t lane = threadIdx.x & 31;
+    uint32_t ut[kTeams] = {};
+    bool stop = false;
+    for (int i = 0; !stop && !warp_any(sm.abort); ++i) {
+        const int b = i % kMetaBufs;
+        if (!warp_wait(&sm.meta_ready[b], (uint32_t)(i / kMetaBufs) & 1u)) {
             if (lane == 0) set_abort(so, sm);
             break;
         }
-        const uint64_t g = sm.gid[b];
-        if (g == kNoGroup) break;
-        const uint32_t mine = lane < (uint32_t)kTeams ? sm.size[b][lane] : 0u;
-        const bool failed = warp_any(lane < (uint32_t)kTeams && sm.failed[b][lane] != 0);
-        uint32_t incl = mine;
+        const ReduceMeta& m = sm.meta[b];
+        if (m.g == kNoGroup) break;
+        const uint32_t n_out = m.n_out;
+        if (m.ok) {
+            for (int r = 0; r < R && !stop; ++r) {
 #pragma unroll
-        for (int d = 1; d < kTeams; d <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-            if (lane >= (uint32_t)d) incl += t;
+                for (int t = 0; t < kTeams; ++t) {
+                    if (t >= (int)n_out) break;
+                    const uint32_t s = ut[t] % kRSlots;
+                    if (ut[t] >= (uint32_t)kRSlots && !warp_wait(&sm.free_[t][s], (ut[t] / kRSlots - 1) & 1u)) {
+                        if (lane == 0) set_abort(so, sm);
+                        stop = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        fence_proxy_async_smem();
+                        uint8_t* slot = ring + ((size_t)t * kRSlots + s) * max_chunk_bytes<D>();
+                        if (r != 0 || inputs.local == nullptr)
+                            bulk_load(slot, inputs.in[r] + m.off[t][r], m.bytes[t][r], &sm.full[t][s]);
+                        else if (m.bytes[t][r] == kRawBytes)
+                            bulk_load(slot, static_cast<const uint8_t*>(inputs.local) + m.off[t][r], kRawBytes,
+                                      &sm.full[t][s]);
+                        else
+                            mbar_arrive(&sm.full[t][s]);
+                    }
+                    __syncwarp();
+                    ++ut[t];
+                }
+            }
         }
-        const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, kTeams - 1);
-        uint64_t go;
-        if (failed) {
-            if (lane == 0) st_relaxed_u64(&so.status[g], kFlagPoison);
-            go = kFlagPoison;
-        } else {
-            go = lookback_offset_wide(so.status, g, total, data_start(so.n_chunks), so.ws, true);
-        }
-        if (lane < (uint32_t)kTeams) sm.off[b][lane] = go == kFlagPoison ? kFlagPoison : go + (incl - mine);
-        if (lane == 0) sm.tally[b] = 0;  // next used for group i + kPB, sized after group i is written
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.placed[b]);
+        if (lane == 0) mbar_arrive(&sm.decoded[b]);
     }
+    for (int t = 0; t < kTeams; ++t)
+        for (uint32_t v = ut[t] > (uint32_t)kRSlots ? ut[t] - kRSlots : 0u; v < ut[t]; ++v)
+            mbar_wait(&sm.full[t][v % kRSlots], (v / kRSlots) & 1u);
 }
 
 // --------------------------------------------------------------------------- teams
@@ -380,12 +490,22 @@ __device__ __forceinline__ void read_raw_partial(const uint8_t* vals_bytes, uint
 
 // acc (16 binary32 pairs, or for min/max 16 words of raw values: the 16-bit
 // types keep a pair-word per entry, fp32 two words) op= V, in rank order.
+// acc (a binary32 pair, low element in the low word) + the pair-word p of the
+// 16-bit type, each element widened exactly and added with one rounding to
+// nearest even: the mixed-precision add takes the 16-bit operand as it is.
 template <class D>
-__device__ __forceinline__ uint64_t widen(uint32_t v) {
+__device__ __forceinline__ uint64_t add_pair_widened(uint64_t acc, uint32_t p) {
     if constexpr (D::kExpBits == 5)
-        return widen_pair_fp16(v);
+        asm("{ .reg .b16 l, h; .reg .f32 a, b; mov.b32 {l, h}, %1; mov.b64 {a, b}, %0;"
+            " add.rn.f32.f16 a, l, a; add.rn.f32.f16 b, h, b; mov.b64 %0, {a, b}; }"
+            : "+l"(acc)
+            : "r"(p));
     else
-        return widen_pair(v);
+        asm("{ .reg .b16 l, h; .reg .f32 a, b; mov.b32 {l, h}, %1; mov.b64 {a, b}, %0;"
+            " add.rn.f32.bf16 a, l, a; add.rn.f32.bf16 b, h, b; mov.b64 %0, {a, b}; }"
+            : "+l"(acc)
+            : "r"(p));
+    return acc;
 }
 template <class D>
 __device__ __forceinline__ void accumulate(uint64_t* acc, const uint32_t* V, uint32_t op, bool first) {
@@ -410,10 +530,10 @@ __device__ __forceinline__ void accumulate(uint64_t* acc, const uint32_t* V, uin
             for (int x = 0; x < 16; ++x) acc[x] = first ? V[x] : minmax_pair<D>((uint32_t)acc[x], V[x], op);
         } else if (first) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) acc[x] = widen<D>(V[x]);
+            for (int x = 0; x < 16; ++x) acc[x] = add_pair_widened<D>(0x8000000080000000ull, V[x]);  // x + (-0) = x
         } else {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) acc[x] = add_f32x2(acc[x], widen<D>(V[x]));
+            for (int x = 0; x < 16; ++x) acc[x] = add_pair_widened<D>(acc[x], V[x]);
         }
     }
 }
@@ -444,243 +564,268 @@ __device__ __forceinline__ void finish_values(const uint64_t* acc, uint32_t op, 
     }
 }
 
-// Write this team's pending chunk of group j (sized pend_depth iterations
-// earlier) once the placer has placed group j.  `st`: the chunk's state slot.
+// --------------------------------------------------------------------------- placer
+// Per group: the look-back gives the group's offset; the teams' staged chunks
+// then leave by one bulk (TMA) store each, issued by lane t for team t, which
+// also writes the chunk's offset-table entry (and the stream header or size).
 template <class D>
-__device__ __forceinline__ void write_pending(const StreamOut& so, ReduceSmem& sm, int j, uint32_t* st) {
-    constexpr int kW = thread_words<D>();
-    constexpr int kPB = place_bufs<D>();
-    const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127, wq = tt >> 5;
-    const int slot = j % state_slots<D>();
-    const uint32_t bytes = sm.pend_bytes[team][slot];
-    if (bytes == 0) return;
-    const int pb = j % kPB;
-    if (!warp_wait(&sm.placed[pb], (uint32_t)(j / kPB) & 1u)) {
-        if (lane == 0) set_abort(so, sm);
-        return;
-    }
-    const uint64_t off = sm.off[pb][team];
-    if (off == kFlagPoison) return;
-    if (off + bytes > so.capacity) {  // cannot happen for a correct placement
-        if (tt == 0) record_error(so.ws, kStatusCorrupt);
-        return;
-    }
-    const uint64_t c = sm.pend_c[team][slot];
-    const uint64_t n_full = so.n_elems / kChunkElems;
-    uint32_t Pp[kW], Qp[8];
+__device__ __forceinline__ void reduce_placer(const StreamOut& so, const uint8_t* staging, ReduceSmem& sm) {
+    constexpr int kSB = sbufs<D>();
+    constexpr int kTeams = teams<D>();
+    const uint32_t lane = threadIdx.x & 31;
+    for (int i = 0; !warp_any(sm.abort); ++i) {
+        const int b = i % kSB;
+        const uint32_t ph = (uint32_t)(i / kSB) & 1u;
+        if (!warp_wait(&sm.sized[b], ph)) {
+            if (lane == 0) set_abort(so, sm);
+            break;
+        }
+        const uint64_t g = sm.gid[b];
+        if (g == kNoGroup) break;
+        const uint32_t mine = lane < (uint32_t)kTeams ? sm.size[b][lane] : 0u;
+        const bool failed = warp_any(lane < (uint32_t)kTeams && sm.failed[b][lane] != 0);
+        uint32_t incl = mine;
 #pragma unroll
-    for (int x = 0; x < kW; ++x) Pp[x] = st[kTeamThreads * x];
-#pragma unroll
-    for (int x = 0; x < 8; ++x) Qp[x] = st[kTeamThreads * (kW + x)];
-    uint8_t* dst = so.out + off;
-    if (c < n_full)
-        write_chunk_team<D>(Pp, Qp, sm.pend_pl[team][slot][wq], dst, st);
-    else
-        write_tail_chunk_team<D>(Pp, (uint32_t)(so.n_elems - c * kChunkElems), dst);
-    if (tt == 64) finish_chunk(so, c, off, bytes);  // warp 0 wrote the chunk header
+        for (int d = 1; d < kTeams; d <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= (uint32_t)d) incl += t;
+        }
+        const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, kTeams - 1);
+        uint64_t go;
+        if (failed) {
+            if (lane == 0) st_relaxed_u64(&so.status[g], kFlagPoison);
+            go = kFlagPoison;
+        } else {
+            go = lookback_offset_wide(so.status, g, total, data_start(so.n_chunks), so.ws, true);
+        }
+        if (lane == 0) sm.tally[b] = 0;  // next added to for group i + kSB, after `stored` below
+        if (!warp_wait(&sm.staged[b], ph)) {
+            if (lane == 0) set_abort(so, sm);
+            break;
+        }
+        if (go != kFlagPoison && lane < (uint32_t)kTeams && mine > 0) {
+            const uint64_t off = go + (incl - mine);
+            if (off + mine > so.capacity) {  // cannot happen for a correct placement
+                record_error(so.ws, kStatusCorrupt);
+            } else {
+                bulk_store(so.out + off, staging + ((size_t)lane * kSB + b) * max_chunk_bytes<D>(), mine);
+                bulk_commit();
+                finish_chunk(so, g * kTeams + lane, off, mine);
+                bulk_wait_read();
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.stored[b]);
+    }
+    bulk_wait_all();  // every copy out has completed
 }
 
 template <class D>
 __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t op, const StreamOut& so,
-                                            uint8_t* ring_base, uint32_t* prev_base, ReduceSmem& sm) {
+                                            uint8_t* ring_base, uint8_t* staging_base, ReduceSmem& sm) {
     constexpr int kRSlots = rslots<D>();
     constexpr int kW = thread_words<D>();
-    constexpr int kPrevWords = prev_words<D>();
-    constexpr int kPend = pend_depth<D>();
-    constexpr int kSlots = state_slots<D>();
-    constexpr int kPB = place_bufs<D>();
+    constexpr int kSB = sbufs<D>();
     constexpr uint32_t kSlotBytes = max_chunk_bytes<D>();
     constexpr int kTeams = teams<D>();
     const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127, wq = tt >> 5;
     const TeamBarrier bar{1u + team};
     uint8_t* ring = ring_base + (size_t)team * kRSlots * kSlotBytes;
-    // pending chunk slot s of this team: word w at st(s)[128 w]
-    auto st_of = [&](int s) { return prev_base + ((size_t)team * kSlots + s) * kPrevWords * kTeamThreads + tt; };
     const uint64_t n_full = so.n_elems / kChunkElems;
-    if (tt == 0)
-        for (int s = 0; s < kSlots; ++s) sm.pend_bytes[team][s] = 0;
-    bar.sync();
-    uint32_t u = 0;  // rank chunks consumed (the loader's order for this team)
+    uint32_t s = 0, ph = 0;  // this team's next ring slot and its phase (the loader's order)
     for (int i = 0;; ++i) {
-        const int b = i & 1, pb = i % kPB;
-        const bool ready = mbar_wait(&sm.meta_ready[b], (uint32_t)(i >> 1) & 1u);
+        const int b = i % kMetaBufs, sb = i % kSB;
+        const bool ready = mbar_wait(&sm.meta_ready[b], (uint32_t)(i / kMetaBufs) & 1u);
         if (bar.any(!ready || sm.abort)) {
             if (tt == 0) set_abort(so, sm);
             return;  // the whole team
         }
+        // every thread has read iteration i - 1's flag: clear it for i + 1
+        if (tt == 0) sm.corrupt[team][(i + 1) & 1] = 0;
         const ReduceMeta& m = sm.meta[b];
         const uint64_t g = m.g;
-        TeamPlan pl{};
-        uint32_t P[kW], planes[8];
-        uint32_t bytes = 0, fail = 0;
-        uint64_t c = 0;
-        uint32_t n_c = 0;
-        if (g != kNoGroup) {
-            c = g * kTeams + team;
-            const bool mine = team < m.n_out;  // uniform over the team
-            const uint64_t left = mine ? so.n_elems - c * kChunkElems : 0;
-            n_c = left < kChunkElems ? (uint32_t)left : kChunkElems;
-            fail = m.ok ? 0u : kStatusCorrupt;
-            if (mine && m.ok) {
-                uint64_t acc[16];
-                bool special = false;
-                for (int r = 0; r < R; ++r, ++u) {
-                    const uint32_t s = u % kRSlots;
-                    uint8_t* buf = ring + (size_t)s * kSlotBytes;
-                    const bool landed = !sm.abort && mbar_wait(&sm.full[team][s], (u / kRSlots) & 1u);
-                    // one meeting per rank: slot s has landed for every warp,
-                    // and every warp is done with the previous rank's slot and
-                    // row_tot
-                    if (bar.any(!landed)) {
-                        if (tt == 0) set_abort(so, sm);
-                        return;  // the whole team
-                    }
-                    if (r > 0 && tt == 32) mbar_arrive(&sm.free_[team][(u - 1) % kRSlots]);
-                    uint32_t V[kW];
-                    if (fail == 0 && r == 0 && local != nullptr) {
-                        // the uncompressed local operand: staged raw, or read in place
-                        if (n_c == kChunkElems) {
-                            load_raw_full<D>(buf, V);
-                        } else {
-                            read_raw_partial<D>(static_cast<const uint8_t*>(local) +
-                                                    (size_t)D::kElemBytes * c * kChunkElems,
-                                                n_c, V);
-                        }
-                        special = true;
-                        accumulate<D>(acc, V, op, true);
-                    } else if (fail == 0) {
-                        const ChunkHeader h = read_chunk_header(buf);
-                        bool good = chunk_header_valid<D>(h, m.bytes[team][r], n_c);  // same for the team
-                        if (good) {
-                            if (n_c < kChunkElems) {  // partial last chunk: raw values, read those that exist
-                                read_raw_partial<D>(buf + kChunkHeaderBytes, n_c, V);
-                                special = true;
-                            } else {
-                                bool sp = false;
-                                good = decode_full_chunk<D>(bar, buf, h, V, sm.row_tot[team], sp);
-                                special = special || sp;
-                            }
-                        }
-                        if (!good)
-                            fail = kStatusCorrupt;
-                        else
-                            accumulate<D>(acc, V, op, r == 0);
-                    }
-                }
-                // the last rank's slot is released once the team meets again
-                const bool any_special = bar.any(special);
-                if (tt == 32) mbar_arrive(&sm.free_[team][(u - 1) % kRSlots]);
-                if (fail == 0) finish_values<D>(acc, op, any_special, P);
-            }
-            if (lane == 0) mbar_arrive(&sm.decoded[b]);
-            if (mine && fail == 0) {
-                if (c < n_full) {
-                    pl = plan_chunk_team<D>(bar, P, planes, sm.xch[team]);
-                    bytes = pl.bytes;
-                } else {
-                    bytes = tail_chunk_bytes<D>(n_c);
-                }
-            }
-            if (tt == 96) {  // lane 0 of warp 3: warp 0 writes headers, warp 2 the table
-                sm.size[pb][team] = bytes;
-                sm.failed[pb][team] = fail;
-                if (team == 0) sm.gid[pb] = g;
-                if (fail) {
-                    record_error(so.ws, fail);
-                } else {
-                    // the last team to size the group publishes its size at once,
-                    // so later groups' look-backs need not wait for the placer
-                    const unsigned long long old = atomicAdd(&sm.tally[pb], (1ull << 32) | bytes);
-                    if ((old >> 32) == kTeams - 1)
-                        publish_unit_size(so.status, g, (uint32_t)old + bytes, data_start(so.n_chunks));
-                }
-                mbar_arrive(&sm.sized[pb]);
-            }
-        } else if (tt == 96) {
-            if (team == 0) sm.gid[pb] = kNoGroup;
-            mbar_arrive(&sm.sized[pb]);
-        }
-        // this chunk waits in shared memory for its placement; the chunk of
-        // group i - kPend is written (at the end, every chunk still pending)
-        auto save = [&]() {
-            const int slot = i % kSlots;
-            uint32_t* st = st_of(slot);
-            const uint32_t keep = fail ? 0u : bytes;
-            if (keep > 0) {
-#pragma unroll
-                for (int x = 0; x < kW; ++x) st[kTeamThreads * x] = P[x];
-#pragma unroll
-                for (int x = 0; x < 8; ++x) st[kTeamThreads * (kW + x)] = planes[x];
-            }
-            if (lane == 0) sm.pend_pl[team][slot][wq] = pl;
-            if (tt == 0) {
-                sm.pend_c[team][slot] = c;
-                sm.pend_bytes[team][slot] = keep;
-            }
-        };
-        if (kSlots > kPend && g != kNoGroup) save();
-        if (i >= kPend) write_pending<D>(so, sm, i - kPend, st_of((i - kPend) % kSlots));
         if (g == kNoGroup) {
-            for (int j = i - kPend + 1; j < i; ++j)
-                if (j >= 0) write_pending<D>(so, sm, j, st_of(j % kSlots));
+            // tell the placer, once it is done with the buffers' last group
+            if (i >= kSB) warp_wait(&sm.stored[sb], (uint32_t)((i - kSB) / kSB) & 1u);
+            if (tt == 96) {
+                if (team == 0) sm.gid[sb] = kNoGroup;
+                mbar_arrive(&sm.sized[sb]);
+            }
             return;
         }
-        if (kSlots == kPend) save();
-        // (the next iteration's team barrier orders these writes before any read)
+        const uint64_t c = g * kTeams + team;
+        const bool mine = team < m.n_out;  // uniform over the team
+        const uint64_t left = mine ? so.n_elems - c * kChunkElems : 0;
+        const uint32_t n_c = left < kChunkElems ? (uint32_t)left : kChunkElems;
+        uint32_t fail = m.ok ? 0u : kStatusCorrupt;
+        bool timed_out = false, special = false;
+        uint64_t acc[16];
+        if (mine && m.ok) {
+            for (int r = 0; r < R; ++r) {
+                uint8_t* buf = ring + (size_t)s * kSlotBytes;
+                if (!warp_wait(&sm.full[team][s], ph)) {
+                    timed_out = true;
+                    break;
+                }
+                uint32_t V[kW];
+                if (fail == 0 && r == 0 && local != nullptr) {
+                    // the uncompressed local operand: staged raw, or read in place
+                    if (n_c == kChunkElems)
+                        load_raw_full<D>(buf, V);
+                    else
+                        read_raw_partial<D>(
+                            static_cast<const uint8_t*>(local) + (size_t)D::kElemBytes * c * kChunkElems, n_c, V);
+                    special = true;
+                    accumulate<D>(acc, V, op, true);
+                } else if (fail == 0) {
+                    const ChunkHeader h = unpack_desc(m.desc[team][r]);  // checked by the loader
+                    if (n_c < kChunkElems) {  // partial last chunk: raw values, read those that exist
+                        read_raw_partial<D>(buf + kChunkHeaderBytes, n_c, V);
+                        special = true;
+                    } else {
+                        bool body_bad = false;
+                        const uint32_t n = decode_quarter<D>(buf, h, V, special, body_bad);
+                        if (lane == 0 && h.mode != kModeRaw) {
+                            atomicAdd(&sm.esc_diff[team][r], (int32_t)n - (wq == 0 ? (int32_t)h.n_esc : 0));
+                            if (body_bad) sm.corrupt[team][i & 1] = 1;
+                        }
+                    }
+                    accumulate<D>(acc, V, op, r == 0);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.free_[team][s]);  // this warp is done with the slot
+                if (++s == (uint32_t)kRSlots) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (lane == 0) mbar_arrive(&sm.decoded[b]);
+        // the team meets: a timed-out wait stops it; Inf or NaN anywhere
+        // makes the rounding canonicalise NaNs
+        if (bar.any(timed_out)) {
+            if (tt == 0) set_abort(so, sm);
+            return;
+        }
+        const bool any_special = bar.any(special);
+        // each rank chunk's quarters must hold exactly its n_esc escapes
+        if (tt < (uint32_t)R) {
+            if (sm.esc_diff[team][tt] != 0) sm.corrupt[team][i & 1] = 1;
+            sm.esc_diff[team][tt] = 0;
+        }
+        TeamPlan pl{};
+        uint32_t P[kW], planes[8];
+        uint32_t bytes = 0;
+        if (mine && fail == 0) {
+            finish_values<D>(acc, op, any_special, P);
+            if (c < n_full) {
+                pl = plan_chunk_team<D>(bar, P, planes, sm.xch[team]);  // two meetings: the flag is in
+                if (sm.corrupt[team][i & 1]) fail = kStatusCorrupt;
+                bytes = pl.bytes;
+            } else {
+                bytes = tail_chunk_bytes<D>(n_c);
+            }
+        }
+        if (fail) bytes = 0;
+        // the placer is done with group i - kSB: its sizes, tally and staging buffers
+        const bool free_buf = i < kSB || warp_wait(&sm.stored[sb], (uint32_t)((i - kSB) / kSB) & 1u);
+        if (!free_buf && lane == 0) set_abort(so, sm);
+        if (tt == 96) {  // lane 0 of warp 3
+            sm.size[sb][team] = bytes;
+            sm.failed[sb][team] = fail;
+            if (team == 0) sm.gid[sb] = g;
+            if (fail) {
+                record_error(so.ws, fail);
+            } else {
+                // the last team to size the group publishes its size at once,
+                // so later groups' look-backs need not wait for the placer
+                const unsigned long long old = atomicAdd(&sm.tally[sb], (1ull << 32) | bytes);
+                if ((old >> 32) == kTeams - 1)
+                    publish_unit_size(so.status, g, (uint32_t)old + bytes, data_start(so.n_chunks));
+            }
+            mbar_arrive(&sm.sized[sb]);
+        }
+        if (free_buf && bytes > 0) {
+            uint8_t* dst = staging_base + ((size_t)team * kSB + sb) * kSlotBytes;
+            if (c < n_full)
+                stage_chunk_team<D>(P, planes, pl, dst);
+            else
+                write_tail_chunk_team<D>(P, n_c, dst);
+            fence_proxy_async_smem();  // the placer's bulk store reads these bytes
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.staged[sb]);
     }
 }
 
 template <class D>
-__global__ void __launch_bounds__(reduce_threads<D>(), 1) reduce_kernel(ReduceInputs inputs, int R, StreamOut so) {
+__global__ void __launch_bounds__(reduce_threads<D>(), 1)
+    reduce_kernel(ReduceInputs inputs, int R, StreamOut so, bool two_loaders) {
     constexpr int kTeams = teams<D>();
-    static_assert(kTeams <= kMaxTeams && rslots<D>() <= kMaxRSlots && state_slots<D>() <= 3 &&
-                      place_bufs<D>() <= kMaxPlaceBufs,
+    static_assert(kTeams <= kMaxTeams && rslots<D>() <= kMaxRSlots && sbufs<D>() <= kMaxSBufs,
                   "the shared-memory bookkeeping arrays are sized for these bounds");
+    static_assert(reduce_smem<D>() + sizeof(ReduceSmem) <= 227 * 1024, "shared memory per CTA");
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ ReduceSmem sm;
     uint8_t* ring = smem;
-    uint32_t* prev = reinterpret_cast<uint32_t*>(smem + ring_bytes<D>());
+    uint8_t* staging = smem + ring_bytes<D>();
     const uint32_t w = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kMetaBufs; ++b) {
             mbar_init(&sm.meta_ready[b], 1);
-            mbar_init(&sm.decoded[b], 4 * kTeams);
+            mbar_init(&sm.decoded[b], 4 * kTeams + 1);
         }
-        for (int b = 0; b < place_bufs<D>(); ++b) {
+        for (int b = 0; b < sbufs<D>(); ++b) {
             mbar_init(&sm.sized[b], kTeams);
-            mbar_init(&sm.placed[b], 1);
+            mbar_init(&sm.staged[b], 4 * kTeams);
+            mbar_init(&sm.stored[b], 1);
             sm.tally[b] = 0;
         }
-        for (int t = 0; t < kTeams; ++t)
+        for (int t = 0; t < kTeams; ++t) {
             for (int s = 0; s < rslots<D>(); ++s) {
                 mbar_init(&sm.full[t][s], 1);
-                mbar_init(&sm.free_[t][s], 1);
+                mbar_init(&sm.free_[t][s], 4);
             }
+            sm.corrupt[t][0] = sm.corrupt[t][1] = 0;
+        }
         sm.abort = 0;
         fence_mbar_init();
     }
+    for (uint32_t x = threadIdx.x; x < kMaxTeams * kMaxRanks; x += blockDim.x) (&sm.esc_diff[0][0])[x] = 0;
     __syncthreads();
-    if (w == loader_warp<D>())
-        reduce_loader<D>(inputs, R, so, ring, sm);
-    else if (w == placer_warp<D>())
-        reduce_placer<D>(so, sm);
-    else
-        reduce_team<D>(R, inputs.local, inputs.op, so, ring, prev, sm);
+    if (w == loader_warp<D>()) {
+        if (two_loaders)
+            reduce_locator<D>(inputs, R, so, sm);
+        else
+            reduce_loader<D>(inputs, R, so, ring, sm);
+    } else if (w == copier_warp<D>()) {
+        if (two_loaders) reduce_copier<D>(inputs, R, so, ring, sm);
+    } else if (w == placer_warp<D>())
+        reduce_placer<D>(so, staging, sm);
+    else if (w < 4 * (uint32_t)kTeams)
+        reduce_team<D>(R, inputs.local, inputs.op, so, ring, staging, sm);
+    // (a warp with no role has nothing to do)
 }
+
+// Per-device record of the shared-memory limit set for reduce_kernel<D>,
+// by element type code.  A plain static array: a function-local static of a
+// template would become one object shared by every copy of this library
+// loaded into the process, and a second copy would then take its own
+// kernel's limit as set.
+static PerDeviceOnce g_reduce_smem_limit[4];
 
 template <class D>
 cudaError_t launch_reduce_t(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,
                             void* ws, cudaStream_t stream) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(reduce_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)reduce_smem<D>());
-    });
-    if (attr != cudaSuccess) return attr;
+    PerDeviceOnce& smem_limit = g_reduce_smem_limit[D::kCode];
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = smem_limit.run(dev, [] {
+            return cudaFuncSetAttribute(reduce_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)reduce_smem<D>());
+        });
     if (e != cudaSuccess) return e;
     StreamOut so;
     so.out = out;
@@ -693,7 +838,15 @@ cudaError_t launch_reduce_t(const ReduceInputs& inputs, int R, uint64_t n_elems,
     so.dtype = D::kCode;
     const uint64_t n_groups = (so.n_chunks + teams<D>() - 1) / teams<D>();
     const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
-    reduce_kernel<D><<<grid, reduce_threads<D>(), reduce_smem<D>(), stream>>>(inputs, R, so);
+    // Nearly incompressible inputs (at least 90% of their raw size) are
+    // mostly raw chunks: the teams are then bound by data arrival, and a
+    // second loader warp keeps their rings full; compressed inputs are bound
+    // by decoding, and one loader warp is faster (both measured on GB300).
+    uint64_t in_total = 0;
+    for (int r = 0; r < R; ++r)
+        in_total += (r == 0 && inputs.local != nullptr) ? (uint64_t)D::kElemBytes * n_elems : inputs.in_bytes[r];
+    const bool two_loaders = 10 * in_total >= 9 * (uint64_t)R * D::kElemBytes * n_elems;
+    reduce_kernel<D><<<grid, reduce_threads<D>(), reduce_smem<D>(), stream>>>(inputs, R, so, two_loaders);
     return cudaGetLastError();
 }
 

@@ -175,3 +175,49 @@ def test_selftest_timeouts_argument_checks(cc):
     assert lib.cccl_selftest_timeouts(base + 4, need, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_selftest_timeouts(base, need - 16, None) == cc.CCCL_ERR_INVALID_ARG
     assert lib.cccl_selftest_timeouts(base, need, None) == cc.CCCL_ERR_INVALID_ARG  # host memory
+
+
+def test_kernel_set_up_is_kept_per_device(tmp_path):
+    """The launchers set a kernel's shared-memory limit through PerDeviceOnce:
+    the step runs once for each device (an attribute belongs to the device's
+    context), is retried after a failure, and a second device is not taken as
+    done because the first one is."""
+    import shutil
+    import subprocess
+
+    gxx = shutil.which("g++")
+    cuda_inc = "/usr/local/cuda/include"
+    if gxx is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
+        pytest.skip("g++ or the CUDA headers are missing")
+    src = tmp_path / "once.cpp"
+    src.write_text(r'''
+#include <cstdio>
+#include "cccl_launch.h"
+int main() {
+    cccl::PerDeviceOnce once;
+    int calls[4] = {0, 0, 0, 0};
+    auto step = [&](int dev, int slot, cudaError_t result) {
+        return (int)once.run(dev, [&] { ++calls[slot]; return result; });
+    };
+    int r[8];
+    r[0] = step(0, 0, cudaSuccess);
+    r[1] = step(0, 0, cudaSuccess);           // device 0 is done: not run again
+    r[2] = step(1, 1, cudaSuccess);           // device 1 is set up on its own
+    r[3] = step(2, 2, cudaErrorInvalidValue); // a failure is returned and not remembered
+    r[4] = step(2, 2, cudaSuccess);
+    r[5] = step(2, 2, cudaSuccess);
+    r[6] = step(70, 3, cudaSuccess);          // beyond 64 devices: run every time
+    r[7] = step(70, 3, cudaSuccess);
+    std::printf("%d %d %d %d", calls[0], calls[1], calls[2], calls[3]);
+    for (int x : r) std::printf(" %d", x);
+    std::printf("\n");
+    return 0;
+}
+''')
+    exe = tmp_path / "once"
+    csrc = os.path.join(ROOT, "compression_coupled_collectives_gb300", "csrc")
+    subprocess.check_call([gxx, "-std=c++17", "-I", csrc, "-I", cuda_inc, str(src), "-o", str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split()
+    calls, results = [int(v) for v in out[:4]], [int(v) for v in out[4:]]
+    assert calls == [1, 1, 2, 2]
+    assert results == [0, 0, 0, 1, 0, 0, 0, 0]  # 1 = cudaErrorInvalidValue
