@@ -1,17 +1,20 @@
 """Benchmark of the compressed data-parallel reduce step on GB300.
 
-One step = the whole hot path over one batch of synthetic input: the 64 MiB
-gradient-like bf16 buffer (33,554,432 values ~ N(0, 1e-3), 1% of positions
-x100) of R = 2 simulated data-parallel ranks held in this GPU's memory:
-    compress(rank 0), compress(rank 1)            split, exponent table, look-back placement
-    fused reduce(stream 0, stream 1)              decompress -> binary32 sum -> bf16 -> compress
-    decompress(reduced stream)                    the receiver's decode
+One step = the fused reduce step of a compressed allreduce over R = 8
+simulated data-parallel ranks held in this GPU's memory, each rank a 256 MiB
+bf16 buffer (134,217,728 values ~ N(0, 0.02), per-rank seeds) held
+pre-compressed: one call of cccl_reduce_compressed, which decodes every rank's
+chunks, adds them in binary32 in rank order 0..7, rounds once to bf16 and
+compresses the result (decompress -> reduce -> compress in one kernel).
 `value` = uncompressed gradient bytes entering the step (R * 2n) / step time,
-timed on the device with CUDA events around each step, the step replayed as
-one captured CUDA graph of the four library calls, L2 flushed (256 MiB write,
-untimed) before every step, max over ranks.  The ops are timed one by one in
-a second pass of plain launches.  N GPUs under torchrun run N independent replicas
-(weak scaling); nothing crosses GPUs.
+timed on the device with CUDA events around each call, the L2 flushed (256 MiB
+write, untimed) before every step, max over ranks.  The inputs (1.76 GB of
+streams) are far larger than the L2 as well.  The end-to-end leg runs the same
+call with the compressed streams uploaded from pinned host memory and the
+result downloaded every step.  N GPUs under torchrun run N independent
+replicas (weak scaling); nothing crosses GPUs.  The other workloads and
+kernels (compress, decompress, the 64 MiB two-rank step, the worst case, the
+KV-cache payload, fp16/fp32, ...) are timed under `extras`.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
 """
@@ -19,10 +22,11 @@ a second pass of plain launches.  N GPUs under torchrun run N independent replic
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
-import platform
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -34,10 +38,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "compress / decompress / fused-reduce uncompressed GB/s and % of HBM roofline; ratio"
-WORKLOAD = 2          # the 64 MiB gradient-like buffer
-RANKS_PER_GPU = 2     # simulated data-parallel ranks reduced on each GPU
+WORKLOAD = 3          # 8 ranks x 256 MiB, N(0, 0.02), fused reduce R=8
+RANKS_PER_GPU = 8     # simulated data-parallel ranks reduced on each GPU
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
+E2E_MIN_STEPS = 50
+E2E_WARMUP = 3
 KERNEL_SOURCES = ["cccl_device.cuh", "cccl_encode.cuh", "cccl_decode.cuh", "cccl_compress.cu",
                   "cccl_decompress.cu", "cccl_reduce.cu"]
 
@@ -120,78 +126,162 @@ def recorded_traffic(kernel: str):
     return rec
 
 
+def workload_config(input_sha256: list[str]) -> dict:
+    return {"workload": "fused decompress -> binary32 reduce in rank order -> bf16 -> compress over R=%d simulated "
+                        "data-parallel ranks per GPU, each a 256 MiB bf16 buffer (134,217,728 values ~ N(0, 0.02), "
+                        "per-rank seeds) held pre-compressed in HBM" % RANKS_PER_GPU,
+            "n_elems": 134217728, "ranks_per_gpu": RANKS_PER_GPU, "chunk_elems": 4096,
+            "l2": "flushed before every timed step (256 MiB write, untimed); the 1.76 GB of input streams are far "
+                  "larger than the L2 as well",
+            "parallelism": "replicas (weak scaling, no cross-GPU traffic)",
+            "input_sha256": input_sha256}
+
+
+def input_hashes(xs_host) -> list[str]:
+    return [hashlib.sha256(x.tobytes()).hexdigest()[:16] for x in xs_host]
+
+
 # ---------------------------------------------------------------- clocks
+# NVML (read-only queries) through ctypes, every millisecond; nvidia-smi at
+# 100 ms when NVML cannot be loaded.  Clock event reason bits of NVML.
+_REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class _NvmlSource:
+    def __init__(self, torch_index: int):
+        import torch
+
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self.lib.nvmlInit_v2.restype = ctypes.c_int
+        rc = self.lib.nvmlInit_v2()
+        if rc != 0:
+            raise OSError("nvmlInit_v2 returned %d" % rc)
+        self.handle = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(torch_index)
+        rc = -1
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            text = str(uuid)
+            if not text.startswith("GPU-"):
+                text = "GPU-" + text
+            rc = self.lib.nvmlDeviceGetHandleByUUID(text.encode(), ctypes.byref(self.handle))
+        if rc != 0 and hasattr(props, "pci_bus_id"):
+            bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                        getattr(props, "pci_device_id", 0))
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.handle))
+        if rc != 0:
+            raise OSError("no NVML handle for torch device %d (rc %d)" % (torch_index, rc))
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        mhz, mx, mw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz))       # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))
+        self.reasons_fn(self.handle, ctypes.byref(reasons))
+        self.lib.nvmlDeviceGetPowerUsage(self.handle, ctypes.byref(mw))
+        return float(mhz.value), float(mx.value), int(reasons.value), mw.value / 1000.0
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """SM clock, its maximum, clock event reasons and power while the work runs."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines: list[tuple[float, str]] = []
+    def __init__(self, torch_index: int, period_s: float = 0.001):
+        self.samples: list[tuple[float, float, float, set, float]] = []
+        self.period = period_s
+        self.source = None
+        self.note = None
+        self.stop_flag = threading.Event()
         self.thread = None
+        self.proc = None
+        try:
+            self.nvml = _NvmlSource(torch_index)
+            self.source = "nvml"
+        except Exception as e:  # no driver, no device, no NVML: fall back, and say why
+            self.nvml = None
+            self.note = "NVML unavailable (%s); nvidia-smi at 100 ms" % e
+            self.smi_index = torch_index
 
     def start(self):
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+                ["nvidia-smi", "-i", str(self.smi_index), "--query-gpu=" + self.SMI_FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                text=True)
+            self.source = "nvidia-smi"
+        except OSError as e:
+            self.note = (self.note or "") + "; nvidia-smi could not start: %s" % e
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread = threading.Thread(target=self._smi_loop, daemon=True)
         self.thread.start()
 
-    def _read(self):
+    def _nvml_loop(self):
+        while not self.stop_flag.is_set():
+            mhz, mx, bits, w = self.nvml.sample()
+            self.samples.append((time.time(), mhz, mx, {n for b, n in _REASON_BITS.items() if bits & b}, w))
+            time.sleep(self.period)
+
+    def _smi_loop(self):
         for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                reasons = {n for n, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                              "sw_power_cap"), parts[3:7]) if v.lower().startswith("active")}
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]), reasons, float(parts[2])))
+            except ValueError:
+                continue
 
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                _, err = self.proc.communicate(timeout=5)
+                if self.proc.returncode not in (0, -15, None) and err:
+                    self.note = (self.note or "") + "; nvidia-smi rc %s: %s" % (self.proc.returncode, err.strip()[:200])
             except subprocess.TimeoutExpired:
                 self.proc.kill()
         if self.thread is not None:
             self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float) -> dict:
-        sm, smax, reasons = [], [], set()
-        for ts, line in self.lines:
-            if not (t0 <= ts <= t1):
-                continue
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
-                                 parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sel = [s for s in self.samples if t0 <= s[0] <= t1]
+        reasons = sorted(set().union(*[s[3] for s in sel])) if sel else []
+        out = {"sm_mhz": statistics.median([s[1] for s in sel]) if sel else None,
+               "sm_max_mhz": max(s[2] for s in sel) if sel else None,
+               "reasons": reasons, "samples": len(sel),
+               "power_w_max": round(max(s[4] for s in sel), 1) if sel else None,
+               "source": self.source, "window_s": round(t1 - t0, 3)}
+        if self.note:
+            out["note"] = self.note
+        return out
 
 
 # ---------------------------------------------------------------- the oracle as a CPU baseline
-def oracle_step_seconds(xs, chunks: int) -> tuple[float, int]:
-    """Time the oracle doing the step on the first `chunks` chunks of each rank."""
+def oracle_reduce_seconds(xs, start_chunk: int, chunks: int) -> tuple[float, int]:
+    """The oracle doing the step on chunks [start_chunk, start_chunk + chunks)
+    of every rank: the ranks' pieces compressed first (the step's inputs are
+    held pre-compressed; not timed), then the fused reduce, timed."""
     import oracle
 
-    n = min(xs[0].size, chunks * 4096)
-    part = [x[:n] for x in xs]
+    a = start_chunk * 4096
+    b = min(xs[0].size, a + chunks * 4096)
+    streams = [oracle.compress(x[a:b]) for x in xs]
     t = time.perf_counter()
-    streams = [oracle.compress(p) for p in part]
-    red = oracle.reduce(streams, n)
-    oracle.decompress(red, n)
-    return time.perf_counter() - t, n
+    oracle.reduce(streams, b - a)
+    return time.perf_counter() - t, b - a
 
 
 def cpu_model() -> str:
@@ -214,9 +304,31 @@ def cpu_model() -> str:
                                               fields.get("CPU part", "?"))
 
 
-def cpu_baseline_all_cores(xs, budget_s: float = 6.0) -> dict:
-    """The oracle, as it stands, on every host core at once: each thread runs
-    the step on its own slice of chunks (the oracle is single-threaded C; the
+def cpu_baseline(xs, budget_s: float = 12.0) -> dict:
+    """The oracle, as it stands, single-threaded, on windows of 256 chunks
+    spread over the whole workload, until about budget_s of reduce time."""
+    import oracle
+
+    oracle.build()
+    n_chunks = xs[0].size // 4096
+    window = 256
+    total_t, total_n, k = 0.0, 0, 0
+    while total_t < budget_s and k < 512:
+        start = (k * 7919 * window) % max(1, n_chunks - window)
+        dt, n = oracle_reduce_seconds(xs, start, window)
+        total_t += dt
+        total_n += n
+        k += 1
+    gbs = len(xs) * 2 * total_n / total_t / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+            "sample": "the step (fused reduce of %d pre-compressed ranks) on %d windows of %d chunks spread over the "
+                      "workload (%d values per rank), %.1f s of reduce time, single-threaded C oracle; the "
+                      "windows' compression is not timed" % (len(xs), k, window, total_n, total_t)}
+
+
+def cpu_baseline_all_cores(xs, budget_s: float = 8.0) -> dict:
+    """The oracle, as it stands, on every host core at once: each thread
+    reduces its own windows of chunks (the oracle is single-threaded C; the
     threads share nothing)."""
     import concurrent.futures as cf
 
@@ -225,52 +337,32 @@ def cpu_baseline_all_cores(xs, budget_s: float = 6.0) -> dict:
     oracle.build()
     cores = max(1, os.cpu_count() or 1)
     n_chunks = xs[0].size // 4096
-    per = max(1, n_chunks // cores)
-    probe_t, _ = oracle_step_seconds(xs, 16)
-    # chunks per thread so that one round takes about budget_s / 2
-    take = max(1, min(per, int(budget_s / 2 / (probe_t / 16))))
+    window = 128
+    per = max(window, n_chunks // cores)
 
-    def one(i):
-        a = (i * per) * 4096
-        part = [x[a:a + take * 4096] for x in xs]
-        return oracle_step_seconds(part, take)
+    def one(i, rnd):
+        start = (i * per + rnd * window) % max(1, n_chunks - window)
+        return oracle_reduce_seconds(xs, start, window)
 
-    total_n, t0 = 0, time.perf_counter()
-    rounds = 0
+    total_n, busy, rounds = 0, 0.0, 0
+    t0 = time.perf_counter()
     with cf.ThreadPoolExecutor(cores) as ex:
-        while time.perf_counter() - t0 < budget_s and rounds < 4:
-            total_n += sum(n for _, n in ex.map(one, range(cores)))
+        while time.perf_counter() - t0 < budget_s and rounds < 16:
+            res = list(ex.map(lambda i: one(i, rounds), range(cores)))
+            total_n += sum(n for _, n in res)
+            busy += max(t for t, _ in res)
             rounds += 1
-    total_t = time.perf_counter() - t0
-    gbs = len(xs) * 2 * total_n / total_t / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "cpu": cpu_model(),
-            "sample": "%d threads, each the full step on its own %d-chunk slice of every rank, %d round(s), %.1f s"
-                      % (cores, take, rounds, total_t)}
-
-
-def cpu_baseline(xs, budget_s: float = 12.0) -> dict:
-    import oracle
-
-    oracle.build()
-    n_full = xs[0].size
-    total_t, total_n, reps = 0.0, 0, 0
-    chunks = n_full // 4096
-    while total_t < budget_s and reps < 8:
-        dt, n = oracle_step_seconds(xs, chunks)
-        total_t += dt
-        total_n += n
-        reps += 1
-    gbs = len(xs) * 2 * total_n / total_t / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
-            "sample": "the full step on the whole workload (%d ranks x %d values), %d repetition(s), "
-                      "%.1f s, single-threaded C oracle" % (len(xs), n_full, reps, total_t)}
+    gbs = len(xs) * 2 * total_n / busy / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu": cpu_model(),
+            "sample": "%d threads, each the step on its own %d-chunk windows, %d round(s); time = the slowest thread's "
+                      "reduce time per round, summed (%.1f s); compression of the windows not timed"
+                      % (cores, window, rounds, busy)}
 
 
 def run_reference(args, rank: int, world: int) -> None:
-    """The reference arm: the CPU oracle, as it stands, on this host's cores."""
-    import numpy as np  # noqa: F401
-
+    """The reference arm: the CPU oracle, as it stands, on this host's cores,
+    doing the same step (the fused reduce of the 8 pre-compressed ranks) on a
+    bounded sample of chunks per step, rotating through the workload."""
     import oracle
     import workloads
 
@@ -278,64 +370,44 @@ def run_reference(args, rank: int, world: int) -> None:
     workloads.build()
     if rank != 0:
         return
-    n = workloads.SIZES[WORKLOAD]
     xs = [workloads.generate(WORKLOAD, r) for r in simulated_ranks(0)]
+    n_chunks = xs[0].size // 4096
     steps, warmup = args.steps, max(args.warmup, 3)
-    # each step: a bounded sample of chunks, rotating through the workload, so
-    # that the whole run stays within about two minutes
+    # each step: a window of chunks sized so that the whole run takes about
+    # two minutes of reduce time
     per_step_s = 100.0 / (steps + warmup)
-    probe_t, probe_n = oracle_step_seconds(xs, 64)
-    chunks = max(1, min(n // 4096, int(per_step_s / (probe_t / 64))))
+    probe_t, _ = oracle_reduce_seconds(xs, 0, 16)
+    chunks = max(1, min(n_chunks, int(per_step_s / (probe_t / 16))))
     offs = 0
     total_t, total_n = 0.0, 0
     for i in range(warmup + steps):
-        a = (offs % (n // 4096)) * 4096
-        b = min(n, a + chunks * 4096)
-        part = [x[a:b] for x in xs]
-        t = time.perf_counter()
-        streams = [oracle.compress(p) for p in part]
-        red = oracle.reduce(streams, b - a)
-        oracle.decompress(red, b - a)
-        dt = time.perf_counter() - t
+        start = offs % max(1, n_chunks - chunks)
+        dt, n = oracle_reduce_seconds(xs, start, chunks)
         offs += chunks
         if i >= warmup:
             total_t += dt
-            total_n += b - a
+            total_n += n
     value = RANKS_PER_GPU * 2 * total_n / total_t / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": round(1e3 * total_t / steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8+f32",
-        "data": "synthetic", "config": workload_config(),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d chunks of each rank per step, rotating through the workload" % chunks},
+        "data": "synthetic", "config": workload_config(input_hashes(xs)),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+                         "sample": "%d chunks of every rank per step, rotating through the workload; the chunks' "
+                                   "compression is not timed (the step's inputs are held pre-compressed)" % chunks},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
-
-
-def workload_config() -> dict:
-    return {"workload": "gradient-like bf16 buffer, 33,554,432 values (64 MiB) ~ N(0, 1e-3) with 1%% of "
-                        "positions x100, on %d simulated data-parallel ranks per GPU: compress each, fused "
-                        "reduce (R=%d), decompress the result" % (RANKS_PER_GPU, RANKS_PER_GPU),
-            "n_elems": 33554432, "ranks_per_gpu": RANKS_PER_GPU, "chunk_elems": 4096,
-            "l2": "flushed before every timed step (256 MiB write, untimed)",
-            "parallelism": "replicas (weak scaling, no cross-GPU traffic)"}
 
 
 # ---------------------------------------------------------------- rows beyond the step
 KV_BLOCK = 16 * 8 * 128  # 16 tokens x 8 heads x 128 dim
 
 
-def measure_extras(cc, torch, np, xs, streams, sizes, n, flush, peak, reps: int = 50) -> dict:
-    """The selective-compression reduce and the paged payload, each timed alone
-    (CUDA events on the current stream, L2 flushed before every repetition,
-    median), with their algorithmic HBM bytes."""
-    import workloads
-
-    stream = torch.cuda.current_stream()
-    out = {}
-
+def make_timer(torch, flush, stream, reps: int):
+    """Median CUDA-event time (ms) of fn() on `stream`, the L2 flushed before
+    every repetition (untimed), after 3 untimed repetitions."""
     def timed(fn):
         ts = []
         for k in range(reps + 3):
@@ -348,22 +420,77 @@ def measure_extras(cc, torch, np, xs, streams, sizes, n, flush, peak, reps: int 
             if k >= 3:
                 ts.append(e0.elapsed_time(e1))
         return statistics.median(ts)
+    return timed
 
-    # local rank-0 buffer + one compressed remote rank, 64 MiB each
-    red = cc.empty_stream(n)
-    ws = cc.empty_workspace(n)
-    ms = timed(lambda: cc.cccl_reduce_mixed(xs[0], [streams[1][:sizes[1]]], red, ws, stream=stream))
-    out_bytes, st = cc.cccl_get_result(ws, stream)
-    algo = 2 * n + sizes[1] + out_bytes
-    out["reduce_mixed"] = {"ms": round(ms, 5), "workload": "local rank-0 buffer (uncompressed) + 1 compressed remote "
-                           "rank of the 64 MiB gradient-like buffer", "status": st,
-                           "uncompressed_gbs": round(2 * 2 * n / (ms * 1e-3) / 1e9, 1), "algorithmic_bytes": algo,
-                           "hbm_gbs": round(algo / (ms * 1e-3) / 1e9, 1),
-                           "frac_of_measured_copy": round(algo / (ms * 1e-3) / 1e9 / peak, 4)}
+
+def op_row(ms, algo, uncompressed, peak, **kw):
+    d = {"ms": round(ms, 5), "algorithmic_bytes": int(algo),
+         "uncompressed_gbs": round(uncompressed / (ms * 1e-3) / 1e9, 1),
+         "hbm_gbs": round(algo / (ms * 1e-3) / 1e9, 1),
+         "frac_of_measured_copy": round(algo / (ms * 1e-3) / 1e9 / peak, 4),
+         "frac_of_8tbs_nominal": round(algo / (ms * 1e-3) / 1e9 / 8000.0, 4)}
+    d.update(kw)
+    return d
+
+
+def measure_extras(cc, torch, np, timed, stream, peak, x0, red, red_bytes, n3) -> dict:
+    """The kernels and workloads outside the timed step, each op timed alone."""
+    import workloads
+
+    out = {}
+    tab3 = 8 * (-(-n3 // 4096))
+    # the step's other kernels on its own data: compress of rank 0's buffer,
+    # decompress of the reduced stream (the receiver's decode)
+    s0 = cc.empty_stream(n3)
+    ws = cc.empty_workspace(n3)
+    ms_c = timed(lambda: cc.cccl_compress(x0, s0, ws, stream=stream))
+    b0, st_c = cc.cccl_get_result(ws, stream)
+    out["workload3_compress"] = op_row(ms_c, 2 * n3 + b0 + tab3, 2 * n3, peak, status=st_c,
+                                       ratio=round(b0 / (2 * n3), 5),
+                                       workload="rank 0's 256 MiB buffer of the timed step")
+    y = torch.empty(n3, dtype=torch.int16, device=x0.device)
+    ms_d = timed(lambda: cc.cccl_decompress(red[:red_bytes], y, ws, stream=stream))
+    _, st_d = cc.cccl_get_result(ws, stream)
+    out["workload3_decompress_reduced"] = op_row(ms_d, red_bytes + tab3 + 2 * n3, 2 * n3, peak, status=st_d,
+                                                 workload="the step's reduced stream, decoded")
+    del s0, y
+    # the 64 MiB gradient-like buffer on two ranks: compress each, fused
+    # reduce, decompress the result
+    n = workloads.SIZES[2]
+    tab = 8 * (-(-n // 4096))
+    xs = [torch.from_numpy(workloads.generate(2, r).view(np.int16)).to(x0.device) for r in range(2)]
+    ss = [cc.empty_stream(n) for _ in xs]
+    ws2 = cc.empty_workspace(n)
+    sizes = []
+    for x, s_ in zip(xs, ss):
+        cc.cccl_compress(x, s_, ws2, stream=stream)
+        sizes.append(cc.cccl_get_result(ws2, stream)[0])
+    ms_c2 = timed(lambda: cc.cccl_compress(xs[0], ss[0], ws2, stream=stream))
+    red2 = cc.empty_stream(n)
+    ins = [s_[:b] for s_, b in zip(ss, sizes)]
+    ms_r2 = timed(lambda: cc.cccl_reduce_compressed(ins, n, red2, ws2, stream=stream))
+    rb2, st_r2 = cc.cccl_get_result(ws2, stream)
+    y2 = torch.empty(n, dtype=torch.int16, device=x0.device)
+    ms_d2 = timed(lambda: cc.cccl_decompress(red2[:rb2], y2, ws2, stream=stream))
+    step = 2 * ms_c2 + ms_r2 + ms_d2
+    w2 = "gradient-like 64 MiB bf16 buffer (33,554,432 values ~ N(0, 1e-3), 1% of positions x100)"
+    out["workload2_compress"] = op_row(ms_c2, 2 * n + sizes[0] + tab, 2 * n, peak,
+                                       ratio=round(sizes[0] / (2 * n), 5), workload=w2)
+    out["workload2_reduce_r2"] = op_row(ms_r2, sum(sizes) + 2 * tab + rb2 + tab, 4 * n, peak, status=st_r2,
+                                        workload=w2 + ", 2 ranks")
+    out["workload2_decompress"] = op_row(ms_d2, rb2 + tab + 2 * n, 2 * n, peak, workload=w2 + ", reduced stream")
+    out["workload2_step"] = {"ms": round(step, 5), "uncompressed_gbs": round(4 * n / (step * 1e-3) / 1e9, 1),
+                             "workload": w2 + ": compress both ranks, fused reduce R=2, decompress (sum of the ops "
+                                          "timed alone)"}
+    # local rank-0 buffer + one compressed remote rank (selective compression)
+    ms = timed(lambda: cc.cccl_reduce_mixed(xs[0], [ins[1]], red2, ws2, stream=stream))
+    out_bytes, st = cc.cccl_get_result(ws2, stream)
+    out["reduce_mixed"] = op_row(ms, 2 * n + sizes[1] + out_bytes, 4 * n, peak, status=st,
+                                 workload="local rank-0 buffer (uncompressed) + 1 compressed remote rank of " + w2)
     # KV-cache blocks of the [32, 2, 4096, 8, 128] shape: 4096 of a pool of 8192 blocks, shuffled
     n_pool, n_blk = 8192, 4096
-    pool = torch.from_numpy(workloads.generate(4, 0, count=n_pool * KV_BLOCK).view(np.int16)).cuda()
-    table = torch.from_numpy(np.random.default_rng(7).permutation(n_pool)[:n_blk].astype(np.int32)).cuda()
+    pool = torch.from_numpy(workloads.generate(4, 0, count=n_pool * KV_BLOCK).view(np.int16)).to(x0.device)
+    table = torch.from_numpy(np.random.default_rng(7).permutation(n_pool)[:n_blk].astype(np.int32)).to(x0.device)
     npg = n_blk * KV_BLOCK
     s_pg = cc.empty_stream(npg)
     ws_pg = cc.empty_workspace(npg)
@@ -373,42 +500,37 @@ def measure_extras(cc, torch, np, xs, streams, sizes, n, flush, peak, reps: int 
     ms_d = timed(lambda: cc.cccl_decompress_paged(s_pg[:pbytes], target, KV_BLOCK, table, ws_pg, stream=stream))
     _, st_d = cc.cccl_get_result(ws_pg, stream)
     ok = bool(torch.equal(target.view(n_pool, KV_BLOCK)[table.long()], pool.view(n_pool, KV_BLOCK)[table.long()]))
-    for name, ms_x, st_x in (("compress_paged", ms_c, st_c), ("decompress_paged", ms_d, st_d)):
-        algo = 2 * npg + pbytes
-        out[name] = {"ms": round(ms_x, 5), "workload": "4096 KV-cache blocks of 16 tokens x 8 heads x 128 dim "
-                     "(64 Mi values) gathered through a shuffled block table from a pool of 8192", "status": st_x,
-                     "uncompressed_gbs": round(2 * npg / (ms_x * 1e-3) / 1e9, 1), "algorithmic_bytes": algo,
-                     "hbm_gbs": round(algo / (ms_x * 1e-3) / 1e9, 1),
-                     "frac_of_measured_copy": round(algo / (ms_x * 1e-3) / 1e9 / peak, 4),
-                     "ratio": round(pbytes / (2 * npg), 5)}
-    out["decompress_paged"]["round_trip_exact"] = ok
+    kv = ("4096 KV-cache blocks of 16 tokens x 8 heads x 128 dim (64 Mi values) gathered through a shuffled block "
+          "table from a pool of 8192")
+    out["compress_paged"] = op_row(ms_c, 2 * npg + pbytes, 2 * npg, peak, status=st_c, workload=kv,
+                                   ratio=round(pbytes / (2 * npg), 5))
+    out["decompress_paged"] = op_row(ms_d, 2 * npg + pbytes, 2 * npg, peak, status=st_d, workload=kv,
+                                     round_trip_exact=ok)
+    del pool, target, s_pg
     # window-base variant (stream version 2) next to the minimum-base stream
     for name, x in (("compress_window", xs[0]),
                     ("compress_window_specials",
-                     torch.from_numpy(workloads.generate(5, 0, start=1 << 27, count=n).view(np.int16)).cuda())):
+                     torch.from_numpy(workloads.generate(5, 0, start=1 << 27, count=n).view(np.int16)).to(x0.device))):
         s_w = cc.empty_stream(n)
-        ws_w = cc.empty_workspace(n)
-        ms_w = timed(lambda: cc.cccl_compress_window(x, s_w, ws_w, stream=stream))
-        wbytes, st_w = cc.cccl_get_result(ws_w, stream)
-        cc.cccl_compress(x, s_w, ws_w, stream=stream)
-        v1bytes, _ = cc.cccl_get_result(ws_w, stream)
-        algo = 2 * n + wbytes
-        out[name] = {"ms": round(ms_w, 5), "workload": "64 MiB gradient-like buffer" if name == "compress_window"
-                     else "64 MiB of N(0, 1) with 0.1% each NaN, +-Inf, +-0, subnormals (second half of the worst-case "
-                     "buffer)", "status": st_w, "uncompressed_gbs": round(2 * n / (ms_w * 1e-3) / 1e9, 1),
-                     "algorithmic_bytes": algo, "hbm_gbs": round(algo / (ms_w * 1e-3) / 1e9, 1),
-                     "frac_of_measured_copy": round(algo / (ms_w * 1e-3) / 1e9 / peak, 4),
-                     "ratio": round(wbytes / (2 * n), 5), "ratio_min_base": round(v1bytes / (2 * n), 5)}
+        ms_w = timed(lambda: cc.cccl_compress_window(x, s_w, ws2, stream=stream))
+        wbytes, st_w = cc.cccl_get_result(ws2, stream)
+        cc.cccl_compress(x, s_w, ws2, stream=stream)
+        v1bytes, _ = cc.cccl_get_result(ws2, stream)
+        out[name] = op_row(ms_w, 2 * n + wbytes, 2 * n, peak, status=st_w,
+                           workload=w2 if name == "compress_window" else
+                           "64 MiB of N(0, 1) with 0.1% each NaN, +-Inf, +-0, subnormals (second half of the worst-case "
+                           "buffer)", ratio=round(wbytes / (2 * n), 5), ratio_min_base=round(v1bytes / (2 * n), 5))
+    del xs, ss, red2, y2
+    torch.cuda.empty_cache()
     out.update(measure_dtypes(cc, torch, np, n, timed, stream, peak))
     out.update(measure_workloads(cc, torch, np, timed, stream, peak))
     return out
 
 
 def measure_workloads(cc, torch, np, timed, stream, peak) -> dict:
-    """The larger bf16 workloads at their full sizes, each op timed alone:
-    the R=8 fused reduce over 8 x 256 MiB pre-compressed ranks; the 512 MiB
-    KV-cache tensor round trip; the 512 MiB worst case (half incompressible)
-    round trip and its R=4 fused reduce.  Inputs are far larger than the L2."""
+    """The 512 MiB workloads at their full sizes, each op timed alone: the
+    KV-cache tensor round trip; the worst case (half incompressible) round
+    trip and its R=4 fused reduce.  Inputs are far larger than the L2."""
     import workloads
 
     out = {}
@@ -460,12 +582,6 @@ def measure_workloads(cc, torch, np, timed, stream, peak) -> dict:
         return (row(ms_c, 2 * n + b + tab, 2 * n, status=st_c, ratio=round(b / (2 * n), 5)),
                 row(ms_d, b + tab + 2 * n, 2 * n, status=st_d, round_trip_exact=bool(torch.equal(x, y))))
 
-    # R = 8 ranks of 134,217,728 values ~ N(0, 0.02)
-    n, x0, ss, sizes, ws = compressed(3, 8)
-    out["workload3_reduce_r8"] = reduce_row(n, ss, sizes, ws, 8)
-    out["workload3_reduce_r8"]["workload"] = "8 pre-compressed ranks of 134,217,728 bf16 values (256 MiB each) " \
-                                             "~ N(0, 0.02), fused reduce in rank order 0..7"
-    del x0, ss, ws
     # KV-cache tensor [32, 2, 4096, 8, 128]
     n, x0, ss, sizes, ws = compressed(4, 1)
     c_row, d_row = round_trip_rows(n, x0, ss[0], sizes[0], ws)
@@ -495,7 +611,7 @@ def measure_dtypes(cc, torch, np, n, timed, stream, peak) -> dict:
     out = {}
     for name, dtype, bits in (("fp16", cc.CCCL_DTYPE_FP16, torch.int16), ("fp32", cc.CCCL_DTYPE_FP32, torch.int32)):
         item = 2 if dtype == cc.CCCL_DTYPE_FP16 else 4
-        xs = [torch.from_numpy(workloads.generate_typed(dtype, WORKLOAD, r).view(np.int16 if item == 2 else np.int32))
+        xs = [torch.from_numpy(workloads.generate_typed(dtype, 2, r).view(np.int16 if item == 2 else np.int32))
               .cuda() for r in range(2)]
         cap = cc.cccl_compress_bound_typed(dtype, n)
         ss = [torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in xs]
@@ -549,210 +665,164 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     xs_host = [workloads.generate(WORKLOAD, r) for r in seeds]
     n = xs_host[0].size
     R = len(xs_host)
-    pinned = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
-    xs = [p.to(device) for p in pinned]
-    cap = cc.cccl_compress_bound(n)
-    streams = [torch.empty(cap, dtype=torch.uint8, device=device) for _ in range(R)]
-    red = torch.empty(cap, dtype=torch.uint8, device=device)
-    y = torch.empty(n, dtype=torch.int16, device=device)
-    y_host = torch.empty(n, dtype=torch.int16).pin_memory()
-    wsb = cc.cccl_workspace_bytes(n)
-    ws = [torch.empty(wsb, dtype=torch.uint8, device=device) for _ in range(R + 2)]
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
+    cap = cc.cccl_compress_bound(n)
+    tab = 8 * (-(-n // 4096))
+    # the ranks' buffers, held pre-compressed in HBM (compression not timed)
+    streams, sizes = [], []
+    ws_c = cc.empty_workspace(n)
+    x0 = None
+    for r, xh in enumerate(xs_host):
+        x = torch.from_numpy(xh.view(np.int16)).to(device)
+        s_ = torch.empty(cap, dtype=torch.uint8, device=device)
+        cc.cccl_compress(x, s_, ws_c, stream=stream)
+        b, st = cc.cccl_get_result(ws_c, stream)
+        if st != 0:
+            raise RuntimeError("compress of rank %d: device status %d" % (r, st))
+        streams.append(s_)
+        sizes.append(b)
+        if r == 0:
+            x0 = x
+        else:
+            del x
+    ins = [s_[:b] for s_, b in zip(streams, sizes)]
+    red = torch.empty(cap, dtype=torch.uint8, device=device)
+    ws = cc.empty_workspace(n)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
-    def step(ev=None, s=stream):
-        # ev: list of (start, end) event pairs, one per op
-        for r in range(R):
-            if ev is not None:
-                ev[r][0].record(s)
-            cc.cccl_compress(xs[r], streams[r], ws[r], s)
-            if ev is not None:
-                ev[r][1].record(s)
-        if ev is not None:
-            ev[R][0].record(s)
-        cc.cccl_reduce_compressed(streams, n, red, ws[R], stream=s)
-        if ev is not None:
-            ev[R][1].record(s)
-            ev[R + 1][0].record(s)
-        cc.cccl_decompress(red, y, ws[R + 1], stream=s)
-        if ev is not None:
-            ev[R + 1][1].record(s)
+    def step(s=stream):
+        cc.cccl_reduce_compressed(ins, n, red, ws, stream=s)
 
-    # one untimed pass: sizes, ratios and a sampled check against the oracle
+    # one untimed step: size, status and a sampled check against the oracle
     step()
-    sizes = [cc.cccl_get_result(w, stream)[0] for w in ws[:R]]
-    red_bytes, red_status = cc.cccl_get_result(ws[R], stream)
-    _, dec_status = cc.cccl_get_result(ws[R + 1], stream)
-    if red_status or dec_status or 0 in sizes:
-        raise RuntimeError("device status %d/%d during the first step" % (red_status, dec_status))
-    check = check_against_oracle(xs_host, streams, sizes, y, n)
+    red_bytes, red_status = cc.cccl_get_result(ws, stream)
+    if red_status:
+        raise RuntimeError("device status %d during the first step" % red_status)
+    check = check_against_oracle(xs_host, streams, sizes, red, red_bytes, n)
 
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
     warmup = max(args.warmup, 3)
     for _ in range(warmup):
         flush.fill_(1)
         step()
     torch.cuda.synchronize()
-    y_plain = y.clone()
-
-    # The timed step is one CUDA graph: the same four library calls captured
-    # once (each call's workspace clear and kernel become graph nodes) and
-    # replayed every step.
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream(device)
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        step(s=side)
-    stream.wait_stream(side)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(graph):
-        step(s=torch.cuda.current_stream(device))
-    y.zero_()
-    for _ in range(warmup):
-        flush.fill_(1)
-        graph.replay()
-    torch.cuda.synchronize()
-    graph_ok = bool(torch.equal(y, y_plain))
-    del y_plain
-
-    sampler = ClockSampler(device.index if device.index is not None else 0)
-    sampler.start()
-    time.sleep(0.3)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    # timed region: K graph replays, the L2 flushed before each (untimed)
+    # timed region: K steps, each one C-ABI call (workspace clear + kernel),
+    # an event pair around it; the L2 flushed before each (untimed)
     t_wall0 = time.time()
-    evg = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for k in range(args.steps):
         flush.fill_(k & 0xFF)
-        evg[k][0].record(stream)
-        graph.replay()
-        evg[k][1].record(stream)
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
     torch.cuda.synchronize()
-    step_ms = [e0.elapsed_time(e1) for e0, e1 in evg]
+    t_wall1 = time.time()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     if world > 1:
         torch.distributed.barrier()
     total_ms = max_over_ranks(sum(step_ms), world, device)
-    # the ops one by one: K more steps of plain launches with an event pair
-    # around every call (the call's workspace clear included), same flush
-    op_ms = [[] for _ in range(R + 2)]
-    plain_ms = []
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R + 2)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        flush.fill_(k & 0xFF)
-        step(evs[k])
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    for k in range(args.steps):
-        e = evs[k]
-        for i in range(R + 2):
-            op_ms[i].append(e[i][0].elapsed_time(e[i][1]))
-        plain_ms.append(e[0][0].elapsed_time(e[R + 1][1]))
+    same_result = cc.cccl_get_result(ws, stream) == (red_bytes, 0)
 
-    # end to end through the same calls: pinned host inputs in, decoded result
-    # out, every step.  Pipelined over three streams with two device buffer
-    # sets: the upload of step k+1 and the download of step k-1 run while
-    # step k computes; the timed region spans the first upload to the last
-    # download.
-    e2e_steps = max(2, min(args.steps, 400))
+    # end to end through the same call: the compressed streams uploaded from
+    # pinned host memory and the result stream (its full bound, which holds
+    # the stream's own size) downloaded every step.  Pipelined over three
+    # streams with two device buffer sets: the upload of step k+1 and the
+    # download of step k-1 run while step k computes.  Untimed warm-up steps
+    # cover both buffer sets first.
+    e2e_steps = max(E2E_MIN_STEPS, args.steps)
     up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    xs2 = [xs, [torch.empty_like(x) for x in xs]]
-    ys2 = [y, torch.empty_like(y)]
-    y_hosts = [y_host, torch.empty(n, dtype=torch.int16).pin_memory()]
-    outs2 = [streams, [torch.empty_like(t) for t in streams]]
-    reds2 = [red, torch.empty_like(red)]
-    wss2 = [ws, [torch.empty_like(w) for w in ws]]
-    ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
-    ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
-    ev_out = [torch.cuda.Event() for _ in range(e2e_steps)]
+    pinned_in = [torch.empty(b, dtype=torch.uint8).pin_memory() for b in sizes]
+    for p, s_, b in zip(pinned_in, streams, sizes):
+        p.copy_(s_[:b])
+    dev_in = [[torch.empty(b, dtype=torch.uint8, device=device) for b in sizes] for _ in range(2)]
+    dev_out = [red, torch.empty_like(red)]
+    dev_ws = [ws, torch.empty_like(ws)]
+    host_out = [torch.empty(cap, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    n_total = E2E_WARMUP + e2e_steps
+    ev_in = [torch.cuda.Event() for _ in range(n_total)]
+    ev_done = [torch.cuda.Event() for _ in range(n_total)]
+    ev_out = [torch.cuda.Event() for _ in range(n_total)]
 
     def e2e_step(k):
         b = k % 2
         with torch.cuda.stream(up):
             if k >= 2:
                 up.wait_event(ev_done[k - 2])  # step k-2 has finished reading this buffer set
-            for r in range(R):
-                xs2[b][r].copy_(pinned[r], non_blocking=True)
+            for d, p in zip(dev_in[b], pinned_in):
+                d.copy_(p, non_blocking=True)
             ev_in[k].record(up)
         stream.wait_event(ev_in[k])
         if k >= 2:
             stream.wait_event(ev_out[k - 2])  # the result buffer of step k-2 was read out
-        for r in range(R):
-            cc.cccl_compress(xs2[b][r], outs2[b][r], wss2[b][r], stream)
-        cc.cccl_reduce_compressed(outs2[b], n, reds2[b], wss2[b][R], stream=stream)
-        cc.cccl_decompress(reds2[b], ys2[b], wss2[b][R + 1], stream=stream)
+        cc.cccl_reduce_compressed(dev_in[b], n, dev_out[b], dev_ws[b], stream=stream)
         ev_done[k].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(ev_done[k])
-            y_hosts[b].copy_(ys2[b], non_blocking=True)
+            host_out[b].copy_(dev_out[b], non_blocking=True)
             ev_out[k].record(down)
 
+    for k in range(E2E_WARMUP):
+        e2e_step(k)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(up)
-    for k in range(e2e_steps):
+    for k in range(E2E_WARMUP, n_total):
         e2e_step(k)
-    down.wait_event(ev_out[e2e_steps - 1])
+    down.wait_event(ev_out[n_total - 1])
     e1.record(down)
     e1.synchronize()
+    t_wall2 = time.time()
     e2e_total = max_over_ranks(e0.elapsed_time(e1), world, device)
-    last = (e2e_steps - 1) % 2
-    e2e_ok = bool(torch.equal(y_hosts[last], ys2[last].cpu()))
-    time.sleep(0.25)
-    sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
+    last = (n_total - 1) % 2
+    e2e_ok = bool(torch.equal(host_out[last][:red_bytes], red[:red_bytes].cpu()))
+    del dev_in, pinned_in, host_out
+    torch.cuda.empty_cache()
 
     bytes_step = R * 2 * n
     value = world * bytes_step * args.steps / (total_ms * 1e-3) / 1e9
     e2e_value = world * bytes_step * e2e_steps / (e2e_total * 1e-3) / 1e9
-
     peak, peak_kind = measured_peaks()
-    mean = lambda v: sum(v) / len(v)
-    ops = {}
-    total_in = sum(sizes)
-    algo = {"compress": 2 * n + mean(sizes), "reduce": total_in + red_bytes, "decompress": red_bytes + 2 * n}
-    comp_ms = mean([mean(op_ms[r]) for r in range(R)])
-    ops["compress"] = {"ms": comp_ms, "launches_per_step": R}
-    ops["reduce"] = {"ms": mean(op_ms[R]), "launches_per_step": 1}
-    ops["decompress"] = {"ms": mean(op_ms[R + 1]), "launches_per_step": 1}
-    for name, o in ops.items():
-        o["ms"] = round(o["ms"], 5)
-        o["uncompressed_gbs"] = round((R if name == "reduce" else 1) * 2 * n / (o["ms"] * 1e-3) / 1e9, 1)
-        o["algorithmic_bytes"] = int(algo[name])
-        o["hbm_gbs"] = round(algo[name] / (o["ms"] * 1e-3) / 1e9, 1)
-        o["frac_of_measured_copy"] = round(o["hbm_gbs"] / peak, 4)
-        o["frac_of_8tbs_nominal"] = round(o["hbm_gbs"] / 8000.0, 4)
-    dominant = max(ops, key=lambda k: ops[k]["ms"] * ops[k]["launches_per_step"])
-    kname = {"compress": "compress_kernel", "reduce": "reduce_kernel", "decompress": "decompress_kernel"}[dominant]
-    traffic = recorded_traffic(kname)
-    roofline = {"bound": "hbm", "kernel": kname, "achieved": ops[dominant]["hbm_gbs"], "peak": peak,
-                "peak_kind": peak_kind, "unit": "GB/s", "frac": ops[dominant]["frac_of_measured_copy"],
+    ms_mean = sum(step_ms) / len(step_ms)
+    algo = sum(sizes) + R * tab + red_bytes + tab
+    ops = {"reduce": op_row(ms_mean, algo, bytes_step, peak, launches_per_step=1,
+                            ms_median=round(statistics.median(step_ms), 5), ms_min=round(min(step_ms), 5))}
+    traffic = recorded_traffic("reduce_kernel")
+    roofline = {"bound": "hbm", "kernel": "reduce_kernel", "achieved": ops["reduce"]["hbm_gbs"], "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": ops["reduce"]["frac_of_measured_copy"],
+                "frac_of_8tbs_nominal": ops["reduce"]["frac_of_8tbs_nominal"],
                 "traffic": None if traffic is None else traffic["bytes_per_launch_scaled"],
-                "algorithmic_bytes_per_launch": ops[dominant]["algorithmic_bytes"]}
+                "algorithmic_bytes_per_launch": int(algo),
+                "duration": "mean CUDA-event time of the timed calls (each call: the workspace clear and the kernel)"}
+    extras = None
+    if not args.no_extras:
+        timed = make_timer(torch, flush, stream, reps=20)
+        extras = measure_extras(cc, torch, np, timed, stream, peak, x0, red, red_bytes, n)
+    t_wall3 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    clocks["whole_run"] = {k: v for k, v in sampler.summary(t_wall0, t_wall3).items() if k != "note"}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8+f32", "data": "synthetic",
-        "config": dict(workload_config(), input_sha256=[hashlib.sha256(x.tobytes()).hexdigest()[:16]
-                                                        for x in xs_host]),
-        "ratio": {"compress": round(mean(sizes) / (2 * n), 5), "reduce_out": round(red_bytes / (2 * n), 5)},
-        "launch": {"step": "one CUDA graph replay per step (the 4 library calls, each a workspace clear and a "
-                           "kernel)", "graph_result_matches_plain": graph_ok,
-                   "ops": "timed in a second pass of %d plain-launch steps, one event pair around each call "
-                          "(its workspace clear included)" % args.steps,
-                   "ms_per_step_plain": round(sum(plain_ms) / len(plain_ms), 5)},
+        "config": workload_config(input_hashes(xs_host)),
+        "ratio": {"inputs": round(sum(sizes) / (R * 2 * n), 5), "reduce_out": round(red_bytes / (2 * n), 5)},
+        "launch": {"step": "one cccl_reduce_compressed call per step (a workspace clear and one kernel)",
+                   "result_unchanged_after_timing": same_result},
         "ops": ops, "roofline": roofline,
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": R * 2 * n,
-                "d2h_bytes_per_step": 2 * n, "steps": e2e_steps,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(sum(sizes)),
+                "d2h_bytes_per_step": int(cap), "steps": e2e_steps, "warmup_steps": E2E_WARMUP,
                 "pipelined": "uploads on one stream, steps on another, downloads on a third; step k+1's "
                              "upload and step k-1's download overlap step k (two device buffer sets)",
-                "l2": "not flushed: every step uploads R x 64 MiB of input, more than the L2",
                 "result_matches_device": e2e_ok},
-        "gpu_launches": (R + 2) * args.steps,
+        "gpu_launches": args.steps,
         "clocks": clocks, "check": check,
-        "extras": measure_extras(cc, torch, np, xs, streams, sizes, n, flush, peak) if not args.no_extras else None,
+        "extras": extras,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(xs_host)
@@ -764,33 +834,47 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         print(json.dumps(line), flush=True)
 
 
-def check_against_oracle(xs_host, streams, sizes, y, n, chunks: int = 64) -> dict:
-    """Byte-exact check of sampled chunks against the oracle (not timed)."""
+def check_against_oracle(xs_host, streams, sizes, red, red_bytes, n, chunks: int = 16) -> dict:
+    """Byte-exact check against the oracle, not timed: three windows of
+    `chunks` chunks (start, middle, end) of every rank's stream and of the
+    reduced stream."""
+    import struct
+
     import numpy as np
 
     import oracle
 
     oracle.build()
-    import struct
-
+    n_chunks = -(-n // 4096)
     ok = True
-    for x, s, nb in zip(xs_host, streams, sizes):
-        head = s[:min(nb, 64 + 8 * (chunks + 1))].cpu().numpy().tobytes()
-        offs = struct.unpack_from("<%dQ" % (chunks + 1), head, 64)
-        body = s[offs[0]:offs[chunks]].cpu().numpy().tobytes()
-        ref = b"".join(oracle.encode_chunk(x[c * 4096:(c + 1) * 4096]) for c in range(chunks))
-        ok = ok and body == ref
-    want = oracle.sum_ranks([x[:chunks * 4096] for x in xs_host])
-    got = y[:chunks * 4096].cpu().numpy().view(np.uint16)
-    ok = ok and bool(np.array_equal(want, got))
-    return {"bit_exact_sample": ok, "sample": "first %d chunks of every stream and of the decoded sum" % chunks}
+    windows = [0, n_chunks // 2, n_chunks - chunks]
+
+    def chunk_bytes(s, nbytes, c0):
+        offs = struct.unpack_from("<%dQ" % (chunks + 1), s[64 + 8 * c0:64 + 8 * (c0 + chunks + 1)].cpu().numpy()
+                                  .tobytes()) if c0 + chunks < n_chunks else None
+        if offs is None:
+            first = struct.unpack_from("<Q", s[64 + 8 * c0:64 + 8 * c0 + 8].cpu().numpy().tobytes())[0]
+            return s[first:nbytes].cpu().numpy().tobytes()
+        return s[offs[0]:offs[chunks]].cpu().numpy().tobytes()
+
+    for c0 in windows:
+        a, b = c0 * 4096, min(n, (c0 + chunks) * 4096)
+        for x, s, nb in zip(xs_host, streams, sizes):
+            ref = b"".join(oracle.encode_chunk(x[c * 4096:(c + 1) * 4096]) for c in range(c0, c0 + chunks))
+            ok = ok and chunk_bytes(s, nb, c0) == ref
+        part = [oracle.compress(x[a:b]) for x in xs_host]
+        want = oracle.reduce(part, b - a)
+        body = want[oracle.data_start(b - a):].tobytes()
+        ok = ok and chunk_bytes(red, red_bytes, c0) == body
+    return {"bit_exact_sample": bool(ok),
+            "sample": "chunks [c, c+%d) for c in %s of every rank's stream and of the reduced stream" % (chunks, windows)}
 
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the rows timed outside the step")

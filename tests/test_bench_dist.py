@@ -51,7 +51,7 @@ def test_two_gloo_ranks():
         assert mx == 15.0  # the slowest rank's time
         assert sm == 3.0
         flat = [s for g in gathered for s in g]
-        assert len(flat) == len(set(flat)) == world * 2  # disjoint seeds per GPU
+        assert len(flat) == len(set(flat)) == world * 8  # disjoint seeds per GPU (8 simulated ranks each)
 
 
 def test_single_process_defaults(monkeypatch):
@@ -61,8 +61,8 @@ def test_single_process_defaults(monkeypatch):
         monkeypatch.delenv(k, raising=False)
     assert bench.dist_env() == (0, 1, 0)
     assert bench.max_over_ranks(3.5, 1) == 3.5
-    assert bench.simulated_ranks(0) == [0, 1]
-    assert bench.simulated_ranks(3) == [6, 7]
+    assert bench.simulated_ranks(0) == list(range(8))
+    assert bench.simulated_ranks(3) == list(range(24, 32))
 
 
 def test_kernel_source_hash_ignores_comments():
@@ -89,3 +89,19 @@ def test_recorded_traffic_is_consistent():
         assert len(rec["source_hash"]) == 16
         # used only while it names the current kernel code
         assert (bench.recorded_traffic(k) is not None) == (rec["source_hash"] == bench.kernel_source_hash())
+
+
+def test_clock_summary_reads_the_window():
+    """The clock record of the line: median SM clock, the maximum, the union
+    of clock event reasons and the power, over the samples inside the window
+    only; with no GPU the sampler says why it has no samples."""
+    import bench
+
+    cs = bench.ClockSampler(0)
+    assert cs.nvml is None and cs.note  # no GPU here: the reason is recorded
+    cs.samples = [(10.0, 1000.0, 2070.0, set(), 100.0), (11.0, 2070.0, 2070.0, {"sw_power_cap"}, 900.0),
+                  (12.0, 2000.0, 2070.0, set(), 800.0), (13.0, 500.0, 2070.0, {"hw_slowdown"}, 50.0)]
+    s = cs.summary(10.5, 12.5)
+    assert s["samples"] == 2 and s["sm_mhz"] == 2035.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 900.0
+    assert cs.summary(20.0, 30.0)["samples"] == 0
