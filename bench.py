@@ -870,6 +870,54 @@ def check_against_oracle(xs_host, streams, sizes, red, red_bytes, n, chunks: int
             "sample": "chunks [c, c+%d) for c in %s of every rank's stream and of the reduced stream" % (chunks, windows)}
 
 
+def run_case(args) -> None:
+    """One kernel alone, for a profiler: --case OP,WORKLOAD,RANKS,VALUES with OP
+    compress, decompress or reduce.  The inputs (VALUES values of WORKLOAD's
+    recipe per rank) are generated and, for decompress and reduce, compressed
+    first; then the op runs --warmup + --steps times, one call after another
+    on the current stream, and one JSON line gives its mean CUDA-event time."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import compression_coupled_collectives_gb300 as cc
+    import workloads
+
+    op, w, ranks, n = args.case.split(",")
+    w, ranks, n = int(w), int(ranks), int(n)
+    stream = torch.cuda.current_stream()
+    xs = [torch.from_numpy(workloads.generate(w, r, count=n, n=max(n, workloads.SIZES[w])).view(np.int16)).cuda()
+          for r in range(ranks)]
+    ws = cc.empty_workspace(n)
+    streams = []
+    for x in xs:
+        s_ = cc.empty_stream(n)
+        cc.cccl_compress(x, s_, ws, stream=stream)
+        streams.append(s_[:cc.cccl_get_result(ws, stream)[0]])
+    out = cc.empty_stream(n)
+    y = torch.empty(n, dtype=torch.int16, device="cuda")
+    calls = {"compress": lambda: cc.cccl_compress(xs[0], out, ws, stream=stream),
+             "decompress": lambda: cc.cccl_decompress(streams[0], y, ws, stream=stream),
+             "reduce": lambda: cc.cccl_reduce_compressed(streams, n, out, ws, stream=stream)}
+    call = calls[op]
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    e1.synchronize()
+    _, st = cc.cccl_get_result(ws, stream)
+    print(json.dumps({"case": args.case, "ms_mean": round(e0.elapsed_time(e1) / args.steps, 5), "status": st,
+                      "input_bytes": [int(t.numel() * t.element_size()) for t in (streams if op != "compress" else [xs[0]])]}))
+    if st != 0:
+        raise RuntimeError("device status %d" % st)
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -878,7 +926,11 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the rows timed outside the step")
+    ap.add_argument("--case", help="OP,WORKLOAD,RANKS,VALUES: time one kernel alone (for profilers)")
     args = ap.parse_args(argv)
+    if args.case:
+        run_case(args)
+        return 0
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)

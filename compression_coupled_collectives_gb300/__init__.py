@@ -71,6 +71,9 @@ _lib.cccl_get_result.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint64), ctyp
 _lib.cccl_get_result.restype = _i
 _lib.cccl_selftest_timeouts.argtypes = [_vp, _sz, _vp]
 _lib.cccl_selftest_timeouts.restype = _i
+_lib.cccl_selftest_lookback.argtypes = [_vp, ctypes.c_uint32, ctypes.c_uint32, _i, _vp, _vp, _sz, _vp]
+_lib.cccl_selftest_lookback.restype = _i
+LOOKBACK_POISON = 0xC000000000000000
 _lib.cccl_status_string.argtypes = [_i]
 _lib.cccl_status_string.restype = ctypes.c_char_p
 
@@ -131,7 +134,8 @@ def cccl_compress_window(x: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, s
 def cccl_compress_noalloc(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
     """Enqueue the same compression as cccl_compress using the library's static
     device scratch instead of a caller workspace (nothing is allocated).  The
-    stream size is then bytes 32..39 of ``out`` (0 if a device wait ran out)."""
+    stream size is then bytes 32..39 of ``out``; no device status is reported
+    (see include/cccl.h)."""
     x = _bf16_bits(x)
     _check(_lib.cccl_compress_noalloc(x.data_ptr(), x.numel(), out.data_ptr(), out.numel() * out.element_size(),
                                       _stream(stream)), "cccl_compress_noalloc")
@@ -269,6 +273,19 @@ def cccl_get_result(ws: torch.Tensor, stream=None) -> tuple[int, int]:
     _check(_lib.cccl_get_result(ws.data_ptr(), _stream(stream), ctypes.byref(nbytes), ctypes.byref(dev)),
            "cccl_get_result")
     return int(nbytes.value), int(dev.value)
+
+
+def cccl_selftest_lookback(sizes: torch.Tensor, result: torch.Tensor, ws: torch.Tensor, poison_unit: int | None = None,
+                           concurrent: bool = False, stream=None) -> None:
+    """Enqueue the look-back self test over len(sizes) units (int32 device
+    tensor of sizes below 2^17); `result` (int64 device tensor, one per unit)
+    receives each unit's offset (4096 + the sizes before it), or
+    LOOKBACK_POISON from the poisoned unit on."""
+    n = sizes.numel()
+    p = n if poison_unit is None else poison_unit
+    _check(_lib.cccl_selftest_lookback(sizes.data_ptr(), n, p, 1 if concurrent else 0, result.data_ptr(),
+                                       ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "cccl_selftest_lookback")
 
 
 def cccl_selftest_timeouts(ws: torch.Tensor, stream=None) -> None:

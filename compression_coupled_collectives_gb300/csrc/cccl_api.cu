@@ -30,6 +30,57 @@ __global__ void selftest_timeouts_kernel(WsHeader* ws) {
     }
 }
 
+// cccl_selftest_lookback.  Publication: unit 0 its end offset, the poisoned
+// unit (if any) the poison flag, every other unit its size alone.
+__global__ void selftest_publish_kernel(const uint32_t* sizes, uint32_t n, uint32_t poison, uint64_t start,
+                                        uint64_t* status) {
+    for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < n; g += gridDim.x * blockDim.x)
+        status[g] = g == poison ? kFlagPoison : (g == 0 ? (kFlagPrefix | (start + sizes[0])) : (kFlagAggregate | sizes[g]));
+}
+// Serial order: one warp runs the look-back of units n-1, n-2, ..., 1 in that
+// order, so no unit finds a prefix but unit 0's: each walks back over every
+// predecessor, many 256-entry windows for the later units.
+// The poisoned unit does not look back (a failed unit never does).
+__global__ void selftest_lookback_serial_kernel(const uint32_t* sizes, uint32_t n, uint32_t poison, uint64_t start,
+                                                WsHeader* ws, uint64_t* status, uint64_t* result) {
+    const uint32_t lane = threadIdx.x & 31;
+    for (uint32_t g = n - 1; g >= 1; --g) {
+        const uint64_t off = g == poison ? kFlagPoison : lookback_offset_wide(status, g, sizes[g], start, ws, true);
+        if (lane == 0) result[g] = off;
+    }
+    if (lane == 0) result[0] = poison == 0 ? kFlagPoison : start;
+}
+// Concurrent order, as the compress and reduce kernels run it: warps take
+// tickets (unit numbers in order, so every predecessor is already being
+// worked on), wait a pseudo-random time (up to 20 us; one unit in 64 up to
+// 200 us, a late publisher), then publish their size and look back.
+__global__ void selftest_lookback_concurrent_kernel(const uint32_t* sizes, uint32_t n, uint32_t poison,
+                                                    uint64_t start, WsHeader* ws, uint64_t* status,
+                                                    uint64_t* result) {
+    const uint32_t lane = threadIdx.x & 31;
+    for (;;) {
+        uint32_t g = 0;
+        if (lane == 0) g = atomicAdd(&ws->ticket, 1u);
+        g = __shfl_sync(0xFFFFFFFFu, g, 0);
+        if (g >= n) return;
+        uint32_t h = g * 2654435761u;
+        h ^= h >> 15;
+        h *= 2246822519u;
+        h ^= h >> 13;
+        const uint64_t wait_ns = (h % 64u == 0u) ? 200000u : (h % 20000u);
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < wait_ns) __nanosleep(1000);  // ends: the timer advances
+        uint64_t off;
+        if (g == poison) {
+            if (lane == 0) st_relaxed_u64(&status[g], kFlagPoison);
+            off = kFlagPoison;
+        } else {
+            off = lookback_offset_wide(status, g, sizes[g], start, ws);
+        }
+        if (lane == 0) result[g] = off;
+    }
+}
+
 }  // namespace cccl
 
 namespace {
@@ -376,6 +427,33 @@ cccl_status cccl_selftest_timeouts(void* d_ws, size_t ws_bytes, cccl_stream_t st
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (clear_ws(d_ws, need, s) != CCCL_OK) return CCCL_ERR_CUDA;
     cccl::selftest_timeouts_kernel<<<1, 64, 0, s>>>(static_cast<cccl::WsHeader*>(d_ws));
+    return cudaGetLastError() == cudaSuccess ? CCCL_OK : CCCL_ERR_CUDA;
+}
+
+cccl_status cccl_selftest_lookback(const uint32_t* d_sizes, uint32_t n_units, uint32_t poison_unit, int concurrent,
+                                   uint64_t* d_result, void* d_ws, size_t ws_bytes, cccl_stream_t stream) {
+    if (n_units == 0 || n_units > CCCL_SELFTEST_MAX_UNITS) return CCCL_ERR_INVALID_ARG;
+    const size_t need = sizeof(cccl::WsHeader) + 8 * (size_t)n_units;
+    if (d_sizes == nullptr || d_result == nullptr || d_ws == nullptr || !aligned16(d_ws) ||
+        (reinterpret_cast<uintptr_t>(d_sizes) & 3) != 0 || (reinterpret_cast<uintptr_t>(d_result) & 7) != 0)
+        return CCCL_ERR_INVALID_ARG;
+    if (ws_bytes < need || !device_range(d_ws, need) || !device_range(d_sizes, 4 * (size_t)n_units) ||
+        !device_range(d_result, 8 * (size_t)n_units))
+        return CCCL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_ws(d_ws, need, s) != CCCL_OK) return CCCL_ERR_CUDA;
+    auto* ws = static_cast<cccl::WsHeader*>(d_ws);
+    auto* status = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(d_ws) + sizeof(cccl::WsHeader));
+    const uint64_t start = 4096;
+    if (concurrent) {
+        cccl::selftest_lookback_concurrent_kernel<<<4 * 152, 128, 0, s>>>(d_sizes, n_units, poison_unit, start, ws,
+                                                                           status, d_result);
+    } else {
+        cccl::selftest_publish_kernel<<<(n_units + 255) / 256, 256, 0, s>>>(d_sizes, n_units, poison_unit, start,
+                                                                            status);
+        cccl::selftest_lookback_serial_kernel<<<1, 32, 0, s>>>(d_sizes, n_units, poison_unit, start, ws, status,
+                                                               d_result);
+    }
     return cudaGetLastError() == cudaSuccess ? CCCL_OK : CCCL_ERR_CUDA;
 }
 

@@ -143,7 +143,12 @@ cccl_status cccl_compress_window(const uint16_t *d_in, size_t n_elems, void *d_o
  * the stream into a CUDA graph.  Each call clears the scratch it uses and the
  * 64-byte stream header on `stream` before compressing.
  * The compressed size is the stream header's total_bytes (bytes 32..39 of
- * d_out) once the work is done; it stays 0 if a device-side wait ran out.
+ * d_out) once the work is done: the header is cleared first, and the size is
+ * written when the last chunk has been placed.  There is no workspace to
+ * report a device-side error in: a wait that ran out (TIMEOUT, which only a
+ * fault inside the kernel could cause) goes unreported, and the stream can
+ * then lack chunks even though total_bytes is set.  A caller that needs the
+ * device status uses cccl_compress with a workspace and cccl_get_result.
  * All calls on a device share the one scratch array: calls that may overlap
  * on the GPU (different streams without ordering between them) race and must
  * not be issued; calls on one stream are ordered and safe.
@@ -330,6 +335,41 @@ cccl_status cccl_get_result(const void *d_ws, cccl_stream_t stream, uint64_t *ou
  * workspace, CUDA if the clear or the launch failed, else OK; then
  * cccl_get_result reports TIMEOUT (after about 2 s). */
 cccl_status cccl_selftest_timeouts(void *d_ws, size_t ws_bytes, cccl_stream_t stream);
+
+/* Largest n_units cccl_selftest_lookback accepts. */
+#define CCCL_SELFTEST_MAX_UNITS ((uint32_t)1 << 20)
+
+/* Self test of the decoupled look-back that places variable-size units of
+ * chunks densely in a stream (section 4.4 of "CCCL: In-GPU Compression-
+ * Coupled Collective Communication" writes each block straight into its
+ * final place; here every unit's place is the exclusive prefix sum of the
+ * sizes before it, found by looking back over its predecessors' published
+ * sizes).  It runs the library's own look-back over n_units units of the
+ * given sizes and writes each unit's offset (the prefix sum plus 4096).
+ *   d_sizes       n_units device uint32 sizes, each below 2^17 (a unit of the
+ *                 compress and reduce kernels is at most 8 chunks of 16,400
+ *                 bytes); read only.
+ *   poison_unit   a unit that publishes the poison flag instead of its size
+ *                 (as a failed unit would); every later unit then reports
+ *                 poison; n_units or more for none.
+ *   concurrent    0: every unit's size is published first (unit 0 as its end
+ *                 offset), then one warp looks back for units n_units-1 down
+ *                 to 1, so each walks over all its predecessors (many 256-unit
+ *                 windows).  1: warps take units in ticket order, wait a
+ *                 pseudo-random time (up to 20 us, one unit in 64 up to
+ *                 200 us), publish and look back concurrently, as the
+ *                 kernels do.
+ *   d_result      n_units device uint64: the offset of each unit, or
+ *                 0xC000000000000000 (poison) for the poisoned unit and every
+ *                 unit after it.
+ *   d_ws          workspace of at least 16 + 8 * n_units bytes, 16-byte
+ *                 aligned; cleared here first.
+ * Every wait is the library's bounded one: a wait that runs out records
+ * TIMEOUT, which cccl_get_result reports.
+ * Returns INVALID_ARG for an argument outside these rules, CUDA if the clear
+ * or a launch failed, else OK. */
+cccl_status cccl_selftest_lookback(const uint32_t *d_sizes, uint32_t n_units, uint32_t poison_unit, int concurrent,
+                                   uint64_t *d_result, void *d_ws, size_t ws_bytes, cccl_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char *cccl_status_string(cccl_status status);

@@ -36,7 +36,7 @@ def test_header_declares_the_boundary():
                             "cccl_status_string", "cccl_compress_paged", "cccl_decompress_paged",
                             "cccl_compress_window", "cccl_reduce_op", "cccl_compress_bound_typed",
                             "cccl_compress_typed", "cccl_decompress_typed", "cccl_reduce_typed",
-                            "cccl_selftest_timeouts"]), names
+                            "cccl_selftest_timeouts", "cccl_selftest_lookback"]), names
 
 
 def test_library_exports_every_declared_symbol(cc):
@@ -221,3 +221,21 @@ int main() {
     calls, results = [int(v) for v in out[:4]], [int(v) for v in out[4:]]
     assert calls == [1, 1, 2, 2]
     assert results == [0, 0, 0, 1, 0, 0, 0, 0]  # 1 = cudaErrorInvalidValue
+
+
+def test_selftest_lookback_argument_checks(cc):
+    lib = cc._lib
+    n = 100
+    sizes = np.zeros(n + 4, np.uint32)
+    res = np.zeros(n + 2, np.uint64)
+    ws = np.zeros(16 + 8 * n + 16, np.uint8)
+    base = (ws.ctypes.data + 15) // 16 * 16
+    s_ptr, r_ptr = (sizes.ctypes.data + 3) // 4 * 4, (res.ctypes.data + 7) // 8 * 8
+    assert lib.cccl_selftest_lookback(s_ptr, 0, n, 0, r_ptr, base, 16 + 8 * n, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_selftest_lookback(s_ptr, (1 << 20) + 1, n, 0, r_ptr, base, 1 << 30, None) == \
+        cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_selftest_lookback(None, n, n, 0, r_ptr, base, 16 + 8 * n, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_selftest_lookback(s_ptr, n, n, 0, r_ptr, base + 4, 16 + 8 * n, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_selftest_lookback(s_ptr, n, n, 0, r_ptr, base, 8 * n, None) == cc.CCCL_ERR_INVALID_ARG
+    assert lib.cccl_selftest_lookback(s_ptr, n, n, 0, r_ptr, base, 16 + 8 * n, None) == \
+        cc.CCCL_ERR_INVALID_ARG  # host memory

@@ -46,6 +46,22 @@ def test_noalloc_matches_compress_on_two_calls_in_a_row(cc, wl):
         assert torch.equal(out[:size], ref)  # tolerance 0: identical bytes
 
 
+def test_noalloc_larger_call_then_smaller_call(cc, wl):
+    """The scratch keeps the previous call's placement words; a smaller call
+    after a larger one must clear what it uses and give the same bytes as the
+    entry point with its own workspace."""
+    sizes = [2000 * 4096 + 777, 3 * 4096 + 5, 1]
+    for n in sizes:
+        x = torch.from_numpy(wl.generate(2, 5, count=n, n=1 << 24).view(np.int16)).cuda()
+        ref = cc.compress(x)
+        out = cc.empty_stream(n)
+        cc.cccl_compress_noalloc(x, out)
+        torch.cuda.synchronize()
+        size = _stream_size(out)
+        assert size == ref.numel()
+        assert torch.equal(out[:size], ref)
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(cc):
     x = torch.zeros(16, dtype=torch.int16, device="cuda")
     out = torch.zeros(64, dtype=torch.uint8, device="cuda")
