@@ -44,10 +44,16 @@
 namespace cccl {
 
 constexpr int kMaxTeams = 4;
-// decode teams per CTA = output chunks per group: 3, so that the CTA's 14
-// warps (at most 4 per SM sub-partition) get 128 registers per thread
+// The kernel's shape for element type T: T's fields, plus the number of
+// decode teams per CTA (= output chunks per group) and the depth of each
+// team's ring of staged rank chunks.  launch_reduce_t picks one per call.
+template <class T, int kTeamsV, int kRingSlotsV>
+struct ReduceShape : T {
+    static constexpr int kTeams = kTeamsV;
+    static constexpr int kRingSlots = kRingSlotsV;
+};
 template <class D>
-__host__ __device__ constexpr int teams() { return 3; }
+__host__ __device__ constexpr int teams() { return D::kTeams; }
 template <class D>
 __host__ __device__ constexpr int loader_warp() { return 4 * teams<D>(); }   // also the locator
 template <class D>
@@ -60,11 +66,9 @@ constexpr int kMetaBufs = 3;
 template <class D>
 __host__ __device__ constexpr int reduce_threads() { return 32 * (placer_warp<D>() + 1); }
 constexpr uint64_t kNoGroup = ~0ull;
-// staged rank chunks per team: 6 of 8.2 KB for the 16-bit types (the copies
-// for the next output chunk are in flight while the team decodes this one),
-// 2 of 16.4 KB for fp32
+// staged rank chunks per team (8.2 KB each for the 16-bit types, 16.4 KB for fp32)
 template <class D>
-__host__ __device__ constexpr int rslots() { return D::kElemBytes == 4 ? 2 : 6; }
+__host__ __device__ constexpr int rslots() { return D::kRingSlots; }
 constexpr int kMaxRSlots = 6;
 // output staging buffers per team, cycled by group: a team stages the chunk
 // of group i while the placer still copies out the one of group i - 1
@@ -808,16 +812,16 @@ __global__ void __launch_bounds__(reduce_threads<D>(), 1)
 }
 
 // Per-device record of the shared-memory limit set for reduce_kernel<D>,
-// by element type code.  A plain static array: a function-local static of a
-// template would become one object shared by every copy of this library
-// loaded into the process, and a second copy would then take its own
-// kernel's limit as set.
-static PerDeviceOnce g_reduce_smem_limit[4];
+// by element type code and team count.  A plain static array: a
+// function-local static of a template would become one object shared by
+// every copy of this library loaded into the process, and a second copy
+// would then take its own kernel's limit as set.
+static PerDeviceOnce g_reduce_smem_limit[4][kMaxTeams + 1];
 
 template <class D>
-cudaError_t launch_reduce_t(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,
-                            void* ws, cudaStream_t stream) {
-    PerDeviceOnce& smem_limit = g_reduce_smem_limit[D::kCode];
+cudaError_t launch_reduce_shape(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,
+                                void* ws, cudaStream_t stream, bool two_loaders) {
+    PerDeviceOnce& smem_limit = g_reduce_smem_limit[D::kCode][D::kTeams];
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -838,16 +842,38 @@ cudaError_t launch_reduce_t(const ReduceInputs& inputs, int R, uint64_t n_elems,
     so.dtype = D::kCode;
     const uint64_t n_groups = (so.n_chunks + teams<D>() - 1) / teams<D>();
     const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
-    // Nearly incompressible inputs (at least 90% of their raw size) are
-    // mostly raw chunks: the teams are then bound by data arrival, and a
-    // second loader warp keeps their rings full; compressed inputs are bound
-    // by decoding, and one loader warp is faster (both measured on GB300).
-    uint64_t in_total = 0;
-    for (int r = 0; r < R; ++r)
-        in_total += (r == 0 && inputs.local != nullptr) ? (uint64_t)D::kElemBytes * n_elems : inputs.in_bytes[r];
-    const bool two_loaders = 10 * in_total >= 9 * (uint64_t)R * D::kElemBytes * n_elems;
     reduce_kernel<D><<<grid, reduce_threads<D>(), reduce_smem<D>(), stream>>>(inputs, R, so, two_loaders);
     return cudaGetLastError();
+}
+
+// Compressed bf16 inputs are bound by decoding: four teams (96 registers per
+// thread) with four ring slots each and one loader warp run fastest.
+// Nearly incompressible inputs (their streams at least 90% of the raw size:
+// mostly raw chunks, cheap to decode) are bound by data arrival: three teams
+// (128 registers) with six slots each, and a second loader warp that only
+// issues copies, keep the rings fuller.  fp16 keeps three teams (its decode
+// spills at 96 registers); fp32 chunks take twice the shared memory: three
+// teams of two slots.  (All measured on GB300; every shape computes the
+// same bytes.)  in_bytes is the readable size the caller gives for each
+// stream, normally its total size.
+template <class T>
+cudaError_t launch_reduce_t(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,
+                            void* ws, cudaStream_t stream) {
+    uint64_t in_total = 0;
+    for (int r = 0; r < R; ++r)
+        in_total += (r == 0 && inputs.local != nullptr) ? (uint64_t)T::kElemBytes * n_elems : inputs.in_bytes[r];
+    const bool incompressible = 10 * in_total >= 9 * (uint64_t)R * T::kElemBytes * n_elems;
+    if constexpr (T::kElemBytes == 4) {
+        return launch_reduce_shape<ReduceShape<T, 3, 2>>(inputs, R, n_elems, out, capacity, ws, stream,
+                                                          incompressible);
+    } else if constexpr (T::kExpBits == 5) {
+        return launch_reduce_shape<ReduceShape<T, 3, 6>>(inputs, R, n_elems, out, capacity, ws, stream,
+                                                          incompressible);
+    } else {
+        if (incompressible)
+            return launch_reduce_shape<ReduceShape<T, 3, 6>>(inputs, R, n_elems, out, capacity, ws, stream, true);
+        return launch_reduce_shape<ReduceShape<T, 4, 4>>(inputs, R, n_elems, out, capacity, ws, stream, false);
+    }
 }
 
 cudaError_t launch_reduce(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,
