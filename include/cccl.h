@@ -139,9 +139,8 @@ cccl_status cccl_compress_window(const uint16_t *d_in, size_t n_elems, void *d_o
  *   d_in, n_elems, d_out, out_capacity, stream: as for cccl_compress.
  *   n_elems must be 1..CCCL_NOALLOC_MAX_ELEMS, else CCCL_ERR_INVALID_ARG.
  * The first call on a device looks up the scratch's device address (with
- * that device current) and caches it; make that first call before capturing
- * the stream into a CUDA graph.  Each call clears the scratch it uses and the
- * 64-byte stream header on `stream` before compressing.
+ * that device current) and caches it.  Each call clears the scratch it uses
+ * and the 64-byte stream header on `stream` before compressing.
  * The compressed size is the stream header's total_bytes (bytes 32..39 of
  * d_out) once the work is done: the header is cleared first, and the size is
  * written when the last chunk has been placed.  There is no workspace to
