@@ -75,6 +75,14 @@ constexpr int kMaxRSlots = 6;
 template <class D>
 __host__ __device__ constexpr int sbufs() { return 2; }
 constexpr int kMaxSBufs = 2;
+// size records (a group's sizes, tally and index), cycled by group: one more
+// than the staging buffers, so that a team publishes the size of group i
+// before it waits for the placer to free a staging buffer (the record of
+// group i - zslots() is free by then: the team waited for the placer to be
+// done with group i - 1 - sbufs() in its previous iteration)
+template <class D>
+__host__ __device__ constexpr int zslots() { return sbufs<D>() + 1; }
+constexpr int kMaxZSlots = kMaxSBufs + 1;
 template <class D>
 __host__ __device__ constexpr size_t ring_bytes() { return (size_t)teams<D>() * rslots<D>() * max_chunk_bytes<D>(); }
 template <class D>
@@ -183,15 +191,15 @@ struct ReduceMeta {
 struct ReduceSmem {
     uint64_t meta_ready[kMetaBufs];      // loader -> teams: meta[b] describes the next group (1 arrival)
     uint64_t decoded[kMetaBufs];         // teams, loader -> loader: meta[b] read (each team warp and the loader)
-    uint64_t sized[kMaxSBufs];           // teams -> placer: the group's sizes are in (one arrival per team)
+    uint64_t sized[kMaxZSlots];          // teams -> placer: the group's sizes are in (one arrival per team)
     uint64_t staged[kMaxSBufs];          // teams -> placer: the group's chunks are staged (one per team warp)
     uint64_t stored[kMaxSBufs];          // placer -> teams: the group's staging buffers were read (1 arrival)
     uint64_t full[kMaxTeams][kMaxRSlots];   // a rank chunk landed in the slot (transaction count)
     uint64_t free_[kMaxTeams][kMaxRSlots];  // every warp of the team is done with the slot (4 arrivals)
-    unsigned long long tally[kMaxSBufs];    // sized teams (high word) and their bytes (low word)
-    uint32_t size[kMaxSBufs][kMaxTeams];
-    uint32_t failed[kMaxSBufs][kMaxTeams];  // the team's chunk could not be reduced
-    uint64_t gid[kMaxSBufs];                // group sized in buffer p, or kNoGroup
+    unsigned long long tally[kMaxZSlots];   // sized teams (high word) and their bytes (low word)
+    uint32_t size[kMaxZSlots][kMaxTeams];
+    uint32_t failed[kMaxZSlots][kMaxTeams];  // the team's chunk could not be reduced
+    uint64_t gid[kMaxZSlots];               // group sized in record z, or kNoGroup
     int32_t esc_diff[kMaxTeams][kMaxRanks]; // per rank: sentinel codes found minus the header's escapes
     uint32_t corrupt[kMaxTeams][2];         // a rank chunk body is malformed (by iteration parity)
     TeamXch xch[kMaxTeams];                 // the encoder's exchange space
@@ -575,19 +583,20 @@ __device__ __forceinline__ void finish_values(const uint64_t* acc, uint32_t op, 
 template <class D>
 __device__ __forceinline__ void reduce_placer(const StreamOut& so, const uint8_t* staging, ReduceSmem& sm) {
     constexpr int kSB = sbufs<D>();
+    constexpr int kZ = zslots<D>();
     constexpr int kTeams = teams<D>();
     const uint32_t lane = threadIdx.x & 31;
     for (int i = 0; !warp_any(sm.abort); ++i) {
-        const int b = i % kSB;
+        const int b = i % kSB, z = i % kZ;
         const uint32_t ph = (uint32_t)(i / kSB) & 1u;
-        if (!warp_wait(&sm.sized[b], ph)) {
+        if (!warp_wait(&sm.sized[z], (uint32_t)(i / kZ) & 1u)) {
             if (lane == 0) set_abort(so, sm);
             break;
         }
-        const uint64_t g = sm.gid[b];
+        const uint64_t g = sm.gid[z];
         if (g == kNoGroup) break;
-        const uint32_t mine = lane < (uint32_t)kTeams ? sm.size[b][lane] : 0u;
-        const bool failed = warp_any(lane < (uint32_t)kTeams && sm.failed[b][lane] != 0);
+        const uint32_t mine = lane < (uint32_t)kTeams ? sm.size[z][lane] : 0u;
+        const bool failed = warp_any(lane < (uint32_t)kTeams && sm.failed[z][lane] != 0);
         uint32_t incl = mine;
 #pragma unroll
         for (int d = 1; d < kTeams; d <<= 1) {
@@ -602,7 +611,7 @@ __device__ __forceinline__ void reduce_placer(const StreamOut& so, const uint8_t
         } else {
             go = lookback_offset_wide(so.status, g, total, data_start(so.n_chunks), so.ws, true);
         }
-        if (lane == 0) sm.tally[b] = 0;  // next added to for group i + kSB, after `stored` below
+        if (lane == 0) sm.tally[z] = 0;  // next added to for group i + kZ, after `stored` below
         if (!warp_wait(&sm.staged[b], ph)) {
             if (lane == 0) set_abort(so, sm);
             break;
@@ -630,6 +639,7 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
     constexpr int kRSlots = rslots<D>();
     constexpr int kW = thread_words<D>();
     constexpr int kSB = sbufs<D>();
+    constexpr int kZ = zslots<D>();
     constexpr uint32_t kSlotBytes = max_chunk_bytes<D>();
     constexpr int kTeams = teams<D>();
     const uint32_t lane = threadIdx.x & 31, team = threadIdx.x >> 7, tt = threadIdx.x & 127, wq = tt >> 5;
@@ -638,7 +648,7 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
     const uint64_t n_full = so.n_elems / kChunkElems;
     uint32_t s = 0, ph = 0;  // this team's next ring slot and its phase (the loader's order)
     for (int i = 0;; ++i) {
-        const int b = i % kMetaBufs, sb = i % kSB;
+        const int b = i % kMetaBufs, sb = i % kSB, z = i % kZ;
         const bool ready = mbar_wait(&sm.meta_ready[b], (uint32_t)(i / kMetaBufs) & 1u);
         if (bar.any(!ready || sm.abort)) {
             if (tt == 0) set_abort(so, sm);
@@ -649,11 +659,10 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
         const ReduceMeta& m = sm.meta[b];
         const uint64_t g = m.g;
         if (g == kNoGroup) {
-            // tell the placer, once it is done with the buffers' last group
-            if (i >= kSB) warp_wait(&sm.stored[sb], (uint32_t)((i - kSB) / kSB) & 1u);
+            // tell the placer (record z is free: see zslots)
             if (tt == 96) {
-                if (team == 0) sm.gid[sb] = kNoGroup;
-                mbar_arrive(&sm.sized[sb]);
+                if (team == 0) sm.gid[z] = kNoGroup;
+                mbar_arrive(&sm.sized[z]);
             }
             return;
         }
@@ -731,24 +740,24 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
             }
         }
         if (fail) bytes = 0;
-        // the placer is done with group i - kSB: its sizes, tally and staging buffers
-        const bool free_buf = i < kSB || warp_wait(&sm.stored[sb], (uint32_t)((i - kSB) / kSB) & 1u);
-        if (!free_buf && lane == 0) set_abort(so, sm);
         if (tt == 96) {  // lane 0 of warp 3
-            sm.size[sb][team] = bytes;
-            sm.failed[sb][team] = fail;
-            if (team == 0) sm.gid[sb] = g;
+            sm.size[z][team] = bytes;
+            sm.failed[z][team] = fail;
+            if (team == 0) sm.gid[z] = g;
             if (fail) {
                 record_error(so.ws, fail);
             } else {
                 // the last team to size the group publishes its size at once,
                 // so later groups' look-backs need not wait for the placer
-                const unsigned long long old = atomicAdd(&sm.tally[sb], (1ull << 32) | bytes);
+                const unsigned long long old = atomicAdd(&sm.tally[z], (1ull << 32) | bytes);
                 if ((old >> 32) == kTeams - 1)
                     publish_unit_size(so.status, g, (uint32_t)old + bytes, data_start(so.n_chunks));
             }
-            mbar_arrive(&sm.sized[sb]);
+            mbar_arrive(&sm.sized[z]);
         }
+        // the placer is done with group i - kSB: its staging buffers
+        const bool free_buf = i < kSB || warp_wait(&sm.stored[sb], (uint32_t)((i - kSB) / kSB) & 1u);
+        if (!free_buf && lane == 0) set_abort(so, sm);
         if (free_buf && bytes > 0) {
             uint8_t* dst = staging_base + ((size_t)team * kSB + sb) * kSlotBytes;
             if (c < n_full)
@@ -766,7 +775,8 @@ template <class D>
 __global__ void __launch_bounds__(reduce_threads<D>(), 1)
     reduce_kernel(ReduceInputs inputs, int R, StreamOut so, bool two_loaders) {
     constexpr int kTeams = teams<D>();
-    static_assert(kTeams <= kMaxTeams && rslots<D>() <= kMaxRSlots && sbufs<D>() <= kMaxSBufs,
+    static_assert(kTeams <= kMaxTeams && rslots<D>() <= kMaxRSlots && sbufs<D>() <= kMaxSBufs &&
+                      zslots<D>() <= kMaxZSlots,
                   "the shared-memory bookkeeping arrays are sized for these bounds");
     static_assert(reduce_smem<D>() + sizeof(ReduceSmem) <= 227 * 1024, "shared memory per CTA");
     extern __shared__ __align__(128) uint8_t smem[];
@@ -780,10 +790,12 @@ __global__ void __launch_bounds__(reduce_threads<D>(), 1)
             mbar_init(&sm.decoded[b], 4 * kTeams + 1);
         }
         for (int b = 0; b < sbufs<D>(); ++b) {
-            mbar_init(&sm.sized[b], kTeams);
             mbar_init(&sm.staged[b], 4 * kTeams);
             mbar_init(&sm.stored[b], 1);
-            sm.tally[b] = 0;
+        }
+        for (int z = 0; z < zslots<D>(); ++z) {
+            mbar_init(&sm.sized[z], kTeams);
+            sm.tally[z] = 0;
         }
         for (int t = 0; t < kTeams; ++t) {
             for (int s = 0; s < rslots<D>(); ++s) {
