@@ -771,7 +771,9 @@ __device__ __forceinline__ void reduce_team(int R, const void* local, uint32_t o
     }
 }
 
-template <class D>
+// kSum: the operator is the sum (op 0), compiled without the min and max
+// paths (a smaller kernel); otherwise op comes from the inputs.
+template <class D, bool kSum>
 __global__ void __launch_bounds__(reduce_threads<D>(), 1)
     reduce_kernel(ReduceInputs inputs, int R, StreamOut so, bool two_loaders) {
     constexpr int kTeams = teams<D>();
@@ -819,12 +821,12 @@ __global__ void __launch_bounds__(reduce_threads<D>(), 1)
     } else if (w == placer_warp<D>())
         reduce_placer<D>(so, staging, sm);
     else if (w < 4 * (uint32_t)kTeams)
-        reduce_team<D>(R, inputs.local, inputs.op, so, ring, staging, sm);
+        reduce_team<D>(R, inputs.local, kSum ? 0u : inputs.op, so, ring, staging, sm);
     // (a warp with no role has nothing to do)
 }
 
-// Per-device record of the shared-memory limit set for reduce_kernel<D>,
-// by element type code and team count.  A plain static array: a
+// Per-device record of the shared-memory limit set for reduce_kernel<D, *>
+// (both operator variants), by element type code and team count.  A plain static array: a
 // function-local static of a template would become one object shared by
 // every copy of this library loaded into the process, and a second copy
 // would then take its own kernel's limit as set.
@@ -839,8 +841,12 @@ cudaError_t launch_reduce_shape(const ReduceInputs& inputs, int R, uint64_t n_el
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
         e = smem_limit.run(dev, [] {
-            return cudaFuncSetAttribute(reduce_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)reduce_smem<D>());
+            cudaError_t r = cudaFuncSetAttribute(reduce_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)reduce_smem<D>());
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(reduce_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)reduce_smem<D>());
+            return r;
         });
     if (e != cudaSuccess) return e;
     StreamOut so;
@@ -854,7 +860,10 @@ cudaError_t launch_reduce_shape(const ReduceInputs& inputs, int R, uint64_t n_el
     so.dtype = D::kCode;
     const uint64_t n_groups = (so.n_chunks + teams<D>() - 1) / teams<D>();
     const unsigned grid = (unsigned)(n_groups < (uint64_t)sms ? n_groups : (uint64_t)sms);
-    reduce_kernel<D><<<grid, reduce_threads<D>(), reduce_smem<D>(), stream>>>(inputs, R, so, two_loaders);
+    if (inputs.op == 0)
+        reduce_kernel<D, true><<<grid, reduce_threads<D>(), reduce_smem<D>(), stream>>>(inputs, R, so, two_loaders);
+    else
+        reduce_kernel<D, false><<<grid, reduce_threads<D>(), reduce_smem<D>(), stream>>>(inputs, R, so, two_loaders);
     return cudaGetLastError();
 }
 
