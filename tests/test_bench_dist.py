@@ -5,7 +5,6 @@ the slowest rank's time and on the total, and reduce disjoint simulated ranks
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
