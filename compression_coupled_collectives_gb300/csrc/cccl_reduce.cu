@@ -45,12 +45,14 @@ namespace cccl {
 
 constexpr int kMaxTeams = 4;
 // The kernel's shape for element type T: T's fields, plus the number of
-// decode teams per CTA (= output chunks per group) and the depth of each
-// team's ring of staged rank chunks.  launch_reduce_t picks one per call.
-template <class T, int kTeamsV, int kRingSlotsV>
+// decode teams per CTA (= output chunks per group), the depth of each team's
+// ring of staged rank chunks and its number of output staging buffers.
+// launch_reduce_t picks one per call.
+template <class T, int kTeamsV, int kRingSlotsV, int kSBufsV = 2>
 struct ReduceShape : T {
     static constexpr int kTeams = kTeamsV;
     static constexpr int kRingSlots = kRingSlotsV;
+    static constexpr int kSBufs = kSBufsV;
 };
 template <class D>
 __host__ __device__ constexpr int teams() { return D::kTeams; }
@@ -70,10 +72,11 @@ constexpr uint64_t kNoGroup = ~0ull;
 template <class D>
 __host__ __device__ constexpr int rslots() { return D::kRingSlots; }
 constexpr int kMaxRSlots = 6;
-// output staging buffers per team, cycled by group: a team stages the chunk
-// of group i while the placer still copies out the one of group i - 1
+// output staging buffers per team, cycled by group: with two, a team stages
+// the chunk of group i while the placer still copies out the one of group
+// i - 1; one is enough when a group's decodes outlast the placer's work
 template <class D>
-__host__ __device__ constexpr int sbufs() { return 2; }
+__host__ __device__ constexpr int sbufs() { return D::kSBufs; }
 constexpr int kMaxSBufs = 2;
 // size records (a group's sizes, tally and index), cycled by group: one more
 // than the staging buffers, so that a team publishes the size of group i
@@ -826,16 +829,17 @@ __global__ void __launch_bounds__(reduce_threads<D>(), 1)
 }
 
 // Per-device record of the shared-memory limit set for reduce_kernel<D, *>
-// (both operator variants), by element type code and team count.  A plain static array: a
+// (both operator variants), by element type code, team count and staging
+// buffers per team.  A plain static array: a
 // function-local static of a template would become one object shared by
 // every copy of this library loaded into the process, and a second copy
 // would then take its own kernel's limit as set.
-static PerDeviceOnce g_reduce_smem_limit[4][kMaxTeams + 1];
+static PerDeviceOnce g_reduce_smem_limit[4][kMaxTeams + 1][kMaxSBufs + 1];
 
 template <class D>
 cudaError_t launch_reduce_shape(const ReduceInputs& inputs, int R, uint64_t n_elems, uint8_t* out, uint64_t capacity,
                                 void* ws, cudaStream_t stream, bool two_loaders) {
-    PerDeviceOnce& smem_limit = g_reduce_smem_limit[D::kCode][D::kTeams];
+    PerDeviceOnce& smem_limit = g_reduce_smem_limit[D::kCode][D::kTeams][D::kSBufs];
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -868,7 +872,9 @@ cudaError_t launch_reduce_shape(const ReduceInputs& inputs, int R, uint64_t n_el
 }
 
 // Compressed bf16 inputs are bound by decoding: four teams (96 registers per
-// thread) with four ring slots each and one loader warp run fastest.
+// thread) with one loader warp run fastest; from six ranks on, a group's
+// decodes outlast the placer's look-back and stores, so each team keeps one
+// staging buffer and five ring slots, else two and four.
 // Nearly incompressible inputs (their streams at least 90% of the raw size:
 // mostly raw chunks, cheap to decode) are bound by data arrival: three teams
 // (128 registers) with six slots each, and a second loader warp that only
@@ -893,6 +899,8 @@ cudaError_t launch_reduce_t(const ReduceInputs& inputs, int R, uint64_t n_elems,
     } else {
         if (incompressible)
             return launch_reduce_shape<ReduceShape<T, 3, 6>>(inputs, R, n_elems, out, capacity, ws, stream, true);
+        if (R >= 6)
+            return launch_reduce_shape<ReduceShape<T, 4, 5, 1>>(inputs, R, n_elems, out, capacity, ws, stream, false);
         return launch_reduce_shape<ReduceShape<T, 4, 4>>(inputs, R, n_elems, out, capacity, ws, stream, false);
     }
 }

@@ -83,7 +83,7 @@ def test_decompress_writes_only_n_values(cc, wl, n):
 
 
 @pytest.mark.parametrize("n", SIZES)
-@pytest.mark.parametrize("R", [1, 3])
+@pytest.mark.parametrize("R", [1, 3, 8])
 def test_reduce_writes_only_its_stream(cc, wl, n, R):
     streams = [cc.compress(values(wl, 1, r, n)) for r in range(R)]
     full, out = guarded(cc.cccl_compress_bound(n), PAT_OUT)
