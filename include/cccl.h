@@ -40,9 +40,10 @@
  *   raw.  Exactly one stream is valid for each input.
  *
  * Conventions for every entry point:
- *   - The caller owns every buffer.  The library allocates nothing and keeps
- *     no state between calls; calls with distinct workspaces may run
- *     concurrently.
+ *   - The caller owns every buffer.  The library allocates nothing per call.
+ *     Between calls it keeps only cccl_compress_noalloc's static scratch and,
+ *     per device, a record that each kernel's shared-memory limit was set.
+ *     Calls with distinct workspaces may run concurrently.
  *   - d_* pointers are device pointers (cudaMalloc'd or managed), 16-byte
  *     aligned.  h_* pointers are host pointers.  Each device buffer, with the
  *     size passed for it, must lie inside one device allocation; a range that
